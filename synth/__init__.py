@@ -1,0 +1,250 @@
+"""Seeded synthetic inputs for the sparse MoE FFN layer.
+
+This module is shared by the oracle's tests and by the CUDA path's tests and
+benchmark.  It only *draws* numbers (weights, biases, activations) and
+describes layer shapes; it contains none of the layer's arithmetic.
+
+Recipe (the pages publish no weights; all inputs are synthetic):
+
+* every weight matrix ~ N(0, 1/fan_in) (the second parameter read as the
+  variance), fan_in = H for router / gate / up / shared-gate vector, F (or Fs)
+  for the down projections;
+* biases ~ N(0, 0.02) (variance), i.e. std sqrt(0.02);
+* activations x ~ N(0, 1);
+* ``router_init="uniform"``: router rows ~ U(-a, a) with a = sqrt(3/H) (same
+  variance as the normal case);
+* ``router_init="zipf"``: expert load skewed as Zipf(s) over a seeded
+  permutation of the experts: with p_r proportional to r^-s, a seeded unit
+  vector u and alpha = 8, router row e = G_e + (ln p_e / alpha) u and token
+  x_t = z_t + alpha u, so logit_e ~ ln p_e + N(0, ~1): top-k then behaves like
+  drawing k experts without replacement from the Zipf law.
+* bf16 tensors are rounded to nearest-even once; both sides read those values.
+
+The generator is counter-based (SplitMix64 hash + Box-Muller, ``synth.c``), so
+value i of a tensor does not depend on chunking or threads, and token row t of
+x is the same for every token count.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_LIB = os.path.join(_HERE, "libsynth.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile synth.c into libsynth.so next to it (gcc, OpenMP if present)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c99", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _get():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            u64, i64, dbl, vp = ctypes.c_uint64, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+            for name in ("synth_normal_f32", "synth_normal_bf16", "synth_uniform_f32", "synth_uniform_bf16"):
+                fn = getattr(lib, name)
+                fn.argtypes = [u64, u64, u64, i64, dbl, dbl, vp]
+                fn.restype = None
+            lib.synth_u64.argtypes = [u64, u64, u64, i64, vp]
+            lib.synth_u64.restype = None
+            lib.synth_f32_to_bf16.argtypes = [vp, i64, vp]
+            lib.synth_f32_to_bf16.restype = None
+            lib.synth_bf16_to_f32.argtypes = [vp, i64, vp]
+            lib.synth_bf16_to_f32.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def normal(shape, std: float, seed: int, stream: int, dtype: str, offset: int = 0, mean: float = 0.0) -> np.ndarray:
+    n = int(np.prod(shape))
+    if dtype == "bf16":
+        out = np.empty(shape, dtype=np.uint16)
+        _get().synth_normal_bf16(seed, stream, offset, n, mean, std, _ptr(out))
+    else:
+        out = np.empty(shape, dtype=np.float32)
+        _get().synth_normal_f32(seed, stream, offset, n, mean, std, _ptr(out))
+    return out
+
+
+def uniform(shape, lo: float, hi: float, seed: int, stream: int, dtype: str, offset: int = 0) -> np.ndarray:
+    n = int(np.prod(shape))
+    if dtype == "bf16":
+        out = np.empty(shape, dtype=np.uint16)
+        _get().synth_uniform_bf16(seed, stream, offset, n, lo, hi, _ptr(out))
+    else:
+        out = np.empty(shape, dtype=np.float32)
+        _get().synth_uniform_f32(seed, stream, offset, n, lo, hi, _ptr(out))
+    return out
+
+
+def u64(n: int, seed: int, stream: int, offset: int = 0) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint64)
+    _get().synth_u64(seed, stream, offset, n, _ptr(out))
+    return out
+
+
+def to_bf16(a: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest even."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    out = np.empty(a.shape, dtype=np.uint16)
+    _get().synth_f32_to_bf16(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def bf16_to_f32(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    out = np.empty(a.shape, dtype=np.float32)
+    _get().synth_bf16_to_f32(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def as_f32(a: np.ndarray, dtype: str) -> np.ndarray:
+    """The exact stored values of an f32 or bf16 tensor as float32."""
+    return bf16_to_f32(a) if dtype == "bf16" else a
+
+
+# ----------------------------------------------------------------------------
+# layer shapes
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class LayerSpec:
+    name: str
+    hidden: int
+    n_expert: int
+    top_k: int
+    expert_ff: int
+    shared_ff: int = 0
+    router_mode: str = "softmax_topk"      # or "topk_softmax" (gpt-oss)
+    norm_topk_prob: bool = True
+    weights_scale: float = 1.0
+    act: str = "swiglu"                    # or "clamp_glu" (gpt-oss)
+    act_alpha: float = 1.702
+    act_limit: float = 7.0
+    has_bias: bool = False
+    gate_up_interleaved: bool = False
+    dtype: str = "bf16"                    # weights and activations: "f32" / "bf16"
+    router_init: str = "normal"            # "normal" / "uniform" / "zipf"
+    zipf_s: float = 1.1
+
+    def replace(self, **kw) -> "LayerSpec":
+        return dataclasses.replace(self, **kw)
+
+
+TINY = LayerSpec("tiny-f32 (H=64, E=8, top-2, F=32)", 64, 8, 2, 32, dtype="f32")
+QWEN = LayerSpec("qwen35moe-shaped (H=2048, E=256, top-8, F=512, shared 512)", 2048, 256, 8, 512, shared_ff=512)
+QWEN_ZIPF = QWEN.replace(name="qwen35moe-shaped, Zipf s=1.1 expert load (H=2048, E=256, top-8, F=512, shared 512)",
+                         router_init="zipf")
+GPTOSS = LayerSpec("gpt-oss-20b-shaped (H=2880, E=32, top-4, F=2880, biases, clamped GLU)", 2880, 32, 4, 2880,
+                   router_mode="topk_softmax", act="clamp_glu", has_bias=True, gate_up_interleaved=True)
+MIXTRAL = LayerSpec("mixtral-shaped (H=4096, E=8, top-2, F=14336)", 4096, 8, 2, 14336, router_init="uniform")
+
+# workload -> token counts exercised
+WORKLOADS = {
+    "tiny": (TINY, (16,)),
+    "qwen_decode": (QWEN, (1, 4, 8)),
+    "qwen_prefill_zipf": (QWEN_ZIPF, (4096,)),
+    "gptoss": (GPTOSS, (1, 64, 2048)),
+    "mixtral": (MIXTRAL, (1, 16, 256, 4096, 16384)),
+}
+
+# stream ids, one per tensor
+_S = dict(router_w=1, router_b=2, gate_w=3, up_w=4, gate_up_w=5, gate_up_b=6, down_w=7, down_b=8,
+          sh_gate_w=9, sh_up_w=10, sh_down_w=11, sh_gate_inp=12, zipf_perm=20, zipf_dir=21, x=100)
+_ZIPF_ALPHA = 8.0
+_BIAS_STD = math.sqrt(0.02)
+
+
+def _zipf_parts(spec: LayerSpec, seed: int):
+    """Seeded expert permutation -> log p_e, and the unit direction u."""
+    E, H = spec.n_expert, spec.hidden
+    keys = u64(E, seed, _S["zipf_perm"])
+    order = np.argsort(keys, kind="stable")          # rank r of expert order[r]
+    p = np.arange(1, E + 1, dtype=np.float64) ** (-spec.zipf_s)
+    p /= p.sum()
+    logp = np.empty(E, dtype=np.float64)
+    logp[order] = np.log(p)
+    u = normal((H,), 1.0, seed, _S["zipf_dir"], "f32").astype(np.float64)
+    u /= np.linalg.norm(u)
+    return logp, u
+
+
+def make_weights(spec: LayerSpec, seed: int = 0) -> dict:
+    """All weight/bias tensors of one layer as numpy arrays (float32, or
+    uint16 bf16 bit patterns when spec.dtype == "bf16")."""
+    H, E, F, Fs, dt = spec.hidden, spec.n_expert, spec.expert_ff, spec.shared_ff, spec.dtype
+    w = {}
+    if spec.router_init == "uniform":
+        a = math.sqrt(3.0 / H)
+        w["router_w"] = uniform((E, H), -a, a, seed, _S["router_w"], dt)
+    elif spec.router_init == "zipf":
+        g = normal((E, H), 1.0 / math.sqrt(H), seed, _S["router_w"], "f32").astype(np.float64)
+        logp, u = _zipf_parts(spec, seed)
+        r = (g + (logp / _ZIPF_ALPHA)[:, None] * u[None, :]).astype(np.float32)
+        w["router_w"] = to_bf16(r) if dt == "bf16" else r
+    else:
+        w["router_w"] = normal((E, H), 1.0 / math.sqrt(H), seed, _S["router_w"], dt)
+    if spec.has_bias:
+        w["router_b"] = normal((E,), _BIAS_STD, seed, _S["router_b"], dt)
+        w["gate_up_b"] = normal((E, 2 * F), _BIAS_STD, seed, _S["gate_up_b"], dt)
+        w["down_b"] = normal((E, H), _BIAS_STD, seed, _S["down_b"], dt)
+    if spec.gate_up_interleaved:
+        w["gate_up_w"] = normal((E, 2 * F, H), 1.0 / math.sqrt(H), seed, _S["gate_up_w"], dt)
+    else:
+        w["gate_w"] = normal((E, F, H), 1.0 / math.sqrt(H), seed, _S["gate_w"], dt)
+        w["up_w"] = normal((E, F, H), 1.0 / math.sqrt(H), seed, _S["up_w"], dt)
+    w["down_w"] = normal((E, H, F), 1.0 / math.sqrt(F), seed, _S["down_w"], dt)
+    if Fs > 0:
+        w["sh_gate_w"] = normal((Fs, H), 1.0 / math.sqrt(H), seed, _S["sh_gate_w"], dt)
+        w["sh_up_w"] = normal((Fs, H), 1.0 / math.sqrt(H), seed, _S["sh_up_w"], dt)
+        w["sh_down_w"] = normal((H, Fs), 1.0 / math.sqrt(Fs), seed, _S["sh_down_w"], dt)
+        w["sh_gate_inp"] = normal((H,), 1.0 / math.sqrt(H), seed, _S["sh_gate_inp"], dt)
+    return w
+
+
+def make_x(spec: LayerSpec, n_tokens: int, seed: int = 0, first_token: int = 0) -> np.ndarray:
+    """Token activations [n_tokens, H]; row t is token first_token + t of the
+    seeded stream (the same values whatever n_tokens is)."""
+    H = spec.hidden
+    off = first_token * H
+    if spec.router_init == "zipf":
+        z = normal((n_tokens, H), 1.0, seed, _S["x"], "f32", offset=off).astype(np.float64)
+        _, u = _zipf_parts(spec, seed)
+        x = (z + _ZIPF_ALPHA * u[None, :]).astype(np.float32)
+        return to_bf16(x) if spec.dtype == "bf16" else x
+    return normal((n_tokens, H), 1.0, seed, _S["x"], spec.dtype, offset=off)
+
+
+def weight_bytes_per_expert(spec: LayerSpec) -> int:
+    """Bytes of one routed expert's weights (and biases) as stored."""
+    el = 2 if spec.dtype == "bf16" else 4
+    n = 3 * spec.hidden * spec.expert_ff
+    if spec.has_bias:
+        n += 2 * spec.expert_ff + spec.hidden
+    return n * el
