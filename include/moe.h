@@ -1,0 +1,224 @@
+/*
+ * moe.h -- C ABI of libmoe, a GB300 (sm_103a) implementation of the sparse
+ * Mixture-of-Experts FFN sublayer of an LLM decoder.
+ *
+ * The layer takes the post-norm hidden state x [T][H] and returns the FFN
+ * output [T][H] without the residual (the caller adds it):
+ *
+ *   l      = Wr x (+ b_r)                                        router logits
+ *   (idx, w) = softmax -> top-k -> renormalise -> * scale        (mode 0), or
+ *              top-k on l -> softmax over the k                  (mode 1)
+ *   y_e    = W_down,e act(W_gate,e x, W_up,e x) (+ b_down,e)     each selected e
+ *   out    = sum_j w_j y_{idx_j}  +  sigmoid(w_sh . x) * SwiGLU_shared(x)
+ *
+ * Passages defining the operation:
+ *   - "Qwen3.5-MoE Model Implementation" (Pantheon), section "MoE routing":
+ *     router [n_expert, n_embd] -> softmax -> top-8 -> norm_topk_prob
+ *     renormalisation -> expert_weights_scale; SwiGLU experts; shared expert
+ *     with scalar sigmoid gate [n_embd]; out = moe_out + shexp_out, residual
+ *     by the caller.
+ *   - "Phase 19: MoE -- gpt-oss-20b" (xserv), section 2, Router and Experts:
+ *     logits with bias, top-4 then softmax over the 4; fused interleaved
+ *     gate_up with bias (gate = even rows, up = odd rows), gate <= limit,
+ *     -limit <= up <= limit, h = (up + 1) * gate * sigmoid(alpha * gate),
+ *     down with bias.  Measured tensor layout: weights stored [out][in].
+ *   - "Llama Forward Pass" (Pantheon), sections "Mixture of Experts
+ *     (Mixtral)" and "Expert weight formats in GGUF": merged expert tensors
+ *     gate/up [E][F][H], down [E][H][F].
+ *   - "Engine" (cherenkov), section "Prefill": tokens grouped by expert,
+ *     gathered, projected and scattered back.
+ *
+ * Conventions for every entry point:
+ *   - Matrices are row-major [out][in] (the input dimension contiguous).
+ *   - All calls return a moe_status; on failure moe_last_error() describes it
+ *     (a per-thread string, valid until the next call on that thread).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is asynchronous on it.
+ *   - The library uses the CUDA device that is current when the layer is
+ *     created; later calls on that layer must run with the same device
+ *     current.
+ *   - Public structs carry no build-dependent fields ("Llama Forward Pass",
+ *     ABI note on pn_qweight.gpu).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,     /* bad pointer, size, alignment or config */
+    MOE_ERR_UNSUPPORTED = -2,     /* valid but not implemented combination */
+    MOE_ERR_OOM = -3,             /* device allocation failed at create */
+    MOE_ERR_CUDA = -4,            /* a CUDA runtime call failed */
+    MOE_ERR_TOO_MANY_TOKENS = -5, /* n_tokens > config.max_tokens */
+    MOE_ERR_DEVICE_TIMEOUT = -6   /* a bounded device-side wait gave up */
+} moe_status;
+
+typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
+
+typedef enum {
+    /* softmax over all experts -> top-k -> (renormalise) -> * weights_scale
+     * ("Qwen3.5-MoE Model Implementation", MoE routing; "Llama Forward
+     * Pass", Mixture of Experts) */
+    MOE_ROUTER_SOFTMAX_TOPK = 0,
+    /* top-k on the (biased) logits -> softmax over the k selected
+     * ("Phase 19: MoE -- gpt-oss-20b", section 2, Router) */
+    MOE_ROUTER_TOPK_SOFTMAX = 1
+} moe_router_mode;
+
+typedef enum {
+    MOE_ACT_SWIGLU = 0,      /* h = silu(gate) * up */
+    MOE_ACT_CLAMP_GLU = 1    /* gpt-oss: g = min(gate, limit), u = clamp(up, -limit, limit),
+                                h = (u + 1) * g * sigmoid(alpha * g) */
+} moe_act;
+
+typedef struct {
+    int32_t hidden;              /* H; multiple of 8 (64 for the tensor-core path) */
+    int32_t n_expert;            /* E; 1 .. 1024 */
+    int32_t top_k;               /* k; 1 .. min(E, 32) */
+    int32_t expert_ff;           /* F; multiple of 8 (64 for the tensor-core path) */
+    int32_t shared_ff;           /* Fs; 0 = no shared expert, else multiple of 8 (64 for tensor cores) */
+    int32_t router_mode;         /* moe_router_mode */
+    int32_t norm_topk_prob;      /* mode 0: 1 = divide the kept probabilities by their sum */
+    float weights_scale;         /* mode 0: multiplier after renormalisation (1.0) */
+    int32_t act;                 /* moe_act (the routed experts; the shared expert is SwiGLU) */
+    float act_alpha;             /* MOE_ACT_CLAMP_GLU: 1.702 */
+    float act_limit;             /* MOE_ACT_CLAMP_GLU: 7.0 */
+    int32_t has_bias;            /* router [E], gate_up [E][2F], down [E][H] biases */
+    int32_t gate_up_interleaved; /* 1: one [E][2F][H] gate_up tensor, gate = even rows */
+    int32_t w_dtype;             /* moe_dtype of every weight and bias */
+    int32_t act_dtype;           /* moe_dtype of x; must equal w_dtype */
+    int32_t out_dtype;           /* moe_dtype of out */
+    int32_t max_tokens;          /* workspace is sized once for this many tokens */
+} moe_config;
+
+/* Weights: pointers to memory that cudaMemcpy can read (device memory, or
+ * host memory under unified addressing), in w_dtype.  moe_layer_create copies
+ * (and repacks) them into library-owned device memory; the caller may free its
+ * copies when create returns.  Unused fields must be NULL. */
+typedef struct {
+    const void *router_w;    /* [E][H] */
+    const void *router_b;    /* [E]            (has_bias) */
+    const void *gate_w;      /* [E][F][H]      (!gate_up_interleaved) */
+    const void *up_w;        /* [E][F][H]      (!gate_up_interleaved) */
+    const void *gate_up_w;   /* [E][2F][H]     (gate_up_interleaved) */
+    const void *gate_up_b;   /* [E][2F]        (has_bias): interleaved order when
+                                gate_up_interleaved, else [gate F | up F] */
+    const void *down_w;      /* [E][H][F] */
+    const void *down_b;      /* [E][H]         (has_bias) */
+    const void *sh_gate_w;   /* [Fs][H]        (shared_ff > 0) */
+    const void *sh_up_w;     /* [Fs][H] */
+    const void *sh_down_w;   /* [H][Fs] */
+    const void *sh_gate_inp; /* [H] scalar-gate vector */
+} moe_weights;
+
+typedef struct moe_layer moe_layer;
+
+/* Validates the config, copies/repacks the weights and allocates all device
+ * workspace for config.max_tokens.  Synchronous.  On failure *out is NULL and
+ * nothing stays allocated.  Errors: INVALID_ARG (NULL pointer, inconsistent
+ * config, a required weight missing), UNSUPPORTED (act_dtype != w_dtype,
+ * sizes not multiples of 8), OOM, CUDA. */
+moe_status moe_layer_create(const moe_config *config, const moe_weights *weights, moe_layer **out);
+
+/* out[n_tokens][H] (out_dtype) = the layer applied to x[n_tokens][H]
+ * (act_dtype).  x and out are caller-owned device pointers, 16-byte aligned,
+ * non-overlapping.  Asynchronous on `stream`; allocates nothing and never
+ * synchronises the host.  Results are bitwise reproducible for the same
+ * inputs (fixed-order combine, no floating-point atomics).  n_tokens == 0 is
+ * a no-op.  Errors: INVALID_ARG (NULL / misaligned / aliasing pointers,
+ * n_tokens < 0), TOO_MANY_TOKENS (n_tokens > max_tokens), CUDA (launch
+ * failure).  Device-side wait timeouts are reported by moe_get_status.
+ * Calls on one layer must not overlap on the GPU (they share its workspace):
+ * issue them on one stream or order them with events. */
+moe_status moe_forward(moe_layer *layer, const void *x, int32_t n_tokens, void *out, void *stream);
+
+/* Same as moe_forward with x and out in HOST memory (pinned memory makes the
+ * copies asynchronous).  The copies in and out go through device staging
+ * buffers allocated at create and are issued on `stream`; the caller must
+ * synchronise `stream` before reading out. */
+moe_status moe_forward_host(moe_layer *layer, const void *x_host, int32_t n_tokens, void *out_host,
+                            void *stream);
+
+/* Routing of the last forward: idx[n][k] (int32, descending weight, ties to
+ * the lower expert index) and w[n][k] (fp32), n = that forward's n_tokens.
+ * Device pointers; either may be NULL.  Asynchronous on `stream`. */
+moe_status moe_get_routing(moe_layer *layer, int32_t *idx, float *w, void *stream);
+
+/* Router logits of the last forward: logits[n][E] fp32 (router bias included)
+ * and, with a shared expert, its gate logit sh[n] (w_sh . x).  Device
+ * pointers; either may be NULL.  Asynchronous on `stream`. */
+moe_status moe_get_logits(moe_layer *layer, float *logits, float *sh_logit, void *stream);
+
+/* Number of token rows routed to each expert in the last forward:
+ * counts[E] int32 (device pointer).  Asynchronous on `stream`. */
+moe_status moe_get_expert_counts(moe_layer *layer, int32_t *counts, void *stream);
+
+/* Kernel-path selection, for tests and benchmarks. */
+typedef enum {
+    MOE_PATH_AUTO = 0,     /* by tokens per expert (default) */
+    MOE_PATH_STREAM = 1,   /* weight-streaming CUDA-core kernels (any dtype) */
+    MOE_PATH_TC = 2        /* tcgen05 grouped GEMMs (bf16, H, F, Fs multiples of 64);
+                              UNSUPPORTED otherwise */
+} moe_path;
+moe_status moe_set_path(moe_layer *layer, int32_t path);
+
+/* Per-kernel timing (tracing).  While enabled, each forward records a CUDA
+ * event before and after every kernel it launches, on the forward's stream
+ * (events created here, once; nothing is allocated per forward).  Up to
+ * `max_forwards` forwards are recorded between two moe_timing_read calls; later
+ * ones are not recorded.  max_forwards = 0 disables timing and frees the
+ * events.  Errors: INVALID_ARG (max_forwards < 0 or > 4096), CUDA. */
+moe_status moe_timing_enable(moe_layer *layer, int32_t max_forwards);
+
+/* Kernel kinds reported by moe_timing_read, in this order. */
+typedef enum {
+    MOE_KERNEL_ROUTER = 0,   /* router logits */
+    MOE_KERNEL_SELECT = 1,   /* softmax / top-k / weights */
+    MOE_KERNEL_GROUP = 2,    /* grouping by expert */
+    MOE_KERNEL_UP = 3,       /* gate/up projection + activation */
+    MOE_KERNEL_DOWN = 4,     /* down projection + routing weight */
+    MOE_KERNEL_COMBINE = 5,  /* fixed-order combine */
+    MOE_KERNEL_GATHER = 6,   /* token-row gather (tensor-core path) */
+    MOE_KERNEL_COUNT = 7
+} moe_kernel_kind;
+
+/* Synchronises the device, then writes, per kernel kind, the summed device
+ * time in milliseconds (total_ms[MOE_KERNEL_COUNT]) and the number of
+ * launches (launches[MOE_KERNEL_COUNT]) of the forwards recorded since the
+ * last read, and starts a new recording window.  Errors: INVALID_ARG (timing
+ * not enabled, NULL pointer), CUDA. */
+moe_status moe_timing_read(moe_layer *layer, float *total_ms, int32_t *launches);
+
+/* Synchronises the device and reports a device-side error recorded by the
+ * layer's kernels (MOE_ERR_DEVICE_TIMEOUT), then clears it.  MOE_OK if none. */
+moe_status moe_get_status(moe_layer *layer);
+
+/* Number of kernel launches the last forward issued. */
+int32_t moe_last_launch_count(const moe_layer *layer);
+
+/* Device bytes owned by the layer (weights + workspace). */
+size_t moe_device_bytes(const moe_layer *layer);
+
+/* Frees everything the layer owns.  Synchronises the device first.  NULL is
+ * a no-op. */
+void moe_destroy(moe_layer *layer);
+
+/* Description of the last error on this thread ("" if none). */
+const char *moe_last_error(void);
+
+/* MOE_ABI_VERSION of the loaded library. */
+int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

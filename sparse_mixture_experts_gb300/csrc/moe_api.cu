@@ -1,0 +1,484 @@
+// moe_api.cu -- the C ABI of libmoe (declared in include/moe.h).
+//
+// create : validate the config, copy / repack the weights into library-owned
+//          device memory ([out][in] layouts; the gpt-oss interleaved gate_up
+//          tensor is split into gate and up tensors, even rows -> gate, odd
+//          rows -> up, as "Phase 19: MoE -- gpt-oss-20b", section 2 Experts,
+//          defines them; biases are widened to fp32), allocate the workspace.
+// forward: router -> select -> group -> experts (weight-streaming or tensor
+//          cores) -> combine, all on the caller's stream, nothing allocated.
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct moe_layer : public Layer {};
+
+namespace {
+
+thread_local std::string g_error;
+
+moe_status fail(moe_status st, const std::string &msg)
+{
+    g_error = msg;
+    return st;
+}
+
+moe_status cuda_fail(cudaError_t e, const char *what)
+{
+    g_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA;
+}
+
+#define CUDA_TRY(call)                                     \
+    do {                                                   \
+        cudaError_t e_ = (call);                           \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+    } while (0)
+
+moe_status dev_alloc(Layer &L, void **p, size_t bytes)
+{
+    *p = nullptr;
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        return cuda_fail(e, "cudaMalloc");
+    }
+    L.allocations.push_back(*p);
+    L.device_bytes += bytes;
+    return MOE_OK;
+}
+
+template <typename T>
+moe_status dev_alloc_t(Layer &L, T **p, size_t count)
+{
+    return dev_alloc(L, reinterpret_cast<void **>(p), count * sizeof(T));
+}
+
+void timing_free(Layer &L)
+{
+    for (cudaEvent_t e : L.timing_events) cudaEventDestroy(e);
+    L.timing_events.clear();
+    L.timing_kind.clear();
+    L.timing_max = L.timing_recorded = L.timing_pairs = 0;
+}
+
+void free_all(Layer &L)
+{
+    timing_free(L);
+    if (L.tmaps) tc_release(L);
+    for (void *p : L.allocations) cudaFree(p);
+    L.allocations.clear();
+}
+
+// ---- repacking kernels ------------------------------------------------------
+__global__ void widen_kernel(const void *src, int dtype, size_t n, float *dst)
+{
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        if (dtype == MOE_DT_BF16) dst[i] = __bfloat162float(((const __nv_bfloat16 *)src)[i]);
+        else dst[i] = ((const float *)src)[i];
+    }
+}
+
+// src [E][2F][H] interleaved (gate = even rows) -> gate [E][F][H], up [E][F][H]
+__global__ void deinterleave_rows_kernel(const uint4 *src, size_t rows_2f, size_t row_vecs, uint4 *gate, uint4 *up)
+{
+    const size_t n = rows_2f * row_vecs;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / row_vecs, c = i - r * row_vecs;
+        const size_t dst = (r >> 1) * row_vecs + c;
+        if (r & 1) up[dst] = src[i];
+        else gate[dst] = src[i];
+    }
+}
+
+// bias [E][2F] (interleaved or [gate F | up F]) -> fp32 gate_b [E][F], up_b [E][F]
+__global__ void split_bias_kernel(const void *src, int dtype, int E, int F, int interleaved, float *gb, float *ub)
+{
+    const size_t n = (size_t)E * 2 * F;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const float v = dtype == MOE_DT_BF16 ? __bfloat162float(((const __nv_bfloat16 *)src)[i]) : ((const float *)src)[i];
+        const size_t e = i / (2 * F), r = i - e * 2 * F;
+        size_t f;
+        bool is_up;
+        if (interleaved) { f = r >> 1; is_up = r & 1; }
+        else { f = r % F; is_up = r >= (size_t)F; }
+        (is_up ? ub : gb)[e * F + f] = v;
+    }
+}
+
+moe_status upload(void *dst, const void *src, size_t bytes, const char *name)
+{
+    if (!src) return fail(MOE_ERR_INVALID_ARG, std::string("missing weight: ") + name);
+    cudaError_t e = cudaMemcpy(dst, src, bytes, cudaMemcpyDefault);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return MOE_OK;
+}
+
+moe_status upload_f32(Layer &L, float **dst, const void *src, size_t n, const char *name)
+{
+    if (!src) return fail(MOE_ERR_INVALID_ARG, std::string("missing bias: ") + name);
+    moe_status st = dev_alloc_t(L, dst, n);
+    if (st) return st;
+    void *tmp = nullptr;
+    CUDA_TRY(cudaMalloc(&tmp, n * L.wbytes));
+    cudaError_t e = cudaMemcpy(tmp, src, n * L.wbytes, cudaMemcpyDefault);
+    if (e == cudaSuccess) {
+        widen_kernel<<<256, 256>>>(tmp, L.cfg.w_dtype, n, *dst);
+        e = cudaDeviceSynchronize();
+    }
+    cudaFree(tmp);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return MOE_OK;
+}
+
+moe_status validate(const moe_config &c)
+{
+    if (c.hidden <= 0 || c.n_expert <= 0 || c.top_k <= 0 || c.expert_ff <= 0 || c.shared_ff < 0 || c.max_tokens < 0)
+        return fail(MOE_ERR_INVALID_ARG, "sizes must be positive (shared_ff, max_tokens >= 0)");
+    if (c.top_k > c.n_expert) return fail(MOE_ERR_INVALID_ARG, "top_k > n_expert");
+    if (c.top_k > 32) return fail(MOE_ERR_UNSUPPORTED, "top_k > 32");
+    if (c.n_expert > 1024) return fail(MOE_ERR_UNSUPPORTED, "n_expert > 1024");
+    if (c.router_mode != MOE_ROUTER_SOFTMAX_TOPK && c.router_mode != MOE_ROUTER_TOPK_SOFTMAX)
+        return fail(MOE_ERR_INVALID_ARG, "unknown router_mode");
+    if (c.act != MOE_ACT_SWIGLU && c.act != MOE_ACT_CLAMP_GLU) return fail(MOE_ERR_INVALID_ARG, "unknown act");
+    for (int d : {c.w_dtype, c.act_dtype, c.out_dtype})
+        if (d != MOE_DT_F32 && d != MOE_DT_BF16) return fail(MOE_ERR_INVALID_ARG, "unknown dtype");
+    if (c.act_dtype != c.w_dtype) return fail(MOE_ERR_UNSUPPORTED, "act_dtype must equal w_dtype");
+    if (c.hidden % 8 || c.expert_ff % 8 || c.shared_ff % 8)
+        return fail(MOE_ERR_UNSUPPORTED, "hidden, expert_ff and shared_ff must be multiples of 8");
+    if ((long long)c.max_tokens * c.top_k > (1LL << 30)) return fail(MOE_ERR_UNSUPPORTED, "max_tokens too large");
+    return MOE_OK;
+}
+
+moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
+{
+    moe_status st = validate(*cfg);
+    if (st) return st;
+    const moe_config &c = *cfg;
+    L.cfg = c;
+    CUDA_TRY(cudaGetDevice(&L.device));
+    CUDA_TRY(cudaDeviceGetAttribute(&L.num_sms, cudaDevAttrMultiProcessorCount, L.device));
+    L.E = c.n_expert; L.H = c.hidden; L.F = c.expert_ff; L.Fs = c.shared_ff; L.K = c.top_k;
+    L.R = L.E + (L.Fs > 0 ? 1 : 0);
+    L.Fmax = L.F > L.Fs ? L.F : L.Fs;
+    L.Tmax = c.max_tokens > 0 ? c.max_tokens : 1;
+    L.wbytes = c.w_dtype == MOE_DT_BF16 ? 2 : 4;
+    const size_t E = L.E, H = L.H, F = L.F, Fs = L.Fs, K = L.K, T = L.Tmax, eb = L.wbytes;
+
+    if (!w->router_w || !w->down_w) return fail(MOE_ERR_INVALID_ARG, "missing router_w or down_w");
+    if (c.gate_up_interleaved ? !w->gate_up_w : (!w->gate_w || !w->up_w))
+        return fail(MOE_ERR_INVALID_ARG, "missing gate/up weights");
+    if (c.has_bias && (!w->router_b || !w->gate_up_b || !w->down_b))
+        return fail(MOE_ERR_INVALID_ARG, "has_bias set but a bias is missing");
+    if (Fs && (!w->sh_gate_w || !w->sh_up_w || !w->sh_down_w || !w->sh_gate_inp))
+        return fail(MOE_ERR_INVALID_ARG, "shared_ff > 0 but a shared-expert weight is missing");
+
+    // ---- weights ----
+    if ((st = dev_alloc(L, &L.router_w, (size_t)L.R * H * eb))) return st;
+    if ((st = upload(L.router_w, w->router_w, E * H * eb, "router_w"))) return st;
+    if (Fs && (st = upload((char *)L.router_w + E * H * eb, w->sh_gate_inp, H * eb, "sh_gate_inp"))) return st;
+    if ((st = dev_alloc(L, &L.gate_w, E * F * H * eb))) return st;
+    if ((st = dev_alloc(L, &L.up_w, E * F * H * eb))) return st;
+    if (c.gate_up_interleaved) {
+        void *tmp = nullptr;
+        CUDA_TRY(cudaMalloc(&tmp, E * 2 * F * H * eb));
+        cudaError_t e = cudaMemcpy(tmp, w->gate_up_w, E * 2 * F * H * eb, cudaMemcpyDefault);
+        if (e == cudaSuccess) {
+            deinterleave_rows_kernel<<<4 * L.num_sms, 256>>>((const uint4 *)tmp, E * 2 * F, H * eb / 16,
+                                                             (uint4 *)L.gate_w, (uint4 *)L.up_w);
+            e = cudaDeviceSynchronize();
+        }
+        cudaFree(tmp);
+        if (e != cudaSuccess) return cuda_fail(e, "gate_up_w");
+    } else {
+        if ((st = upload(L.gate_w, w->gate_w, E * F * H * eb, "gate_w"))) return st;
+        if ((st = upload(L.up_w, w->up_w, E * F * H * eb, "up_w"))) return st;
+    }
+    if ((st = dev_alloc(L, &L.down_w, E * H * F * eb))) return st;
+    if ((st = upload(L.down_w, w->down_w, E * H * F * eb, "down_w"))) return st;
+    if (c.has_bias) {
+        if ((st = upload_f32(L, &L.router_b, w->router_b, E, "router_b"))) return st;
+        if ((st = upload_f32(L, &L.down_b, w->down_b, E * H, "down_b"))) return st;
+        if ((st = dev_alloc_t(L, &L.gate_b, E * F))) return st;
+        if ((st = dev_alloc_t(L, &L.up_b, E * F))) return st;
+        void *tmp = nullptr;
+        CUDA_TRY(cudaMalloc(&tmp, E * 2 * F * eb));
+        cudaError_t e = cudaMemcpy(tmp, w->gate_up_b, E * 2 * F * eb, cudaMemcpyDefault);
+        if (e == cudaSuccess) {
+            split_bias_kernel<<<256, 256>>>(tmp, c.w_dtype, L.E, L.F, c.gate_up_interleaved, L.gate_b, L.up_b);
+            e = cudaDeviceSynchronize();
+        }
+        cudaFree(tmp);
+        if (e != cudaSuccess) return cuda_fail(e, "gate_up_b");
+    }
+    if (Fs) {
+        if ((st = dev_alloc(L, &L.sh_gate_w, Fs * H * eb))) return st;
+        if ((st = dev_alloc(L, &L.sh_up_w, Fs * H * eb))) return st;
+        if ((st = dev_alloc(L, &L.sh_down_w, H * Fs * eb))) return st;
+        if ((st = upload(L.sh_gate_w, w->sh_gate_w, Fs * H * eb, "sh_gate_w"))) return st;
+        if ((st = upload(L.sh_up_w, w->sh_up_w, Fs * H * eb, "sh_up_w"))) return st;
+        if ((st = upload(L.sh_down_w, w->sh_down_w, H * Fs * eb, "sh_down_w"))) return st;
+    }
+
+    // ---- workspace ----
+    if ((st = dev_alloc_t(L, &L.logits, T * L.R))) return st;
+    if ((st = dev_alloc_t(L, &L.topk_idx, T * K))) return st;
+    if ((st = dev_alloc_t(L, &L.topk_w, T * K))) return st;
+    if ((st = dev_alloc_t(L, &L.sh_gate, T))) return st;
+    if ((st = dev_alloc_t(L, &L.counts, E))) return st;
+    if ((st = dev_alloc_t(L, &L.offsets, E + 1))) return st;
+    if ((st = dev_alloc_t(L, &L.expert_rows, E * T))) return st;
+    if ((st = dev_alloc_t(L, &L.active, E))) return st;
+    if ((st = dev_alloc_t(L, &L.meta, 1))) return st;
+    if ((st = dev_alloc(L, &L.h, (T * K + T) * (size_t)L.Fmax * eb))) return st;
+    if ((st = dev_alloc_t(L, &L.ys, T * (K + 1) * H))) return st;
+    if ((st = dev_alloc_t(L, &L.status, 1))) return st;
+    if ((st = dev_alloc(L, &L.x_stage, T * H * eb))) return st;
+    if ((st = dev_alloc(L, &L.out_stage, T * H * (c.out_dtype == MOE_DT_BF16 ? 2 : 4)))) return st;
+    CUDA_TRY(cudaMemset(L.meta, 0, sizeof(RouteMeta)));
+    CUDA_TRY(cudaMemset(L.status, 0, sizeof(int)));
+    CUDA_TRY(cudaMemset(L.counts, 0, E * sizeof(int)));
+
+    std::string why;
+    L.tc_capable = tc_supported(L, why);
+    if (L.tc_capable) {
+        tc_tile_caps(L, L.max_up_tiles, L.max_down_tiles);
+        if ((st = dev_alloc(L, &L.xp, T * K * H * eb))) return st;
+        if ((st = dev_alloc_t(L, &L.up_tiles, (size_t)L.max_up_tiles))) return st;
+        if ((st = dev_alloc_t(L, &L.down_tiles, (size_t)L.max_down_tiles))) return st;
+        if (tc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "tensor map creation failed");
+    }
+    CUDA_TRY(cudaDeviceSynchronize());
+    return MOE_OK;
+}
+
+bool use_tc(const Layer &L, int T)
+{
+    if (!L.tc_capable) return false;
+    if (L.path == MOE_PATH_TC) return true;
+    if (L.path == MOE_PATH_STREAM) return false;
+    // expected rows per routed expert; the streaming kernels win while each
+    // expert sees only a few tokens
+    return (long long)T * L.K >= 16LL * L.E;
+}
+
+moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t s)
+{
+    if (T < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens < 0");
+    if (T > L.cfg.max_tokens) return fail(MOE_ERR_TOO_MANY_TOKENS, "n_tokens > max_tokens");
+    if (T == 0) {
+        L.last_T = 0;
+        L.last_launches = 0;
+        return MOE_OK;
+    }
+    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x and out must be non-NULL");
+    if (((uintptr_t)x & 15) || ((uintptr_t)out & 15)) return fail(MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+    const size_t xb = (size_t)T * L.H * L.wbytes;
+    const size_t ob = (size_t)T * L.H * (L.cfg.out_dtype == MOE_DT_BF16 ? 2 : 4);
+    const char *xs = (const char *)x, *os = (const char *)out;
+    if (xs < os + ob && os < xs + xb) return fail(MOE_ERR_INVALID_ARG, "x and out overlap");
+    const bool tc = use_tc(L, T);
+    const bool rec = L.timing_max > 0 && L.timing_recorded < L.timing_max;
+    int n = 0;
+    auto run = [&](int kind, auto &&launch) {
+        if (rec) {
+            cudaEventRecord(L.timing_events[2 * L.timing_pairs], s);
+            L.timing_kind[L.timing_pairs] = kind;
+        }
+        n += launch();
+        if (rec) cudaEventRecord(L.timing_events[2 * L.timing_pairs + 1], s), ++L.timing_pairs;
+    };
+    run(MOE_KERNEL_ROUTER, [&] { return launch_router(L, x, T, s); });
+    run(MOE_KERNEL_SELECT, [&] { return launch_select(L, T, s); });
+    run(MOE_KERNEL_GROUP, [&] { return launch_group(L, T, tc, s); });
+    if (tc) {
+        run(MOE_KERNEL_GATHER, [&] { return launch_experts_tc(L, x, T, 0, s); });
+        run(MOE_KERNEL_UP, [&] { return launch_experts_tc(L, x, T, 1, s); });
+        run(MOE_KERNEL_DOWN, [&] { return launch_experts_tc(L, x, T, 2, s); });
+    } else {
+        run(MOE_KERNEL_UP, [&] { return launch_experts_stream(L, x, T, 0, s); });
+        run(MOE_KERNEL_DOWN, [&] { return launch_experts_stream(L, x, T, 1, s); });
+    }
+    run(MOE_KERNEL_COMBINE, [&] { return launch_combine(L, T, out, s); });
+    if (rec) ++L.timing_recorded;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    L.last_T = T;
+    L.last_launches = n;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_layer_create(const moe_config *config, const moe_weights *weights, moe_layer **out)
+{
+    g_error.clear();
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!config || !weights) return fail(MOE_ERR_INVALID_ARG, "config and weights must be non-NULL");
+    moe_layer *L = new (std::nothrow) moe_layer();
+    if (!L) return fail(MOE_ERR_OOM, "host allocation failed");
+    moe_status st = create_impl(config, weights, *L);
+    if (st != MOE_OK) {
+        cudaDeviceSynchronize();
+        free_all(*L);
+        delete L;
+        return st;
+    }
+    *out = L;
+    return MOE_OK;
+}
+
+moe_status moe_forward(moe_layer *layer, const void *x, int32_t n_tokens, void *out, void *stream)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    return forward_impl(*layer, x, n_tokens, out, (cudaStream_t)stream);
+}
+
+moe_status moe_forward_host(moe_layer *layer, const void *x_host, int32_t n_tokens, void *out_host, void *stream)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    Layer &L = *layer;
+    if (n_tokens < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens < 0");
+    if (n_tokens > L.cfg.max_tokens) return fail(MOE_ERR_TOO_MANY_TOKENS, "n_tokens > max_tokens");
+    if (n_tokens == 0) return forward_impl(L, nullptr, 0, nullptr, (cudaStream_t)stream);
+    if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x and out must be non-NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t xb = (size_t)n_tokens * L.H * L.wbytes;
+    const size_t ob = (size_t)n_tokens * L.H * (L.cfg.out_dtype == MOE_DT_BF16 ? 2 : 4);
+    CUDA_TRY(cudaMemcpyAsync(L.x_stage, x_host, xb, cudaMemcpyHostToDevice, s));
+    moe_status st = forward_impl(L, L.x_stage, n_tokens, L.out_stage, s);
+    if (st) return st;
+    CUDA_TRY(cudaMemcpyAsync(out_host, L.out_stage, ob, cudaMemcpyDeviceToHost, s));
+    return MOE_OK;
+}
+
+moe_status moe_get_routing(moe_layer *layer, int32_t *idx, float *w, void *stream)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    const Layer &L = *layer;
+    const size_t n = (size_t)L.last_T * L.K;
+    if (n == 0) return MOE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (idx) CUDA_TRY(cudaMemcpyAsync(idx, L.topk_idx, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+    if (w) CUDA_TRY(cudaMemcpyAsync(w, L.topk_w, n * sizeof(float), cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+moe_status moe_get_logits(moe_layer *layer, float *logits, float *sh_logit, void *stream)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    const Layer &L = *layer;
+    if (L.last_T == 0) return MOE_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (logits)
+        CUDA_TRY(cudaMemcpy2DAsync(logits, L.E * sizeof(float), L.logits, L.R * sizeof(float), L.E * sizeof(float),
+                                   L.last_T, cudaMemcpyDeviceToDevice, s));
+    if (sh_logit && L.Fs > 0)
+        CUDA_TRY(cudaMemcpy2DAsync(sh_logit, sizeof(float), L.logits + L.E, L.R * sizeof(float), sizeof(float),
+                                   L.last_T, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+moe_status moe_get_expert_counts(moe_layer *layer, int32_t *counts, void *stream)
+{
+    if (!layer || !counts) return fail(MOE_ERR_INVALID_ARG, "layer and counts must be non-NULL");
+    const Layer &L = *layer;
+    CUDA_TRY(cudaMemcpyAsync(counts, L.counts, L.E * sizeof(int32_t), cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_set_path(moe_layer *layer, int32_t path)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (path != MOE_PATH_AUTO && path != MOE_PATH_STREAM && path != MOE_PATH_TC)
+        return fail(MOE_ERR_INVALID_ARG, "unknown path");
+    if (path == MOE_PATH_TC && !layer->tc_capable) {
+        std::string why;
+        tc_supported(*layer, why);
+        return fail(MOE_ERR_UNSUPPORTED, "tensor-core path unavailable: " + why);
+    }
+    layer->path = path;
+    return MOE_OK;
+}
+
+moe_status moe_timing_enable(moe_layer *layer, int32_t max_forwards)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (max_forwards < 0 || max_forwards > 4096) return fail(MOE_ERR_INVALID_ARG, "max_forwards out of range");
+    Layer &L = *layer;
+    CUDA_TRY(cudaDeviceSynchronize());
+    timing_free(L);
+    if (max_forwards == 0) return MOE_OK;
+    const size_t pairs = (size_t)max_forwards * MAX_LAUNCHES_PER_FORWARD;
+    L.timing_events.resize(2 * pairs);
+    for (size_t i = 0; i < 2 * pairs; ++i) {
+        cudaError_t e = cudaEventCreate(&L.timing_events[i]);
+        if (e != cudaSuccess) {
+            L.timing_events.resize(i);
+            timing_free(L);
+            return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    L.timing_kind.assign(pairs, 0);
+    L.timing_max = max_forwards;
+    return MOE_OK;
+}
+
+moe_status moe_timing_read(moe_layer *layer, float *total_ms, int32_t *launches)
+{
+    if (!layer || !total_ms || !launches) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    Layer &L = *layer;
+    if (L.timing_max == 0) return fail(MOE_ERR_INVALID_ARG, "timing is not enabled");
+    CUDA_TRY(cudaDeviceSynchronize());
+    for (int k = 0; k < MOE_KERNEL_COUNT; ++k) { total_ms[k] = 0.0f; launches[k] = 0; }
+    for (int p = 0; p < L.timing_pairs; ++p) {
+        float ms = 0.0f;
+        CUDA_TRY(cudaEventElapsedTime(&ms, L.timing_events[2 * p], L.timing_events[2 * p + 1]));
+        total_ms[L.timing_kind[p]] += ms;
+        launches[L.timing_kind[p]] += 1;
+    }
+    L.timing_pairs = 0;
+    L.timing_recorded = 0;
+    return MOE_OK;
+}
+
+moe_status moe_get_status(moe_layer *layer)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    CUDA_TRY(cudaDeviceSynchronize());
+    int code = 0;
+    CUDA_TRY(cudaMemcpy(&code, layer->status, sizeof(int), cudaMemcpyDeviceToHost));
+    if (code != 0) {
+        CUDA_TRY(cudaMemset(layer->status, 0, sizeof(int)));
+        char buf[96];
+        snprintf(buf, sizeof buf, "device-side error %d recorded by a kernel", code);
+        return fail(code == DEV_BAD_TILE ? MOE_ERR_CUDA : MOE_ERR_DEVICE_TIMEOUT, buf);
+    }
+    return MOE_OK;
+}
+
+int32_t moe_last_launch_count(const moe_layer *layer) { return layer ? layer->last_launches : 0; }
+
+size_t moe_device_bytes(const moe_layer *layer) { return layer ? layer->device_bytes : 0; }
+
+void moe_destroy(moe_layer *layer)
+{
+    if (!layer) return;
+    cudaDeviceSynchronize();
+    free_all(*layer);
+    delete layer;
+}
+
+const char *moe_last_error(void) { return g_error.c_str(); }
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,199 @@
+// moe_internal.cuh -- layer object, device helpers and kernel entry points
+// shared by the translation units of libmoe.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// device status word: kernels record the first error they hit here
+// ---------------------------------------------------------------------------
+enum DeviceError : int {
+    DEV_OK = 0,
+    DEV_TIMEOUT_FULL_BARRIER = 1,   // producer->MMA smem stage never filled
+    DEV_TIMEOUT_EMPTY_BARRIER = 2,  // MMA->producer smem stage never drained
+    DEV_TIMEOUT_ACCUM_BARRIER = 3,  // MMA->epilogue accumulator never ready
+    DEV_TIMEOUT_ACCUM_FREE = 4,     // epilogue->MMA accumulator never released
+    DEV_BAD_TILE = 5,               // a tile descriptor outside the problem
+};
+
+// Groups of rows a grouped kernel walks over: the routed experts that
+// received at least one token (ascending expert index), then the shared
+// expert (all tokens) when the layer has one.
+struct RouteMeta {
+    int ticket;       // arrival counter of the grouping kernel (reset by its last block)
+    int n_active;     // routed experts with count > 0
+    int n_up_tiles;   // tensor-core tiles of the gate/up GEMM
+    int n_down_tiles; // tensor-core tiles of the down GEMM
+    int n_pairs;      // T * k
+    int pad[3];
+};
+
+// Tensor-core tile descriptor: group g (expert index, or E for the shared
+// expert), first row m0 within the group, first output column n0.
+struct TileDesc {
+    int g;
+    int m0;
+    int n0;
+    int pad;
+};
+
+struct TensorMaps;  // defined in expert_tc.cu
+
+struct Layer {
+    moe_config cfg{};
+    int device = 0;
+    int num_sms = 0;
+    int path = MOE_PATH_AUTO;
+    bool tc_capable = false;
+    int E = 0, H = 0, F = 0, Fs = 0, K = 0, R = 0;  // R = router rows (E, +1 for the shared gate)
+    int Fmax = 0;
+    int Tmax = 0;
+    size_t wbytes = 0;  // element size of weights / activations
+
+    // weights, library-owned, [out][in]
+    void *router_w = nullptr;  // [R][H]; row E = shared gate vector when Fs > 0
+    float *router_b = nullptr; // [E]
+    void *gate_w = nullptr;    // [E][F][H]
+    void *up_w = nullptr;      // [E][F][H]
+    float *gate_b = nullptr;   // [E][F]
+    float *up_b = nullptr;     // [E][F]
+    void *down_w = nullptr;    // [E][H][F]
+    float *down_b = nullptr;   // [E][H]
+    void *sh_gate_w = nullptr; // [Fs][H]
+    void *sh_up_w = nullptr;   // [Fs][H]
+    void *sh_down_w = nullptr; // [H][Fs]
+
+    // workspace, sized for Tmax tokens
+    float *logits = nullptr;   // [Tmax][R]
+    int *topk_idx = nullptr;   // [Tmax][K]
+    float *topk_w = nullptr;   // [Tmax][K]
+    float *sh_gate = nullptr;  // [Tmax]
+    int *counts = nullptr;     // [E]
+    int *offsets = nullptr;    // [E + 1]
+    int *expert_rows = nullptr;// [E][Tmax] pair ids t*K+slot, ascending t
+    int *active = nullptr;     // [E]
+    RouteMeta *meta = nullptr;
+    void *h = nullptr;         // [Tmax*K + Tmax][Fmax] activations (routed rows sorted by expert, then shared)
+    void *xp = nullptr;        // [Tmax*K][H] x rows gathered in expert order (tensor-core path)
+    float *ys = nullptr;       // [Tmax][K+1][H] weighted expert outputs per (token, slot)
+    TileDesc *up_tiles = nullptr;
+    TileDesc *down_tiles = nullptr;
+    int max_up_tiles = 0, max_down_tiles = 0;
+    int *status = nullptr;     // DeviceError
+    void *x_stage = nullptr;   // [Tmax][H] for moe_forward_host
+    void *out_stage = nullptr; // [Tmax][H]
+    TensorMaps *tmaps = nullptr;  // host copy of the tensor maps (tensor-core path)
+
+    // per-kernel timing (moe_timing_enable / moe_timing_read)
+    int timing_max = 0;         // forwards recorded per window; 0 = off
+    int timing_recorded = 0;    // forwards recorded in the current window
+    int timing_pairs = 0;       // event pairs used in the current window
+    std::vector<cudaEvent_t> timing_events;  // 2 per pair
+    std::vector<int> timing_kind;            // moe_kernel_kind per pair
+
+    std::vector<void *> allocations;
+    size_t device_bytes = 0;
+    int last_T = 0;
+    int last_launches = 0;
+};
+
+// ---------------------------------------------------------------------------
+// small device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
+// routed-expert activation; ACT = moe_act
+template <int ACT>
+__device__ __forceinline__ float activation(float gate, float up, float alpha, float limit)
+{
+    if (ACT == MOE_ACT_SWIGLU) {
+        return gate * sigmoidf_(gate) * up;
+    } else {
+        float g = fminf(gate, limit);
+        float u = fminf(fmaxf(up, -limit), limit);
+        return (u + 1.0f) * g * sigmoidf_(alpha * g);
+    }
+}
+
+template <typename T> struct Vec;  // 16-byte vector of T
+template <> struct Vec<float> {
+    static constexpr int N = 4;
+    float v[4];
+    __device__ __forceinline__ void load(const float *p) {
+        float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    }
+    __device__ __forceinline__ void load_stream(const float *p) {
+        float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    }
+};
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    float v[8];
+    __device__ __forceinline__ void unpack(uint4 a) {
+        v[0] = bf16_lo(a.x); v[1] = bf16_hi(a.x); v[2] = bf16_lo(a.y); v[3] = bf16_hi(a.y);
+        v[4] = bf16_lo(a.z); v[5] = bf16_hi(a.z); v[6] = bf16_lo(a.w); v[7] = bf16_hi(a.w);
+    }
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+        unpack(__ldg(reinterpret_cast<const uint4 *>(p)));
+    }
+    __device__ __forceinline__ void load_stream(const __nv_bfloat16 *p) {
+        unpack(__ldcs(reinterpret_cast<const uint4 *>(p)));
+    }
+};
+
+__device__ __forceinline__ void store_out(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ void record_error(int *status, int code)
+{
+    atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// host-side launchers (each returns the number of kernels it launched, or -1)
+// ---------------------------------------------------------------------------
+int launch_router(const Layer &L, const void *x, int T, cudaStream_t s);
+int launch_select(const Layer &L, int T, cudaStream_t s);
+int launch_group(const Layer &L, int T, bool build_tiles, cudaStream_t s);
+// which: 0 = gate/up + activation, 1 = down + routing weight
+int launch_experts_stream(const Layer &L, const void *x, int T, int which, cudaStream_t s);
+int launch_combine(const Layer &L, int T, void *out, cudaStream_t s);
+
+// tensor-core path (expert_tc.cu)
+bool tc_supported(const Layer &L, std::string &why);
+int tc_prepare(Layer &L);  // tensor maps over the layer's weights/workspace; 0 on success
+void tc_release(Layer &L);
+// which: 0 = gather token rows, 1 = gate/up GEMM + activation, 2 = down GEMM + weight
+int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStream_t s);
+void tc_tile_caps(const Layer &L, int &max_up, int &max_down);
+
+constexpr int MAX_LAUNCHES_PER_FORWARD = 8;
+
+// tile geometry of the tensor-core path (used by the grouping kernel)
+constexpr int TC_BM = 128;       // token rows per tile
+constexpr int TC_BN_UP = 128;    // gate/up tile: 64 gate + 64 up columns -> 64 h columns
+constexpr int TC_BN_DOWN = 128;  // down tile: output columns
+constexpr int TC_BK = 64;        // K elements per pipeline stage (128 bytes of bf16)
+
+}  // namespace moe

@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every symbol include/moe.h
+declares; host-side validation rejects bad configs before touching the GPU.
+No compute call is made here (this runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_mixture_experts_gb300 import build
+    build.build()
+    import sparse_mixture_experts_gb300 as moe
+    return moe.load_library()
+
+
+def _declared_symbols():
+    names = set()
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_symbols()
+    for required in ("moe_layer_create", "moe_forward", "moe_destroy", "moe_get_routing", "moe_get_status",
+                     "moe_last_error", "moe_forward_host"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_abi_version(lib):
+    assert lib.moe_abi_version() == 1
+
+
+def test_config_struct_layout_matches_header():
+    import sparse_mixture_experts_gb300 as moe
+    # 17 four-byte fields, no padding
+    assert ctypes.sizeof(moe._Config) == 17 * 4
+    assert ctypes.sizeof(moe._Weights) == 12 * ctypes.sizeof(ctypes.c_void_p)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(top_k=9),                 # top_k > n_expert
+    dict(top_k=0),
+    dict(hidden=0),
+    dict(hidden=60),               # not a multiple of 8
+    dict(router_mode=7),
+    dict(act=5),
+    dict(w_dtype=3),
+    dict(act_dtype=1, w_dtype=0),  # mixed activation / weight dtype
+    dict(max_tokens=-1),
+])
+def test_create_rejects_bad_configs_on_the_host(lib, bad):
+    import sparse_mixture_experts_gb300 as moe
+    kw = dict(hidden=64, n_expert=8, top_k=2, expert_ff=32, w_dtype=moe.DT_F32, act_dtype=moe.DT_F32,
+              max_tokens=16)
+    kw.update(bad)
+    cfg = moe.MoEConfig(**kw)._c()
+    w = moe._Weights()
+    h = ctypes.c_void_p()
+    rc = lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h))
+    assert rc in (moe.ERR_INVALID_ARG, moe.ERR_UNSUPPORTED)
+    assert h.value is None
+    assert lib.moe_last_error()
+
+
+def test_null_arguments_are_rejected(lib):
+    import sparse_mixture_experts_gb300 as moe
+    assert lib.moe_layer_create(None, None, None) == moe.ERR_INVALID_ARG
+    assert lib.moe_forward(None, None, 1, None, None) == moe.ERR_INVALID_ARG
+    lib.moe_destroy(None)  # no-op
+
+
+def test_binding_does_not_import_the_oracle():
+    import subprocess
+    import sys
+    code = ("import sys, sparse_mixture_experts_gb300 as m; "
+            "bad=[k for k in sys.modules if k=='oracle' or k.startswith('oracle.')]; "
+            "print(bad); sys.exit(1 if bad else 0)")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
