@@ -1,23 +1,620 @@
-// expert_tc.cu -- tcgen05 grouped-GEMM path (placeholder until the kernels land)
+// expert_tc.cu -- grouped expert GEMMs on the 5th-generation tensor cores
+// (tcgen05 + TMEM, operands staged by TMA), for token counts where every
+// routed expert sees many rows (prefill).
+//
+// Per group g (a routed expert with n_g rows, or the shared expert with all T
+// rows), rows taken in the expert-sorted order the grouping kernel produced
+// ("Engine", Prefill: tokens grouped by expert, gathered, projected,
+// scattered back):
+//   gate/up GEMM : [gate | up] = Xp_g W^T over H, then h = act(gate, up)
+//                  ("Llama Forward Pass", SwiGLU FFN; "Phase 19: MoE --
+//                  gpt-oss-20b", section 2 Experts, with biases and clamps)
+//   down GEMM    : y = h_g W_down^T over F (+ b_down), written as
+//                  w_slot * y to the (token, slot) row of the combine buffer
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0    TMA producer: A (token rows) and B (weight rows) tiles of
+//             128 x 64 bf16, 128-byte swizzled, into an S-stage ring
+//   warp 1    TMEM allocator and MMA issuer (one elected thread):
+//             tcgen05.mma.cta_group::1.kind::f16, M=128, N=128, K=16,
+//             fp32 accumulators in TMEM, two accumulator buffers
+//   warps 2-5 epilogue: tcgen05.ld of the accumulators, activation or
+//             routing weight, stores
+// Every mbarrier wait is bounded (about a second of %globaltimer); on
+// timeout the kernel records an error in the status word, stops issuing
+// work, waits (bounded) for its own copies and MMAs in flight, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "moe_internal.cuh"
 
 namespace moe {
 
-struct TensorMaps {};
+constexpr int TC_STAGES = 6;
+constexpr int TC_THREADS = 192;
+constexpr int A_TILE_BYTES = TC_BM * TC_BK * 2;        // 16 KB
+constexpr int B_TILE_BYTES = 128 * TC_BK * 2;          // 16 KB (both GEMMs use N = 128)
+constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int TMEM_COLS = 256;                         // 2 accumulators x 128 fp32 columns
+constexpr size_t TC_SMEM = (size_t)TC_STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;  // one second
+
+struct TensorMaps {
+    CUtensorMap xp;       // A of gate/up: [Tmax*K + Tmax][H]
+    CUtensorMap h;        // A of down:    [Tmax*K + Tmax][Fmax]
+    CUtensorMap gate;     // [E*F][H], box 64 rows
+    CUtensorMap up;       // [E*F][H]
+    CUtensorMap down;     // [E*H][F], box 128 rows
+    CUtensorMap sh_gate;  // [Fs][H]
+    CUtensorMap sh_up;    // [Fs][H]
+    CUtensorMap sh_down;  // [H][Fs]
+};
+
+// A operand, then the B operand(s) of the routed experts and of the shared
+// expert; the gate/up GEMM loads two 64-row B boxes (gate rows, up rows), the
+// down GEMM one 128-row box (b1 / sb1 unused).
+struct TcMaps {
+    CUtensorMap a, b0, b1, sb0, sb1;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: true when the phase completed, false on timeout or when
+// another role of the CTA has aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmap_prefetch(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major operand, 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);   // start address
+    d |= (uint64_t)1 << 16;                     // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                     // descriptor version
+    d |= (uint64_t)2 << 61;                     // SWIZZLE_128B
+    return d;
+}
+
+// kind::f16 instruction descriptor: D f32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// the grouped GEMM kernel
+// ---------------------------------------------------------------------------
+enum { EPI_UP = 0, EPI_DOWN = 1 };
+
+struct TcArgs {
+    const TileDesc *tiles;
+    const RouteMeta *meta;
+    const int *counts, *offsets, *expert_rows;
+    const float *gate_b, *up_b, *down_b;
+    const float *topk_w, *sh_gate;
+    __nv_bfloat16 *h;   // EPI_UP output
+    float *ys;          // EPI_DOWN output
+    int *status;
+    int T, K, E, H, F, Fs, Fmax, Tmax;
+    int act;
+    float alpha, limit;
+};
+
+struct TileInfo {
+    int g, m0, n0;
+    int rows;     // rows of the group
+    int a_row0;   // first row of the group in the A tensor
+    int nk;       // K blocks
+    bool shared;
+};
+
+template <int EPI>
+__device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti)
+{
+    const TileDesc d = a.tiles[t];
+    ti.g = d.g;
+    ti.m0 = d.m0;
+    ti.n0 = d.n0;
+    ti.shared = d.g == a.E;
+    if (d.g < 0 || d.g > a.E || (ti.shared && a.Fs == 0)) return false;
+    ti.rows = ti.shared ? a.T : a.counts[d.g];
+    ti.a_row0 = ti.shared ? a.T * a.K : a.offsets[d.g];
+    if (EPI == EPI_UP) ti.nk = a.H / TC_BK;
+    else ti.nk = (ti.shared ? a.Fs : a.F) / TC_BK;
+    return ti.m0 >= 0 && ti.m0 < ti.rows && ti.n0 >= 0;
+}
+
+template <int EPI, typename Maps>
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ Maps maps, const TcArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + TC_STAGES * STAGE_BYTES);
+    uint64_t *empty = full + TC_STAGES;
+    uint64_t *acc_full = empty + TC_STAGES;   // [2]
+    uint64_t *acc_empty = acc_full + 2;       // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = EPI == EPI_UP ? a.meta->n_up_tiles : a.meta->n_down_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TC_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            tmap_prefetch(&maps.a);
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t last_phase[TC_STAGES];
+            bool used[TC_STAGES];
+            for (int s = 0; s < TC_STAGES; ++s) used[s] = false, last_phase[s] = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                TileInfo ti;
+                if (!tile_info<EPI>(a, t, ti)) {
+                    record_error(a.status, DEV_BAD_TILE);
+                    *abort_flag = 1;
+                    break;
+                }
+                for (int kb = 0; kb < ti.nk; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                        record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = smem + stage * STAGE_BYTES;
+                    uint8_t *sb = sa + A_TILE_BYTES;
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+                    const int kc = kb * TC_BK;
+                    tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
+                    if (EPI == EPI_UP) {
+                        const int brow = ti.shared ? ti.n0 : ti.g * a.F + ti.n0;
+                        tma_load_2d(sb, ti.shared ? &maps.sb0 : &maps.b0, &full[stage], kc, brow);
+                        tma_load_2d(sb + B_TILE_BYTES / 2, ti.shared ? &maps.sb1 : &maps.b1, &full[stage], kc, brow);
+                    } else {
+                        const int brow = ti.shared ? ti.n0 : ti.g * a.H + ti.n0;
+                        tma_load_2d(sb, ti.shared ? &maps.sb0 : &maps.b0, &full[stage], kc, brow);
+                    }
+                    used[stage] = true;
+                    last_phase[stage] = phase;
+                    if (++stage == TC_STAGES) stage = 0, phase ^= 1;
+                }
+            }
+            // drain: no copy of ours may still be landing when the CTA exits
+            volatile int never = 0;
+            for (int s = 0; s < TC_STAGES; ++s)
+                if (used[s]) mbar_wait(&full[s], last_phase[s], &never);
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, 128);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            int last_acc = -1;
+            uint32_t last_acc_phase = 0;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
+                TileInfo ti;
+                if (!tile_info<EPI>(a, t, ti)) break;
+                const int b = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!mbar_wait(&acc_empty[b], acc_phase ^ 1, abort_flag)) {
+                    record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(b * 128);
+                for (int kb = 0; kb < ti.nk; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                        record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_TILE_BYTES;
+#pragma unroll
+                    for (int k = 0; k < TC_BK / 16; ++k) {
+                        // advance 16 bf16 = 32 bytes along K inside the swizzled row
+                        mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
+                                 (kb | k) != 0);
+                    }
+                    mma_commit(&empty[stage]);
+                    if (++stage == TC_STAGES) stage = 0, phase ^= 1;
+                }
+                if (!ok) break;
+                mma_commit(&acc_full[b]);
+                last_acc = b;
+                last_acc_phase = acc_phase;
+            }
+            // on abort, let the MMAs already issued finish before TMEM is freed
+            if (*abort_flag && last_acc >= 0) {
+                volatile int never = 0;
+                mbar_wait(&acc_full[last_acc], last_acc_phase, &never);
+            }
+        }
+    } else {
+        // ------------------------------ epilogue (warps 2..5) ------------------------------
+        const int q = warp & 3;             // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;        // accumulator row (tile row) of this thread
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        int it = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+            TileInfo ti;
+            if (!tile_info<EPI>(a, t, ti)) break;
+            const int b = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            if (!mbar_wait(&acc_full[b], acc_phase, abort_flag)) {
+                record_error(a.status, DEV_TIMEOUT_ACCUM_BARRIER);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + lane_addr + (uint32_t)(b * 128);
+            const int j = ti.m0 + r;              // row within the group
+            const bool valid = j < ti.rows;
+            if (EPI == EPI_UP) {
+                const int fd = ti.shared ? a.Fs : a.F;
+                (void)fd;
+                const float *bg = (!ti.shared && a.gate_b) ? a.gate_b + (size_t)ti.g * a.F + ti.n0 : nullptr;
+                const float *bu = (!ti.shared && a.up_b) ? a.up_b + (size_t)ti.g * a.F + ti.n0 : nullptr;
+                __nv_bfloat16 *hrow = a.h + (size_t)(ti.a_row0 + j) * a.Fmax + ti.n0;
+#pragma unroll 1
+                for (int c = 0; c < 64; c += 16) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tbase + c, g);
+                    tmem_ld16(tbase + 64 + c, u);
+                    tmem_ld_wait();
+                    uint32_t packed[8];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        float v[2];
+#pragma unroll
+                        for (int z = 0; z < 2; ++z) {
+                            float gv = __uint_as_float(g[i + z]), uv = __uint_as_float(u[i + z]);
+                            if (bg) gv += bg[c + i + z];
+                            if (bu) uv += bu[c + i + z];
+                            v[z] = (ti.shared || a.act == MOE_ACT_SWIGLU)
+                                       ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
+                                       : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
+                        }
+                        __nv_bfloat162 p2 = __floats2bfloat162_rn(v[0], v[1]);
+                        packed[i / 2] = *reinterpret_cast<uint32_t *>(&p2);
+                    }
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(hrow + c);
+                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    }
+                }
+            } else {
+                int tok = 0, slot = 0;
+                float wgt = 0.0f;
+                if (valid) {
+                    if (ti.shared) { tok = j; slot = a.K; wgt = a.sh_gate[tok]; }
+                    else {
+                        const int p = a.expert_rows[(size_t)ti.g * a.Tmax + j];
+                        tok = p / a.K; slot = p - tok * a.K; wgt = a.topk_w[p];
+                    }
+                }
+                const float *bd = (!ti.shared && a.down_b) ? a.down_b + (size_t)ti.g * a.H + ti.n0 : nullptr;
+                float *yrow = a.ys + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n0;
+                const int ncols = min(128, a.H - ti.n0);
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tbase + c, v);
+                    tmem_ld_wait();
+                    if (valid && c < ncols) {
+                        float o[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float y = __uint_as_float(v[i]);
+                            if (bd && c + i < ncols) y += bd[c + i];
+                            o[i] = wgt * y;
+                        }
+                        float4 *dst = reinterpret_cast<float4 *>(yrow + c);
+                        // H is a multiple of 64, so a 16-column chunk is either fully in or fully out
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[b]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// gather: Xp[sorted row] = x[token]; routed rows then the shared rows (= x)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, int T, int K, int E,
+                                                          int H, int Tmax, int has_shared,
+                                                          const int *__restrict__ offsets,
+                                                          const int *__restrict__ expert_rows,
+                                                          __nv_bfloat16 *__restrict__ xp)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int P = T * K;
+    const int n_rows = P + (has_shared ? T : 0);
+    const int r = blockIdx.x * 8 + warp;
+    if (r >= n_rows) return;
+    int tok;
+    if (r < P) {
+        // expert of sorted row r: last e with offsets[e] <= r
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (offsets[mid] <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        tok = expert_rows[(size_t)lo * Tmax + (r - offsets[lo])] / K;
+    } else {
+        tok = r - P;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)tok * H);
+    uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * H);
+    for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor [rows][inner], row pitch = inner elements, box = 64 x box_rows, 128-byte swizzle
+static bool encode_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows)
+{
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {(cuuint32_t)TC_BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
 
 bool tc_supported(const Layer &L, std::string &why)
 {
-    (void)L;
-    why = "tensor-core kernels not built";
-    return false;
+    if (L.cfg.w_dtype != MOE_DT_BF16) { why = "tensor-core path needs bf16 weights"; return false; }
+    if (L.H % 64 || L.F % 64 || L.Fs % 64) { why = "tensor-core path needs H, F, Fs multiples of 64"; return false; }
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, L.device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, L.device);
+    if (major != 10 || minor != 3) { why = "tensor-core kernels are built for sm_103a"; return false; }
+    if (!get_encode()) { why = "cuTensorMapEncodeTiled unavailable"; return false; }
+    return true;
 }
-int tc_prepare(Layer &L) { (void)L; return -1; }
-void tc_release(Layer &L) { L.tmaps = nullptr; }
-void tc_tile_caps(const Layer &L, int &max_up, int &max_down) { (void)L; max_up = max_down = 0; }
+
+void tc_tile_caps(const Layer &L, int &max_up, int &max_down)
+{
+    const long long P = (long long)L.Tmax * L.K;
+    const long long mt_routed = (P + TC_BM - 1) / TC_BM + L.E;
+    const long long mt_shared = L.Fs ? (L.Tmax + TC_BM - 1) / TC_BM + 1 : 0;
+    const long long n_dn = (L.H + TC_BN_DOWN - 1) / TC_BN_DOWN;
+    max_up = (int)(mt_routed * (L.F / (TC_BN_UP / 2)) + mt_shared * (L.Fs / (TC_BN_UP / 2)));
+    max_down = (int)((mt_routed + mt_shared) * n_dn);
+}
+
+int tc_prepare(Layer &L)
+{
+    TensorMaps *m = new (std::nothrow) TensorMaps();
+    if (!m) return -1;
+    const uint64_t rows_all = (uint64_t)L.Tmax * L.K + L.Tmax;
+    bool ok = encode_2d(&m->xp, L.xp, L.H, rows_all, TC_BM) && encode_2d(&m->h, L.h, L.Fmax, rows_all, TC_BM) &&
+              encode_2d(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
+              encode_2d(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, 64) &&
+              encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, 128);
+    if (ok && L.Fs) {
+        ok = encode_2d(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, 64) && encode_2d(&m->sh_up, L.sh_up_w, L.H, L.Fs, 64) &&
+             encode_2d(&m->sh_down, L.sh_down_w, L.Fs, L.H, 128);
+    } else if (ok) {
+        m->sh_gate = m->gate;
+        m->sh_up = m->up;
+        m->sh_down = m->down;
+    }
+    if (!ok) { delete m; return -1; }
+    if (cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TC_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TC_SMEM) != cudaSuccess) {
+        delete m;
+        return -1;
+    }
+    L.tmaps = m;
+    return 0;
+}
+
+void tc_release(Layer &L)
+{
+    delete L.tmaps;
+    L.tmaps = nullptr;
+}
+
+static TcArgs make_tc_args(const Layer &L, int T)
+{
+    TcArgs a;
+    a.meta = L.meta;
+    a.counts = L.counts; a.offsets = L.offsets; a.expert_rows = L.expert_rows;
+    a.gate_b = L.gate_b; a.up_b = L.up_b; a.down_b = L.down_b;
+    a.topk_w = L.topk_w; a.sh_gate = L.sh_gate;
+    a.h = (__nv_bfloat16 *)L.h;
+    a.ys = L.ys;
+    a.status = L.status;
+    a.T = T; a.K = L.K; a.E = L.E; a.H = L.H; a.F = L.F; a.Fs = L.Fs; a.Fmax = L.Fmax; a.Tmax = L.Tmax;
+    a.act = L.cfg.act;
+    a.alpha = L.cfg.act_alpha; a.limit = L.cfg.act_limit;
+    return a;
+}
+
 int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStream_t s)
 {
-    (void)L; (void)x; (void)T; (void)s; (void)which;
-    return 0;
+    const TensorMaps &m = *L.tmaps;
+    if (which == 0) {
+        const int rows = T * L.K + (L.Fs ? T : 0);
+        gather_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const __nv_bfloat16 *)x, T, L.K, L.E, L.H, L.Tmax, L.Fs > 0,
+                                                          L.offsets, L.expert_rows, (__nv_bfloat16 *)L.xp);
+        return 1;
+    }
+    TcArgs a = make_tc_args(L, T);
+    const int grid = L.num_sms;
+    if (which == 1) {
+        TcMaps mu{m.xp, m.gate, m.up, m.sh_gate, m.sh_up};
+        a.tiles = L.up_tiles;
+        tc_gemm_kernel<EPI_UP, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(mu, a);
+    } else {
+        TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down};
+        a.tiles = L.down_tiles;
+        tc_gemm_kernel<EPI_DOWN, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(md, a);
+    }
+    return 1;
 }
 
 }  // namespace moe

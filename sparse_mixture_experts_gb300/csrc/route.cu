@@ -242,7 +242,6 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
 
     // ---- last block: prefix sums, active list, tile lists ----
     __shared__ int s_cnt[1024];
-    __shared__ int s_off[1024];
     __shared__ int s_act[1024];
     __shared__ int s_nact;
     for (int i = threadIdx.x; i < a.E; i += GT) s_cnt[i] = __ldcg(&a.counts[i]);
@@ -257,7 +256,6 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
     int off = block_exclusive_scan(run, &tot);
     int aoff = block_exclusive_scan(run_act, &tot_act);
     for (int i = beg; i < end; ++i) {
-        s_off[i] = off;
         a.offsets[i] = off;
         off += s_cnt[i];
         if (s_cnt[i] > 0) { s_act[aoff] = i; a.active[aoff] = i; ++aoff; }
