@@ -161,20 +161,21 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample of the workload
 # ---------------------------------------------------------------------------
-def oracle_rate(spec, w, x_pool, budget_s: float = 12.0, max_tokens: int = 4096):
-    """Tokens/s of the oracle (all host cores) on a sample of the workload's
-    tokens, sized to take about budget_s seconds."""
+def oracle_rate(spec, w, budget_s: float = 12.0, max_tokens: int = 1 << 16, seed: int = 1):
+    """Tokens/s of the oracle (all host cores) on a sample of tokens drawn like
+    the workload's, sized to take about budget_s seconds."""
     import oracle
     orc = oracle.Oracle(spec, w)
     cores = oracle.max_threads()
-    n = min(max_tokens, max(1, cores))
+    n = max(1, cores)
+    x = synth.make_x(spec, n, seed=seed)
     t0 = time.perf_counter()
-    orc.forward(np.ascontiguousarray(x_pool[:n]))
-    dt = time.perf_counter() - t0
-    per_tok = dt / n
-    m = int(max(n, min(max_tokens, x_pool.shape[0], budget_s / max(per_tok, 1e-9))))
+    orc.forward(x)
+    per_tok = (time.perf_counter() - t0) / n
+    m = int(max(n, min(max_tokens, budget_s / max(per_tok, 1e-9))))
+    x = synth.make_x(spec, m, seed=seed, first_token=n)
     t0 = time.perf_counter()
-    orc.forward(np.ascontiguousarray(x_pool[:m]))
+    orc.forward(x)
     dt = time.perf_counter() - t0
     return m / dt, cores, m, dt
 
@@ -374,9 +375,16 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
     total_k = sum(ms for ms, _ in ktimes.values())
     kernel_share = {k: (ms / total_k if total_k else None) for k, (ms, _) in ktimes.items()}
     top = max((k for k in ktimes if ktimes[k][1]), key=lambda k: ktimes[k][0])
-    decode_like = T * spec.top_k < 16 * E  # the same threshold the library uses to pick the path
+    path = "fused" if ktimes.get("fused", (0, 0))[1] else ("tensor-core" if ktimes.get("gather", (0, 0))[1]
+                                                           else "stream")
+    decode_like = path != "tensor-core"
     up_rows = T * spec.top_k
-    if top == "up":
+    if top == "fused":
+        # the whole layer in one kernel: its algorithmic bytes are the step's
+        alg = step_bytes
+        bound, unit, peak = "hbm", "GB/s", hbm_peak
+        achieved = alg / (kernel_avg_us["fused"] * 1e-6) / 1e9
+    elif top == "up":
         if decode_like:
             alg = d_avg * per_expert_up + 2 * Fs * H * eb + T * H * eb + (up_rows + T) * max(F, Fs) * eb
             bound, unit, peak = "hbm", "GB/s", hbm_peak
@@ -450,9 +458,9 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
     # ---- CPU baseline (rank 0, N = 1 only) ----
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rate, cores, m, dt = oracle_rate(spec, w, x_np, budget_s=args.cpu_budget)
+        rate, cores, m, dt = oracle_rate(spec, w, budget_s=args.cpu_budget)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{m} tokens of this workload's batches in one oracle call ({dt:.1f} s)"}
+               "sample": f"{m} tokens drawn like this workload's, one oracle call over all cores ({dt:.1f} s)"}
 
     if rank == 0:
         line = {
@@ -464,7 +472,7 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
                        "l2": (f"inputs larger than L2: steps rotate over {n_layers} layers with distinct weight "
                               f"memory ({layers[0].device_bytes * n_layers / 1e9:.1f} GB)"),
                        "token_batches": N_BATCHES, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "distinct_experts_per_step": d_avg, "path": "stream" if decode_like else "tensor-core"},
+                       "distinct_experts_per_step": d_avg, "path": path},
             "roofline": roofline,
             "step_roofline": step_roofline,
             "kernels": {k: {"avg_us": kernel_avg_us[k], "share": kernel_share[k], "launches": ktimes[k][1]}

@@ -164,10 +164,13 @@ moe_status moe_get_expert_counts(moe_layer *layer, int32_t *counts, void *stream
 
 /* Kernel-path selection, for tests and benchmarks. */
 typedef enum {
-    MOE_PATH_AUTO = 0,     /* by tokens per expert (default) */
+    MOE_PATH_AUTO = 0,     /* default: FUSED when it applies, else TC when it applies, else STREAM */
     MOE_PATH_STREAM = 1,   /* weight-streaming CUDA-core kernels (any dtype) */
-    MOE_PATH_TC = 2        /* tcgen05 grouped GEMMs (bf16, H, F, Fs multiples of 64);
+    MOE_PATH_TC = 2,       /* tcgen05 grouped GEMMs (bf16, H, F, Fs multiples of 64);
                               UNSUPPORTED otherwise */
+    MOE_PATH_FUSED = 3     /* the whole layer in one cooperative kernel, for up to 8 tokens
+                              (top_k * n_tokens <= 256, F a multiple of 16); forward returns
+                              UNSUPPORTED for larger batches while this path is forced */
 } moe_path;
 moe_status moe_set_path(moe_layer *layer, int32_t path);
 
@@ -188,7 +191,8 @@ typedef enum {
     MOE_KERNEL_DOWN = 4,     /* down projection + routing weight */
     MOE_KERNEL_COMBINE = 5,  /* fixed-order combine */
     MOE_KERNEL_GATHER = 6,   /* token-row gather (tensor-core path) */
-    MOE_KERNEL_COUNT = 7
+    MOE_KERNEL_FUSED = 7,    /* whole layer in one kernel (fused decode path) */
+    MOE_KERNEL_COUNT = 8
 } moe_kernel_kind;
 
 /* Synchronises the device, then writes, per kernel kind, the summed device

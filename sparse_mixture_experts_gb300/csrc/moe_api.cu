@@ -238,17 +238,21 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     if ((st = dev_alloc(L, &L.h, (T * K + T) * (size_t)L.Fmax * eb))) return st;
     if ((st = dev_alloc_t(L, &L.ys, T * (K + 1) * H))) return st;
     if ((st = dev_alloc_t(L, &L.status, 1))) return st;
+    if ((st = dev_alloc_t(L, &L.gbar, 2))) return st;
     if ((st = dev_alloc(L, &L.x_stage, T * H * eb))) return st;
     if ((st = dev_alloc(L, &L.out_stage, T * H * (c.out_dtype == MOE_DT_BF16 ? 2 : 4)))) return st;
     CUDA_TRY(cudaMemset(L.meta, 0, sizeof(RouteMeta)));
     CUDA_TRY(cudaMemset(L.status, 0, sizeof(int)));
+    CUDA_TRY(cudaMemset(L.gbar, 0, 2 * sizeof(unsigned)));
+    decode_prepare(L);
     CUDA_TRY(cudaMemset(L.counts, 0, E * sizeof(int)));
 
     std::string why;
     L.tc_capable = tc_supported(L, why);
     if (L.tc_capable) {
         tc_tile_caps(L, L.max_up_tiles, L.max_down_tiles);
-        if ((st = dev_alloc(L, &L.xp, T * K * H * eb))) return st;
+        // routed rows (T*K, expert-sorted) then the shared expert's rows (T)
+        if ((st = dev_alloc(L, &L.xp, (T * K + T) * H * eb))) return st;
         if ((st = dev_alloc_t(L, &L.up_tiles, (size_t)L.max_up_tiles))) return st;
         if ((st = dev_alloc_t(L, &L.down_tiles, (size_t)L.max_down_tiles))) return st;
         if (tc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "tensor map creation failed");
@@ -257,14 +261,19 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     return MOE_OK;
 }
 
-bool use_tc(const Layer &L, int T)
+enum class Route { Fused, TC, Stream };
+
+Route choose_path(const Layer &L, int T)
 {
-    if (!L.tc_capable) return false;
-    if (L.path == MOE_PATH_TC) return true;
-    if (L.path == MOE_PATH_STREAM) return false;
-    // expected rows per routed expert; the streaming kernels win while each
-    // expert sees only a few tokens
-    return (long long)T * L.K >= 16LL * L.E;
+    switch (L.path) {
+    case MOE_PATH_FUSED: return Route::Fused;
+    case MOE_PATH_TC: return Route::TC;
+    case MOE_PATH_STREAM: return Route::Stream;
+    default: break;
+    }
+    if (decode_supported(L, T)) return Route::Fused;
+    if (L.tc_capable) return Route::TC;
+    return Route::Stream;
 }
 
 moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t s)
@@ -282,7 +291,10 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
     const size_t ob = (size_t)T * L.H * (L.cfg.out_dtype == MOE_DT_BF16 ? 2 : 4);
     const char *xs = (const char *)x, *os = (const char *)out;
     if (xs < os + ob && os < xs + xb) return fail(MOE_ERR_INVALID_ARG, "x and out overlap");
-    const bool tc = use_tc(L, T);
+    const Route route = choose_path(L, T);
+    if (route == Route::Fused && !decode_supported(L, T))
+        return fail(MOE_ERR_UNSUPPORTED, "fused decode path forced for a batch it does not cover");
+    const bool tc = route == Route::TC;
     const bool rec = L.timing_max > 0 && L.timing_recorded < L.timing_max;
     int n = 0;
     auto run = [&](int kind, auto &&launch) {
@@ -293,6 +305,20 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
         n += launch();
         if (rec) cudaEventRecord(L.timing_events[2 * L.timing_pairs + 1], s), ++L.timing_pairs;
     };
+    if (route == Route::Fused) {
+        int launched = 0;
+        run(MOE_KERNEL_FUSED, [&] { return launched = launch_decode(L, x, T, out, s); });
+        if (launched < 0) {
+            cudaError_t e = cudaGetLastError();
+            return cuda_fail(e != cudaSuccess ? e : cudaErrorLaunchFailure, "cooperative launch");
+        }
+        if (rec) ++L.timing_recorded;
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+        L.last_T = T;
+        L.last_launches = n;
+        return MOE_OK;
+    }
     run(MOE_KERNEL_ROUTER, [&] { return launch_router(L, x, T, s); });
     run(MOE_KERNEL_SELECT, [&] { return launch_select(L, T, s); });
     run(MOE_KERNEL_GROUP, [&] { return launch_group(L, T, tc, s); });
@@ -398,8 +424,10 @@ moe_status moe_get_expert_counts(moe_layer *layer, int32_t *counts, void *stream
 moe_status moe_set_path(moe_layer *layer, int32_t path)
 {
     if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
-    if (path != MOE_PATH_AUTO && path != MOE_PATH_STREAM && path != MOE_PATH_TC)
+    if (path != MOE_PATH_AUTO && path != MOE_PATH_STREAM && path != MOE_PATH_TC && path != MOE_PATH_FUSED)
         return fail(MOE_ERR_INVALID_ARG, "unknown path");
+    if (path == MOE_PATH_FUSED && layer->decode_grid == 0)
+        return fail(MOE_ERR_UNSUPPORTED, "cooperative launch unavailable on this device");
     if (path == MOE_PATH_TC && !layer->tc_capable) {
         std::string why;
         tc_supported(*layer, why);

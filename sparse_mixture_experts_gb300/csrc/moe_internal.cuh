@@ -23,6 +23,7 @@ enum DeviceError : int {
     DEV_TIMEOUT_ACCUM_BARRIER = 3,  // MMA->epilogue accumulator never ready
     DEV_TIMEOUT_ACCUM_FREE = 4,     // epilogue->MMA accumulator never released
     DEV_BAD_TILE = 5,               // a tile descriptor outside the problem
+    DEV_TIMEOUT_GRID_BARRIER = 6,   // a block of the cooperative decode kernel never arrived
 };
 
 // Groups of rows a grouped kernel walks over: the routed experts that
@@ -83,12 +84,14 @@ struct Layer {
     int *active = nullptr;     // [E]
     RouteMeta *meta = nullptr;
     void *h = nullptr;         // [Tmax*K + Tmax][Fmax] activations (routed rows sorted by expert, then shared)
-    void *xp = nullptr;        // [Tmax*K][H] x rows gathered in expert order (tensor-core path)
+    void *xp = nullptr;        // [Tmax*K + Tmax][H] x rows gathered in expert order, then x (tensor-core path)
     float *ys = nullptr;       // [Tmax][K+1][H] weighted expert outputs per (token, slot)
     TileDesc *up_tiles = nullptr;
     TileDesc *down_tiles = nullptr;
     int max_up_tiles = 0, max_down_tiles = 0;
     int *status = nullptr;     // DeviceError
+    unsigned *gbar = nullptr;  // [2] grid-barrier arrivals / generation (decode kernel)
+    int decode_grid = 0;       // blocks of the cooperative decode kernel (0 = unavailable)
     void *x_stage = nullptr;   // [Tmax][H] for moe_forward_host
     void *out_stage = nullptr; // [Tmax][H]
     TensorMaps *tmaps = nullptr;  // host copy of the tensor maps (tensor-core path)
@@ -179,6 +182,11 @@ int launch_group(const Layer &L, int T, bool build_tiles, cudaStream_t s);
 // which: 0 = gate/up + activation, 1 = down + routing weight
 int launch_experts_stream(const Layer &L, const void *x, int T, int which, cudaStream_t s);
 int launch_combine(const Layer &L, int T, void *out, cudaStream_t s);
+
+// fused decode kernel (decode.cu)
+int decode_prepare(Layer &L);
+bool decode_supported(const Layer &L, int T);
+int launch_decode(const Layer &L, const void *x, int T, void *out, cudaStream_t s);
 
 // tensor-core path (expert_tc.cu)
 bool tc_supported(const Layer &L, std::string &why);

@@ -73,9 +73,16 @@ def _flops(spec, T):
     return 2.0 * T * spec.top_k * 3 * spec.hidden * spec.expert_ff
 
 
-@pytest.mark.parametrize("path", [moe.PATH_STREAM, moe.PATH_TC], ids=["stream", "tc"])
+PATHS = [moe.PATH_STREAM, moe.PATH_TC, moe.PATH_FUSED]
+PATH_IDS = ["stream", "tc", "fused"]
+FUSED_MAX_TOKENS = 8
+
+
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("name,T,n_rows", CASES, ids=[f"{c[0]}-T{c[1]}" for c in CASES])
 def test_layer_parity(name, T, n_rows, path):
+    if path == moe.PATH_FUSED and T > FUSED_MAX_TOKENS:
+        pytest.skip("the fused decode kernel covers up to 8 tokens")
     wl = workload(name)
     spec = wl.spec
     if path == moe.PATH_STREAM and _flops(spec, T) > STREAM_MAX_FLOP:
@@ -120,14 +127,14 @@ def test_layer_parity(name, T, n_rows, path):
     assert rep.ok(spec.dtype), str(rep)
 
 
-@pytest.mark.parametrize("path", [moe.PATH_STREAM, moe.PATH_TC], ids=["stream", "tc"])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_deterministic_bitwise(path):
     wl = workload("qwen_prefill_zipf")
     try:
         wl.layer.set_path(path)
     except moe.MoEError as e:
         pytest.skip(str(e))
-    T = 1024
+    T = 8 if path == moe.PATH_FUSED else 1024
     a = wl.layer.forward(wl.x_dev[:T]).clone()
     b = wl.layer.forward(wl.x_dev[:T]).clone()
     torch.cuda.synchronize()
@@ -173,6 +180,8 @@ def test_misaligned_and_overlapping_pointers_rejected():
 
 
 def _small_case(spec, T, path, seed=21, out_dtype="f32", mutate=None):
+    if path == moe.PATH_FUSED and T > FUSED_MAX_TOKENS:
+        T = 7  # a ragged decode batch
     w = synth.make_weights(spec, seed=seed)
     if mutate:
         mutate(w)
@@ -211,7 +220,7 @@ EDGE_SPECS = [
 ]
 
 
-@pytest.mark.parametrize("path", [moe.PATH_STREAM, moe.PATH_TC], ids=["stream", "tc"])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 @pytest.mark.parametrize("name,spec,T", EDGE_SPECS, ids=[e[0] for e in EDGE_SPECS])
 def test_edge_cases(name, spec, T, path):
     rep = _small_case(spec, T, path)
@@ -219,7 +228,7 @@ def test_edge_cases(name, spec, T, path):
     assert rep.ok(spec.dtype), str(rep)
 
 
-@pytest.mark.parametrize("path", [moe.PATH_STREAM, moe.PATH_TC], ids=["stream", "tc"])
+@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
 def test_all_tokens_to_one_expert(path):
     """Degenerate routing: one router row dominates, so every token picks
     expert 5 first through its router bias (the hot-expert case of a skewed
@@ -235,8 +244,40 @@ def test_all_tokens_to_one_expert(path):
     assert rep.ok(spec.dtype), str(rep)
 
 
-def test_bf16_output():
+@pytest.mark.parametrize("T", [5, 24])
+def test_bf16_output(T):
     spec = synth.QWEN.replace(name="qwen-like bf16 out", hidden=256, n_expert=32, top_k=8, expert_ff=128,
                               shared_ff=128)
-    rep = _small_case(spec, 24, moe.PATH_AUTO, out_dtype="bf16")
+    rep = _small_case(spec, T, moe.PATH_AUTO, out_dtype="bf16")
     assert rep.ok("bf16"), str(rep)
+
+
+def test_fused_path_rejects_large_batches():
+    spec = synth.TINY
+    w = synth.make_weights(spec, seed=3)
+    layer = helpers.make_layer(spec, w, 16)
+    layer.set_path(moe.PATH_FUSED)
+    x = helpers.to_torch(synth.make_x(spec, 16, seed=3))
+    with pytest.raises(moe.MoEError) as ei:
+        layer.forward(x)
+    assert ei.value.status == moe.ERR_UNSUPPORTED
+    layer.forward(x[:8])
+    torch.cuda.synchronize()
+    layer.close()
+
+
+def test_paths_agree_on_decode_batch():
+    """The three kernel paths give the same selection and outputs within the
+    bf16 bar on one decode batch."""
+    wl = workload("qwen_decode")
+    outs = {}
+    for path in PATHS:
+        wl.layer.set_path(path)
+        outs[path] = wl.layer.forward(wl.x_dev[:8]).cpu().numpy().astype(np.float64)
+        idx, _ = wl.layer.routing(8)
+        outs[(path, "idx")] = idx.cpu().numpy()
+    wl.layer.set_path(moe.PATH_AUTO)
+    for path in PATHS[1:]:
+        np.testing.assert_array_equal(outs[(path, "idx")], outs[(PATHS[0], "idx")])
+        ref = outs[PATHS[0]]
+        assert np.linalg.norm(outs[path] - ref) <= 1e-2 * np.linalg.norm(ref)
