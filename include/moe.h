@@ -164,13 +164,16 @@ moe_status moe_get_expert_counts(moe_layer *layer, int32_t *counts, void *stream
 
 /* Kernel-path selection, for tests and benchmarks. */
 typedef enum {
-    MOE_PATH_AUTO = 0,     /* default: FUSED when it applies, else TC when it applies, else STREAM */
+    MOE_PATH_AUTO = 0,     /* default: DECODE_TC, else FUSED, else TC, else STREAM (first that applies) */
     MOE_PATH_STREAM = 1,   /* weight-streaming CUDA-core kernels (any dtype) */
     MOE_PATH_TC = 2,       /* tcgen05 grouped GEMMs (bf16, H, F, Fs multiples of 64);
                               UNSUPPORTED otherwise */
-    MOE_PATH_FUSED = 3     /* the whole layer in one cooperative kernel, for up to 8 tokens
-                              (top_k * n_tokens <= 256, F a multiple of 16); forward returns
-                              UNSUPPORTED for larger batches while this path is forced */
+    MOE_PATH_FUSED = 3,    /* the whole layer in one cooperative CUDA-core kernel, for up to 8
+                              tokens (top_k * n_tokens <= 256, F a multiple of 16) */
+    MOE_PATH_DECODE_TC = 4 /* weight-streaming tcgen05 kernels for up to 16 tokens (bf16, H, F,
+                              Fs multiples of 64): weight rows are the MMA's M operand */
+    /* While FUSED or DECODE_TC is forced, forward returns UNSUPPORTED for a
+     * batch the path does not cover. */
 } moe_path;
 moe_status moe_set_path(moe_layer *layer, int32_t path);
 

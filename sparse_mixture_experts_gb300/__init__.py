@@ -24,7 +24,7 @@ _STATUS_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "
 DT_F32, DT_BF16 = 0, 1
 ROUTER_SOFTMAX_TOPK, ROUTER_TOPK_SOFTMAX = 0, 1
 ACT_SWIGLU, ACT_CLAMP_GLU = 0, 1
-PATH_AUTO, PATH_STREAM, PATH_TC, PATH_FUSED = 0, 1, 2, 3
+PATH_AUTO, PATH_STREAM, PATH_TC, PATH_FUSED, PATH_DECODE_TC = 0, 1, 2, 3, 4
 KERNEL_KINDS = ("router", "select", "group", "up", "down", "combine", "gather", "fused")
 
 _DT = {"f32": DT_F32, "bf16": DT_BF16}

@@ -71,6 +71,7 @@ void free_all(Layer &L)
 {
     timing_free(L);
     if (L.tmaps) tc_release(L);
+    if (L.dectc) dectc_release(L);
     for (void *p : L.allocations) cudaFree(p);
     L.allocations.clear();
 }
@@ -256,21 +257,32 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
         if ((st = dev_alloc_t(L, &L.up_tiles, (size_t)L.max_up_tiles))) return st;
         if ((st = dev_alloc_t(L, &L.down_tiles, (size_t)L.max_down_tiles))) return st;
         if (tc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "tensor map creation failed");
+        size_t hp_b, part_b, tab_b, tick_b;
+        dectc_workspace(L, hp_b, part_b, tab_b, tick_b);
+        if ((st = dev_alloc(L, &L.dec_hp, hp_b))) return st;
+        if ((st = dev_alloc(L, (void **)&L.dec_partials, part_b))) return st;
+        if ((st = dev_alloc(L, (void **)&L.dec_wtab, tab_b))) return st;
+        if ((st = dev_alloc(L, (void **)&L.dec_tickets, tick_b))) return st;
+        CUDA_TRY(cudaMemset(L.dec_tickets, 0, tick_b));
+        CUDA_TRY(cudaMemset(L.dec_hp, 0, hp_b));
+        if (dectc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "decode tensor map creation failed");
     }
     CUDA_TRY(cudaDeviceSynchronize());
     return MOE_OK;
 }
 
-enum class Route { Fused, TC, Stream };
+enum class Route { DecodeTC, Fused, TC, Stream };
 
 Route choose_path(const Layer &L, int T)
 {
     switch (L.path) {
+    case MOE_PATH_DECODE_TC: return Route::DecodeTC;
     case MOE_PATH_FUSED: return Route::Fused;
     case MOE_PATH_TC: return Route::TC;
     case MOE_PATH_STREAM: return Route::Stream;
     default: break;
     }
+    if (dectc_supported(L, T)) return Route::DecodeTC;
     if (decode_supported(L, T)) return Route::Fused;
     if (L.tc_capable) return Route::TC;
     return Route::Stream;
@@ -294,6 +306,8 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
     const Route route = choose_path(L, T);
     if (route == Route::Fused && !decode_supported(L, T))
         return fail(MOE_ERR_UNSUPPORTED, "fused decode path forced for a batch it does not cover");
+    if (route == Route::DecodeTC && !dectc_supported(L, T))
+        return fail(MOE_ERR_UNSUPPORTED, "weight-streaming tensor-core path forced for a batch it does not cover");
     const bool tc = route == Route::TC;
     const bool rec = L.timing_max > 0 && L.timing_recorded < L.timing_max;
     int n = 0;
@@ -305,6 +319,18 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
         n += launch();
         if (rec) cudaEventRecord(L.timing_events[2 * L.timing_pairs + 1], s), ++L.timing_pairs;
     };
+    if (route == Route::DecodeTC) {
+        int bad = 0;
+        run(MOE_KERNEL_ROUTER, [&] { int r = launch_dectc(L, x, T, out, 0, s); bad |= r < 0; return r < 0 ? 0 : r; });
+        run(MOE_KERNEL_UP, [&] { int r = launch_dectc(L, x, T, out, 1, s); bad |= r < 0; return r < 0 ? 0 : r; });
+        run(MOE_KERNEL_DOWN, [&] { int r = launch_dectc(L, x, T, out, 2, s); bad |= r < 0; return r < 0 ? 0 : r; });
+        if (rec) ++L.timing_recorded;
+        cudaError_t e = cudaGetLastError();
+        if (bad || e != cudaSuccess) return cuda_fail(e != cudaSuccess ? e : cudaErrorLaunchFailure, "decode launch");
+        L.last_T = T;
+        L.last_launches = n;
+        return MOE_OK;
+    }
     if (route == Route::Fused) {
         int launched = 0;
         run(MOE_KERNEL_FUSED, [&] { return launched = launch_decode(L, x, T, out, s); });
@@ -424,8 +450,9 @@ moe_status moe_get_expert_counts(moe_layer *layer, int32_t *counts, void *stream
 moe_status moe_set_path(moe_layer *layer, int32_t path)
 {
     if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
-    if (path != MOE_PATH_AUTO && path != MOE_PATH_STREAM && path != MOE_PATH_TC && path != MOE_PATH_FUSED)
-        return fail(MOE_ERR_INVALID_ARG, "unknown path");
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_DECODE_TC) return fail(MOE_ERR_INVALID_ARG, "unknown path");
+    if (path == MOE_PATH_DECODE_TC && !layer->dectc)
+        return fail(MOE_ERR_UNSUPPORTED, "weight-streaming tensor-core path unavailable (needs the tensor-core path)");
     if (path == MOE_PATH_FUSED && layer->decode_grid == 0)
         return fail(MOE_ERR_UNSUPPORTED, "cooperative launch unavailable on this device");
     if (path == MOE_PATH_TC && !layer->tc_capable) {

@@ -95,6 +95,12 @@ struct Layer {
     void *x_stage = nullptr;   // [Tmax][H] for moe_forward_host
     void *out_stage = nullptr; // [Tmax][H]
     TensorMaps *tmaps = nullptr;  // host copy of the tensor maps (tensor-core path)
+    // weight-streaming tensor-core decode path
+    struct DecMaps *dectc = nullptr;
+    void *dec_hp = nullptr;          // [groups_max*16][Fmax] bf16: routing-weighted activations
+    float *dec_partials = nullptr;   // split-K partial sums
+    float *dec_wtab = nullptr;       // [groups_max][16] routing weight of token t for group g
+    int *dec_tickets = nullptr;      // per-tile arrival counters
 
     // per-kernel timing (moe_timing_enable / moe_timing_read)
     int timing_max = 0;         // forwards recorded per window; 0 = off
@@ -187,6 +193,14 @@ int launch_combine(const Layer &L, int T, void *out, cudaStream_t s);
 int decode_prepare(Layer &L);
 bool decode_supported(const Layer &L, int T);
 int launch_decode(const Layer &L, const void *x, int T, void *out, cudaStream_t s);
+
+// weight-streaming tensor-core decode path (decode_tc.cu)
+bool dectc_supported(const Layer &L, int T);
+size_t dectc_workspace(const Layer &L, size_t &hp_bytes, size_t &part_bytes, size_t &tab_bytes, size_t &ticket_bytes);
+int dectc_prepare(Layer &L);
+void dectc_release(Layer &L);
+// which: 0 = router + selection, 1 = gate/up, 2 = down (writes out)
+int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s);
 
 // tensor-core path (expert_tc.cu)
 bool tc_supported(const Layer &L, std::string &why);

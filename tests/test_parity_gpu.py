@@ -73,9 +73,10 @@ def _flops(spec, T):
     return 2.0 * T * spec.top_k * 3 * spec.hidden * spec.expert_ff
 
 
-PATHS = [moe.PATH_STREAM, moe.PATH_TC, moe.PATH_FUSED]
-PATH_IDS = ["stream", "tc", "fused"]
+PATHS = [moe.PATH_STREAM, moe.PATH_TC, moe.PATH_FUSED, moe.PATH_DECODE_TC]
+PATH_IDS = ["stream", "tc", "fused", "dectc"]
 FUSED_MAX_TOKENS = 8
+DECODE_TC_MAX_TOKENS = 16
 
 
 @pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
@@ -83,6 +84,8 @@ FUSED_MAX_TOKENS = 8
 def test_layer_parity(name, T, n_rows, path):
     if path == moe.PATH_FUSED and T > FUSED_MAX_TOKENS:
         pytest.skip("the fused decode kernel covers up to 8 tokens")
+    if path == moe.PATH_DECODE_TC and T > DECODE_TC_MAX_TOKENS:
+        pytest.skip("the weight-streaming tensor-core kernels cover up to 16 tokens")
     wl = workload(name)
     spec = wl.spec
     if path == moe.PATH_STREAM and _flops(spec, T) > STREAM_MAX_FLOP:
@@ -134,7 +137,7 @@ def test_deterministic_bitwise(path):
         wl.layer.set_path(path)
     except moe.MoEError as e:
         pytest.skip(str(e))
-    T = 8 if path == moe.PATH_FUSED else 1024
+    T = 8 if path in (moe.PATH_FUSED, moe.PATH_DECODE_TC) else 1024
     a = wl.layer.forward(wl.x_dev[:T]).clone()
     b = wl.layer.forward(wl.x_dev[:T]).clone()
     torch.cuda.synchronize()
@@ -182,6 +185,8 @@ def test_misaligned_and_overlapping_pointers_rejected():
 def _small_case(spec, T, path, seed=21, out_dtype="f32", mutate=None):
     if path == moe.PATH_FUSED and T > FUSED_MAX_TOKENS:
         T = 7  # a ragged decode batch
+    if path == moe.PATH_DECODE_TC and T > DECODE_TC_MAX_TOKENS:
+        T = 13
     w = synth.make_weights(spec, seed=seed)
     if mutate:
         mutate(w)
@@ -192,7 +197,13 @@ def _small_case(spec, T, path, seed=21, out_dtype="f32", mutate=None):
     except moe.MoEError as e:
         layer.close()
         pytest.skip(str(e))
-    out = layer.forward(helpers.to_torch(x)).float().cpu().numpy()
+    try:
+        out = layer.forward(helpers.to_torch(x)).float().cpu().numpy()
+    except moe.MoEError as e:
+        layer.close()
+        if e.status == moe.ERR_UNSUPPORTED:
+            pytest.skip(str(e))
+        raise
     idx, _ = layer.routing(T)
     idx = idx.cpu().numpy()
     layer.status()
