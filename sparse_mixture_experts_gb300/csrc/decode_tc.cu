@@ -43,9 +43,10 @@ constexpr int DT_THREADS = 192;
 constexpr int DT_A_BYTES = 128 * 64 * 2;        // 16 KB weight tile
 constexpr int DT_B_BYTES = DT_TOK * 64 * 2;     // 2 KB token tile
 constexpr int DT_STAGE_BYTES = DT_A_BYTES + DT_B_BYTES;
-constexpr int DT_TMEM_COLS = 32;                // 2 accumulators x 16 fp32 columns
+constexpr int DT_ACC = 8;                       // TMEM accumulator buffers (MMA runs ahead of the epilogue)
+constexpr int DT_TMEM_COLS = DT_ACC * 16;       // 16 fp32 columns each
 constexpr int DT_XCH_BYTES = 64 * DT_TOK * 4;   // up-row values handed to the gate rows
-constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 256;
+constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 512;
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
 
 struct DecMaps {
@@ -269,12 +270,15 @@ __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
 // 1; at most max_units units.
 __device__ __forceinline__ int choose_splits(int tiles, int nkb, int smax, int G, int max_units)
 {
+    // no split when every CTA already has a tile: a split costs a partial-sum
+    // round trip through global memory per unit
+    if (tiles >= G) return 1;
     int best = 1;
     long long best_cost = -1;
     for (int S = 1; S <= smax; ++S) {
         if ((long long)tiles * S > max_units && S > 1) break;
         const long long per_cta = ((long long)tiles * S + G - 1) / G;
-        const long long cost = per_cta * (((nkb + S - 1) / S) * (long long)DT_STAGE_BYTES + (S > 1 ? 16384 : 0));
+        const long long cost = per_cta * (((nkb + S - 1) / S) * (long long)DT_STAGE_BYTES + (S > 1 ? 32768 : 0));
         if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = S; }
     }
     return best;
@@ -354,9 +358,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
     float *xch = reinterpret_cast<float *>(smem + DT_STAGES * DT_STAGE_BYTES);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + DT_STAGES * DT_STAGE_BYTES + DT_XCH_BYTES);
     uint64_t *empty = full + DT_STAGES;
-    uint64_t *acc_full = empty + DT_STAGES;   // [2]
-    uint64_t *acc_empty = acc_full + 2;       // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *acc_full = empty + DT_STAGES;   // [DT_ACC]
+    uint64_t *acc_empty = acc_full + DT_ACC;  // [DT_ACC]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + DT_ACC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
 
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < DT_ACC; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 128);
         }
@@ -485,8 +489,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
             int last_acc = -1;
             uint32_t last_acc_phase = 0;
             for (int u = blockIdx.x; u < units && ok; u += G, ++it) {
-                const int b = it & 1;
-                const uint32_t acc_phase = (it >> 1) & 1;
+                const int b = it % DT_ACC;
+                const uint32_t acc_phase = (it / DT_ACC) & 1;
                 if (!mbar_wait(&acc_empty[b], acc_phase ^ 1, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
                     *abort_flag = 1;
@@ -540,8 +544,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
         const int et = threadIdx.x - 64;            // 0..127 within the epilogue group
         int it = 0;
         for (int u = blockIdx.x; u < units; u += G, ++it) {
-            const int b = it & 1;
-            const uint32_t acc_phase = (it >> 1) & 1;
+            const int b = it % DT_ACC;
+            const uint32_t acc_phase = (it / DT_ACC) & 1;
             // one thread waits (bounded) and tells the others, so that all 128
             // leave together on a timeout and no named barrier below can hang
             if (et == 0) {
