@@ -219,6 +219,36 @@ size_t moe_device_bytes(const moe_layer *layer);
  * a no-op. */
 void moe_destroy(moe_layer *layer);
 
+/* Routing without any device allocation: router logits, top-k selection with
+ * routing weights, and per-expert token counts, for callers that must not call
+ * cudaMalloc (an application that owns all device memory through its own pool,
+ * a process whose allocator is frozen after start-up, a real-time loop where
+ * an allocation and the synchronisation it can bring are not allowed).  The
+ * pages have no counterpart of this entry point; it computes the same routing
+ * as moe_forward (moe_get_routing / moe_get_expert_counts) without a layer.
+ *
+ * x [n_tokens][hidden], router_w [n_expert][hidden] and the optional router_b
+ * [n_expert] are device pointers in `dtype` (x and router_w 16-byte aligned);
+ * outputs are device pointers: idx [n_tokens][top_k] int32 (descending weight,
+ * ties to the lower expert index), w [n_tokens][top_k] fp32, counts [n_expert]
+ * int32 (zeroed by the call).  router_mode, norm_topk_prob and weights_scale
+ * mean what they mean in moe_config.  Asynchronous on `stream`.
+ *
+ * The logits are kept in a static device array of 262144 floats (1 MiB) that
+ * every GPU holding the library keeps until the process exits:
+ * n_tokens * n_expert above 262144 returns MOE_ERR_TOO_MANY_TOKENS.  All calls
+ * on a device share that array and it keeps the last call's contents, so calls
+ * that overlap on the GPU race; order them (one stream, or events).  The first
+ * call on each device looks the array's address up (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  Other
+ * errors: INVALID_ARG (NULL or misaligned pointer, bad size, mode or dtype),
+ * UNSUPPORTED (top_k > 32, n_expert > 1024, hidden not a multiple of 8, device
+ * ordinal >= 64), CUDA. */
+moe_status moe_route_noalloc(const void *x, const void *router_w, const void *router_b, int32_t n_tokens,
+                             int32_t hidden, int32_t n_expert, int32_t top_k, int32_t router_mode,
+                             int32_t norm_topk_prob, float weights_scale, int32_t dtype, int32_t *idx, float *w,
+                             int32_t *counts, void *stream);
+
 /* Description of the last error on this thread ("" if none). */
 const char *moe_last_error(void);
 

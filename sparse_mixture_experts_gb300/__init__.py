@@ -82,6 +82,8 @@ def load_library(path: str = LIB_PATH):
         "moe_destroy": ([VP], None),
         "moe_last_error": ([], ctypes.c_char_p),
         "moe_abi_version": ([], I32),
+        "moe_route_noalloc": ([VP, VP, VP, I32, I32, I32, I32, I32, I32, ctypes.c_float, I32, VP, VP, VP, VP],
+                              ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)

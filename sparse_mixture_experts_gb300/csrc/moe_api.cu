@@ -367,6 +367,11 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
 
 }  // namespace
 
+namespace moe {
+// lets other translation units report through moe_last_error()
+void set_last_error(const char *msg) { g_error = msg; }
+}  // namespace moe
+
 extern "C" {
 
 moe_status moe_layer_create(const moe_config *config, const moe_weights *weights, moe_layer **out)

@@ -179,6 +179,9 @@ __device__ __forceinline__ void record_error(int *status, int code)
     atomicCAS(status, 0, code);
 }
 
+// message returned by moe_last_error() on this thread
+void set_last_error(const char *msg);
+
 // ---------------------------------------------------------------------------
 // host-side launchers (each returns the number of kernels it launched, or -1)
 // ---------------------------------------------------------------------------
