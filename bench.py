@@ -375,15 +375,21 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
     total_k = sum(ms for ms, _ in ktimes.values())
     kernel_share = {k: (ms / total_k if total_k else None) for k, (ms, _) in ktimes.items()}
     top = max((k for k in ktimes if ktimes[k][1]), key=lambda k: ktimes[k][0])
-    path = "fused" if ktimes.get("fused", (0, 0))[1] else ("tensor-core" if ktimes.get("gather", (0, 0))[1]
-                                                           else "stream")
+    if ktimes.get("experts", (0, 0))[1]:
+        path = "weight-streaming tensor-core"
+    elif ktimes.get("fused", (0, 0))[1]:
+        path = "fused"
+    elif ktimes.get("gather", (0, 0))[1]:
+        path = "tensor-core"
+    else:
+        path = "stream"
     decode_like = path != "tensor-core"
     up_rows = T * spec.top_k
-    if top == "fused":
-        # the whole layer in one kernel: its algorithmic bytes are the step's
-        alg = step_bytes
+    if top in ("fused", "experts"):
+        # all expert weights of the step stream through this one kernel
+        alg = step_bytes - (router_bytes if top == "experts" else 0)
         bound, unit, peak = "hbm", "GB/s", hbm_peak
-        achieved = alg / (kernel_avg_us["fused"] * 1e-6) / 1e9
+        achieved = alg / (kernel_avg_us[top] * 1e-6) / 1e9
     elif top == "up":
         if decode_like:
             alg = d_avg * per_expert_up + 2 * Fs * H * eb + T * H * eb + (up_rows + T) * max(F, Fs) * eb

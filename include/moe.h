@@ -195,7 +195,9 @@ typedef enum {
     MOE_KERNEL_COMBINE = 5,  /* fixed-order combine */
     MOE_KERNEL_GATHER = 6,   /* token-row gather (tensor-core path) */
     MOE_KERNEL_FUSED = 7,    /* whole layer in one kernel (fused decode path) */
-    MOE_KERNEL_COUNT = 8
+    MOE_KERNEL_EXPERTS = 8,  /* selection, gate/up and down in one persistent kernel
+                                (weight-streaming tensor-core decode path) */
+    MOE_KERNEL_COUNT = 9
 } moe_kernel_kind;
 
 /* Synchronises the device, then writes, per kernel kind, the summed device

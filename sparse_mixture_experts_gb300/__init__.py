@@ -25,7 +25,7 @@ DT_F32, DT_BF16 = 0, 1
 ROUTER_SOFTMAX_TOPK, ROUTER_TOPK_SOFTMAX = 0, 1
 ACT_SWIGLU, ACT_CLAMP_GLU = 0, 1
 PATH_AUTO, PATH_STREAM, PATH_TC, PATH_FUSED, PATH_DECODE_TC = 0, 1, 2, 3, 4
-KERNEL_KINDS = ("router", "select", "group", "up", "down", "combine", "gather", "fused")
+KERNEL_KINDS = ("router", "select", "group", "up", "down", "combine", "gather", "fused", "experts")
 
 _DT = {"f32": DT_F32, "bf16": DT_BF16}
 _TORCH_DT = {DT_F32: torch.float32, DT_BF16: torch.bfloat16}

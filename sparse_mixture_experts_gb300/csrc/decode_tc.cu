@@ -7,28 +7,36 @@
 //   out[t] = sum_j w[t][j] (W_down,e_j act(W_gate,e_j x_t, W_up,e_j x_t) + b_e_j)
 //            + sigmoid(w_sh . x_t) W_sh_down (silu(W_sh_gate x_t) * W_sh_up x_t)
 // At decode sizes the time is the HBM stream of the selected experts' weights,
-// so the tensor cores run with the operands swapped: the weight rows are the
+// so the tensor cores run with the operands swapped: weight rows are the
 // M = 128 operand, streamed once by TMA through an 8-stage ring, and all (up to
 // 16) tokens are the N = 16 operand.
 //
-//   kernel 1  router logits (one warp per router row); the last block to
-//             finish selects the top-k of every token, lists the experts that
-//             received tokens ("groups", ascending, then the shared expert) and
-//             writes a weight table wtab[g][t] = routing weight of token t for
-//             group g (0 when t is not routed to it; sigmoid gate for the
-//             shared expert).
-//   kernel 2  gate/up: per group, 64 gate rows + 64 up rows x 16 tokens per
-//             tile, K = H split into S parts when there are few tiles; the last
-//             split to finish sums the partials in split order, applies the
-//             activation and stores h'[g][t][f] = wtab[g][t] * act(gate, up).
-//   kernel 3  down: per tile of 128 output rows, one TMEM accumulator
-//             collects W_down,g h'[g] over all groups (experts in ascending
-//             order, then the shared expert), so the routing-weighted sum
-//             needs no separate combine; groups split in S parts with the same
-//             ordered reduction; the epilogue adds the weighted down biases
-//             and writes out.
-// Kernels 2 and 3 use programmatic dependent launch so their prologues overlap
-// the previous kernel.  All waits are bounded; results are deterministic.
+//   kernel 1  router logits, one CTA per router row (the shared-expert gate
+//             vector is row E); it also resets the work counters of kernel 2.
+//   kernel 2  one persistent CTA per SM.  Every CTA first selects the top-k of
+//             every token from the logits (the same code on the same inputs,
+//             so every CTA gets the same routing) and lists the experts that
+//             received tokens ("groups", ascending, then the shared expert).
+//             Work units, claimed in order from a global counter:
+//               gate/up units: 64 gate + 64 up rows of one group x all tokens,
+//                 K = H (split in S parts when there are fewer tiles than
+//                 CTAs; the last split sums the partials in split order);
+//                 epilogue h'[g][t][f] = w(t, g) * act(gate, up), with w(t, g)
+//                 the routing weight of token t for group g (0 if not routed,
+//                 sigmoid gate for the shared expert); then the group's
+//                 completion counter is raised.
+//               down units: 128 output rows x all tokens, accumulating
+//                 W_down,g h'[g] over a range of groups in one TMEM
+//                 accumulator (so the routing-weighted sum needs no combine);
+//                 the producer waits for each group's counter before loading
+//                 its h' rows; ranges are summed in range order by the last
+//                 one to arrive, which adds the weighted down biases and
+//                 writes out.
+//             All gate/up units are claimed before any down unit, so a waiting
+//             down unit only depends on work that CTAs already hold.
+// The producer hands each claimed unit to the MMA and epilogue roles through a
+// queue of 8 slots; slot i also owns TMEM accumulator i.  All waits are bounded
+// (about a second); results are deterministic.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,11 +51,16 @@ constexpr int DT_THREADS = 192;
 constexpr int DT_A_BYTES = 128 * 64 * 2;        // 16 KB weight tile
 constexpr int DT_B_BYTES = DT_TOK * 64 * 2;     // 2 KB token tile
 constexpr int DT_STAGE_BYTES = DT_A_BYTES + DT_B_BYTES;
-constexpr int DT_ACC = 8;                       // TMEM accumulator buffers (MMA runs ahead of the epilogue)
-constexpr int DT_TMEM_COLS = DT_ACC * 16;       // 16 fp32 columns each
+constexpr int DT_ACC = 8;                       // unit queue slots = TMEM accumulators
+constexpr int DT_TMEM_COLS = DT_ACC * DT_TOK;   // 16 fp32 columns each
 constexpr int DT_XCH_BYTES = 64 * DT_TOK * 4;   // up-row values handed to the gate rows
-constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 512;
+constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
+constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 1024;
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
+constexpr int DT_TICKET_DOWN = 8192;            // offset of the down tiles' tickets
+constexpr int DT_GROUP_DONE = 12288;            // offset of the per-group completion counters
+constexpr int DT_NEXT_UNIT = 16000;             // offset of the work counter
+constexpr int DT_COUNTERS = 16384;              // ints
 
 struct DecMaps {
     CUtensorMap gate, up, sh_gate, sh_up;  // box 64 rows x 64
@@ -57,221 +70,151 @@ struct DecMaps {
 };
 
 struct DecArgs {
-    const RouteMeta *meta;
-    const int *active;
-    const float *wtab;      // [groups_max][16]
-    const int *topk_idx;
-    const float *topk_w;
+    const float *logits;  // [T][R]
+    int *topk_idx;        // outputs for moe_get_routing & co. (written by CTA 0)
+    float *topk_w;
+    float *sh_gate;
+    int *counts;
+    int *active;
+    RouteMeta *meta;
     const float *gate_b, *up_b, *down_b;
-    __nv_bfloat16 *hp;      // [groups_max*16][Fmax]
-    float *partials;        // [units][128][16]
-    int *tickets;           // [max tiles]
+    __nv_bfloat16 *hp;    // [groups_max*16][Fmax]
+    float *partials;      // [units][128][16]
+    int *counters;        // tickets, group completion, work counter
     void *out;
     int *status;
-    int T, K, E, H, F, Fs, Fmax;
+    int T, K, E, H, F, Fs, Fmax, R;
+    int mode, norm;
+    float scale;
     int act, out_bf16;
     float alpha, limit;
     int max_units;
 };
 
 // ---------------------------------------------------------------------------
-// kernel 1: router logits + selection + group tables (T <= 16)
+// kernel 1: router logits (T <= 16), one CTA per router row
 // ---------------------------------------------------------------------------
 struct DecRouteArgs {
     const __nv_bfloat16 *x;
     const __nv_bfloat16 *router_w;
     const float *router_b;
     float *logits;
-    int *topk_idx;
-    float *topk_w;
-    float *sh_gate;
-    int *counts;
-    int *active;
-    float *wtab;
-    RouteMeta *meta;
-    int T, K, E, H, R, Fs;
-    int mode, norm;
-    float scale;
+    int *counters;
+    int T, E, H, R;
+    int n_reset;  // per-group counters to clear
 };
-
-__device__ __forceinline__ bool rt_better(float v, int i, float bv, int bi)
-{
-    return v > bv || (v == bv && i < bi);
-}
 
 __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
 {
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int T = a.T, K = a.K, E = a.E, H = a.H, R = a.R;
-    const int r = blockIdx.x * 8 + warp;
-    if (r < R) {
-        float acc[DT_TOK];
+    const int T = a.T, H = a.H, R = a.R;
+    if (blockIdx.x == 0) {
+        // kernel 2 of the previous forward has finished (stream order)
+        for (int i = threadIdx.x; i < a.n_reset; i += 256) a.counters[DT_GROUP_DONE + i] = 0;
+        if (threadIdx.x == 0) a.counters[DT_NEXT_UNIT] = 0;
+    }
+    __shared__ float s_part[8][DT_TOK];
+    const int r = blockIdx.x;
+    float acc[DT_TOK];
 #pragma unroll
-        for (int t = 0; t < DT_TOK; ++t) acc[t] = 0.0f;
-        const __nv_bfloat16 *w = a.router_w + (size_t)r * H;
-#pragma unroll 4
-        for (int c = lane; c < H / 8; c += 32) {
-            Vec<__nv_bfloat16> wv;
-            wv.load_stream(w + (size_t)c * 8);
-#pragma unroll
-            for (int t = 0; t < DT_TOK; ++t) {
-                if (t < T) {
-                    Vec<__nv_bfloat16> xv;
-                    xv.load(a.x + (size_t)t * H + (size_t)c * 8);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[t] = fmaf(wv.v[q], xv.v[q], acc[t]);
-                }
-            }
-        }
-        const float b = (a.router_b && r < E) ? a.router_b[r] : 0.0f;
+    for (int t = 0; t < DT_TOK; ++t) acc[t] = 0.0f;
+    const __nv_bfloat16 *w = a.router_w + (size_t)r * H;
+    for (int c = threadIdx.x; c < H / 8; c += 256) {
+        Vec<__nv_bfloat16> wv;
+        wv.load_stream(w + (size_t)c * 8);
 #pragma unroll
         for (int t = 0; t < DT_TOK; ++t) {
             if (t < T) {
-                float s = warp_sum(acc[t]);
-                if (lane == 0) a.logits[(size_t)t * R + r] = s + b;
+                Vec<__nv_bfloat16> xv;
+                xv.load(a.x + (size_t)t * H + (size_t)c * 8);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[t] = fmaf(wv.v[q], xv.v[q], acc[t]);
             }
         }
     }
-    __shared__ int s_last;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        s_last = atomicAdd(&a.meta->ticket, 1) == (int)gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-
-    // ---- last block: selection for every token ----
-    __shared__ int s_idx[DT_TOK * 32];
-    __shared__ float s_w[DT_TOK * 32];
-    __shared__ float s_g[DT_TOK];
-    __shared__ int s_cnt[1024];
-    __shared__ int s_act[1024];
-    __shared__ int s_wtot[8];
-    __shared__ int s_nact;
-    for (int t = warp; t < T; t += 8) {
-        const float *l = a.logits + (size_t)t * R;
-        float v[32];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = (lane + 32 * q < E) ? __ldcg(l + lane + 32 * q) : -INFINITY;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) mx = fmaxf(mx, v[q]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        unsigned taken = 0;
-        int sel_i = -1;
-        float sel_v = 0.0f;
-        for (int j = 0; j < K; ++j) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int e = lane + 32 * q;
-                if (e < E && !(taken & (1u << q)) && (bi == 0x7fffffff || rt_better(v[q], e, bv, bi))) {
-                    bv = v[q];
-                    bi = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (oi != 0x7fffffff && (bi == 0x7fffffff || rt_better(ov, oi, bv, bi))) { bv = ov; bi = oi; }
-            }
-            if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            if (lane == j) { sel_i = bi; sel_v = bv; }
-        }
-        float w;
-        if (a.mode == MOE_ROUTER_SOFTMAX_TOPK) {
-            float z = 0.0f;
-#pragma unroll
-            for (int q = 0; q < 32; ++q)
-                if (lane + 32 * q < E) z += __expf(v[q] - mx);
-            z = warp_sum(z);
-            float p = (lane < K) ? __expf(sel_v - mx) / z : 0.0f;
-            float ps = warp_sum(p);
-            w = (a.norm ? p / ps : p) * a.scale;
-        } else {
-            float m0 = __shfl_sync(0xffffffffu, sel_v, 0);
-            float ex = (lane < K) ? __expf(sel_v - m0) : 0.0f;
-            w = ex / warp_sum(ex);
-        }
-        if (lane < K) {
-            s_idx[t * K + lane] = sel_i;
-            s_w[t * K + lane] = w;
-        }
-        if (lane == 0) s_g[t] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-__ldcg(l + E))) : 0.0f;
-    }
-    for (int e = threadIdx.x; e < E; e += 256) s_cnt[e] = 0;
-    __syncthreads();
-    const int P = T * K;
-    for (int p = threadIdx.x; p < P; p += 256) atomicAdd(&s_cnt[s_idx[p]], 1);
-    __syncthreads();
-    {
-        int base = 0;
-        for (int e0 = 0; e0 < E; e0 += 256) {
-            const int e = e0 + threadIdx.x;
-            const bool on = e < E && s_cnt[e] > 0;
-            const unsigned m = __ballot_sync(0xffffffffu, on);
-            if (lane == 0) s_wtot[warp] = __popc(m);
-            __syncthreads();
-            int before = 0, all = 0;
-#pragma unroll
-            for (int w8 = 0; w8 < 8; ++w8) {
-                before += w8 < warp ? s_wtot[w8] : 0;
-                all += s_wtot[w8];
-            }
-            if (on) s_act[base + before + __popc(m & ((1u << lane) - 1u))] = e;
-            base += all;
-            __syncthreads();
-        }
-        if (threadIdx.x == 0) s_nact = base;
-    }
-    __syncthreads();
-    const int n_act = s_nact;
-    for (int p = threadIdx.x; p < P; p += 256) {
-        a.topk_idx[p] = s_idx[p];
-        a.topk_w[p] = s_w[p];
-    }
-    for (int e = threadIdx.x; e < E; e += 256) a.counts[e] = s_cnt[e];
-    for (int g = threadIdx.x; g < n_act; g += 256) a.active[g] = s_act[g];
-    if (a.Fs > 0)
-        for (int t = threadIdx.x; t < T; t += 256) a.sh_gate[t] = s_g[t];
-    const int n_groups = n_act + (a.Fs > 0 ? 1 : 0);
-    for (int q = threadIdx.x; q < n_groups * DT_TOK; q += 256) {
-        const int g = q / DT_TOK, t = q - g * DT_TOK;
-        float w = 0.0f;
+    for (int t = 0; t < DT_TOK; ++t) {
         if (t < T) {
-            if (g < n_act) {
-                const int e = s_act[g];
-                for (int j = 0; j < K; ++j)
-                    if (s_idx[t * K + j] == e) w = s_w[t * K + j];
-            } else {
-                w = s_g[t];
-            }
+            const float sum = warp_sum(acc[t]);
+            if (lane == 0) s_part[warp][t] = sum;
         }
-        a.wtab[q] = w;
     }
-    if (threadIdx.x == 0) {
-        a.meta->n_active = n_act;
-        a.meta->n_pairs = P;
-        a.meta->ticket = 0;
+    __syncthreads();
+    if (threadIdx.x < T) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) sum += s_part[w8][threadIdx.x];
+        const float b = (a.router_b && r < a.E) ? a.router_b[r] : 0.0f;
+        a.logits[(size_t)threadIdx.x * R + r] = sum + b;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// selection for one token by one warp: lane j < k ends with the j-th pick
+// (descending logit, lower index on ties) and its routing weight.  Each lane
+// holds NQ >= ceil(E/32) logits in registers (expert lane + 32 q).
+// ---------------------------------------------------------------------------
+template <int NQ>
+__device__ __forceinline__ void warp_select(const float *l, int E, int K, int mode, int norm, float scale, int lane,
+                                            int &sel_i, float &sel_v, float &w)
+{
+    float v[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) v[q] = (lane + 32 * q < E) ? __ldcg(l + lane + 32 * q) : -INFINITY;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) mx = fmaxf(mx, v[q]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float z = 0.0f;
+    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) z += (lane + 32 * q < E) ? __expf(v[q] - mx) : 0.0f;
+        z = warp_sum(z);
+    }
+    sel_i = -1;
+    sel_v = 0.0f;
+    for (int j = 0; j < K; ++j) {
+        // lane-local best (ascending q: a later q never beats an equal earlier one)
+        float bv = v[0];
+        int bq = 0;
+#pragma unroll
+        for (int q = 1; q < NQ; ++q)
+            if (v[q] > bv) { bv = v[q]; bq = q; }
+        int bi = (bv == -INFINITY) ? 0x7fffffff : lane + 32 * bq;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+        }
+        if ((bi & 31) == lane) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+                if (q == (bi >> 5)) v[q] = -INFINITY;  // taken
+        }
+        if (lane == j) { sel_i = bi; sel_v = bv; }
+    }
+    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
+        const float p = (lane < K) ? __expf(sel_v - mx) / z : 0.0f;
+        const float ps = warp_sum(p);
+        w = (norm ? p / ps : p) * scale;
+    } else {
+        const float m0 = __shfl_sync(0xffffffffu, sel_v, 0);
+        const float ex = (lane < K) ? __expf(sel_v - m0) : 0.0f;
+        w = ex / warp_sum(ex);
     }
 }
 
 // ---------------------------------------------------------------------------
 // schedules (every CTA computes the same ones from the group count)
 // ---------------------------------------------------------------------------
-// Split count S in [1, smax] minimising the busiest CTA's bytes: ceil(tiles*S /
-// G) units of ceil(nkb/S) k-blocks, plus a partial write+read per unit when S >
-// 1; at most max_units units.
+// Split count S in [1, smax] minimising the busiest CTA's bytes when there
+// are fewer tiles than CTAs; no split otherwise (a split costs a partial-sum
+// round trip through global memory).
 __device__ __forceinline__ int choose_splits(int tiles, int nkb, int smax, int G, int max_units)
 {
-    // no split when every CTA already has a tile: a split costs a partial-sum
-    // round trip through global memory per unit
     if (tiles >= G) return 1;
     int best = 1;
     long long best_cost = -1;
@@ -284,38 +227,45 @@ __device__ __forceinline__ int choose_splits(int tiles, int nkb, int smax, int G
     return best;
 }
 
+struct Sched {
+    int n_act, groups;
+    int tiles_routed, up_tiles, nkb, S_up, up_units;  // gate/up
+    int ot, S_dn, dn_units;                          // down
+    int total;
+};
+
+__device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act, int G)
+{
+    Sched s;
+    s.n_act = n_act;
+    s.groups = n_act + (a.Fs > 0 ? 1 : 0);
+    s.tiles_routed = n_act * (a.F / 64);
+    s.up_tiles = s.tiles_routed + a.Fs / 64;
+    s.nkb = a.H / 64;
+    s.S_up = choose_splits(s.up_tiles, s.nkb, max(1, min(16, s.nkb / 2)), G, a.max_units);
+    s.up_units = s.up_tiles * s.S_up;
+    s.ot = (a.H + 127) / 128;
+    s.S_dn = choose_splits(s.ot, s.groups * (a.Fmax / 64), s.groups, G, a.max_units);
+    s.dn_units = s.ot * s.S_dn;
+    s.total = s.up_units + s.dn_units;
+    return s;
+}
+
+// gate/up unit u (< up_units): tile = u / S_up (group-major), split s
 struct UpUnit {
     int g, ft, kb0, kb1, tile, s;
     bool shared;
 };
 
-struct UpSched {
-    int n_act, groups, tiles_routed, tiles, nkb, S, units;
-};
-
-__device__ __forceinline__ UpSched up_sched(const DecArgs &a, int G)
-{
-    UpSched s;
-    s.n_act = a.meta->n_active;
-    s.groups = s.n_act + (a.Fs > 0 ? 1 : 0);
-    s.tiles_routed = s.n_act * (a.F / 64);
-    s.tiles = s.tiles_routed + a.Fs / 64;
-    s.nkb = a.H / 64;
-    const int smax = max(1, min(16, s.nkb / 2));
-    s.S = choose_splits(s.tiles, s.nkb, smax, G, a.max_units);
-    s.units = s.tiles * s.S;
-    return s;
-}
-
-__device__ __forceinline__ UpUnit up_unit(const UpSched &s, int u)
+__device__ __forceinline__ UpUnit up_unit(const Sched &s, int u, int F)
 {
     UpUnit x;
-    x.tile = u / s.S;
-    x.s = u - x.tile * s.S;
-    x.kb0 = (int)((long long)s.nkb * x.s / s.S);
-    x.kb1 = (int)((long long)s.nkb * (x.s + 1) / s.S);
+    x.tile = u / s.S_up;
+    x.s = u - x.tile * s.S_up;
+    x.kb0 = (int)((long long)s.nkb * x.s / s.S_up);
+    x.kb1 = (int)((long long)s.nkb * (x.s + 1) / s.S_up);
+    const int per = F / 64;
     if (x.tile < s.tiles_routed) {
-        const int per = s.tiles_routed / max(s.n_act, 1);
         x.g = x.tile / per;
         x.ft = x.tile - x.g * per;
         x.shared = false;
@@ -327,31 +277,47 @@ __device__ __forceinline__ UpUnit up_unit(const UpSched &s, int u)
     return x;
 }
 
-struct DownSched {
-    int n_act, groups, ot, S, units;
+// down unit d (= u - up_units): split s = d / ot (so early units need early groups), tile ot
+struct DnUnit {
+    int tile, s, g0, g1;
 };
 
-__device__ __forceinline__ DownSched down_sched(const DecArgs &a, int G)
+__device__ __forceinline__ DnUnit dn_unit(const Sched &s, int d)
 {
-    DownSched s;
-    s.n_act = a.meta->n_active;
-    s.groups = s.n_act + (a.Fs > 0 ? 1 : 0);
-    s.ot = (a.H + 127) / 128;
-    // cost model over group splits: each group is F/64 k-blocks
-    const int kb_per_group = a.Fmax / 64;
-    s.S = choose_splits(s.ot, s.groups * kb_per_group, s.groups, G, a.max_units);
-    // choose_splits counts k-blocks; keep whole groups per split
-    s.units = s.ot * s.S;
-    return s;
+    DnUnit x;
+    x.s = d / s.ot;
+    x.tile = d - x.s * s.ot;
+    x.g0 = (int)((long long)s.groups * x.s / s.S_dn);
+    x.g1 = (int)((long long)s.groups * (x.s + 1) / s.S_dn);
+    return x;
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// routing weight of token t for group g (0 when t is not routed to it)
+__device__ __forceinline__ float group_weight(int g, int t, int n_act, int K, const int *s_act, const int *s_idx,
+                                              const float *s_w, const float *s_gsh)
+{
+    if (g == n_act) return s_gsh[t];
+    const int e = s_act[g];
+    float w = 0.0f;
+    for (int j = 0; j < K; ++j)
+        if (s_idx[t * K + j] == e) w = s_w[t * K + j];
+    return w;
 }
 
 // ---------------------------------------------------------------------------
-// kernels 2 and 3: weight-streaming tcgen05 GEMMs
+// kernel 2: selection + gate/up + down, persistent, dynamic work claiming
 // ---------------------------------------------------------------------------
-enum { DEC_UP = 0, DEC_DOWN = 1 };
-
-template <int PH>
-__global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_constant__ DecMaps maps, const DecArgs a)
+__global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid_constant__ DecMaps maps,
+                                                                     const DecArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -359,13 +325,24 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + DT_STAGES * DT_STAGE_BYTES + DT_XCH_BYTES);
     uint64_t *empty = full + DT_STAGES;
     uint64_t *acc_full = empty + DT_STAGES;   // [DT_ACC]
-    uint64_t *acc_empty = acc_full + DT_ACC;  // [DT_ACC]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + DT_ACC);
+    uint64_t *uq_full = acc_full + DT_ACC;    // [DT_ACC] unit handed out
+    uint64_t *uq_empty = uq_full + DT_ACC;    // [DT_ACC] unit finished, slot and accumulator free
+    int *uq = reinterpret_cast<int *>(uq_empty + DT_ACC);  // [DT_ACC]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(uq + DT_ACC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *bcast = reinterpret_cast<int *>(tmem_slot + 2);
+    int *bcast = reinterpret_cast<int *>(tmem_slot + 2);  // [4]
+
+    __shared__ int s_idx[DT_MAX_PAIRS];
+    __shared__ float s_w[DT_MAX_PAIRS];
+    __shared__ float s_gsh[DT_TOK];
+    __shared__ int s_cnt[1024];
+    __shared__ int s_act[DT_MAX_PAIRS];
+    __shared__ int s_wtot[DT_THREADS / 32];
+    __shared__ int s_nact;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
+    const int T = a.T, K = a.K, E = a.E;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < DT_STAGES; ++s) {
@@ -374,7 +351,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
         }
         for (int b = 0; b < DT_ACC; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 128);
+            mbar_init(&uq_full[b], 1);
+            mbar_init(&uq_empty[b], 1);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -385,69 +363,146 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (warp == 0 && lane == 0) {
-        if (PH == DEC_UP) {
-            tmap_prefetch(&maps.gate);
-            tmap_prefetch(&maps.up);
-            tmap_prefetch(&maps.x);
-        } else {
-            tmap_prefetch(&maps.down);
-            tmap_prefetch(&maps.hp);
-        }
+        tmap_prefetch(&maps.gate);
+        tmap_prefetch(&maps.up);
+        tmap_prefetch(&maps.x);
+        tmap_prefetch(&maps.down);
+        tmap_prefetch(&maps.hp);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // the previous kernel's results (routing tables, h') are read from here on
+    // the router's logits (and the reset counters) are read from here on
     pdl_wait();
-    pdl_launch_dependents();
 
-    UpSched us;
-    DownSched ds;
-    int units;
-    if (PH == DEC_UP) { us = up_sched(a, G); units = us.units; }
-    else { ds = down_sched(a, G); units = ds.units; }
+    // ---- routing, the same in every CTA ----
+    for (int t = warp; t < T; t += DT_THREADS / 32) {
+        const float *l = a.logits + (size_t)t * a.R;
+        int sel_i;
+        float sel_v, w;
+        const int nq = (E + 31) / 32;
+        if (nq <= 1) warp_select<1>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
+        else if (nq <= 2) warp_select<2>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
+        else if (nq <= 4) warp_select<4>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
+        else if (nq <= 8) warp_select<8>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
+        else if (nq <= 16) warp_select<16>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
+        else warp_select<32>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
+        if (lane < K) {
+            s_idx[t * K + lane] = sel_i;
+            s_w[t * K + lane] = w;
+        }
+        if (lane == 0) s_gsh[t] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-__ldcg(l + E))) : 0.0f;
+    }
+    for (int e = threadIdx.x; e < E; e += DT_THREADS) s_cnt[e] = 0;
+    __syncthreads();
+    const int P = T * K;
+    for (int p = threadIdx.x; p < P; p += DT_THREADS) atomicAdd(&s_cnt[s_idx[p]], 1);
+    __syncthreads();
+    {
+        int base = 0;
+        for (int e0 = 0; e0 < E; e0 += DT_THREADS) {
+            const int e = e0 + threadIdx.x;
+            const bool on = e < E && s_cnt[e] > 0;
+            const unsigned m = __ballot_sync(0xffffffffu, on);
+            if (lane == 0) s_wtot[warp] = __popc(m);
+            __syncthreads();
+            int before = 0, all = 0;
+#pragma unroll
+            for (int w6 = 0; w6 < DT_THREADS / 32; ++w6) {
+                before += w6 < warp ? s_wtot[w6] : 0;
+                all += s_wtot[w6];
+            }
+            if (on) s_act[base + before + __popc(m & ((1u << lane) - 1u))] = e;
+            base += all;
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) s_nact = base;
+    }
+    __syncthreads();
+    const int n_act = s_nact;
+    if (blockIdx.x == 0) {
+        for (int p = threadIdx.x; p < P; p += DT_THREADS) {
+            a.topk_idx[p] = s_idx[p];
+            a.topk_w[p] = s_w[p];
+        }
+        for (int e = threadIdx.x; e < E; e += DT_THREADS) a.counts[e] = s_cnt[e];
+        for (int g = threadIdx.x; g < n_act; g += DT_THREADS) a.active[g] = s_act[g];
+        if (a.Fs > 0)
+            for (int t = threadIdx.x; t < T; t += DT_THREADS) a.sh_gate[t] = s_gsh[t];
+        if (threadIdx.x == 0) {
+            a.meta->n_active = n_act;
+            a.meta->n_pairs = P;
+        }
+    }
+    const Sched sc = make_sched(a, n_act, G);
+    int *tickets = a.counters;
+    int *group_done = a.counters + DT_GROUP_DONE;
+    int *next_unit = a.counters + DT_NEXT_UNIT;
 
     if (warp == 0) {
-        // ------------------------------ TMA producer ------------------------------
+        // ------------------------------ producer ------------------------------
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t last_phase[DT_STAGES];
             bool used[DT_STAGES];
             for (int s = 0; s < DT_STAGES; ++s) used[s] = false, last_phase[s] = 0;
+            int qi = 0;
+            uint32_t qph = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += G) {
-                int g0, g1;
-                if (PH == DEC_UP) { g0 = 0; g1 = 1; }
-                else {
-                    const int s = u % ds.S;
-                    g0 = (int)((long long)ds.groups * s / ds.S);
-                    g1 = (int)((long long)ds.groups * (s + 1) / ds.S);
+            while (ok) {
+                int u = atomicAdd(next_unit, 1);
+                if (u >= sc.total) u = -1;
+                if (!mbar_wait(&uq_empty[qi], qph ^ 1, abort_flag)) {
+                    record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
+                    *abort_flag = 1;
+                    break;
+                }
+                uq[qi] = u;
+                mbar_arrive(&uq_full[qi]);
+                if (++qi == DT_ACC) qi = 0, qph ^= 1;
+                if (u < 0) break;
+                const bool is_up = u < sc.up_units;
+                int g0 = 0, g1 = 1;
+                DnUnit dn;
+                if (!is_up) {
+                    dn = dn_unit(sc, u - sc.up_units);
+                    g0 = dn.g0;
+                    g1 = dn.g1;
                 }
                 for (int gi = g0; gi < g1 && ok; ++gi) {
-                    int kb0, kb1;
+                    int kb0, kb1, arow, brow;
                     const CUtensorMap *ma, *mb = nullptr;
-                    int arow, arow2 = 0, brow;
-                    if (PH == DEC_UP) {
-                        const UpUnit x = up_unit(us, u);
+                    if (is_up) {
+                        const UpUnit x = up_unit(sc, u, a.F);
                         kb0 = x.kb0; kb1 = x.kb1;
-                        if (x.shared) { ma = &maps.sh_gate; mb = &maps.sh_up; arow = arow2 = x.ft * 64; }
-                        else {
-                            const int e = a.active[x.g];
-                            ma = &maps.gate; mb = &maps.up;
-                            arow = arow2 = e * a.F + x.ft * 64;
-                        }
+                        if (x.shared) { ma = &maps.sh_gate; mb = &maps.sh_up; arow = x.ft * 64; }
+                        else { ma = &maps.gate; mb = &maps.up; arow = s_act[x.g] * a.F + x.ft * 64; }
                         brow = 0;
                     } else {
-                        const int ot = u / ds.S;
-                        const bool shared = gi == ds.n_act;
+                        const bool shared = gi == sc.n_act;
                         const int fd = shared ? a.Fs : a.F;
                         kb0 = 0; kb1 = fd / 64;
-                        if (shared) { ma = &maps.sh_down; arow = ot * 128; }
-                        else { ma = &maps.down; arow = a.active[gi] * a.H + ot * 128; }
+                        if (shared) { ma = &maps.sh_down; arow = dn.tile * 128; }
+                        else { ma = &maps.down; arow = s_act[gi] * a.H + dn.tile * 128; }
                         brow = gi * DT_TOK;
+                        // h'[gi] is complete once every gate/up tile of the group is
+                        const int need = fd / 64;
+                        if (ld_acquire(group_done + gi) < need) {
+                            const unsigned long long t0 = globaltimer();
+                            while (ld_acquire(group_done + gi) < need) {
+                                if (*abort_flag || globaltimer() - t0 > WAIT_LIMIT_NS) {
+                                    record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                                    *abort_flag = 1;
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                        }
+                        fence_proxy_async_global();
+                        if (!ok) break;
                     }
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
@@ -460,9 +515,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
                         uint8_t *sb = sa + DT_A_BYTES;
                         mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
                         const int kc = kb * 64;
-                        if (PH == DEC_UP) {
+                        if (is_up) {
                             tma_load_2d(sa, ma, &full[stage], kc, arow);
-                            tma_load_2d(sa + DT_A_BYTES / 2, mb, &full[stage], kc, arow2);
+                            tma_load_2d(sa + DT_A_BYTES / 2, mb, &full[stage], kc, arow);
                             tma_load_2d(sb, &maps.x, &full[stage], kc, brow);
                         } else {
                             tma_load_2d(sa, ma, &full[stage], kc, arow);
@@ -472,6 +527,14 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
                         last_phase[stage] = phase;
                         if (++stage == DT_STAGES) stage = 0, phase ^= 1;
                     }
+                }
+            }
+            if (*abort_flag) {
+                // let the other roles leave: hand out the end-of-work marker
+                for (int i = 0; i < DT_ACC; ++i) {
+                    uq[qi] = -1;
+                    mbar_arrive(&uq_full[qi]);
+                    if (++qi == DT_ACC) qi = 0, qph ^= 1;
                 }
             }
             volatile int never = 0;
@@ -484,31 +547,30 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
             constexpr uint32_t idesc = idesc_bf16_f32(128, DT_TOK);
             int stage = 0;
             uint32_t phase = 0;
-            int it = 0;
-            bool ok = true;
+            int qi = 0;
+            uint32_t qph = 0;
             int last_acc = -1;
             uint32_t last_acc_phase = 0;
-            for (int u = blockIdx.x; u < units && ok; u += G, ++it) {
-                const int b = it % DT_ACC;
-                const uint32_t acc_phase = (it / DT_ACC) & 1;
-                if (!mbar_wait(&acc_empty[b], acc_phase ^ 1, abort_flag)) {
+            for (;;) {
+                if (!mbar_wait(&uq_full[qi], qph, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
                     *abort_flag = 1;
                     break;
                 }
+                const int u = uq[qi];
+                if (u < 0) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(b * DT_TOK);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(qi * DT_TOK);
                 int nk;
-                if (PH == DEC_UP) {
-                    const UpUnit x = up_unit(us, u);
+                if (u < sc.up_units) {
+                    const UpUnit x = up_unit(sc, u, a.F);
                     nk = x.kb1 - x.kb0;
                 } else {
-                    const int s = u % ds.S;
-                    const int g0 = (int)((long long)ds.groups * s / ds.S);
-                    const int g1 = (int)((long long)ds.groups * (s + 1) / ds.S);
+                    const DnUnit d = dn_unit(sc, u - sc.up_units);
                     nk = 0;
-                    for (int gi = g0; gi < g1; ++gi) nk += (gi == ds.n_act ? a.Fs : a.F) / 64;
+                    for (int gi = d.g0; gi < d.g1; ++gi) nk += (gi == sc.n_act ? a.Fs : a.F) / 64;
                 }
+                bool ok = true;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
@@ -527,9 +589,10 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
                     if (++stage == DT_STAGES) stage = 0, phase ^= 1;
                 }
                 if (!ok) break;
-                mma_commit(&acc_full[b]);
-                last_acc = b;
-                last_acc_phase = acc_phase;
+                mma_commit(&acc_full[qi]);
+                last_acc = qi;
+                last_acc_phase = qph;
+                if (++qi == DT_ACC) qi = 0, qph ^= 1;
             }
             if (*abort_flag && last_acc >= 0) {
                 volatile int never = 0;
@@ -542,54 +605,60 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
         const int r = q * 32 + lane;                // accumulator row = weight row of the tile
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         const int et = threadIdx.x - 64;            // 0..127 within the epilogue group
-        int it = 0;
-        for (int u = blockIdx.x; u < units; u += G, ++it) {
-            const int b = it % DT_ACC;
-            const uint32_t acc_phase = (it / DT_ACC) & 1;
+        int qi = 0;
+        uint32_t qph = 0;
+        for (;;) {
             // one thread waits (bounded) and tells the others, so that all 128
-            // leave together on a timeout and no named barrier below can hang
+            // leave together and no named barrier below can hang
             if (et == 0) {
-                const bool okw = mbar_wait(&acc_full[b], acc_phase, abort_flag);
-                if (!okw) {
+                int go = 1;
+                if (!mbar_wait(&uq_full[qi], qph, abort_flag)) go = 0;
+                else if (uq[qi] < 0) go = 2;
+                else if (!mbar_wait(&acc_full[qi], qph, abort_flag)) go = 0;
+                if (go == 0) {
                     record_error(a.status, DEV_TIMEOUT_ACCUM_BARRIER);
                     *abort_flag = 1;
                 }
-                bcast[1] = okw ? 1 : 0;
+                bcast[1] = go;
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            const bool go = bcast[1] != 0;
+            const int go = bcast[1];
+            const int u = uq[qi];
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (!go) break;
+            if (go != 1) break;
             tc_fence_after();
             uint32_t raw[16];
-            tmem_ld16(tmem_base + lane_addr + (uint32_t)(b * DT_TOK), raw);
+            tmem_ld16(tmem_base + lane_addr + (uint32_t)(qi * DT_TOK), raw);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&acc_empty[b]);
             float v[DT_TOK];
 #pragma unroll
             for (int t = 0; t < DT_TOK; ++t) v[t] = __uint_as_float(raw[t]);
-
-            int tile, S;
-            if (PH == DEC_UP) { const UpUnit x = up_unit(us, u); tile = x.tile; S = us.S; }
-            else { tile = u / ds.S; S = ds.S; }
+            const bool is_up = u < sc.up_units;
+            UpUnit ux;
+            DnUnit dx;
+            int tile, S, tbase;
+            if (is_up) { ux = up_unit(sc, u, a.F); tile = ux.tile; S = sc.S_up; tbase = 0; }
+            else { dx = dn_unit(sc, u - sc.up_units); tile = dx.tile; S = sc.S_dn; tbase = DT_TICKET_DOWN; }
 
             bool finalize = true;
             if (S > 1) {
-                // partial to global, then the last split of the tile reduces in split order
-                float4 *dst = reinterpret_cast<float4 *>(a.partials + ((size_t)u * 128 + r) * DT_TOK);
+                // the partial of this split to global; the last split of the tile
+                // sums all of them in split order
+                const int split = is_up ? ux.s : dx.s;
+                const size_t pbase = (size_t)(is_up ? 0 : a.max_units) + (size_t)tile * S;
+                float4 *dst = reinterpret_cast<float4 *>(a.partials + ((pbase + split) * 128 + r) * DT_TOK);
 #pragma unroll
                 for (int i = 0; i < DT_TOK / 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
                 __threadfence();
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (et == 0) {
-                    const int prev = atomicAdd(&a.tickets[(PH == DEC_UP ? 0 : 8192) + tile], 1);
+                    const int prev = atomicAdd(&tickets[tbase + tile], 1);
                     const int last = prev == S - 1;
-                    if (last) a.tickets[(PH == DEC_UP ? 0 : 8192) + tile] = 0;
-                    *bcast = last;
+                    if (last) tickets[tbase + tile] = 0;
+                    bcast[2] = last;
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-                finalize = *bcast != 0;
+                finalize = bcast[2] != 0;
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (finalize) {
                     __threadfence();
@@ -597,19 +666,16 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
                     for (int t = 0; t < DT_TOK; ++t) v[t] = 0.0f;
                     for (int s = 0; s < S; ++s) {
                         const float4 *src =
-                            reinterpret_cast<const float4 *>(a.partials + ((size_t)(tile * S + s) * 128 + r) * DT_TOK);
+                            reinterpret_cast<const float4 *>(a.partials + ((pbase + s) * 128 + r) * DT_TOK);
 #pragma unroll
                         for (int i = 0; i < DT_TOK / 4; ++i) {
-                            float4 p = __ldcg(src + i);
+                            const float4 p = __ldcg(src + i);
                             v[4 * i] += p.x; v[4 * i + 1] += p.y; v[4 * i + 2] += p.z; v[4 * i + 3] += p.w;
                         }
                     }
                 }
             }
-            if (!finalize) continue;
-
-            if (PH == DEC_UP) {
-                const UpUnit x = up_unit(us, u);
+            if (finalize && is_up) {
                 // rows 64..127 are the up projections of rows 0..63
                 if (r >= 64) {
 #pragma unroll
@@ -617,39 +683,49 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (r < 64) {
-                    const int f = x.ft * 64 + r;
-                    const int e = x.shared ? -1 : a.active[x.g];
-                    const float bg = (!x.shared && a.gate_b) ? a.gate_b[(size_t)e * a.F + f] : 0.0f;
-                    const float bu = (!x.shared && a.up_b) ? a.up_b[(size_t)e * a.F + f] : 0.0f;
-                    const float *wt = a.wtab + (size_t)x.g * DT_TOK;
+                    const int f = ux.ft * 64 + r;
+                    const int e = ux.shared ? -1 : s_act[ux.g];
+                    const float bg = (!ux.shared && a.gate_b) ? a.gate_b[(size_t)e * a.F + f] : 0.0f;
+                    const float bu = (!ux.shared && a.up_b) ? a.up_b[(size_t)e * a.F + f] : 0.0f;
 #pragma unroll
                     for (int t = 0; t < DT_TOK; ++t) {
-                        const float gv = v[t] + bg, uv = xch[r * DT_TOK + t] + bu;
-                        float hval = (x.shared || a.act == MOE_ACT_SWIGLU)
-                                         ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
-                                         : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
-                        hval *= __ldcg(wt + t);
-                        a.hp[((size_t)x.g * DT_TOK + t) * a.Fmax + f] = __float2bfloat16_rn(hval);
+                        float hval = 0.0f;
+                        if (t < T) {
+                            const float gv = v[t] + bg, uv = xch[r * DT_TOK + t] + bu;
+                            const float wt = group_weight(ux.g, t, sc.n_act, K, s_act, s_idx, s_w, s_gsh);
+                            hval = (ux.shared || a.act == MOE_ACT_SWIGLU)
+                                       ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
+                                       : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
+                            hval *= wt;
+                        }
+                        a.hp[((size_t)ux.g * DT_TOK + t) * a.Fmax + f] = __float2bfloat16_rn(hval);
                     }
                 }
+                // publish: h' of this tile is written (generic proxy) and will be
+                // read by TMA (async proxy) in other CTAs
+                fence_proxy_async_global();
+                __threadfence();
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-            } else {
-                const int row = tile * 128 + r;
+                if (et == 0) atomicAdd(&group_done[ux.g], 1);
+            } else if (finalize) {
+                const int row = dx.tile * 128 + r;
                 if (row < a.H) {
-                    for (int t = 0; t < a.T; ++t) {
+                    for (int t = 0; t < T; ++t) {
                         float o = v[t];
-                        if (a.down_b) {
-                            for (int j = 0; j < a.K; ++j) {
-                                const int p = t * a.K + j;
-                                o += __ldcg(a.topk_w + p) * a.down_b[(size_t)__ldcg(a.topk_idx + p) * a.H + row];
-                            }
-                        }
+                        if (a.down_b)
+                            for (int j = 0; j < K; ++j)
+                                o += s_w[t * K + j] * a.down_b[(size_t)s_idx[t * K + j] * a.H + row];
                         const size_t oi = (size_t)t * a.H + row;
                         if (a.out_bf16) reinterpret_cast<__nv_bfloat16 *>(a.out)[oi] = __float2bfloat16_rn(o);
                         else reinterpret_cast<float *>(a.out)[oi] = o;
                     }
                 }
             }
+            // the accumulator and the queue slot are free again
+            tc_fence_before();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (et == 0) mbar_arrive(&uq_empty[qi]);
+            if (++qi == DT_ACC) qi = 0, qph ^= 1;
         }
     }
 
@@ -667,10 +743,10 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_tc_kernel(const __grid_cons
 // ---------------------------------------------------------------------------
 static bool dec_encode(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows)
 {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
     static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     if (!enc) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
             q != cudaDriverEntryPointSuccess)
             return false;
@@ -690,7 +766,7 @@ bool dectc_supported(const Layer &L, int T)
     return L.dectc != nullptr && T >= 1 && T <= DT_TOK;
 }
 
-int dectc_groups_max(const Layer &L)
+static int dectc_groups_max(const Layer &L)
 {
     const int routed = L.E < DT_TOK * L.K ? L.E : DT_TOK * L.K;
     return routed + (L.Fs > 0 ? 1 : 0);
@@ -699,14 +775,15 @@ int dectc_groups_max(const Layer &L)
 size_t dectc_workspace(const Layer &L, size_t &hp_bytes, size_t &part_bytes, size_t &tab_bytes, size_t &ticket_bytes)
 {
     hp_bytes = (size_t)dectc_groups_max(L) * DT_TOK * L.Fmax * 2;
-    part_bytes = (size_t)L.num_sms * DT_UNITS_PER_CTA * 128 * DT_TOK * 4;
-    tab_bytes = (size_t)dectc_groups_max(L) * DT_TOK * 4;
-    ticket_bytes = 16384 * 4;
+    part_bytes = (size_t)L.num_sms * DT_UNITS_PER_CTA * 128 * DT_TOK * 4 * 2;  // gate/up and down partials
+    tab_bytes = 16;
+    ticket_bytes = (size_t)DT_COUNTERS * 4;
     return hp_bytes + part_bytes + tab_bytes + ticket_bytes;
 }
 
 int dectc_prepare(Layer &L)
 {
+    if (dectc_groups_max(L) > DT_NEXT_UNIT - DT_GROUP_DONE) return -1;
     DecMaps *m = new (std::nothrow) DecMaps();
     if (!m) return -1;
     bool ok = dec_encode(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
@@ -722,10 +799,8 @@ int dectc_prepare(Layer &L)
         m->sh_down = m->down;
     }
     if (ok)
-        ok = cudaFuncSetAttribute(dec_tc_kernel<DEC_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DT_SMEM) ==
-                 cudaSuccess &&
-             cudaFuncSetAttribute(dec_tc_kernel<DEC_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)DT_SMEM) == cudaSuccess;
+        ok = cudaFuncSetAttribute(dec_experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DT_SMEM) ==
+             cudaSuccess;
     if (!ok) { delete m; return -1; }
     L.dectc = m;
     return 0;
@@ -737,29 +812,7 @@ void dectc_release(Layer &L)
     L.dectc = nullptr;
 }
 
-static DecArgs make_dec_args(const Layer &L, int T, void *out)
-{
-    DecArgs a;
-    a.meta = L.meta;
-    a.active = L.active;
-    a.wtab = L.dec_wtab;
-    a.topk_idx = L.topk_idx;
-    a.topk_w = L.topk_w;
-    a.gate_b = L.gate_b; a.up_b = L.up_b; a.down_b = L.down_b;
-    a.hp = (__nv_bfloat16 *)L.dec_hp;
-    a.partials = L.dec_partials;
-    a.tickets = L.dec_tickets;
-    a.out = out;
-    a.status = L.status;
-    a.T = T; a.K = L.K; a.E = L.E; a.H = L.H; a.F = L.F; a.Fs = L.Fs; a.Fmax = L.Fmax;
-    a.act = L.cfg.act;
-    a.out_bf16 = L.cfg.out_dtype == MOE_DT_BF16;
-    a.alpha = L.cfg.act_alpha; a.limit = L.cfg.act_limit;
-    a.max_units = L.num_sms * DT_UNITS_PER_CTA;
-    return a;
-}
-
-// which: 0 = router + selection, 1 = gate/up, 2 = down
+// which: 0 = router logits, 1 = selection + experts (writes out)
 int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s)
 {
     if (which == 0) {
@@ -767,16 +820,31 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
         r.x = (const __nv_bfloat16 *)x;
         r.router_w = (const __nv_bfloat16 *)L.router_w;
         r.router_b = L.router_b;
-        r.logits = L.logits; r.topk_idx = L.topk_idx; r.topk_w = L.topk_w; r.sh_gate = L.sh_gate;
-        r.counts = L.counts; r.active = L.active; r.wtab = L.dec_wtab; r.meta = L.meta;
-        r.T = T; r.K = L.K; r.E = L.E; r.H = L.H; r.R = L.R; r.Fs = L.Fs;
-        r.mode = L.cfg.router_mode; r.norm = L.cfg.norm_topk_prob; r.scale = L.cfg.weights_scale;
-        dec_route_kernel<<<(L.R + 7) / 8, 256, 0, s>>>(r);
+        r.logits = L.logits;
+        r.counters = L.dec_tickets;
+        r.T = T; r.E = L.E; r.H = L.H; r.R = L.R;
+        r.n_reset = dectc_groups_max(L);
+        dec_route_kernel<<<L.R, 256, 0, s>>>(r);
         return 1;
     }
     DecMaps m = *L.dectc;
-    if (which == 1 && !dec_encode(&m.x, x, L.H, (uint64_t)T, DT_TOK)) return -1;
-    DecArgs a = make_dec_args(L, T, out);
+    if (!dec_encode(&m.x, x, L.H, (uint64_t)T, DT_TOK)) return -1;
+    DecArgs a;
+    a.logits = L.logits;
+    a.topk_idx = L.topk_idx; a.topk_w = L.topk_w; a.sh_gate = L.sh_gate; a.counts = L.counts; a.active = L.active;
+    a.meta = L.meta;
+    a.gate_b = L.gate_b; a.up_b = L.up_b; a.down_b = L.down_b;
+    a.hp = (__nv_bfloat16 *)L.dec_hp;
+    a.partials = L.dec_partials;
+    a.counters = L.dec_tickets;
+    a.out = out;
+    a.status = L.status;
+    a.T = T; a.K = L.K; a.E = L.E; a.H = L.H; a.F = L.F; a.Fs = L.Fs; a.Fmax = L.Fmax; a.R = L.R;
+    a.mode = L.cfg.router_mode; a.norm = L.cfg.norm_topk_prob; a.scale = L.cfg.weights_scale;
+    a.act = L.cfg.act;
+    a.out_bf16 = L.cfg.out_dtype == MOE_DT_BF16;
+    a.alpha = L.cfg.act_alpha; a.limit = L.cfg.act_limit;
+    a.max_units = L.num_sms * DT_UNITS_PER_CTA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.num_sms);
     cfg.blockDim = dim3(DT_THREADS);
@@ -787,9 +855,7 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = which == 1 ? cudaLaunchKernelEx(&cfg, dec_tc_kernel<DEC_UP>, m, a)
-                               : cudaLaunchKernelEx(&cfg, dec_tc_kernel<DEC_DOWN>, m, a);
-    return e == cudaSuccess ? 1 : -1;
+    return cudaLaunchKernelEx(&cfg, dec_experts_kernel, m, a) == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace moe

@@ -322,8 +322,7 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
     if (route == Route::DecodeTC) {
         int bad = 0;
         run(MOE_KERNEL_ROUTER, [&] { int r = launch_dectc(L, x, T, out, 0, s); bad |= r < 0; return r < 0 ? 0 : r; });
-        run(MOE_KERNEL_UP, [&] { int r = launch_dectc(L, x, T, out, 1, s); bad |= r < 0; return r < 0 ? 0 : r; });
-        run(MOE_KERNEL_DOWN, [&] { int r = launch_dectc(L, x, T, out, 2, s); bad |= r < 0; return r < 0 ? 0 : r; });
+        run(MOE_KERNEL_EXPERTS, [&] { int r = launch_dectc(L, x, T, out, 1, s); bad |= r < 0; return r < 0 ? 0 : r; });
         if (rec) ++L.timing_recorded;
         cudaError_t e = cudaGetLastError();
         if (bad || e != cudaSuccess) return cuda_fail(e != cudaSuccess ? e : cudaErrorLaunchFailure, "decode launch");

@@ -202,7 +202,7 @@ bool dectc_supported(const Layer &L, int T);
 size_t dectc_workspace(const Layer &L, size_t &hp_bytes, size_t &part_bytes, size_t &tab_bytes, size_t &ticket_bytes);
 int dectc_prepare(Layer &L);
 void dectc_release(Layer &L);
-// which: 0 = router + selection, 1 = gate/up, 2 = down (writes out)
+// which: 0 = router logits, 1 = selection + gate/up + down (writes out)
 int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s);
 
 // tensor-core path (expert_tc.cu)
