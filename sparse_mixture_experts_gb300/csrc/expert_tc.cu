@@ -49,6 +49,7 @@ struct TensorMaps {
     CUtensorMap sh_gate;  // [Fs][H]
     CUtensorMap sh_up;    // [Fs][H]
     CUtensorMap sh_down;  // [H][Fs]
+    CUtensorMap router;   // [R][H], box 128 rows
 };
 
 // A operand, then the B operand(s) of the routed experts and of the shared
@@ -61,7 +62,7 @@ struct TcMaps {
 // ---------------------------------------------------------------------------
 // the grouped GEMM kernel
 // ---------------------------------------------------------------------------
-enum { EPI_UP = 0, EPI_DOWN = 1 };
+enum { EPI_UP = 0, EPI_DOWN = 1, EPI_ROUTER = 2 };
 
 struct TcArgs {
     const TileDesc *tiles;
@@ -71,6 +72,9 @@ struct TcArgs {
     const float *topk_w, *sh_gate;
     __nv_bfloat16 *h;   // EPI_UP output
     float *ys;          // EPI_DOWN output
+    float *logits;      // EPI_ROUTER output [T][R]
+    const float *router_b;
+    int R, router_nt;   // router rows, router N tiles
     int *status;
     int T, K, E, H, F, Fs, Fmax, Tmax;
     int act;
@@ -88,6 +92,17 @@ struct TileInfo {
 template <int EPI>
 __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti)
 {
+    if (EPI == EPI_ROUTER) {
+        // dense: every 128-token tile against every 128-row tile of the router
+        ti.g = 0;
+        ti.m0 = (t / a.router_nt) * TC_BM;
+        ti.n0 = (t % a.router_nt) * 128;
+        ti.shared = false;
+        ti.rows = a.T;
+        ti.a_row0 = 0;
+        ti.nk = a.H / TC_BK;
+        return true;
+    }
     const TileDesc d = a.tiles[t];
     ti.g = d.g;
     ti.m0 = d.m0;
@@ -114,7 +129,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = EPI == EPI_UP ? a.meta->n_up_tiles : a.meta->n_down_tiles;
+    const int n_tiles = EPI == EPI_ROUTER ? ((a.T + TC_BM - 1) / TC_BM) * a.router_nt
+                                          : (EPI == EPI_UP ? a.meta->n_up_tiles : a.meta->n_down_tiles);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
@@ -257,7 +273,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const uint32_t tbase = tmem_base + lane_addr + (uint32_t)(b * 128);
             const int j = ti.m0 + r;              // row within the group
             const bool valid = j < ti.rows;
-            if (EPI == EPI_UP) {
+            if (EPI == EPI_ROUTER) {
+                // logits[t][n] (+ router bias), fp32; R need not be a multiple of 4
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tbase + c, v);
+                    tmem_ld_wait();
+                    if (valid) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int n = ti.n0 + c + i;
+                            if (n < a.R) {
+                                const float b = (a.router_b && n < a.E) ? a.router_b[n] : 0.0f;
+                                a.logits[(size_t)j * a.R + n] = __uint_as_float(v[i]) + b;
+                            }
+                        }
+                    }
+                }
+            } else if (EPI == EPI_UP) {
                 const int fd = ti.shared ? a.Fs : a.F;
                 (void)fd;
                 const float *bg = (!ti.shared && a.gate_b) ? a.gate_b + (size_t)ti.g * a.F + ti.n0 : nullptr;
@@ -431,7 +465,8 @@ int tc_prepare(Layer &L)
     bool ok = encode_2d(&m->xp, L.xp, L.H, rows_all, TC_BM) && encode_2d(&m->h, L.h, L.Fmax, rows_all, TC_BM) &&
               encode_2d(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
               encode_2d(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, 64) &&
-              encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, 128);
+              encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, 128) &&
+              encode_2d(&m->router, L.router_w, L.H, (uint64_t)L.R, 128);
     if (ok && L.Fs) {
         ok = encode_2d(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, 64) && encode_2d(&m->sh_up, L.sh_up_w, L.H, L.Fs, 64) &&
              encode_2d(&m->sh_down, L.sh_down_w, L.Fs, L.H, 128);
@@ -444,6 +479,8 @@ int tc_prepare(Layer &L)
     if (cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)TC_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TC_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_ROUTER, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)TC_SMEM) != cudaSuccess) {
         delete m;
         return -1;
@@ -471,6 +508,7 @@ static TcArgs make_tc_args(const Layer &L, int T)
     a.T = T; a.K = L.K; a.E = L.E; a.H = L.H; a.F = L.F; a.Fs = L.Fs; a.Fmax = L.Fmax; a.Tmax = L.Tmax;
     a.act = L.cfg.act;
     a.alpha = L.cfg.act_alpha; a.limit = L.cfg.act_limit;
+    a.logits = nullptr; a.router_b = nullptr; a.R = L.R; a.router_nt = 1;
     return a;
 }
 
@@ -494,6 +532,26 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
         a.tiles = L.down_tiles;
         tc_gemm_kernel<EPI_DOWN, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(md, a);
     }
+    return 1;
+}
+
+// router logits on the tensor cores: logits[T][R] = x Wr^T (+ b); the x
+// tensor map is encoded for this forward's x pointer
+int launch_tc_router(const Layer &L, const void *x, int T, cudaStream_t s)
+{
+    const TensorMaps &m = *L.tmaps;
+    TcMaps mr{};
+    if (!encode_2d(&mr.a, x, L.H, (uint64_t)T, TC_BM)) return -1;
+    mr.b0 = mr.b1 = mr.sb0 = mr.sb1 = m.router;
+    TcArgs a = make_tc_args(L, T);
+    a.tiles = nullptr;
+    a.logits = L.logits;
+    a.router_b = L.router_b;
+    a.R = L.R;
+    a.router_nt = (L.R + 127) / 128;
+    const int tiles = ((T + TC_BM - 1) / TC_BM) * a.router_nt;
+    const int grid = tiles < L.num_sms ? tiles : L.num_sms;
+    tc_gemm_kernel<EPI_ROUTER, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(mr, a);
     return 1;
 }
 

@@ -344,7 +344,14 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
         L.last_launches = n;
         return MOE_OK;
     }
-    run(MOE_KERNEL_ROUTER, [&] { return launch_router(L, x, T, s); });
+    int router_bad = 0;
+    run(MOE_KERNEL_ROUTER, [&] {
+        if (!tc) return launch_router(L, x, T, s);
+        const int r = launch_tc_router(L, x, T, s);
+        router_bad = r < 0;
+        return r < 0 ? 0 : r;
+    });
+    if (router_bad) return fail(MOE_ERR_CUDA, "tensor map for x could not be encoded");
     run(MOE_KERNEL_SELECT, [&] { return launch_select(L, T, s); });
     run(MOE_KERNEL_GROUP, [&] { return launch_group(L, T, tc, s); });
     if (tc) {

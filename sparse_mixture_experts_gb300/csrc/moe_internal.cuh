@@ -212,6 +212,7 @@ void tc_release(Layer &L);
 // which: 0 = gather token rows, 1 = gate/up GEMM + activation, 2 = down GEMM + weight
 int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStream_t s);
 void tc_tile_caps(const Layer &L, int &max_up, int &max_down);
+int launch_tc_router(const Layer &L, const void *x, int T, cudaStream_t s);
 
 constexpr int MAX_LAUNCHES_PER_FORWARD = 8;
 
