@@ -151,63 +151,6 @@ __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
 }
 
 // ---------------------------------------------------------------------------
-// selection for one token by one warp: lane j < k ends with the j-th pick
-// (descending logit, lower index on ties) and its routing weight.  Each lane
-// holds NQ >= ceil(E/32) logits in registers (expert lane + 32 q).
-// ---------------------------------------------------------------------------
-template <int NQ>
-__device__ __forceinline__ void warp_select(const float *l, int E, int K, int mode, int norm, float scale, int lane,
-                                            int &sel_i, float &sel_v, float &w)
-{
-    float v[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) v[q] = (lane + 32 * q < E) ? __ldcg(l + lane + 32 * q) : -INFINITY;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) mx = fmaxf(mx, v[q]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float z = 0.0f;
-    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) z += (lane + 32 * q < E) ? __expf(v[q] - mx) : 0.0f;
-        z = warp_sum(z);
-    }
-    sel_i = -1;
-    sel_v = 0.0f;
-    for (int j = 0; j < K; ++j) {
-        // lane-local best (ascending q: a later q never beats an equal earlier one)
-        float bv = v[0];
-        int bq = 0;
-#pragma unroll
-        for (int q = 1; q < NQ; ++q)
-            if (v[q] > bv) { bv = v[q]; bq = q; }
-        int bi = (bv == -INFINITY) ? 0x7fffffff : lane + 32 * bq;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) {
-#pragma unroll
-            for (int q = 0; q < NQ; ++q)
-                if (q == (bi >> 5)) v[q] = -INFINITY;  // taken
-        }
-        if (lane == j) { sel_i = bi; sel_v = bv; }
-    }
-    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-        const float p = (lane < K) ? __expf(sel_v - mx) / z : 0.0f;
-        const float ps = warp_sum(p);
-        w = (norm ? p / ps : p) * scale;
-    } else {
-        const float m0 = __shfl_sync(0xffffffffu, sel_v, 0);
-        const float ex = (lane < K) ? __expf(sel_v - m0) : 0.0f;
-        w = ex / warp_sum(ex);
-    }
-}
-
-// ---------------------------------------------------------------------------
 // schedules (every CTA computes the same ones from the group count)
 // ---------------------------------------------------------------------------
 // Split count S in [1, smax] minimising the busiest CTA's bytes when there
@@ -382,13 +325,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
         const float *l = a.logits + (size_t)t * a.R;
         int sel_i;
         float sel_v, w;
-        const int nq = (E + 31) / 32;
-        if (nq <= 1) warp_select<1>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
-        else if (nq <= 2) warp_select<2>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
-        else if (nq <= 4) warp_select<4>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
-        else if (nq <= 8) warp_select<8>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
-        else if (nq <= 16) warp_select<16>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
-        else warp_select<32>(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
+        warp_select_any(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
         if (lane < K) {
             s_idx[t * K + lane] = sel_i;
             s_w[t * K + lane] = w;

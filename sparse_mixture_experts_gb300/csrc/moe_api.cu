@@ -237,7 +237,7 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     if ((st = dev_alloc_t(L, &L.active, E))) return st;
     if ((st = dev_alloc_t(L, &L.meta, 1))) return st;
     if ((st = dev_alloc(L, &L.h, (T * K + T) * (size_t)L.Fmax * eb))) return st;
-    if ((st = dev_alloc_t(L, &L.ys, T * (K + 1) * H))) return st;
+    if ((st = dev_alloc(L, &L.ys, T * (K + 1) * H * eb))) return st;
     if ((st = dev_alloc_t(L, &L.status, 1))) return st;
     if ((st = dev_alloc_t(L, &L.gbar, 2))) return st;
     if ((st = dev_alloc(L, &L.x_stage, T * H * eb))) return st;

@@ -91,11 +91,6 @@ int launch_router(const Layer &L, const void *x, int T, cudaStream_t s)
 // ---------------------------------------------------------------------------
 // selection: one warp per token
 // ---------------------------------------------------------------------------
-// (value, index) ordering: larger value first, lower index on equal values
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi)
-{
-    return v > bv || (v == bv && i < bi);
-}
 
 __global__ void __launch_bounds__(256) select_kernel(const float *__restrict__ logits, int T, int E, int R, int K,
                                                      int mode, int norm, float scale, int has_shared,
@@ -106,51 +101,9 @@ __global__ void __launch_bounds__(256) select_kernel(const float *__restrict__ l
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
     const float *l = logits + (size_t)t * R;
-
-    // row maximum (used by the softmax form) and the k best, in order
-    float mx = -INFINITY;
-    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-
-    int sel_i = -1;     // lane j < K holds the j-th selection
-    float sel_v = 0.0f;
-    unsigned taken = 0; // bit q: expert lane + 32 q already selected (E <= 1024)
-    for (int j = 0; j < K; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        int q = 0;
-        for (int e = lane; e < E; e += 32, ++q) {
-            if (taken & (1u << q)) continue;
-            float v = l[e];
-            if (bi == 0x7fffffff || better(v, e, bv, bi)) { bv = v; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) { sel_i = bi; sel_v = bv; }
-    }
-
-    float w = 0.0f;
-    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-        float z = 0.0f;
-        for (int e = lane; e < E; e += 32) z += __expf(l[e] - mx);
-        z = warp_sum(z);
-        float p = (lane < K) ? __expf(sel_v - mx) / z : 0.0f;
-        float ps = warp_sum(p);
-        w = norm ? p / ps : p;
-        w *= scale;
-    } else {
-        // softmax over the k selected logits; lane 0 holds the largest
-        float m0 = __shfl_sync(0xffffffffu, sel_v, 0);
-        float ex = (lane < K) ? __expf(sel_v - m0) : 0.0f;
-        float zs = warp_sum(ex);
-        w = ex / zs;
-    }
+    int sel_i;
+    float sel_v, w;
+    warp_select_any(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
     if (lane < K) {
         topk_idx[(size_t)t * K + lane] = sel_i;
         topk_w[(size_t)t * K + lane] = w;
@@ -216,16 +169,31 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
     if (threadIdx.x == 0) s_base = 0;
     __syncthreads();
 
-    // pairs routed to expert e, in ascending token order (stable compaction)
-    for (int t0 = 0; t0 < a.T; t0 += GT) {
-        const int t = t0 + threadIdx.x;
-        int slot = -1;
-        if (t < a.T)
-            for (int q = 0; q < a.K; ++q)
-                if (__ldg(&a.topk_idx[(size_t)t * a.K + q]) == e) slot = q;
+    // pairs routed to expert e, in ascending token order (stable compaction);
+    // each thread looks at TPT consecutive tokens per pass
+    constexpr int TPT = 8;
+    for (int t0 = 0; t0 < a.T; t0 += GT * TPT) {
+        int slots[TPT];
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            const int t = t0 + threadIdx.x * TPT + i;
+            int slot = -1;
+            if (t < a.T)
+                for (int q = 0; q < a.K; ++q)
+                    if (__ldg(&a.topk_idx[(size_t)t * a.K + q]) == e) slot = q;
+            slots[i] = slot;
+            cnt += slot >= 0;
+        }
         int total;
-        int pos = block_exclusive_scan(slot >= 0 ? 1 : 0, &total);
-        if (slot >= 0) a.expert_rows[(size_t)e * a.Tmax + s_base + pos] = t * a.K + slot;
+        int pos = block_exclusive_scan(cnt, &total);
+#pragma unroll
+        for (int i = 0; i < TPT; ++i) {
+            if (slots[i] >= 0) {
+                a.expert_rows[(size_t)e * a.Tmax + s_base + pos] = (t0 + threadIdx.x * TPT + i) * a.K + slots[i];
+                ++pos;
+            }
+        }
         __syncthreads();
         if (threadIdx.x == 0) s_base += total;
         __syncthreads();
