@@ -46,7 +46,7 @@
 namespace moe {
 
 constexpr int DT_TOK = 16;                      // N: token columns
-constexpr int DT_STAGES = 11;
+constexpr int DT_STAGES = 8;
 constexpr int DT_THREADS = 192;
 constexpr int DT_A_BYTES = 128 * 64 * 2;        // 16 KB weight tile
 constexpr int DT_B_BYTES = DT_TOK * 64 * 2;     // 2 KB token tile

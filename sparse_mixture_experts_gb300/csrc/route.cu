@@ -169,22 +169,18 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
     if (threadIdx.x == 0) s_base = 0;
     __syncthreads();
 
-    // pairs routed to expert e, in ascending pair (= token) order: each thread
-    // owns a contiguous run of pairs, counts its matches, one block scan gives
-    // its first position, a second pass writes them (stable compaction)
-    {
-        const int P = a.T * a.K;
-        const int per = (P + GT - 1) / GT;
-        const int pb = min(P, threadIdx.x * per), pe = min(P, pb + per);
-        int cnt = 0;
-#pragma unroll 4
-        for (int p = pb; p < pe; ++p) cnt += __ldg(&a.topk_idx[p]) == e;
+    // pairs routed to expert e, in ascending token order (stable compaction)
+    for (int t0 = 0; t0 < a.T; t0 += GT) {
+        const int t = t0 + threadIdx.x;
+        int slot = -1;
+        if (t < a.T)
+            for (int q = 0; q < a.K; ++q)
+                if (__ldg(&a.topk_idx[(size_t)t * a.K + q]) == e) slot = q;
         int total;
-        int pos = block_exclusive_scan(cnt, &total);
-        if (cnt > 0)
-            for (int p = pb; p < pe; ++p)
-                if (__ldg(&a.topk_idx[p]) == e) a.expert_rows[(size_t)e * a.Tmax + pos++] = p;
-        if (threadIdx.x == 0) s_base = total;
+        int pos = block_exclusive_scan(slot >= 0 ? 1 : 0, &total);
+        if (slot >= 0) a.expert_rows[(size_t)e * a.Tmax + s_base + pos] = t * a.K + slot;
+        __syncthreads();
+        if (threadIdx.x == 0) s_base += total;
         __syncthreads();
     }
     if (threadIdx.x == 0) {
