@@ -188,7 +188,8 @@ __device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act, int G)
     s.S_up = choose_splits(s.up_tiles, s.nkb, max(1, min(16, s.nkb / 2)), G, a.max_units);
     s.up_units = s.up_tiles * s.S_up;
     s.ot = (a.H + 127) / 128;
-    s.S_dn = choose_splits(s.ot, s.groups * (a.Fmax / 64), s.groups, G, a.max_units);
+    // about one down unit per CTA: fewer, longer units mean fewer partial sums
+    s.S_dn = max(1, min(s.groups, (G + s.ot - 1) / s.ot));
     s.dn_units = s.ot * s.S_dn;
     s.total = s.up_units + s.dn_units;
     return s;
@@ -282,6 +283,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     __shared__ int s_act[DT_MAX_PAIRS];
     __shared__ int s_wtot[DT_THREADS / 32];
     __shared__ int s_nact;
+    __shared__ float s_wt[DT_TOK];  // routing weight per token of the current gate/up unit
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
@@ -321,16 +323,29 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     pdl_wait();
 
     // ---- routing, the same in every CTA ----
-    for (int t = warp; t < T; t += DT_THREADS / 32) {
+    // two tokens per warp at a time, so their load latencies and dependent
+    // compare chains overlap
+    constexpr int NW = DT_THREADS / 32;
+    for (int t = warp; t < T; t += 2 * NW) {
+        const int t2 = t + NW;
+        const bool two = t2 < T;
         const float *l = a.logits + (size_t)t * a.R;
-        int sel_i;
-        float sel_v, w;
-        warp_select_any(l, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
+        const float *l2 = a.logits + (size_t)(two ? t2 : t) * a.R;
+        int sel_i[2];
+        float sel_v[2], w[2];
+        warp_select2_any(l, l2, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
         if (lane < K) {
-            s_idx[t * K + lane] = sel_i;
-            s_w[t * K + lane] = w;
+            s_idx[t * K + lane] = sel_i[0];
+            s_w[t * K + lane] = w[0];
+            if (two) {
+                s_idx[t2 * K + lane] = sel_i[1];
+                s_w[t2 * K + lane] = w[1];
+            }
         }
-        if (lane == 0) s_gsh[t] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-__ldcg(l + E))) : 0.0f;
+        if (lane == 0) {
+            s_gsh[t] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-__ldcg(l + E))) : 0.0f;
+            if (two) s_gsh[t2] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-__ldcg(l2 + E))) : 0.0f;
+        }
     }
     for (int e = threadIdx.x; e < E; e += DT_THREADS) s_cnt[e] = 0;
     __syncthreads();
@@ -586,19 +601,23 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 float4 *dst = reinterpret_cast<float4 *>(a.partials + ((pbase + split) * 128 + r) * DT_TOK);
 #pragma unroll
                 for (int i = 0; i < DT_TOK / 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                __threadfence();
+                // the named barrier orders the group's stores; one thread fences
+                // (cumulative, device scope) and takes the ticket
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (et == 0) {
+                    __threadfence();
                     const int prev = atomicAdd(&tickets[tbase + tile], 1);
                     const int last = prev == S - 1;
-                    if (last) tickets[tbase + tile] = 0;
+                    if (last) {
+                        tickets[tbase + tile] = 0;
+                        __threadfence();  // the other splits' partials are read below
+                    }
                     bcast[2] = last;
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 finalize = bcast[2] != 0;
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (finalize) {
-                    __threadfence();
 #pragma unroll
                     for (int t = 0; t < DT_TOK; ++t) v[t] = 0.0f;
                     for (int s = 0; s < S; ++s) {
@@ -613,11 +632,14 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 }
             }
             if (finalize && is_up) {
-                // rows 64..127 are the up projections of rows 0..63
+                // rows 64..127 are the up projections of rows 0..63; 16 threads
+                // also look up the routing weight of each token for this group
                 if (r >= 64) {
 #pragma unroll
                     for (int t = 0; t < DT_TOK; ++t) xch[(r - 64) * DT_TOK + t] = v[t];
                 }
+                if (et < DT_TOK)
+                    s_wt[et] = et < T ? group_weight(ux.g, et, sc.n_act, K, s_act, s_idx, s_w, s_gsh) : 0.0f;
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (r < 64) {
                     const int f = ux.ft * 64 + r;
@@ -629,7 +651,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                         float hval = 0.0f;
                         if (t < T) {
                             const float gv = v[t] + bg, uv = xch[r * DT_TOK + t] + bu;
-                            const float wt = group_weight(ux.g, t, sc.n_act, K, s_act, s_idx, s_w, s_gsh);
+                            const float wt = s_wt[t];
                             hval = (ux.shared || a.act == MOE_ACT_SWIGLU)
                                        ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
                                        : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
@@ -641,9 +663,11 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 // publish: h' of this tile is written (generic proxy) and will be
                 // read by TMA (async proxy) in other CTAs
                 fence_proxy_async_global();
-                __threadfence();
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (et == 0) atomicAdd(&group_done[ux.g], 1);
+                if (et == 0) {
+                    __threadfence();
+                    atomicAdd(&group_done[ux.g], 1);
+                }
             } else if (finalize) {
                 const int row = dx.tile * 128 + r;
                 if (row < a.H) {

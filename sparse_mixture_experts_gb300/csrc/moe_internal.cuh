@@ -231,6 +231,105 @@ __device__ __forceinline__ void warp_select(const float *l, int E, int K, int mo
     }
 }
 
+// The same for two tokens at once (two independent register sets, so the
+// compiler interleaves their loads and compare chains).
+template <int NQ>
+__device__ __forceinline__ void warp_select2(const float *la, const float *lb, int E, int K, int mode, int norm,
+                                             float scale, int lane, int (&sel_i)[2], float (&sel_v)[2],
+                                             float (&w)[2])
+{
+    float v[2][NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        const bool in = lane + 32 * q < E;
+        v[0][q] = in ? __ldcg(la + lane + 32 * q) : -INFINITY;
+        v[1][q] = in ? __ldcg(lb + lane + 32 * q) : -INFINITY;
+    }
+    float mx[2], z[2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        mx[s] = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) mx[s] = fmaxf(mx[s], v[s][q]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int s = 0; s < 2; ++s) mx[s] = fmaxf(mx[s], __shfl_xor_sync(0xffffffffu, mx[s], o));
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        z[s] = 0.0f;
+        if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) z[s] += (lane + 32 * q < E) ? __expf(v[s][q] - mx[s]) : 0.0f;
+        }
+    }
+    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int s = 0; s < 2; ++s) z[s] += __shfl_xor_sync(0xffffffffu, z[s], o);
+    }
+    sel_i[0] = sel_i[1] = -1;
+    sel_v[0] = sel_v[1] = 0.0f;
+    for (int j = 0; j < K; ++j) {
+        float bv[2];
+        int bi[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            bv[s] = v[s][0];
+            int bq = 0;
+#pragma unroll
+            for (int q = 1; q < NQ; ++q)
+                if (v[s][q] > bv[s]) { bv[s] = v[s][q]; bq = q; }
+            bi[s] = (bv[s] == -INFINITY) ? 0x7fffffff : lane + 32 * bq;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv[s], o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi[s], o);
+                if (ov > bv[s] || (ov == bv[s] && oi < bi[s])) { bv[s] = ov; bi[s] = oi; }
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            if ((bi[s] & 31) == lane) {
+#pragma unroll
+                for (int q = 0; q < NQ; ++q)
+                    if (q == (bi[s] >> 5)) v[s][q] = -INFINITY;  // taken
+            }
+            if (lane == j) { sel_i[s] = bi[s]; sel_v[s] = bv[s]; }
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
+            const float p = (lane < K) ? __expf(sel_v[s] - mx[s]) / z[s] : 0.0f;
+            const float ps = warp_sum(p);
+            w[s] = (norm ? p / ps : p) * scale;
+        } else {
+            const float m0 = __shfl_sync(0xffffffffu, sel_v[s], 0);
+            const float ex = (lane < K) ? __expf(sel_v[s] - m0) : 0.0f;
+            w[s] = ex / warp_sum(ex);
+        }
+    }
+}
+
+__device__ __forceinline__ void warp_select2_any(const float *la, const float *lb, int E, int K, int mode, int norm,
+                                                 float scale, int lane, int (&sel_i)[2], float (&sel_v)[2],
+                                                 float (&w)[2])
+{
+    const int nq = (E + 31) / 32;
+    if (nq <= 1) warp_select2<1>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else if (nq <= 2) warp_select2<2>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else if (nq <= 4) warp_select2<4>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else if (nq <= 8) warp_select2<8>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else if (nq <= 16) warp_select2<16>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else warp_select2<32>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+}
+
 // dispatch on the number of logits per lane (E <= 1024)
 __device__ __forceinline__ void warp_select_any(const float *l, int E, int K, int mode, int norm, float scale, int lane,
                                                 int &sel_i, float &sel_v, float &w)
