@@ -280,9 +280,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     __shared__ float s_w[DT_MAX_PAIRS];
     __shared__ float s_gsh[DT_TOK];
     __shared__ int s_cnt[1024];
+    __shared__ uint32_t s_mask[32];  // bit e: expert e has at least one pair
     __shared__ int s_act[DT_MAX_PAIRS];
-    __shared__ int s_wtot[DT_THREADS / 32];
-    __shared__ int s_nact;
     __shared__ float s_wt[DT_TOK];  // routing weight per token of the current gate/up unit
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -314,6 +313,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
         tmap_prefetch(&maps.down);
         tmap_prefetch(&maps.hp);
     }
+    for (int e = threadIdx.x; e < E; e += DT_THREADS) s_cnt[e] = 0;
+    if (threadIdx.x < 32) s_mask[threadIdx.x] = 0u;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -324,56 +325,52 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
 
     // ---- routing, the same in every CTA ----
     // two tokens per warp at a time, so their load latencies and dependent
-    // compare chains overlap
+    // reductions overlap
     constexpr int NW = DT_THREADS / 32;
     for (int t = warp; t < T; t += 2 * NW) {
         const int t2 = t + NW;
         const bool two = t2 < T;
         const float *l = a.logits + (size_t)t * a.R;
         const float *l2 = a.logits + (size_t)(two ? t2 : t) * a.R;
+        // the shared expert's gate logit sits after the E router logits
+        const float gl = (lane == 0 && a.Fs > 0) ? __ldcg(l + E) : 0.0f;
+        const float gl2 = (lane == 0 && a.Fs > 0 && two) ? __ldcg(l2 + E) : 0.0f;
         int sel_i[2];
         float sel_v[2], w[2];
         warp_select2_any(l, l2, E, K, a.mode, a.norm, a.scale, lane, sel_i, sel_v, w);
         if (lane < K) {
             s_idx[t * K + lane] = sel_i[0];
             s_w[t * K + lane] = w[0];
+            atomicAdd(&s_cnt[sel_i[0]], 1);
+            atomicOr(&s_mask[sel_i[0] >> 5], 1u << (sel_i[0] & 31));
             if (two) {
                 s_idx[t2 * K + lane] = sel_i[1];
                 s_w[t2 * K + lane] = w[1];
+                atomicAdd(&s_cnt[sel_i[1]], 1);
+                atomicOr(&s_mask[sel_i[1] >> 5], 1u << (sel_i[1] & 31));
             }
         }
         if (lane == 0) {
-            s_gsh[t] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-__ldcg(l + E))) : 0.0f;
-            if (two) s_gsh[t2] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-__ldcg(l2 + E))) : 0.0f;
+            s_gsh[t] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-gl)) : 0.0f;
+            if (two) s_gsh[t2] = a.Fs > 0 ? 1.0f / (1.0f + __expf(-gl2)) : 0.0f;
         }
     }
-    for (int e = threadIdx.x; e < E; e += DT_THREADS) s_cnt[e] = 0;
     __syncthreads();
     const int P = T * K;
-    for (int p = threadIdx.x; p < P; p += DT_THREADS) atomicAdd(&s_cnt[s_idx[p]], 1);
-    __syncthreads();
-    {
-        int base = 0;
-        for (int e0 = 0; e0 < E; e0 += DT_THREADS) {
-            const int e = e0 + threadIdx.x;
-            const bool on = e < E && s_cnt[e] > 0;
-            const unsigned m = __ballot_sync(0xffffffffu, on);
-            if (lane == 0) s_wtot[warp] = __popc(m);
-            __syncthreads();
-            int before = 0, all = 0;
-#pragma unroll
-            for (int w6 = 0; w6 < DT_THREADS / 32; ++w6) {
-                before += w6 < warp ? s_wtot[w6] : 0;
-                all += s_wtot[w6];
-            }
-            if (on) s_act[base + before + __popc(m & ((1u << lane) - 1u))] = e;
-            base += all;
-            __syncthreads();
+    // active experts in ascending order: each one's slot is the number of
+    // selected experts below it
+    const int nwords = (E + 31) / 32;
+    int n_act = 0;
+    for (int wd = 0; wd < nwords; ++wd) n_act += __popc(s_mask[wd]);
+    for (int e = threadIdx.x; e < E; e += DT_THREADS) {
+        const uint32_t m = s_mask[e >> 5];
+        if ((m >> (e & 31)) & 1u) {
+            int r = __popc(m & ((1u << (e & 31)) - 1u));
+            for (int wd = 0; wd < (e >> 5); ++wd) r += __popc(s_mask[wd]);
+            s_act[r] = e;
         }
-        if (threadIdx.x == 0) s_nact = base;
     }
     __syncthreads();
-    const int n_act = s_nact;
     if (blockIdx.x == 0) {
         for (int p = threadIdx.x; p < P; p += DT_THREADS) {
             a.topk_idx[p] = s_idx[p];

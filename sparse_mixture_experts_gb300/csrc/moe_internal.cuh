@@ -175,172 +175,211 @@ __device__ __forceinline__ float warp_sum(float v)
 }
 
 // ---------------------------------------------------------------------------
-// selection for one token by one warp: lane j < k ends with the j-th pick
-// (descending logit, lower index on ties) and its routing weight.  Each lane
-// holds NQ >= ceil(E/32) logits in registers (expert lane + 32 q).
+// Selection by one warp for NT tokens at once: lane j < k ends with the j-th
+// pick of each token (descending logit, lower expert index on equal logits)
+// and its routing weight.  Each lane holds NQ >= ceil(E/32) logits in
+// registers (expert lane + 32 q).
+//
+// For NQ <= 8 every lane first sorts its candidates by a 64-bit key (the
+// logit's order-preserving bit pattern above the complemented expert index),
+// then each pick is two warp-wide integer max reductions over the lanes'
+// heads (the larger logit, then among equal logits the lower index) and the
+// winning lane pops its head.  For larger NQ each pick rescans the lane's
+// candidates and reduces with shuffles.  Both orders are the same total order
+// (value descending, index ascending), so the picks are identical.  -0 and
+// +0 compare equal, as they do for the scan.
 // ---------------------------------------------------------------------------
-template <int NQ>
-__device__ __forceinline__ void warp_select(const float *l, int E, int K, int mode, int norm, float scale, int lane,
-                                            int &sel_i, float &sel_v, float &w)
+__device__ __forceinline__ uint32_t logit_key(float f)
 {
-    float v[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) v[q] = (lane + 32 * q < E) ? __ldcg(l + lane + 32 * q) : -INFINITY;
-    float mx = -INFINITY;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) mx = fmaxf(mx, v[q]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float z = 0.0f;
-    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) z += (lane + 32 * q < E) ? __expf(v[q] - mx) : 0.0f;
-        z = warp_sum(z);
-    }
-    sel_i = -1;
-    sel_v = 0.0f;
-    for (int j = 0; j < K; ++j) {
-        // lane-local best (ascending q: a later q never beats an equal earlier one)
-        float bv = v[0];
-        int bq = 0;
-#pragma unroll
-        for (int q = 1; q < NQ; ++q)
-            if (v[q] > bv) { bv = v[q]; bq = q; }
-        int bi = (bv == -INFINITY) ? 0x7fffffff : lane + 32 * bq;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) {
-#pragma unroll
-            for (int q = 0; q < NQ; ++q)
-                if (q == (bi >> 5)) v[q] = -INFINITY;  // taken
-        }
-        if (lane == j) { sel_i = bi; sel_v = bv; }
-    }
-    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-        const float p = (lane < K) ? __expf(sel_v - mx) / z : 0.0f;
-        const float ps = warp_sum(p);
-        w = (norm ? p / ps : p) * scale;
-    } else {
-        const float m0 = __shfl_sync(0xffffffffu, sel_v, 0);
-        const float ex = (lane < K) ? __expf(sel_v - m0) : 0.0f;
-        w = ex / warp_sum(ex);
-    }
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;  // -0 == +0
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// The same for two tokens at once (two independent register sets, so the
-// compiler interleaves their loads and compare chains).
-template <int NQ>
-__device__ __forceinline__ void warp_select2(const float *la, const float *lb, int E, int K, int mode, int norm,
-                                             float scale, int lane, int (&sel_i)[2], float (&sel_v)[2],
-                                             float (&w)[2])
+__device__ __forceinline__ float key_logit(uint32_t k)
 {
-    float v[2][NQ];
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+template <int N>
+__device__ __forceinline__ void sort_desc(unsigned long long (&c)[N])
+{
+    // bitonic network: every index is a compile-time constant, so c stays in registers
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        const bool in = lane + 32 * q < E;
-        v[0][q] = in ? __ldcg(la + lane + 32 * q) : -INFINITY;
-        v[1][q] = in ? __ldcg(lb + lane + 32 * q) : -INFINITY;
-    }
-    float mx[2], z[2];
+    for (int k = 2; k <= N; k <<= 1)
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        mx[s] = -INFINITY;
+        for (int j = k >> 1; j > 0; j >>= 1)
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) mx[s] = fmaxf(mx[s], v[s][q]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int s = 0; s < 2; ++s) mx[s] = fmaxf(mx[s], __shfl_xor_sync(0xffffffffu, mx[s], o));
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        z[s] = 0.0f;
-        if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) z[s] += (lane + 32 * q < E) ? __expf(v[s][q] - mx[s]) : 0.0f;
-        }
-    }
-    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int s = 0; s < 2; ++s) z[s] += __shfl_xor_sync(0xffffffffu, z[s], o);
-    }
-    sel_i[0] = sel_i[1] = -1;
-    sel_v[0] = sel_v[1] = 0.0f;
-    for (int j = 0; j < K; ++j) {
-        float bv[2];
-        int bi[2];
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            bv[s] = v[s][0];
-            int bq = 0;
-#pragma unroll
-            for (int q = 1; q < NQ; ++q)
-                if (v[s][q] > bv[s]) { bv[s] = v[s][q]; bq = q; }
-            bi[s] = (bv[s] == -INFINITY) ? 0x7fffffff : lane + 32 * bq;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv[s], o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi[s], o);
-                if (ov > bv[s] || (ov == bv[s] && oi < bi[s])) { bv[s] = ov; bi[s] = oi; }
+            for (int i = 0; i < N; ++i) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const unsigned long long x = c[i], y = c[p];
+                    const bool sw = ((i & k) == 0) ? (x < y) : (x > y);
+                    c[i] = sw ? y : x;
+                    c[p] = sw ? x : y;
+                }
             }
-        }
+}
+
+template <int NQ, int NT>
+__device__ __forceinline__ void warp_topk(const float *const (&l)[NT], int E, int K, int mode, int norm, float scale,
+                                          int lane, int (&sel_i)[NT], float (&sel_v)[NT], float (&w)[NT])
+{
+    float v[NT][NQ];
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-            if ((bi[s] & 31) == lane) {
+    for (int s = 0; s < NT; ++s)
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) v[s][q] = (lane + 32 * q < E) ? __ldcg(l[s] + lane + 32 * q) : -INFINITY;
+
+    // softmax over all E is only needed when the picks are not renormalised
+    const bool need_z = mode == MOE_ROUTER_SOFTMAX_TOPK && !norm;
+    float z[NT];
+    if (need_z) {
+#pragma unroll
+        for (int s = 0; s < NT; ++s) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) mx = fmaxf(mx, v[s][q]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float zs = 0.0f;
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) zs += (lane + 32 * q < E) ? __expf(v[s][q] - mx) : 0.0f;
+            z[s] = warp_sum(zs);
+        }
+    }
+
+    constexpr bool SORTED = NQ <= 8;
+    unsigned long long c[NT][SORTED ? NQ : 1];
+    uint32_t avail[NT];  // scan path: bit q set while candidate lane + 32 q is in range and not taken
+#pragma unroll
+    for (int s = 0; s < NT; ++s) {
+        avail[s] = 0u;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) avail[s] |= (lane + 32 * q < E) ? (1u << q) : 0u;
+    }
+    if constexpr (SORTED) {
+#pragma unroll
+        for (int s = 0; s < NT; ++s) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const uint32_t idx = lane + 32 * q;
+                c[s][q] = idx < (uint32_t)E ? ((unsigned long long)logit_key(v[s][q]) << 32) | (0xffffffffu - idx)
+                                            : 0ull;
+            }
+            sort_desc<NQ>(c[s]);
+        }
+    }
+
+    float top[NT], esum[NT], ex[NT];
+#pragma unroll
+    for (int s = 0; s < NT; ++s) {
+        sel_i[s] = -1;
+        sel_v[s] = 0.0f;
+        esum[s] = 0.0f;
+        ex[s] = 0.0f;
+        top[s] = 0.0f;
+    }
+    for (int j = 0; j < K; ++j) {
+        float bv[NT];
+        int bi[NT];
+        if constexpr (SORTED) {
+            uint32_t hk[NT], hl[NT], m1[NT], m2[NT];
+#pragma unroll
+            for (int s = 0; s < NT; ++s) {
+                hk[s] = (uint32_t)(c[s][0] >> 32);
+                hl[s] = (uint32_t)c[s][0];
+                m1[s] = __reduce_max_sync(0xffffffffu, hk[s]);
+            }
+#pragma unroll
+            for (int s = 0; s < NT; ++s) m2[s] = __reduce_max_sync(0xffffffffu, hk[s] == m1[s] ? hl[s] : 0u);
+#pragma unroll
+            for (int s = 0; s < NT; ++s) {
+                if (hk[s] == m1[s] && hl[s] == m2[s]) {  // this lane's head was picked
+#pragma unroll
+                    for (int q = 0; q + 1 < NQ; ++q) c[s][q] = c[s][q + 1];
+                    c[s][NQ - 1] = 0ull;
+                }
+                bv[s] = key_logit(m1[s]);
+                bi[s] = (int)(0xffffffffu - m2[s]);
+            }
+        } else {
+#pragma unroll
+            for (int s = 0; s < NT; ++s) {
+                // lane-local best among the candidates not yet taken (ascending q:
+                // a later q never beats an equal earlier one)
+                int bq = -1;
+                bv[s] = -INFINITY;
 #pragma unroll
                 for (int q = 0; q < NQ; ++q)
-                    if (q == (bi[s] >> 5)) v[s][q] = -INFINITY;  // taken
+                    if (((avail[s] >> q) & 1u) && (bq < 0 || v[s][q] > bv[s])) { bv[s] = v[s][q]; bq = q; }
+                bi[s] = bq < 0 ? 0x7fffffff : lane + 32 * bq;
             }
-            if (lane == j) { sel_i[s] = bi[s]; sel_v[s] = bv[s]; }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                for (int s = 0; s < NT; ++s) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv[s], o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, bi[s], o);
+                    if (ov > bv[s] || (ov == bv[s] && oi < bi[s])) { bv[s] = ov; bi[s] = oi; }
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < NT; ++s)
+                if ((bi[s] & 31) == lane) avail[s] &= ~(1u << (bi[s] >> 5));  // taken
+        }
+        // every lane sees each pick, so each keeps the running sum of exp(pick - first pick)
+#pragma unroll
+        for (int s = 0; s < NT; ++s) {
+            if (j == 0) top[s] = bv[s];
+            const float e = __expf(bv[s] - top[s]);
+            esum[s] += e;
+            if (lane == j) { sel_i[s] = bi[s]; sel_v[s] = bv[s]; ex[s] = e; }
         }
     }
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-            const float p = (lane < K) ? __expf(sel_v[s] - mx[s]) / z[s] : 0.0f;
-            const float ps = warp_sum(p);
-            w[s] = (norm ? p / ps : p) * scale;
-        } else {
-            const float m0 = __shfl_sync(0xffffffffu, sel_v[s], 0);
-            const float ex = (lane < K) ? __expf(sel_v[s] - m0) : 0.0f;
-            w[s] = ex / warp_sum(ex);
-        }
+    for (int s = 0; s < NT; ++s) {
+        if (lane >= K) w[s] = 0.0f;
+        else if (mode == MOE_ROUTER_SOFTMAX_TOPK) w[s] = (need_z ? ex[s] / z[s] : ex[s] / esum[s]) * scale;
+        else w[s] = ex[s] / esum[s];
     }
 }
 
+template <int NT>
+__device__ __forceinline__ void warp_topk_any(const float *const (&l)[NT], int E, int K, int mode, int norm,
+                                              float scale, int lane, int (&sel_i)[NT], float (&sel_v)[NT],
+                                              float (&w)[NT])
+{
+    const int nq = (E + 31) / 32;
+    if (nq <= 1) warp_topk<1, NT>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else if (nq <= 2) warp_topk<2, NT>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else if (nq <= 4) warp_topk<4, NT>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else if (nq <= 8) warp_topk<8, NT>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else if (nq <= 16) warp_topk<16, NT>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    else warp_topk<32, NT>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+}
+
+// one token per warp
+__device__ __forceinline__ void warp_select_any(const float *l, int E, int K, int mode, int norm, float scale, int lane,
+                                                int &sel_i, float &sel_v, float &w)
+{
+    const float *ls[1] = {l};
+    int i[1];
+    float v[1], ww[1];
+    warp_topk_any<1>(ls, E, K, mode, norm, scale, lane, i, v, ww);
+    sel_i = i[0];
+    sel_v = v[0];
+    w = ww[0];
+}
+
+// two tokens per warp (independent register sets, so their load latencies and
+// dependent reductions overlap)
 __device__ __forceinline__ void warp_select2_any(const float *la, const float *lb, int E, int K, int mode, int norm,
                                                  float scale, int lane, int (&sel_i)[2], float (&sel_v)[2],
                                                  float (&w)[2])
 {
-    const int nq = (E + 31) / 32;
-    if (nq <= 1) warp_select2<1>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else if (nq <= 2) warp_select2<2>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else if (nq <= 4) warp_select2<4>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else if (nq <= 8) warp_select2<8>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else if (nq <= 16) warp_select2<16>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else warp_select2<32>(la, lb, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-}
-
-// dispatch on the number of logits per lane (E <= 1024)
-__device__ __forceinline__ void warp_select_any(const float *l, int E, int K, int mode, int norm, float scale, int lane,
-                                                int &sel_i, float &sel_v, float &w)
-{
-    const int nq = (E + 31) / 32;
-    if (nq <= 1) warp_select<1>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else if (nq <= 2) warp_select<2>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else if (nq <= 4) warp_select<4>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else if (nq <= 8) warp_select<8>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else if (nq <= 16) warp_select<16>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    else warp_select<32>(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+    const float *ls[2] = {la, lb};
+    warp_topk_any<2>(ls, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
 }
 
 __device__ __forceinline__ void record_error(int *status, int code)
