@@ -57,6 +57,10 @@ constexpr int DT_XCH_BYTES = 64 * DT_TOK * 4;   // up-row values handed to the g
 constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
 constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 1024;
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
+constexpr int DT_SATURATING_CTAS = 64;          // CTAs streaming at once that saturate HBM
+constexpr int DT_DOWN_GUIDE = 1;                // down ranges: a round of units takes 1/GUIDE of the groups left
+constexpr int DT_MAX_DOWN_SPLITS = 64;
+constexpr int DT_CLAIM_AHEAD = 4;               // stages before a unit's end at which the next one is claimed
 constexpr int DT_TICKET_DOWN = 8192;            // offset of the down tiles' tickets
 constexpr int DT_GROUP_DONE = 12288;            // offset of the per-group completion counters
 constexpr int DT_NEXT_UNIT = 16000;             // offset of the work counter
@@ -79,7 +83,7 @@ struct DecArgs {
     RouteMeta *meta;
     const float *gate_b, *up_b, *down_b;
     __nv_bfloat16 *hp;    // [groups_max*16][Fmax]
-    float *partials;      // [units][128][16]
+    float *partials;      // [gate/up, down][units][T][128]
     int *counters;        // tickets, group completion, work counter
     void *out;
     int *status;
@@ -153,21 +157,35 @@ __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
 // ---------------------------------------------------------------------------
 // schedules (every CTA computes the same ones from the group count)
 // ---------------------------------------------------------------------------
-// Split count S in [1, smax] minimising the busiest CTA's bytes when there
-// are fewer tiles than CTAs; no split otherwise (a split costs a partial-sum
-// round trip through global memory).
-__device__ __forceinline__ int choose_splits(int tiles, int nkb, int smax, int G, int max_units)
+// Gate/up split count.  One SM streams at most about 120 GB/s, so about 64
+// CTAs streaming at once already saturate HBM; below that many tiles, each
+// tile is split along K into S parts (each split costs a partial-sum round
+// trip through L2), otherwise not at all.
+__device__ __forceinline__ int up_splits(int tiles, int smax, int max_units)
 {
-    if (tiles >= G) return 1;
-    int best = 1;
-    long long best_cost = -1;
-    for (int S = 1; S <= smax; ++S) {
-        if ((long long)tiles * S > max_units && S > 1) break;
-        const long long per_cta = ((long long)tiles * S + G - 1) / G;
-        const long long cost = per_cta * (((nkb + S - 1) / S) * (long long)DT_STAGE_BYTES + (S > 1 ? 32768 : 0));
-        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = S; }
+    if (tiles >= DT_SATURATING_CTAS) return 1;
+    int S = min(smax, (DT_SATURATING_CTAS + tiles - 1) / tiles);
+    while (S > 1 && tiles * S > max_units) --S;
+    return max(1, S);
+}
+
+// Down split boundaries (group ranges), the same in every CTA.  Units are
+// claimed split-major, so the ranges shrink toward the end (guided
+// self-scheduling): about one round of units (G / ot splits) covers
+// 1 / DT_DOWN_GUIDE of the groups still left, and the last units claimed are
+// one group each; at most maxs splits.  Returns the split count; b[0..S]
+// are the boundaries.
+__device__ __forceinline__ int down_bounds(int groups, int ot, int G, int maxs, int *b)
+{
+    const int per_round = max(1, G / ot) * DT_DOWN_GUIDE;
+    int s = 0, g = 0;
+    b[0] = 0;
+    while (g < groups) {
+        const int left = groups - g;
+        g += (s == maxs - 1) ? left : (left + per_round - 1) / per_round;
+        b[++s] = g;
     }
-    return best;
+    return s;
 }
 
 struct Sched {
@@ -177,7 +195,7 @@ struct Sched {
     int total;
 };
 
-__device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act, int G)
+__device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act, int G, int S_dn)
 {
     Sched s;
     s.n_act = n_act;
@@ -185,11 +203,10 @@ __device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act, int G)
     s.tiles_routed = n_act * (a.F / 64);
     s.up_tiles = s.tiles_routed + a.Fs / 64;
     s.nkb = a.H / 64;
-    s.S_up = choose_splits(s.up_tiles, s.nkb, max(1, min(16, s.nkb / 2)), G, a.max_units);
+    s.S_up = up_splits(s.up_tiles, max(1, min(16, s.nkb / 2)), a.max_units);
     s.up_units = s.up_tiles * s.S_up;
     s.ot = (a.H + 127) / 128;
-    // about one down unit per CTA: fewer, longer units mean fewer partial sums
-    s.S_dn = max(1, min(s.groups, (G + s.ot - 1) / s.ot));
+    s.S_dn = S_dn;
     s.dn_units = s.ot * s.S_dn;
     s.total = s.up_units + s.dn_units;
     return s;
@@ -226,13 +243,13 @@ struct DnUnit {
     int tile, s, g0, g1;
 };
 
-__device__ __forceinline__ DnUnit dn_unit(const Sched &s, int d)
+__device__ __forceinline__ DnUnit dn_unit(const Sched &s, int d, const int *bounds)
 {
     DnUnit x;
     x.s = d / s.ot;
     x.tile = d - x.s * s.ot;
-    x.g0 = (int)((long long)s.groups * x.s / s.S_dn);
-    x.g1 = (int)((long long)s.groups * (x.s + 1) / s.S_dn);
+    x.g0 = bounds[x.s];
+    x.g1 = bounds[x.s + 1];
     return x;
 }
 
@@ -244,6 +261,21 @@ __device__ __forceinline__ int ld_acquire(const int *p)
 }
 
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// counter increment that releases this thread's earlier writes (and, through
+// the preceding named barrier, its group's) to the GPU; no value comes back
+__device__ __forceinline__ void red_release_add(int *p, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ticket: releases the group's partial sums and acquires the other arrivals'
+__device__ __forceinline__ int atom_acq_rel_add(int *p, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
 
 // routing weight of token t for group g (0 when t is not routed to it)
 __device__ __forceinline__ float group_weight(int g, int t, int n_act, int K, const int *s_act, const int *s_idx,
@@ -282,6 +314,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     __shared__ int s_cnt[1024];
     __shared__ uint32_t s_mask[32];  // bit e: expert e has at least one pair
     __shared__ int s_act[DT_MAX_PAIRS];
+    __shared__ int s_dnb[DT_MAX_DOWN_SPLITS + 1];  // down split boundaries
+    __shared__ int s_sdn;
     __shared__ float s_wt[DT_TOK];  // routing weight per token of the current gate/up unit
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -320,8 +354,15 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // the selection's parameters are read before the wait, so that their
+    // first (cold) reads overlap it
+    asm volatile("" ::"l"(a.logits), "r"(a.R), "r"(a.Fs), "r"(a.mode), "r"(a.norm), "f"(a.scale), "l"(a.counters));
+
     // the router's logits (and the reset counters) are read from here on
     pdl_wait();
+    // the producer's first claim; its latency overlaps the selection below
+    int first_unit = 0;
+    if (threadIdx.x == 0) first_unit = atomicAdd(a.counters + DT_NEXT_UNIT, 1);
 
     // ---- routing, the same in every CTA ----
     // two tokens per warp at a time, so their load latencies and dependent
@@ -362,6 +403,10 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     const int nwords = (E + 31) / 32;
     int n_act = 0;
     for (int wd = 0; wd < nwords; ++wd) n_act += __popc(s_mask[wd]);
+    if (threadIdx.x == 0) {
+        const int ot = (a.H + 127) / 128;
+        s_sdn = down_bounds(n_act + (a.Fs > 0 ? 1 : 0), ot, G, min(DT_MAX_DOWN_SPLITS, a.max_units / ot), s_dnb);
+    }
     for (int e = threadIdx.x; e < E; e += DT_THREADS) {
         const uint32_t m = s_mask[e >> 5];
         if ((m >> (e & 31)) & 1u) {
@@ -385,7 +430,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             a.meta->n_pairs = P;
         }
     }
-    const Sched sc = make_sched(a, n_act, G);
+    const Sched sc = make_sched(a, n_act, G, s_sdn);
     int *tickets = a.counters;
     int *group_done = a.counters + DT_GROUP_DONE;
     int *next_unit = a.counters + DT_NEXT_UNIT;
@@ -401,9 +446,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             int qi = 0;
             uint32_t qph = 0;
             bool ok = true;
+            int u_next = first_unit;
             while (ok) {
-                int u = atomicAdd(next_unit, 1);
-                if (u >= sc.total) u = -1;
+                int u = u_next < sc.total ? u_next : -1;
                 if (!mbar_wait(&uq_empty[qi], qph ^ 1, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
                     *abort_flag = 1;
@@ -414,13 +459,23 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 if (++qi == DT_ACC) qi = 0, qph ^= 1;
                 if (u < 0) break;
                 const bool is_up = u < sc.up_units;
-                int g0 = 0, g1 = 1;
+                int g0 = 0, g1 = 1, left;
                 DnUnit dn;
-                if (!is_up) {
-                    dn = dn_unit(sc, u - sc.up_units);
+                if (is_up) {
+                    const UpUnit x = up_unit(sc, u, a.F);
+                    left = x.kb1 - x.kb0;
+                } else {
+                    dn = dn_unit(sc, u - sc.up_units, s_dnb);
                     g0 = dn.g0;
                     g1 = dn.g1;
+                    left = 0;
+                    for (int gi = g0; gi < g1; ++gi) left += (gi == sc.n_act ? a.Fs : a.F) / 64;
                 }
+                // the next unit is claimed a few stages before this one ends, so
+                // the counter's round trip overlaps this unit's loads.  Claims stay
+                // in order: a CTA holds at most one unclaimed-ahead unit, and a
+                // down unit only waits for gate/up units, which never wait.
+                bool claimed = false;
                 for (int gi = g0; gi < g1 && ok; ++gi) {
                     int kb0, kb1, arow, brow;
                     const CUtensorMap *ma, *mb = nullptr;
@@ -453,7 +508,11 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                         fence_proxy_async_global();
                         if (!ok) break;
                     }
-                    for (int kb = kb0; kb < kb1; ++kb) {
+                    for (int kb = kb0; kb < kb1; ++kb, --left) {
+                        if (!claimed && left <= DT_CLAIM_AHEAD) {
+                            u_next = atomicAdd(next_unit, 1);
+                            claimed = true;
+                        }
                         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
                             record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
                             *abort_flag = 1;
@@ -477,6 +536,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                         if (++stage == DT_STAGES) stage = 0, phase ^= 1;
                     }
                 }
+                if (!claimed) u_next = atomicAdd(next_unit, 1);
             }
             if (*abort_flag) {
                 // let the other roles leave: hand out the end-of-work marker
@@ -515,7 +575,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                     const UpUnit x = up_unit(sc, u, a.F);
                     nk = x.kb1 - x.kb0;
                 } else {
-                    const DnUnit d = dn_unit(sc, u - sc.up_units);
+                    const DnUnit d = dn_unit(sc, u - sc.up_units, s_dnb);
                     nk = 0;
                     for (int gi = d.g0; gi < d.g1; ++gi) nk += (gi == sc.n_act ? a.Fs : a.F) / 64;
                 }
@@ -587,28 +647,25 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             DnUnit dx;
             int tile, S, tbase;
             if (is_up) { ux = up_unit(sc, u, a.F); tile = ux.tile; S = sc.S_up; tbase = 0; }
-            else { dx = dn_unit(sc, u - sc.up_units); tile = dx.tile; S = sc.S_dn; tbase = DT_TICKET_DOWN; }
+            else { dx = dn_unit(sc, u - sc.up_units, s_dnb); tile = dx.tile; S = sc.S_dn; tbase = DT_TICKET_DOWN; }
 
             bool finalize = true;
             if (S > 1) {
-                // the partial of this split to global; the last split of the tile
-                // sums all of them in split order
+                // the partial of this split to global, one row of 128 floats per
+                // token; the last split of the tile to arrive sums all of them in
+                // split order
                 const int split = is_up ? ux.s : dx.s;
                 const size_t pbase = (size_t)(is_up ? 0 : a.max_units) + (size_t)tile * S;
-                float4 *dst = reinterpret_cast<float4 *>(a.partials + ((pbase + split) * 128 + r) * DT_TOK);
+                float *pt = a.partials + (size_t)T * 128 * pbase;
 #pragma unroll
-                for (int i = 0; i < DT_TOK / 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                // the named barrier orders the group's stores; one thread fences
-                // (cumulative, device scope) and takes the ticket
+                for (int t = 0; t < DT_TOK; ++t)
+                    if (t < T) pt[((size_t)split * T + t) * 128 + r] = v[t];
+                // the named barrier orders the group's stores before one thread's
+                // acquire-release ticket
                 asm volatile("bar.sync 1, 128;" ::: "memory");
                 if (et == 0) {
-                    __threadfence();
-                    const int prev = atomicAdd(&tickets[tbase + tile], 1);
-                    const int last = prev == S - 1;
-                    if (last) {
-                        tickets[tbase + tile] = 0;
-                        __threadfence();  // the other splits' partials are read below
-                    }
+                    const int last = atom_acq_rel_add(&tickets[tbase + tile], 1) == S - 1;
+                    if (last) tickets[tbase + tile] = 0;
                     bcast[2] = last;
                 }
                 asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -617,14 +674,14 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 if (finalize) {
 #pragma unroll
                     for (int t = 0; t < DT_TOK; ++t) v[t] = 0.0f;
-                    for (int s = 0; s < S; ++s) {
-                        const float4 *src =
-                            reinterpret_cast<const float4 *>(a.partials + ((pbase + s) * 128 + r) * DT_TOK);
+                    for (int sp = 0; sp < S; ++sp) {
+                        // all of a split's loads are issued before any is used
+                        const float *src = pt + (size_t)sp * T * 128 + r;
+                        float pv[DT_TOK];
 #pragma unroll
-                        for (int i = 0; i < DT_TOK / 4; ++i) {
-                            const float4 p = __ldcg(src + i);
-                            v[4 * i] += p.x; v[4 * i + 1] += p.y; v[4 * i + 2] += p.z; v[4 * i + 3] += p.w;
-                        }
+                        for (int t = 0; t < DT_TOK; ++t) pv[t] = t < T ? __ldcg(src + (size_t)t * 128) : 0.0f;
+#pragma unroll
+                        for (int t = 0; t < DT_TOK; ++t) v[t] += pv[t];
                     }
                 }
             }
@@ -661,10 +718,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 // read by TMA (async proxy) in other CTAs
                 fence_proxy_async_global();
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (et == 0) {
-                    __threadfence();
-                    atomicAdd(&group_done[ux.g], 1);
-                }
+                if (et == 0) red_release_add(&group_done[ux.g], 1);
             } else if (finalize) {
                 const int row = dx.tile * 128 + r;
                 if (row < a.H) {
