@@ -57,14 +57,15 @@ constexpr int DT_XCH_BYTES = 64 * DT_TOK * 4;   // up-row values handed to the g
 constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
 constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 1024;
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
-constexpr int DT_SATURATING_CTAS = 64;          // CTAs streaming at once that saturate HBM
+constexpr int DT_SATURATING_CTAS = 128;         // CTAs streaming at once that saturate HBM
 constexpr int DT_DOWN_GUIDE = 1;                // down ranges: a round of units takes 1/GUIDE of the groups left
 constexpr int DT_MAX_DOWN_SPLITS = 64;
 constexpr int DT_CLAIM_AHEAD = 4;               // stages before a unit's end at which the next one is claimed
 constexpr int DT_TICKET_DOWN = 8192;            // offset of the down tiles' tickets
 constexpr int DT_GROUP_DONE = 12288;            // offset of the per-group completion counters
-constexpr int DT_NEXT_UNIT = 16000;             // offset of the work counter
-constexpr int DT_COUNTERS = 16384;              // ints
+constexpr int DT_DONE_STRIDE = 32;              // one 128-byte line per group counter
+constexpr int DT_NEXT_UNIT = 32736;             // offset of the work counter (a line of its own)
+constexpr int DT_COUNTERS = 32768;              // ints
 
 struct DecMaps {
     CUtensorMap gate, up, sh_gate, sh_up;  // box 64 rows x 64
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
     const int T = a.T, H = a.H, R = a.R;
     if (blockIdx.x == 0) {
         // kernel 2 of the previous forward has finished (stream order)
-        for (int i = threadIdx.x; i < a.n_reset; i += 256) a.counters[DT_GROUP_DONE + i] = 0;
+        for (int i = threadIdx.x; i < a.n_reset; i += 256) a.counters[DT_GROUP_DONE + i * DT_DONE_STRIDE] = 0;
         if (threadIdx.x == 0) a.counters[DT_NEXT_UNIT] = 0;
     }
     __shared__ float s_part[8][DT_TOK];
@@ -157,8 +158,9 @@ __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
 // ---------------------------------------------------------------------------
 // schedules (every CTA computes the same ones from the group count)
 // ---------------------------------------------------------------------------
-// Gate/up split count.  One SM streams at most about 120 GB/s, so about 64
-// CTAs streaming at once already saturate HBM; below that many tiles, each
+// Gate/up split count.  One SM streams at most about 120 GB/s by TMA alone
+// and less beside the MMA and handoffs, so about 128 CTAs streaming at once
+// saturate HBM; below that many tiles, each
 // tile is split along K into S parts (each split costs a partial-sum round
 // trip through L2), otherwise not at all.
 __device__ __forceinline__ int up_splits(int tiles, int smax, int max_units)
@@ -191,11 +193,10 @@ __device__ __forceinline__ int down_bounds(int groups, int ot, int G, int maxs, 
 struct Sched {
     int n_act, groups;
     int tiles_routed, up_tiles, nkb, S_up, up_units;  // gate/up
-    int ot, S_dn, dn_units;                          // down
-    int total;
+    int ot;                                          // down output tiles (the split count comes later)
 };
 
-__device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act, int G, int S_dn)
+__device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act)
 {
     Sched s;
     s.n_act = n_act;
@@ -206,9 +207,6 @@ __device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act, int G, 
     s.S_up = up_splits(s.up_tiles, max(1, min(16, s.nkb / 2)), a.max_units);
     s.up_units = s.up_tiles * s.S_up;
     s.ot = (a.H + 127) / 128;
-    s.S_dn = S_dn;
-    s.dn_units = s.ot * s.S_dn;
-    s.total = s.up_units + s.dn_units;
     return s;
 }
 
@@ -277,6 +275,25 @@ __device__ __forceinline__ int atom_acq_rel_add(int *p, int v)
     return old;
 }
 
+// v[t] += the S split partials of row r, in split order; U splits' loads are
+// in flight at a time (TT >= T token slots)
+template <int TT, int U>
+__device__ __forceinline__ void sum_partials(const float *pt, int S, int T, int r, float (&v)[DT_TOK])
+{
+    for (int s0 = 0; s0 < S; s0 += U) {
+        float pv[U][TT];
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int t = 0; t < TT; ++t)
+                pv[j][t] = (s0 + j < S && t < T) ? __ldcg(pt + ((size_t)(s0 + j) * T + t) * 128 + r) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < U; ++j)
+#pragma unroll
+            for (int t = 0; t < TT; ++t) v[t] += pv[j][t];
+    }
+}
+
 // routing weight of token t for group g (0 when t is not routed to it)
 __device__ __forceinline__ float group_weight(int g, int t, int n_act, int K, const int *s_act, const int *s_idx,
                                               const float *s_w, const float *s_gsh)
@@ -315,7 +332,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     __shared__ uint32_t s_mask[32];  // bit e: expert e has at least one pair
     __shared__ int s_act[DT_MAX_PAIRS];
     __shared__ int s_dnb[DT_MAX_DOWN_SPLITS + 1];  // down split boundaries
-    __shared__ int s_sdn;
+    __shared__ int s_sdn;                          // down split count
+    __shared__ __align__(8) uint64_t s_bnd_bar;    // s_dnb and s_sdn are written
     __shared__ float s_wt[DT_TOK];  // routing weight per token of the current gate/up unit
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -327,6 +345,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(&s_bnd_bar, 1);
         for (int b = 0; b < DT_ACC; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&uq_full[b], 1);
@@ -403,10 +422,6 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     const int nwords = (E + 31) / 32;
     int n_act = 0;
     for (int wd = 0; wd < nwords; ++wd) n_act += __popc(s_mask[wd]);
-    if (threadIdx.x == 0) {
-        const int ot = (a.H + 127) / 128;
-        s_sdn = down_bounds(n_act + (a.Fs > 0 ? 1 : 0), ot, G, min(DT_MAX_DOWN_SPLITS, a.max_units / ot), s_dnb);
-    }
     for (int e = threadIdx.x; e < E; e += DT_THREADS) {
         const uint32_t m = s_mask[e >> 5];
         if ((m >> (e & 31)) & 1u) {
@@ -430,7 +445,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             a.meta->n_pairs = P;
         }
     }
-    const Sched sc = make_sched(a, n_act, G, s_sdn);
+    const Sched sc = make_sched(a, n_act);
     int *tickets = a.counters;
     int *group_done = a.counters + DT_GROUP_DONE;
     int *next_unit = a.counters + DT_NEXT_UNIT;
@@ -447,8 +462,19 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             uint32_t qph = 0;
             bool ok = true;
             int u_next = first_unit;
+            bool bounds = false;
             while (ok) {
-                int u = u_next < sc.total ? u_next : -1;
+                int u = u_next;
+                if (u >= sc.up_units) {
+                    // the down split count is computed off the critical path (epilogue role)
+                    if (!bounds && !mbar_wait(&s_bnd_bar, 0, abort_flag)) {
+                        record_error(a.status, DEV_TIMEOUT_ACCUM_BARRIER);
+                        *abort_flag = 1;
+                        u = -1;
+                    }
+                    bounds = true;
+                    if (u >= sc.up_units + sc.ot * s_sdn) u = -1;
+                }
                 if (!mbar_wait(&uq_empty[qi], qph ^ 1, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
                     *abort_flag = 1;
@@ -494,9 +520,13 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                         brow = gi * DT_TOK;
                         // h'[gi] is complete once every gate/up tile of the group is
                         const int need = fd / 64;
-                        if (ld_acquire(group_done + gi) < need) {
+                        int *done = group_done + gi * DT_DONE_STRIDE;
+                        if (ld_acquire(done) < need) {
+                            // poll with a short back-off: many producers may wait on
+                            // the same counter, and the increment must get through
                             const unsigned long long t0 = globaltimer();
-                            while (ld_acquire(group_done + gi) < need) {
+                            while (ld_acquire(done) < need) {
+                                __nanosleep(128);
                                 if (*abort_flag || globaltimer() - t0 > WAIT_LIMIT_NS) {
                                     record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
                                     *abort_flag = 1;
@@ -614,6 +644,14 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
         const int r = q * 32 + lane;                // accumulator row = weight row of the tile
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         const int et = threadIdx.x - 64;            // 0..127 within the epilogue group
+        if (et == 96) {
+            // the down split ranges; only needed once the gate/up units are all
+            // claimed, so they are computed here rather than in the prologue.  A
+            // down unit reaches the MMA and epilogue roles only through the
+            // producer, which waits for this barrier first.
+            s_sdn = down_bounds(sc.groups, sc.ot, G, min(DT_MAX_DOWN_SPLITS, a.max_units / sc.ot), s_dnb);
+            mbar_arrive(&s_bnd_bar);
+        }
         int qi = 0;
         uint32_t qph = 0;
         for (;;) {
@@ -647,7 +685,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             DnUnit dx;
             int tile, S, tbase;
             if (is_up) { ux = up_unit(sc, u, a.F); tile = ux.tile; S = sc.S_up; tbase = 0; }
-            else { dx = dn_unit(sc, u - sc.up_units, s_dnb); tile = dx.tile; S = sc.S_dn; tbase = DT_TICKET_DOWN; }
+            else { dx = dn_unit(sc, u - sc.up_units, s_dnb); tile = dx.tile; S = s_sdn; tbase = DT_TICKET_DOWN; }
 
             bool finalize = true;
             if (S > 1) {
@@ -674,15 +712,10 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 if (finalize) {
 #pragma unroll
                     for (int t = 0; t < DT_TOK; ++t) v[t] = 0.0f;
-                    for (int sp = 0; sp < S; ++sp) {
-                        // all of a split's loads are issued before any is used
-                        const float *src = pt + (size_t)sp * T * 128 + r;
-                        float pv[DT_TOK];
-#pragma unroll
-                        for (int t = 0; t < DT_TOK; ++t) pv[t] = t < T ? __ldcg(src + (size_t)t * 128) : 0.0f;
-#pragma unroll
-                        for (int t = 0; t < DT_TOK; ++t) v[t] += pv[t];
-                    }
+                    if (T <= 2) sum_partials<2, 16>(pt, S, T, r, v);
+                    else if (T <= 4) sum_partials<4, 8>(pt, S, T, r, v);
+                    else if (T <= 8) sum_partials<8, 4>(pt, S, T, r, v);
+                    else sum_partials<16, 2>(pt, S, T, r, v);
                 }
             }
             if (finalize && is_up) {
@@ -718,7 +751,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 // read by TMA (async proxy) in other CTAs
                 fence_proxy_async_global();
                 asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (et == 0) red_release_add(&group_done[ux.g], 1);
+                if (et == 0) red_release_add(&group_done[ux.g * DT_DONE_STRIDE], 1);
             } else if (finalize) {
                 const int row = dx.tile * 128 + r;
                 if (row < a.H) {
@@ -795,7 +828,7 @@ size_t dectc_workspace(const Layer &L, size_t &hp_bytes, size_t &part_bytes, siz
 
 int dectc_prepare(Layer &L)
 {
-    if (dectc_groups_max(L) > DT_NEXT_UNIT - DT_GROUP_DONE) return -1;
+    if ((long long)dectc_groups_max(L) * DT_DONE_STRIDE > DT_NEXT_UNIT - DT_GROUP_DONE) return -1;
     DecMaps *m = new (std::nothrow) DecMaps();
     if (!m) return -1;
     bool ok = dec_encode(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
