@@ -53,7 +53,8 @@ constexpr int DT_B_BYTES = DT_TOK * 64 * 2;     // 2 KB token tile
 constexpr int DT_STAGE_BYTES = DT_A_BYTES + DT_B_BYTES;
 constexpr int DT_ACC = 8;                       // unit queue slots = TMEM accumulators
 constexpr int DT_TMEM_COLS = DT_ACC * DT_TOK;   // 16 fp32 columns each
-constexpr int DT_XCH_BYTES = 64 * DT_TOK * 4;   // up-row values handed to the gate rows
+constexpr int DT_EP_LD = DT_TOK + 1;            // row pitch (floats) of the epilogue's accumulator copy
+constexpr int DT_XCH_BYTES = 128 * DT_EP_LD * 4; // the accumulator tile in shared memory
 constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
 constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 1024;
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
@@ -455,9 +456,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t last_phase[DT_STAGES];
-            bool used[DT_STAGES];
-            for (int s = 0; s < DT_STAGES; ++s) used[s] = false, last_phase[s] = 0;
+            uint32_t used = 0, last_phase = 0;  // per stage: loads issued, parity of the last
             int qi = 0;
             uint32_t qph = 0;
             bool ok = true;
@@ -561,8 +560,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                             tma_load_2d(sa, ma, &full[stage], kc, arow);
                             tma_load_2d(sb, &maps.hp, &full[stage], kc, brow);
                         }
-                        used[stage] = true;
-                        last_phase[stage] = phase;
+                        used |= 1u << stage;
+                        last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                         if (++stage == DT_STAGES) stage = 0, phase ^= 1;
                     }
                 }
@@ -578,7 +577,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             }
             volatile int never = 0;
             for (int s = 0; s < DT_STAGES; ++s)
-                if (used[s]) mbar_wait(&full[s], last_phase[s], &never);
+                if ((used >> s) & 1u) mbar_wait(&full[s], (last_phase >> s) & 1u, &never);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
@@ -712,39 +711,39 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 if (finalize) {
 #pragma unroll
                     for (int t = 0; t < DT_TOK; ++t) v[t] = 0.0f;
-                    if (T <= 2) sum_partials<2, 16>(pt, S, T, r, v);
-                    else if (T <= 4) sum_partials<4, 8>(pt, S, T, r, v);
-                    else if (T <= 8) sum_partials<8, 4>(pt, S, T, r, v);
+                    if (T <= 4) sum_partials<4, 8>(pt, S, T, r, v);
                     else sum_partials<16, 2>(pt, S, T, r, v);
                 }
             }
-            if (finalize && is_up) {
-                // rows 64..127 are the up projections of rows 0..63; 16 threads
-                // also look up the routing weight of each token for this group
-                if (r >= 64) {
+            if (finalize) {
+                // the tile to shared memory, so that the per-token loops below
+                // need not be unrolled (row pitch 17: conflict-free by row)
 #pragma unroll
-                    for (int t = 0; t < DT_TOK; ++t) xch[(r - 64) * DT_TOK + t] = v[t];
-                }
-                if (et < DT_TOK)
+                for (int t = 0; t < DT_TOK; ++t) xch[r * DT_EP_LD + t] = v[t];
+                // 16 threads look up each token's routing weight for this group
+                if (is_up && et < DT_TOK)
                     s_wt[et] = et < T ? group_weight(ux.g, et, sc.n_act, K, s_act, s_idx, s_w, s_gsh) : 0.0f;
                 asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
+            if (finalize && is_up) {
+                // rows 0..63 are gate projections, rows 64..127 the matching up projections
                 if (r < 64) {
                     const int f = ux.ft * 64 + r;
                     const int e = ux.shared ? -1 : s_act[ux.g];
                     const float bg = (!ux.shared && a.gate_b) ? a.gate_b[(size_t)e * a.F + f] : 0.0f;
                     const float bu = (!ux.shared && a.up_b) ? a.up_b[(size_t)e * a.F + f] : 0.0f;
-#pragma unroll
+                    const bool swiglu = ux.shared || a.act == MOE_ACT_SWIGLU;
+                    __nv_bfloat16 *dst = a.hp + (size_t)ux.g * DT_TOK * a.Fmax + f;
+#pragma unroll 1
                     for (int t = 0; t < DT_TOK; ++t) {
                         float hval = 0.0f;
                         if (t < T) {
-                            const float gv = v[t] + bg, uv = xch[r * DT_TOK + t] + bu;
-                            const float wt = s_wt[t];
-                            hval = (ux.shared || a.act == MOE_ACT_SWIGLU)
-                                       ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
-                                       : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
-                            hval *= wt;
+                            const float gv = xch[r * DT_EP_LD + t] + bg, uv = xch[(r + 64) * DT_EP_LD + t] + bu;
+                            hval = swiglu ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
+                                          : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
+                            hval *= s_wt[t];
                         }
-                        a.hp[((size_t)ux.g * DT_TOK + t) * a.Fmax + f] = __float2bfloat16_rn(hval);
+                        dst[(size_t)t * a.Fmax] = __float2bfloat16_rn(hval);
                     }
                 }
                 // publish: h' of this tile is written (generic proxy) and will be
@@ -755,8 +754,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             } else if (finalize) {
                 const int row = dx.tile * 128 + r;
                 if (row < a.H) {
+#pragma unroll 1
                     for (int t = 0; t < T; ++t) {
-                        float o = v[t];
+                        float o = xch[r * DT_EP_LD + t];
                         if (a.down_b)
                             for (int j = 0; j < K; ++j)
                                 o += s_w[t * K + j] * a.down_b[(size_t)s_idx[t * K + j] * a.H + row];
