@@ -390,24 +390,23 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
         alg = step_bytes - (router_bytes if top == "experts" else 0)
         bound, unit, peak = "hbm", "GB/s", hbm_peak
         achieved = alg / (kernel_avg_us[top] * 1e-6) / 1e9
-    elif top == "up":
-        if decode_like:
-            alg = d_avg * per_expert_up + 2 * Fs * H * eb + T * H * eb + (up_rows + T) * max(F, Fs) * eb
-            bound, unit, peak = "hbm", "GB/s", hbm_peak
-            achieved = alg / (kernel_avg_us["up"] * 1e-6) / 1e9
+    elif top in ("up", "down"):
+        # bytes and flops of this kernel; the larger of its two floors names the bound
+        hrows = (up_rows + T) * max(F, Fs) * eb
+        if top == "up":
+            kbytes = d_avg * per_expert_up + 2 * Fs * H * eb + (T if decode_like else up_rows + T) * H * eb + hrows
+            kflops = 2.0 * up_rows * 2 * F * H + 2.0 * T * 2 * Fs * H
         else:
-            alg = 2.0 * up_rows * 2 * F * H + 2.0 * T * 2 * Fs * H
-            bound, unit, peak = "tensor", "TFLOP/s", tc_peak
-            achieved = alg / (kernel_avg_us["up"] * 1e-6) / 1e12
-    elif top == "down":
-        if decode_like:
-            alg = d_avg * per_expert_down + Fs * H * eb + (up_rows + T) * H * 4
-            bound, unit, peak = "hbm", "GB/s", hbm_peak
-            achieved = alg / (kernel_avg_us["down"] * 1e-6) / 1e9
+            ys = (up_rows + T) * H * (4 if decode_like else eb)
+            kbytes = d_avg * per_expert_down + Fs * H * eb + hrows + ys
+            kflops = 2.0 * up_rows * F * H + 2.0 * T * Fs * H
+        kt = kernel_avg_us[top] * 1e-6
+        if kbytes / (hbm_peak * 1e9) >= kflops / (tc_peak * 1e12):
+            alg, bound, unit, peak = kbytes, "hbm", "GB/s", hbm_peak
+            achieved = alg / kt / 1e9
         else:
-            alg = 2.0 * up_rows * F * H + 2.0 * T * Fs * H
-            bound, unit, peak = "tensor", "TFLOP/s", tc_peak
-            achieved = alg / (kernel_avg_us["down"] * 1e-6) / 1e12
+            alg, bound, unit, peak = kflops, "tensor", "TFLOP/s", tc_peak
+            achieved = alg / kt / 1e12
     else:
         alg, bound, unit, peak, achieved = None, "hbm", "GB/s", hbm_peak, None
     traffic = _traffic_from_profiles(top, workload)
