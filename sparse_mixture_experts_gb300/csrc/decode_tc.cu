@@ -59,7 +59,9 @@ constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
 constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 1024;
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
 constexpr int DT_SATURATING_CTAS = 128;         // CTAs streaming at once that saturate HBM
-constexpr int DT_DOWN_GUIDE = 1;                // down ranges: a round of units takes 1/GUIDE of the groups left
+constexpr int DT_UP_MIN_KB = 8;                 // smallest gate/up split, in 64-wide K blocks
+constexpr int DT_DOWN_GUIDE = 1;                // down ranges: a round of units takes 1/GUIDE of the K blocks left
+constexpr int DT_DOWN_MIN_KB = 16;              // smallest down range, in 64-wide K blocks (but the last)
 constexpr int DT_MAX_DOWN_SPLITS = 64;
 constexpr int DT_CLAIM_AHEAD = 4;               // stages before a unit's end at which the next one is claimed
 constexpr int DT_TICKET_DOWN = 8192;            // offset of the down tiles' tickets
@@ -159,45 +161,62 @@ __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
 // ---------------------------------------------------------------------------
 // schedules (every CTA computes the same ones from the group count)
 // ---------------------------------------------------------------------------
-// Gate/up split count.  One SM streams at most about 120 GB/s by TMA alone
-// and less beside the MMA and handoffs, so about 128 CTAs streaming at once
-// saturate HBM; below that many tiles, each
-// tile is split along K into S parts (each split costs a partial-sum round
-// trip through L2), otherwise not at all.
-__device__ __forceinline__ int up_splits(int tiles, int smax, int max_units)
+// Gate/up splits.  One SM streams at most about 120 GB/s by TMA alone and
+// less beside the MMA and handoffs, so about 128 CTAs streaming at once
+// saturate HBM.  Below that many tiles every tile is split along K into S
+// parts.  Otherwise the tiles of the last, partial round of claims (tiles mod
+// G, when that is at most G / 2) are split so that round has about G units of
+// at least DT_UP_MIN_KB K blocks, and the others are not.  Each split costs a partial-sum round trip
+// through L2.  Sets the first split tile and the split count of the rest.
+__device__ __forceinline__ void up_splits(int tiles, int nkb, int G, int max_units, int &full, int &S)
 {
-    if (tiles >= DT_SATURATING_CTAS) return 1;
-    int S = min(smax, (DT_SATURATING_CTAS + tiles - 1) / tiles);
-    while (S > 1 && tiles * S > max_units) --S;
-    return max(1, S);
+    const int smax = max(1, min(16, nkb / DT_UP_MIN_KB));
+    int r;
+    if (tiles < DT_SATURATING_CTAS) {
+        full = 0;
+        r = tiles;
+        S = min(smax, (DT_SATURATING_CTAS + tiles - 1) / tiles);
+    } else {
+        r = tiles % G;
+        if (2 * r > G) r = 0;  // the last round is more than half full already
+        full = tiles - r;
+        S = r > 0 ? min(smax, (G + r - 1) / r) : 1;
+    }
+    while (S > 1 && r * S > max_units) --S;
+    S = max(1, S);
 }
 
-// Down split boundaries (group ranges), the same in every CTA.  Units are
-// claimed split-major, so the ranges shrink toward the end (guided
-// self-scheduling): about one round of units (G / ot splits) covers
-// 1 / DT_DOWN_GUIDE of the groups still left, and the last units claimed are
-// one group each; at most maxs splits.  Returns the split count; b[0..S]
-// are the boundaries.
-__device__ __forceinline__ int down_bounds(int groups, int ot, int G, int maxs, int *b)
+// Down split boundaries, the same in every CTA.  The down projection's K is
+// the concatenation of every group's h' (F / 64 blocks per routed expert, then
+// Fs / 64 for the shared expert); a down unit is one output tile over a range
+// of those K blocks, which may span groups.  Units are claimed split-major, so
+// the ranges shrink toward the end (guided self-scheduling): about one round
+// of units (G / ot splits) covers 1 / DT_DOWN_GUIDE of the blocks still left,
+// down to DT_DOWN_MIN_KB; at most maxs splits.  Returns the split count;
+// b[0..S] are the boundaries in K blocks.
+__device__ __forceinline__ int down_bounds(int total_kb, int ot, int G, int maxs, int *b)
 {
     const int per_round = max(1, G / ot) * DT_DOWN_GUIDE;
-    int s = 0, g = 0;
+    int s = 0, k = 0;
     b[0] = 0;
-    while (g < groups) {
-        const int left = groups - g;
-        g += (s == maxs - 1) ? left : (left + per_round - 1) / per_round;
-        b[++s] = g;
+    while (k < total_kb) {
+        const int left = total_kb - k;
+        int size = max(DT_DOWN_MIN_KB, (left + per_round - 1) / per_round);
+        if (s == maxs - 1 || size > left) size = left;
+        k += size;
+        b[++s] = k;
     }
     return s;
 }
 
 struct Sched {
     int n_act, groups;
-    int tiles_routed, up_tiles, nkb, S_up, up_units;  // gate/up
+    int tiles_routed, up_tiles, nkb, up_full, S_up, up_units;  // gate/up: tiles [up_full, up_tiles) are split S_up ways
     int ot;                                          // down output tiles (the split count comes later)
+    int per, kb_routed, total_kb;                    // down K blocks: per routed group, all routed, all
 };
 
-__device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act)
+__device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act, int G)
 {
     Sched s;
     s.n_act = n_act;
@@ -205,25 +224,40 @@ __device__ __forceinline__ Sched make_sched(const DecArgs &a, int n_act)
     s.tiles_routed = n_act * (a.F / 64);
     s.up_tiles = s.tiles_routed + a.Fs / 64;
     s.nkb = a.H / 64;
-    s.S_up = up_splits(s.up_tiles, max(1, min(16, s.nkb / 2)), a.max_units);
-    s.up_units = s.up_tiles * s.S_up;
+    up_splits(s.up_tiles, s.nkb, G, a.max_units, s.up_full, s.S_up);
+    s.up_units = s.up_full + (s.up_tiles - s.up_full) * s.S_up;
     s.ot = (a.H + 127) / 128;
+    s.per = a.F / 64;
+    s.kb_routed = n_act * s.per;
+    s.total_kb = s.kb_routed + a.Fs / 64;
     return s;
 }
 
-// gate/up unit u (< up_units): tile = u / S_up (group-major), split s
+// gate/up unit u (< up_units): tiles in group-major order, the split ones last;
+// split s of S, whose partial goes to slot pslot + s
 struct UpUnit {
-    int g, ft, kb0, kb1, tile, s;
+    int g, ft, kb0, kb1, tile, s, S, pslot;
     bool shared;
 };
 
 __device__ __forceinline__ UpUnit up_unit(const Sched &s, int u, int F)
 {
     UpUnit x;
-    x.tile = u / s.S_up;
-    x.s = u - x.tile * s.S_up;
-    x.kb0 = (int)((long long)s.nkb * x.s / s.S_up);
-    x.kb1 = (int)((long long)s.nkb * (x.s + 1) / s.S_up);
+    if (u < s.up_full) {
+        x.tile = u;
+        x.s = 0;
+        x.S = 1;
+        x.pslot = 0;
+    } else {
+        const int v = u - s.up_full;
+        const int i = v / s.S_up;
+        x.tile = s.up_full + i;
+        x.s = v - i * s.S_up;
+        x.S = s.S_up;
+        x.pslot = i * s.S_up;
+    }
+    x.kb0 = s.nkb * x.s / x.S;
+    x.kb1 = s.nkb * (x.s + 1) / x.S;
     const int per = F / 64;
     if (x.tile < s.tiles_routed) {
         x.g = x.tile / per;
@@ -237,9 +271,10 @@ __device__ __forceinline__ UpUnit up_unit(const Sched &s, int u, int F)
     return x;
 }
 
-// down unit d (= u - up_units): split s = d / ot (so early units need early groups), tile ot
+// down unit d (= u - up_units): split s = d / ot (so early units need early
+// groups), output tile d % ot, K blocks [kb0, kb1) of the concatenated groups
 struct DnUnit {
-    int tile, s, g0, g1;
+    int tile, s, kb0, kb1;
 };
 
 __device__ __forceinline__ DnUnit dn_unit(const Sched &s, int d, const int *bounds)
@@ -247,9 +282,21 @@ __device__ __forceinline__ DnUnit dn_unit(const Sched &s, int d, const int *boun
     DnUnit x;
     x.s = d / s.ot;
     x.tile = d - x.s * s.ot;
-    x.g0 = bounds[x.s];
-    x.g1 = bounds[x.s + 1];
+    x.kb0 = bounds[x.s];
+    x.kb1 = bounds[x.s + 1];
     return x;
+}
+
+// the group of concatenated down K block kb, and the block within that group
+__device__ __forceinline__ int dn_group(const Sched &s, int kb, int &local)
+{
+    if (kb < s.kb_routed) {
+        const int g = kb / s.per;
+        local = kb - g * s.per;
+        return g;
+    }
+    local = kb - s.kb_routed;
+    return s.n_act;
 }
 
 __device__ __forceinline__ int ld_acquire(const int *p)
@@ -446,7 +493,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             a.meta->n_pairs = P;
         }
     }
-    const Sched sc = make_sched(a, n_act);
+    const Sched sc = make_sched(a, n_act, G);
     int *tickets = a.counters;
     int *group_done = a.counters + DT_GROUP_DONE;
     int *next_unit = a.counters + DT_NEXT_UNIT;
@@ -484,36 +531,42 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 if (++qi == DT_ACC) qi = 0, qph ^= 1;
                 if (u < 0) break;
                 const bool is_up = u < sc.up_units;
-                int g0 = 0, g1 = 1, left;
+                UpUnit ux;
                 DnUnit dn;
+                int seg_k, seg_end;  // K blocks of the unit (down: of the concatenated groups)
                 if (is_up) {
-                    const UpUnit x = up_unit(sc, u, a.F);
-                    left = x.kb1 - x.kb0;
+                    ux = up_unit(sc, u, a.F);
+                    seg_k = ux.kb0;
+                    seg_end = ux.kb1;
                 } else {
                     dn = dn_unit(sc, u - sc.up_units, s_dnb);
-                    g0 = dn.g0;
-                    g1 = dn.g1;
-                    left = 0;
-                    for (int gi = g0; gi < g1; ++gi) left += (gi == sc.n_act ? a.Fs : a.F) / 64;
+                    seg_k = dn.kb0;
+                    seg_end = dn.kb1;
                 }
+                int left = seg_end - seg_k;
                 // the next unit is claimed a few stages before this one ends, so
                 // the counter's round trip overlaps this unit's loads.  Claims stay
                 // in order: a CTA holds at most one unclaimed-ahead unit, and a
                 // down unit only waits for gate/up units, which never wait.
                 bool claimed = false;
-                for (int gi = g0; gi < g1 && ok; ++gi) {
+                // one segment per group the unit's K blocks fall in (gate/up: one)
+                while (seg_k < seg_end && ok) {
                     int kb0, kb1, arow, brow;
                     const CUtensorMap *ma, *mb = nullptr;
                     if (is_up) {
-                        const UpUnit x = up_unit(sc, u, a.F);
-                        kb0 = x.kb0; kb1 = x.kb1;
-                        if (x.shared) { ma = &maps.sh_gate; mb = &maps.sh_up; arow = x.ft * 64; }
-                        else { ma = &maps.gate; mb = &maps.up; arow = s_act[x.g] * a.F + x.ft * 64; }
+                        kb0 = seg_k; kb1 = seg_end;
+                        seg_k = seg_end;
+                        if (ux.shared) { ma = &maps.sh_gate; mb = &maps.sh_up; arow = ux.ft * 64; }
+                        else { ma = &maps.gate; mb = &maps.up; arow = s_act[ux.g] * a.F + ux.ft * 64; }
                         brow = 0;
                     } else {
+                        int local;
+                        const int gi = dn_group(sc, seg_k, local);
                         const bool shared = gi == sc.n_act;
                         const int fd = shared ? a.Fs : a.F;
-                        kb0 = 0; kb1 = fd / 64;
+                        const int n = min(fd / 64 - local, seg_end - seg_k);
+                        kb0 = local; kb1 = local + n;
+                        seg_k += n;
                         if (shared) { ma = &maps.sh_down; arow = dn.tile * 128; }
                         else { ma = &maps.down; arow = s_act[gi] * a.H + dn.tile * 128; }
                         brow = gi * DT_TOK;
@@ -605,8 +658,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                     nk = x.kb1 - x.kb0;
                 } else {
                     const DnUnit d = dn_unit(sc, u - sc.up_units, s_dnb);
-                    nk = 0;
-                    for (int gi = d.g0; gi < d.g1; ++gi) nk += (gi == sc.n_act ? a.Fs : a.F) / 64;
+                    nk = d.kb1 - d.kb0;
                 }
                 bool ok = true;
                 for (int kb = 0; kb < nk; ++kb) {
@@ -648,7 +700,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             // claimed, so they are computed here rather than in the prologue.  A
             // down unit reaches the MMA and epilogue roles only through the
             // producer, which waits for this barrier first.
-            s_sdn = down_bounds(sc.groups, sc.ot, G, min(DT_MAX_DOWN_SPLITS, a.max_units / sc.ot), s_dnb);
+            s_sdn = down_bounds(sc.total_kb, sc.ot, G, min(DT_MAX_DOWN_SPLITS, a.max_units / sc.ot), s_dnb);
             mbar_arrive(&s_bnd_bar);
         }
         int qi = 0;
@@ -682,9 +734,12 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             const bool is_up = u < sc.up_units;
             UpUnit ux;
             DnUnit dx;
-            int tile, S, tbase;
-            if (is_up) { ux = up_unit(sc, u, a.F); tile = ux.tile; S = sc.S_up; tbase = 0; }
-            else { dx = dn_unit(sc, u - sc.up_units, s_dnb); tile = dx.tile; S = s_sdn; tbase = DT_TICKET_DOWN; }
+            int tile, S, tbase, pslot;
+            if (is_up) { ux = up_unit(sc, u, a.F); tile = ux.tile; S = ux.S; tbase = 0; pslot = ux.pslot; }
+            else {
+                dx = dn_unit(sc, u - sc.up_units, s_dnb);
+                tile = dx.tile; S = s_sdn; tbase = DT_TICKET_DOWN; pslot = a.max_units + tile * S;
+            }
 
             bool finalize = true;
             if (S > 1) {
@@ -692,8 +747,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 // token; the last split of the tile to arrive sums all of them in
                 // split order
                 const int split = is_up ? ux.s : dx.s;
-                const size_t pbase = (size_t)(is_up ? 0 : a.max_units) + (size_t)tile * S;
-                float *pt = a.partials + (size_t)T * 128 * pbase;
+                float *pt = a.partials + (size_t)T * 128 * pslot;
 #pragma unroll
                 for (int t = 0; t < DT_TOK; ++t)
                     if (t < T) pt[((size_t)split * T + t) * 128 + r] = v[t];
