@@ -50,7 +50,7 @@ __device__ __forceinline__ bool resolve_group(const StreamArgs &a, int g, Group 
         G.e = a.active[g];
         G.n = a.counts[G.e];
         G.row0 = a.offsets[G.e];
-        G.pairs = a.expert_rows + (size_t)G.e * a.Tmax;
+        G.pairs = a.expert_rows + G.row0;
         G.fd = a.F;
         return G.n > 0;
     }

@@ -65,7 +65,8 @@ struct TcMaps {
 enum { EPI_UP = 0, EPI_DOWN = 1, EPI_ROUTER = 2 };
 
 struct TcArgs {
-    const TileDesc *tiles;
+    const int *gfirst;  // first tile of each group and the total (this GEMM's order)
+    const int *active;  // routed experts with tokens, ascending
     const RouteMeta *meta;
     const int *counts, *offsets, *expert_rows;
     const float *gate_b, *up_b, *down_b;
@@ -89,8 +90,20 @@ struct TileInfo {
     bool shared;
 };
 
+// group tables of this launch in shared memory: first tile of each group (and
+// the total), each group's expert (E for the shared expert), its rows and its
+// first row in the expert-sorted buffers
+struct GroupTab {
+    const int *first;
+    const int *expert;
+    const int *rows, *row0;
+    int n;
+};
+
+// gcur: the caller's group cursor (each role visits its tiles in increasing
+// order, so the group only moves forward); start at 0
 template <int EPI>
-__device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti)
+__device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, const GroupTab &gt, int &gcur)
 {
     if (EPI == EPI_ROUTER) {
         // dense: every 128-token tile against every 128-row tile of the router
@@ -103,14 +116,24 @@ __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti)
         ti.nk = a.H / TC_BK;
         return true;
     }
-    const TileDesc d = a.tiles[t];
-    ti.g = d.g;
-    ti.m0 = d.m0;
-    ti.n0 = d.n0;
-    ti.shared = d.g == a.E;
-    if (d.g < 0 || d.g > a.E || (ti.shared && a.Fs == 0)) return false;
-    ti.rows = ti.shared ? a.T : a.counts[d.g];
-    ti.a_row0 = ti.shared ? a.T * a.K : a.offsets[d.g];
+    // the group of tile t: the last one whose first tile is <= t; within a
+    // group the tiles run (n, m) with m fastest
+    if (gt.n <= 0 || t < 0 || t >= gt.first[gt.n]) return false;
+    int lo = gcur;
+    if (lo < 0 || lo >= gt.n || gt.first[lo] > t) lo = 0;
+    while (lo + 1 < gt.n && gt.first[lo + 1] <= t) ++lo;
+    gcur = lo;
+    ti.g = gt.expert[lo];
+    ti.shared = ti.g == a.E;
+    if (ti.g < 0 || ti.g > a.E || (ti.shared && a.Fs == 0)) return false;
+    ti.rows = gt.rows[lo];
+    ti.a_row0 = gt.row0[lo];
+    const int mt = (ti.rows + TC_BM - 1) / TC_BM;
+    if (mt <= 0) return false;
+    const int local = t - gt.first[lo];
+    const int n = local / mt;
+    ti.m0 = (local - n * mt) * TC_BM;
+    ti.n0 = n * (EPI == EPI_UP ? TC_BN_UP / 2 : TC_BN_DOWN);
     if (EPI == EPI_UP) ti.nk = a.H / TC_BK;
     else ti.nk = (ti.shared ? a.Fs : a.F) / TC_BK;
     return ti.m0 >= 0 && ti.m0 < ti.rows && ti.n0 >= 0;
@@ -149,6 +172,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    __shared__ int s_gfirst[1026];
+    __shared__ int s_gexp[1025], s_grows[1025], s_grow0[1025];
+    GroupTab gt{s_gfirst, s_gexp, s_grows, s_grow0, 0};
+    int gcur = 0;  // this thread's group cursor
+    if constexpr (EPI != EPI_ROUTER) {
+        const int n_act = a.meta->n_active;
+        gt.n = n_act + (a.Fs > 0 ? 1 : 0);
+        const int P = a.E + 2;
+        const int *gf = a.gfirst + (EPI == EPI_UP ? 0 : P);
+        for (int i = threadIdx.x; i <= gt.n; i += TC_THREADS) s_gfirst[i] = gf[i];
+        for (int i = threadIdx.x; i < gt.n; i += TC_THREADS) {
+            s_gexp[i] = a.gfirst[2 * P + i];
+            s_grows[i] = a.gfirst[3 * P + i];
+            s_grow0[i] = a.gfirst[4 * P + i];
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -160,13 +199,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             tmap_prefetch(&maps.a);
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t last_phase[TC_STAGES];
-            bool used[TC_STAGES];
-            for (int s = 0; s < TC_STAGES; ++s) used[s] = false, last_phase[s] = 0;
+            uint32_t used = 0, last_phase = 0;  // per stage: loads issued, parity of the last
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 TileInfo ti;
-                if (!tile_info<EPI>(a, t, ti)) {
+                if (!tile_info<EPI>(a, t, ti, gt, gcur)) {
                     record_error(a.status, DEV_BAD_TILE);
                     *abort_flag = 1;
                     break;
@@ -191,15 +228,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         const int brow = ti.shared ? ti.n0 : ti.g * a.H + ti.n0;
                         tma_load_2d(sb, ti.shared ? &maps.sb0 : &maps.b0, &full[stage], kc, brow);
                     }
-                    used[stage] = true;
-                    last_phase[stage] = phase;
+                    used |= 1u << stage;
+                    last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == TC_STAGES) stage = 0, phase ^= 1;
                 }
             }
             // drain: no copy of ours may still be landing when the CTA exits
             volatile int never = 0;
             for (int s = 0; s < TC_STAGES; ++s)
-                if (used[s]) mbar_wait(&full[s], last_phase[s], &never);
+                if ((used >> s) & 1u) mbar_wait(&full[s], (last_phase >> s) & 1u, &never);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
@@ -213,7 +250,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             uint32_t last_acc_phase = 0;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
                 TileInfo ti;
-                if (!tile_info<EPI>(a, t, ti)) break;
+                if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
                 const int b = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!mbar_wait(&acc_empty[b], acc_phase ^ 1, abort_flag)) {
@@ -261,7 +298,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         int it = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
             TileInfo ti;
-            if (!tile_info<EPI>(a, t, ti)) break;
+            if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
             const int b = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             if (!mbar_wait(&acc_full[b], acc_phase, abort_flag)) {
@@ -331,7 +368,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 if (valid) {
                     if (ti.shared) { tok = j; slot = a.K; wgt = a.sh_gate[tok]; }
                     else {
-                        const int p = a.expert_rows[(size_t)ti.g * a.Tmax + j];
+                        const int p = a.expert_rows[ti.a_row0 + j];
                         tok = p / a.K; slot = p - tok * a.K; wgt = a.topk_w[p];
                     }
                 }
@@ -379,38 +416,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 }
 
 // ---------------------------------------------------------------------------
-// gather: Xp[sorted row] = x[token]; routed rows then the shared rows (= x)
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) gather_rows_kernel(const __nv_bfloat16 *__restrict__ x, int T, int K, int E,
-                                                          int H, int Tmax, int has_shared,
-                                                          const int *__restrict__ offsets,
-                                                          const int *__restrict__ expert_rows,
-                                                          __nv_bfloat16 *__restrict__ xp)
-{
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int P = T * K;
-    const int n_rows = P + (has_shared ? T : 0);
-    const int r = blockIdx.x * 8 + warp;
-    if (r >= n_rows) return;
-    int tok;
-    if (r < P) {
-        // expert of sorted row r: last e with offsets[e] <= r
-        int lo = 0, hi = E - 1;
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (offsets[mid] <= r) lo = mid;
-            else hi = mid - 1;
-        }
-        tok = expert_rows[(size_t)lo * Tmax + (r - offsets[lo])] / K;
-    } else {
-        tok = r - P;
-    }
-    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)tok * H);
-    uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * H);
-    for (int c = lane; c < H / 8; c += 32) dst[c] = __ldg(src + c);
-}
-
-// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
@@ -453,15 +458,6 @@ bool tc_supported(const Layer &L, std::string &why)
     return true;
 }
 
-void tc_tile_caps(const Layer &L, int &max_up, int &max_down)
-{
-    const long long P = (long long)L.Tmax * L.K;
-    const long long mt_routed = (P + TC_BM - 1) / TC_BM + L.E;
-    const long long mt_shared = L.Fs ? (L.Tmax + TC_BM - 1) / TC_BM + 1 : 0;
-    const long long n_dn = (L.H + TC_BN_DOWN - 1) / TC_BN_DOWN;
-    max_up = (int)(mt_routed * (L.F / (TC_BN_UP / 2)) + mt_shared * (L.Fs / (TC_BN_UP / 2)));
-    max_down = (int)((mt_routed + mt_shared) * n_dn);
-}
 
 int tc_prepare(Layer &L)
 {
@@ -506,6 +502,7 @@ static TcArgs make_tc_args(const Layer &L, int T)
     TcArgs a;
     a.meta = L.meta;
     a.counts = L.counts; a.offsets = L.offsets; a.expert_rows = L.expert_rows;
+    a.gfirst = L.gfirst; a.active = L.active;
     a.gate_b = L.gate_b; a.up_b = L.up_b; a.down_b = L.down_b;
     a.topk_w = L.topk_w; a.sh_gate = L.sh_gate;
     a.h = (__nv_bfloat16 *)L.h;
@@ -521,21 +518,13 @@ static TcArgs make_tc_args(const Layer &L, int T)
 int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStream_t s)
 {
     const TensorMaps &m = *L.tmaps;
-    if (which == 0) {
-        const int rows = T * L.K + (L.Fs ? T : 0);
-        gather_rows_kernel<<<(rows + 7) / 8, 256, 0, s>>>((const __nv_bfloat16 *)x, T, L.K, L.E, L.H, L.Tmax, L.Fs > 0,
-                                                          L.offsets, L.expert_rows, (__nv_bfloat16 *)L.xp);
-        return 1;
-    }
     TcArgs a = make_tc_args(L, T);
     const int grid = L.num_sms;
     if (which == 1) {
         TcMaps mu{m.xp, m.gate, m.up, m.sh_gate, m.sh_up};
-        a.tiles = L.up_tiles;
         tc_gemm_kernel<EPI_UP, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(mu, a);
     } else {
         TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down};
-        a.tiles = L.down_tiles;
         tc_gemm_kernel<EPI_DOWN, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(md, a);
     }
     return 1;
@@ -550,7 +539,6 @@ int launch_tc_router(const Layer &L, const void *x, int T, cudaStream_t s)
     if (!encode_2d(&mr.a, x, L.H, (uint64_t)T, TC_BM)) return -1;
     mr.b0 = mr.b1 = mr.sb0 = mr.sb1 = m.router;
     TcArgs a = make_tc_args(L, T);
-    a.tiles = nullptr;
     a.logits = L.logits;
     a.router_b = L.router_b;
     a.R = L.R;

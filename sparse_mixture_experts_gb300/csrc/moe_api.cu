@@ -233,7 +233,10 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     if ((st = dev_alloc_t(L, &L.sh_gate, T))) return st;
     if ((st = dev_alloc_t(L, &L.counts, E))) return st;
     if ((st = dev_alloc_t(L, &L.offsets, E + 1))) return st;
-    if ((st = dev_alloc_t(L, &L.expert_rows, E * T))) return st;
+    if ((st = dev_alloc_t(L, &L.expert_rows, T * K))) return st;
+    L.hist_pitch = (int)(((T + SEL_TOK - 1) / SEL_TOK + 3) / 4 * 4);
+    if ((st = dev_alloc_t(L, &L.chunk_hist, E * (size_t)L.hist_pitch))) return st;
+    if ((st = dev_alloc_t(L, &L.pair_rank, T * K))) return st;
     if ((st = dev_alloc_t(L, &L.active, E))) return st;
     if ((st = dev_alloc_t(L, &L.meta, 1))) return st;
     if ((st = dev_alloc(L, &L.h, (T * K + T) * (size_t)L.Fmax * eb))) return st;
@@ -251,11 +254,9 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     std::string why;
     L.tc_capable = tc_supported(L, why);
     if (L.tc_capable) {
-        tc_tile_caps(L, L.max_up_tiles, L.max_down_tiles);
         // routed rows (T*K, expert-sorted) then the shared expert's rows (T)
         if ((st = dev_alloc(L, &L.xp, (T * K + T) * H * eb))) return st;
-        if ((st = dev_alloc_t(L, &L.up_tiles, (size_t)L.max_up_tiles))) return st;
-        if ((st = dev_alloc_t(L, &L.down_tiles, (size_t)L.max_down_tiles))) return st;
+        if ((st = dev_alloc_t(L, &L.gfirst, 5 * (E + 2)))) return st;
         if (tc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "tensor map creation failed");
         size_t hp_b, part_b, tab_b, tick_b;
         dectc_workspace(L, hp_b, part_b, tab_b, tick_b);
@@ -354,8 +355,8 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
     if (router_bad) return fail(MOE_ERR_CUDA, "tensor map for x could not be encoded");
     run(MOE_KERNEL_SELECT, [&] { return launch_select(L, T, s); });
     run(MOE_KERNEL_GROUP, [&] { return launch_group(L, T, tc, s); });
+    run(MOE_KERNEL_GATHER, [&] { return launch_scatter(L, x, T, tc, s); });
     if (tc) {
-        run(MOE_KERNEL_GATHER, [&] { return launch_experts_tc(L, x, T, 0, s); });
         run(MOE_KERNEL_UP, [&] { return launch_experts_tc(L, x, T, 1, s); });
         run(MOE_KERNEL_DOWN, [&] { return launch_experts_tc(L, x, T, 2, s); });
     } else {

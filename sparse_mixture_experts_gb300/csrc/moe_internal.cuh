@@ -29,6 +29,8 @@ enum DeviceError : int {
 // Groups of rows a grouped kernel walks over: the routed experts that
 // received at least one token (ascending expert index), then the shared
 // expert (all tokens) when the layer has one.
+constexpr int SEL_TOK = 16;  // tokens per selection block (a grouping chunk)
+
 struct RouteMeta {
     int ticket;       // arrival counter of the grouping kernel (reset by its last block)
     int n_active;     // routed experts with count > 0
@@ -36,15 +38,6 @@ struct RouteMeta {
     int n_down_tiles; // tensor-core tiles of the down GEMM
     int n_pairs;      // T * k
     int pad[3];
-};
-
-// Tensor-core tile descriptor: group g (expert index, or E for the shared
-// expert), first row m0 within the group, first output column n0.
-struct TileDesc {
-    int g;
-    int m0;
-    int n0;
-    int pad;
 };
 
 struct TensorMaps;  // defined in expert_tc.cu
@@ -80,15 +73,17 @@ struct Layer {
     float *sh_gate = nullptr;  // [Tmax]
     int *counts = nullptr;     // [E]
     int *offsets = nullptr;    // [E + 1]
-    int *expert_rows = nullptr;// [E][Tmax] pair ids t*K+slot, ascending t
+    int *expert_rows = nullptr;// [Tmax*K] pair ids t*K+slot sorted by expert (from offsets[e]), ascending t
+    int *chunk_hist = nullptr; // [E][hist_pitch] picks per chunk of SEL_TOK tokens, then where they start
+    int *pair_rank = nullptr;  // [Tmax][K] rank of each pick among its chunk's picks of the same expert
+    int hist_pitch = 0;        // chunks per expert row (>= ceil(Tmax / SEL_TOK), a multiple of 4)
     int *active = nullptr;     // [E]
     RouteMeta *meta = nullptr;
     void *h = nullptr;         // [Tmax*K + Tmax][Fmax] activations (routed rows sorted by expert, then shared)
     void *xp = nullptr;        // [Tmax*K + Tmax][H] x rows gathered in expert order, then x (tensor-core path)
     void *ys = nullptr;        // [Tmax][K+1][H] weighted expert outputs per (token, slot), weight dtype
-    TileDesc *up_tiles = nullptr;
-    TileDesc *down_tiles = nullptr;
-    int max_up_tiles = 0, max_down_tiles = 0;
+    int *gfirst = nullptr;     // [5][E + 2] per group: first gate/up tile (and the total), first down tile
+                               // (and the total), expert (E = shared), rows, first row in the sorted buffers
     int *status = nullptr;     // DeviceError
     unsigned *gbar = nullptr;  // [2] grid-barrier arrivals / generation (decode kernel)
     int decode_grid = 0;       // blocks of the cooperative decode kernel (0 = unavailable)
@@ -396,6 +391,8 @@ void set_last_error(const char *msg);
 int launch_router(const Layer &L, const void *x, int T, cudaStream_t s);
 int launch_select(const Layer &L, int T, cudaStream_t s);
 int launch_group(const Layer &L, int T, bool build_tiles, cudaStream_t s);
+// positions of the picks in expert order; with rows, also gathers x into xp
+int launch_scatter(const Layer &L, const void *x, int T, bool rows, cudaStream_t s);
 // which: 0 = gate/up + activation, 1 = down + routing weight
 int launch_experts_stream(const Layer &L, const void *x, int T, int which, cudaStream_t s);
 int launch_combine(const Layer &L, int T, void *out, cudaStream_t s);
@@ -417,9 +414,8 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
 bool tc_supported(const Layer &L, std::string &why);
 int tc_prepare(Layer &L);  // tensor maps over the layer's weights/workspace; 0 on success
 void tc_release(Layer &L);
-// which: 0 = gather token rows, 1 = gate/up GEMM + activation, 2 = down GEMM + weight
+// which: 1 = gate/up GEMM + activation, 2 = down GEMM + weight (the token rows are gathered by launch_scatter)
 int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStream_t s);
-void tc_tile_caps(const Layer &L, int &max_up, int &max_down);
 int launch_tc_router(const Layer &L, const void *x, int T, cudaStream_t s);
 
 constexpr int MAX_LAUNCHES_PER_FORWARD = 8;

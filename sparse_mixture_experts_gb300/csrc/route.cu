@@ -14,7 +14,10 @@
 // ascending token order, their count, the exclusive prefix sum of the counts
 // (the expert's first row in the expert-sorted activation buffer), the list
 // of experts that received tokens, and the tile lists of the tensor-core path.
-// Everything is integer work with a fixed order, so it is deterministic.
+// It is a counting sort in three steps: chunk histograms and in-chunk ranks
+// (in the selection kernel), prefixes over chunks and experts (one block), and
+// the scatter of each pick to its position.  Everything is integer work with
+// a fixed order, so it is deterministic.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -89,38 +92,60 @@ int launch_router(const Layer &L, const void *x, int T, cudaStream_t s)
 }
 
 // ---------------------------------------------------------------------------
-// selection: one warp per token
+// selection: one warp per token, SEL_TOK tokens (a "chunk") per block.  Next to
+// the picks, each block records, for every expert, how many of the chunk's
+// tokens picked it (the chunk histogram, stored expert-major) and, for every
+// pick, how many earlier tokens of the chunk picked the same expert (its rank
+// within the chunk).  Both come from one SEL_TOK-bit token mask per expert.
 // ---------------------------------------------------------------------------
-
-__global__ void __launch_bounds__(256) select_kernel(const float *__restrict__ logits, int T, int E, int R, int K,
-                                                     int mode, int norm, float scale, int has_shared,
-                                                     int *__restrict__ topk_idx, float *__restrict__ topk_w,
-                                                     float *__restrict__ sh_gate)
+__global__ void __launch_bounds__(SEL_TOK * 32) select_kernel(const float *__restrict__ logits, int T, int E, int R,
+                                                              int K, int mode, int norm, float scale, int has_shared,
+                                                              int *__restrict__ topk_idx, float *__restrict__ topk_w,
+                                                              float *__restrict__ sh_gate, int hist_pitch,
+                                                              int *__restrict__ chunk_hist, int *__restrict__ pair_rank)
 {
+    __shared__ uint32_t s_tm[1024];  // bit w: token w of the chunk picked the expert
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= T) return;
-    const float *l = logits + (size_t)t * R;
-    int sel_i;
-    float sel_v, w;
-    warp_select_any(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
-    if (lane < K) {
-        topk_idx[(size_t)t * K + lane] = sel_i;
-        topk_w[(size_t)t * K + lane] = w;
+    for (int e = threadIdx.x; e < E; e += SEL_TOK * 32) s_tm[e] = 0u;
+    __syncthreads();
+    const int t = blockIdx.x * SEL_TOK + warp;
+    int sel_i = -1;
+    if (t < T) {
+        const float *l = logits + (size_t)t * R;
+        float sel_v, w;
+        warp_select_any(l, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
+        if (lane < K) {
+            topk_idx[(size_t)t * K + lane] = sel_i;
+            topk_w[(size_t)t * K + lane] = w;
+            atomicOr(&s_tm[sel_i], 1u << warp);
+        }
+        if (has_shared && lane == 0) sh_gate[t] = 1.0f / (1.0f + __expf(-l[E]));
     }
-    if (has_shared && lane == 0) sh_gate[t] = 1.0f / (1.0f + __expf(-l[E]));
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += SEL_TOK * 32)
+        chunk_hist[(size_t)e * hist_pitch + blockIdx.x] = __popc(s_tm[e]);
+    if (t < T && lane < K) pair_rank[(size_t)t * K + lane] = __popc(s_tm[sel_i] & ((1u << warp) - 1u));
 }
 
 int launch_select(const Layer &L, int T, cudaStream_t s)
 {
     const moe_config &c = L.cfg;
-    select_kernel<<<(T + 7) / 8, 256, 0, s>>>(L.logits, T, L.E, L.R, L.K, c.router_mode, c.norm_topk_prob,
-                                              c.weights_scale, L.Fs > 0, L.topk_idx, L.topk_w, L.sh_gate);
+    select_kernel<<<(T + SEL_TOK - 1) / SEL_TOK, SEL_TOK * 32, 0, s>>>(
+        L.logits, T, L.E, L.R, L.K, c.router_mode, c.norm_topk_prob, c.weights_scale, L.Fs > 0, L.topk_idx, L.topk_w,
+        L.sh_gate, L.hist_pitch, L.chunk_hist, L.pair_rank);
     return 1;
 }
 
 // ---------------------------------------------------------------------------
-// grouping: one block per expert, the last block to finish finalises
+// grouping plan: one block per expert turns its chunk histogram into where
+// each chunk's picks of the expert start (exclusive prefix over chunks) and
+// its count; the last block to finish computes the exclusive prefix of the
+// counts over experts (each expert's first row in the expert-sorted buffers),
+// the list of experts that received tokens, and for the tensor-core path the
+// first tile of every group (the active experts, then the shared expert) in
+// the gate/up and down tile orders, with each group's expert, rows and first
+// row.  The GEMMs map a tile index to its group by walking those firsts, so
+// no tile list is written.
 // ---------------------------------------------------------------------------
 constexpr int GT = 256;  // threads per grouping block
 
@@ -150,59 +175,60 @@ __device__ int block_exclusive_scan(int v, int *total)
 }
 
 struct GroupArgs {
-    const int *topk_idx;
-    int T, K, E, Tmax;
+    int T, K, E, hist_pitch;
     int has_shared, F, Fs, H;
-    int *expert_rows, *counts, *offsets, *active;
+    int *chunk_hist;  // in: [E][hist_pitch] picks per chunk; out: where each chunk's picks start (relative)
+    int *counts, *offsets, *active;
+    int *gfirst;      // [5][E + 2]: per group first gate/up tile (+ total), first down tile (+ total), expert, rows, first row
     RouteMeta *meta;
     int build_tiles;
-    TileDesc *up_tiles, *down_tiles;
-    int max_up, max_down;
-    int *status;
 };
 
 __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
 {
     const int e = blockIdx.x;
-    __shared__ int s_base;
-    __shared__ int s_last;
-    if (threadIdx.x == 0) s_base = 0;
-    __syncthreads();
+    const int tid = threadIdx.x;
+    const int nc = (a.T + SEL_TOK - 1) / SEL_TOK;
+    int *row = a.chunk_hist + (size_t)e * a.hist_pitch;  // hist_pitch is a multiple of 4
 
-    // pairs routed to expert e, in ascending token order (stable compaction)
-    for (int t0 = 0; t0 < a.T; t0 += GT) {
-        const int t = t0 + threadIdx.x;
-        int slot = -1;
-        if (t < a.T)
-            for (int q = 0; q < a.K; ++q)
-                if (__ldg(&a.topk_idx[(size_t)t * a.K + q]) == e) slot = q;
-        int total;
-        int pos = block_exclusive_scan(slot >= 0 ? 1 : 0, &total);
-        if (slot >= 0) a.expert_rows[(size_t)e * a.Tmax + s_base + pos] = t * a.K + slot;
-        __syncthreads();
-        if (threadIdx.x == 0) s_base += total;
-        __syncthreads();
+    // exclusive prefix over chunks, four consecutive chunks per thread (one
+    // 16-byte load), GT * 4 chunks per pass
+    int carry = 0;
+    for (int base = 0; base < nc; base += 4 * GT) {
+        const int c = base + 4 * tid;
+        int4 v = make_int4(0, 0, 0, 0);
+        if (c < nc) {
+            v = *reinterpret_cast<const int4 *>(row + c);
+            if (c + 1 >= nc) v.y = 0;
+            if (c + 2 >= nc) v.z = 0;
+            if (c + 3 >= nc) v.w = 0;
+        }
+        int tot;
+        const int pre = carry + block_exclusive_scan(v.x + v.y + v.z + v.w, &tot);
+        if (c < nc) *reinterpret_cast<int4 *>(row + c) = make_int4(pre, pre + v.x, pre + v.x + v.y, pre + v.x + v.y + v.z);
+        carry += tot;
     }
-    if (threadIdx.x == 0) {
-        a.counts[e] = s_base;
+
+    __shared__ int s_last;
+    if (tid == 0) {
+        a.counts[e] = carry;
+        // release this block's writes, take a ticket; the last block acquires all
         __threadfence();
-        int arrived = atomicAdd(&a.meta->ticket, 1);
-        s_last = (arrived == a.E - 1);
+        s_last = atomicAdd(&a.meta->ticket, 1) == a.E - 1;
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
 
-    // ---- last block: prefix sums, active list, tile lists ----
+    // ---- last block: offsets, active experts, group tile firsts ----
     __shared__ int s_cnt[1024];
     __shared__ int s_act[1024];
-    __shared__ int s_nact;
-    for (int i = threadIdx.x; i < a.E; i += GT) s_cnt[i] = __ldcg(&a.counts[i]);
+    const int E = a.E;
+    for (int i = tid; i < E; i += GT) s_cnt[i] = __ldcg(&a.counts[i]);
     __syncthreads();
-
     // each thread owns a contiguous run of up to 4 experts (E <= 1024)
-    const int per = (a.E + GT - 1) / GT;
-    const int beg = min(a.E, threadIdx.x * per), end = min(a.E, beg + per);
+    const int per = (E + GT - 1) / GT;
+    const int beg = min(E, tid * per), end = min(E, beg + per);
     int run = 0, run_act = 0;
     for (int i = beg; i < end; ++i) { run += s_cnt[i]; run_act += s_cnt[i] > 0; }
     int tot, tot_act;
@@ -213,52 +239,43 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
         off += s_cnt[i];
         if (s_cnt[i] > 0) { s_act[aoff] = i; a.active[aoff] = i; ++aoff; }
     }
-    if (threadIdx.x == 0) {
-        a.offsets[a.E] = tot;
-        s_nact = tot_act;
-    }
+    if (tid == 0) a.offsets[E] = tot;
+    const int n_act = tot_act;
     __syncthreads();
 
     int n_up = 0, n_down = 0;
     if (a.build_tiles) {
-        // groups: active experts, then the shared expert
-        const int n_groups = s_nact + (a.has_shared ? 1 : 0);
+        const int n_groups = n_act + (a.has_shared ? 1 : 0);  // <= E + 1
         const int n_dn = (a.H + TC_BN_DOWN - 1) / TC_BN_DOWN;
-        int cnt_up = 0, cnt_dn = 0;
         const int gper = (n_groups + GT - 1) / GT;
-        const int gb = min(n_groups, threadIdx.x * gper), ge = min(n_groups, gb + gper);
+        const int gb = min(n_groups, tid * gper), ge = min(n_groups, gb + gper);
+        int cu = 0, cd = 0;
         for (int g = gb; g < ge; ++g) {
-            const bool shared = g >= s_nact;
+            const bool shared = g >= n_act;
+            const int mt = ((shared ? a.T : s_cnt[s_act[g]]) + TC_BM - 1) / TC_BM;
+            cu += mt * ((shared ? a.Fs : a.F) / (TC_BN_UP / 2));
+            cd += mt * n_dn;
+        }
+        int fu = block_exclusive_scan(cu, &n_up);
+        int fd = block_exclusive_scan(cd, &n_down);
+        int *gu = a.gfirst, *gd = a.gfirst + (E + 2);
+        int *gx = a.gfirst + 2 * (E + 2), *gr = a.gfirst + 3 * (E + 2), *g0 = a.gfirst + 4 * (E + 2);
+        for (int g = gb; g < ge; ++g) {
+            const bool shared = g >= n_act;
             const int rows = shared ? a.T : s_cnt[s_act[g]];
             const int mt = (rows + TC_BM - 1) / TC_BM;
-            const int fd = shared ? a.Fs : a.F;
-            cnt_up += mt * (fd / (TC_BN_UP / 2));
-            cnt_dn += mt * n_dn;
+            gu[g] = fu;
+            gd[g] = fd;
+            gx[g] = shared ? E : s_act[g];
+            gr[g] = rows;
+            g0[g] = shared ? a.T * a.K : __ldcg(&a.offsets[s_act[g]]);
+            fu += mt * ((shared ? a.Fs : a.F) / (TC_BN_UP / 2));
+            fd += mt * n_dn;
         }
-        int base_up = block_exclusive_scan(cnt_up, &n_up);
-        int base_dn = block_exclusive_scan(cnt_dn, &n_down);
-        if (n_up > a.max_up || n_down > a.max_down) {
-            if (threadIdx.x == 0) record_error(a.status, DEV_BAD_TILE);
-            n_up = n_down = 0;
-        } else {
-            for (int g = gb; g < ge; ++g) {
-                const bool shared = g >= s_nact;
-                const int ge_idx = shared ? a.E : s_act[g];
-                const int rows = shared ? a.T : s_cnt[ge_idx];
-                const int mt = (rows + TC_BM - 1) / TC_BM;
-                const int fd = shared ? a.Fs : a.F;
-                // (group, n, m) order: tiles sharing a weight tile run side by side
-                for (int n = 0; n < fd / (TC_BN_UP / 2); ++n)
-                    for (int m = 0; m < mt; ++m)
-                        a.up_tiles[base_up++] = TileDesc{ge_idx, m * TC_BM, n * (TC_BN_UP / 2), 0};
-                for (int n = 0; n < n_dn; ++n)
-                    for (int m = 0; m < mt; ++m)
-                        a.down_tiles[base_dn++] = TileDesc{ge_idx, m * TC_BM, n * TC_BN_DOWN, 0};
-            }
-        }
+        if (tid == 0) { gu[n_groups] = n_up; gd[n_groups] = n_down; }
     }
-    if (threadIdx.x == 0) {
-        a.meta->n_active = s_nact;
+    if (tid == 0) {
+        a.meta->n_active = n_act;
         a.meta->n_up_tiles = n_up;
         a.meta->n_down_tiles = n_down;
         a.meta->n_pairs = a.T * a.K;
@@ -269,16 +286,72 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
 int launch_group(const Layer &L, int T, bool build_tiles, cudaStream_t s)
 {
     GroupArgs a;
-    a.topk_idx = L.topk_idx;
-    a.T = T; a.K = L.K; a.E = L.E; a.Tmax = L.Tmax;
+    a.T = T; a.K = L.K; a.E = L.E; a.hist_pitch = L.hist_pitch;
     a.has_shared = L.Fs > 0; a.F = L.F; a.Fs = L.Fs; a.H = L.H;
-    a.expert_rows = L.expert_rows; a.counts = L.counts; a.offsets = L.offsets; a.active = L.active;
+    a.chunk_hist = L.chunk_hist;
+    a.counts = L.counts; a.offsets = L.offsets; a.active = L.active;
+    a.gfirst = L.gfirst;
     a.meta = L.meta;
     a.build_tiles = build_tiles ? 1 : 0;
-    a.up_tiles = L.up_tiles; a.down_tiles = L.down_tiles;
-    a.max_up = L.max_up_tiles; a.max_down = L.max_down_tiles;
-    a.status = L.status;
     group_kernel<<<L.E, GT, 0, s>>>(a);
+    return 1;
+}
+
+// ---------------------------------------------------------------------------
+// scatter: the expert-sorted position of pick p = t*K + q of expert e is
+// offsets[e] + (start of t's chunk among e's picks) + (its rank in the chunk):
+// ascending token order within each expert.  expert_rows[position] = p; with
+// rows, also the gather of the token rows into the expert-sorted activation
+// buffer (one warp per row; the shared expert's rows, all tokens in order,
+// follow the T*K routed rows).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) scatter_kernel(const __nv_bfloat16 *__restrict__ x, int T, int K, int H,
+                                                      int has_shared, int hist_pitch, const int *__restrict__ topk_idx,
+                                                      const int *__restrict__ pair_rank,
+                                                      const int *__restrict__ chunk_start,
+                                                      const int *__restrict__ offsets, int *__restrict__ expert_rows,
+                                                      __nv_bfloat16 *__restrict__ xp)
+{
+    const int P = T * K;
+    if (xp == nullptr) {
+        // positions only: one thread per pick
+        const int p = blockIdx.x * 256 + threadIdx.x;
+        if (p >= P) return;
+        const int e = topk_idx[p], t = p / K;
+        expert_rows[offsets[e] + chunk_start[(size_t)e * hist_pitch + t / SEL_TOK] + pair_rank[p]] = p;
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + warp;
+    const int n_rows = P + (has_shared ? T : 0);
+    if (r >= n_rows) return;
+    int tok, dst;
+    if (r < P) {
+        const int e = topk_idx[r];
+        tok = r / K;
+        dst = offsets[e] + chunk_start[(size_t)e * hist_pitch + tok / SEL_TOK] + pair_rank[r];
+        if (lane == 0) expert_rows[dst] = r;
+    } else {
+        tok = r - P;
+        dst = r;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)tok * H);
+    uint4 *d = reinterpret_cast<uint4 *>(xp + (size_t)dst * H);
+    for (int c = lane; c < H / 8; c += 32) d[c] = __ldg(src + c);
+}
+
+int launch_scatter(const Layer &L, const void *x, int T, bool rows, cudaStream_t s)
+{
+    const int P = T * L.K;
+    if (!rows) {
+        scatter_kernel<<<(P + 255) / 256, 256, 0, s>>>(nullptr, T, L.K, L.H, L.Fs > 0, L.hist_pitch, L.topk_idx,
+                                                       L.pair_rank, L.chunk_hist, L.offsets, L.expert_rows, nullptr);
+        return 1;
+    }
+    const int n_rows = P + (L.Fs > 0 ? T : 0);
+    scatter_kernel<<<(n_rows + 7) / 8, 256, 0, s>>>((const __nv_bfloat16 *)x, T, L.K, L.H, L.Fs > 0, L.hist_pitch,
+                                                    L.topk_idx, L.pair_rank, L.chunk_hist, L.offsets, L.expert_rows,
+                                                    (__nv_bfloat16 *)L.xp);
     return 1;
 }
 
