@@ -13,11 +13,12 @@
 //                  w_slot * y to the (token, slot) row of the combine buffer
 //
 // Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0    TMA producer: A (token rows) and B (weight rows) tiles of
-//             128 x 64 bf16, 128-byte swizzled, into an S-stage ring
+//   warp 0    TMA producer: A (128 token rows) and B (N weight rows) tiles,
+//             64 bf16 of K per stage, 128-byte swizzled, into an S-stage ring
 //   warp 1    TMEM allocator and MMA issuer (one elected thread):
-//             tcgen05.mma.cta_group::1.kind::f16, M=128, N=128, K=16,
-//             fp32 accumulators in TMEM, two accumulator buffers
+//             tcgen05.mma.cta_group::1.kind::f16, M=128, N=256 (expert
+//             GEMMs; 128 for the router), K=16, fp32 accumulators in TMEM,
+//             two accumulator buffers
 //   warps 2-5 epilogue: tcgen05.ld of the accumulators, activation or
 //             routing weight, stores
 // Every mbarrier wait is bounded (about a second of %globaltimer); on
@@ -32,20 +33,28 @@
 
 namespace moe {
 
-constexpr int TC_STAGES = 6;
 constexpr int TC_THREADS = 192;
 constexpr int A_TILE_BYTES = TC_BM * TC_BK * 2;        // 16 KB
-constexpr int B_TILE_BYTES = 128 * TC_BK * 2;          // 16 KB (both GEMMs use N = 128)
-constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
-constexpr int TMEM_COLS = 256;                         // 2 accumulators x 128 fp32 columns
-constexpr size_t TC_SMEM = (size_t)TC_STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+// Per tile width BN (the MMA's N): the B tile, the stage, the ring depth and
+// the TMEM columns (two accumulators of BN fp32 columns).  N = 256 halves the
+// A bytes staged per weight byte, which matters because a CTA's TMA stream,
+// not HBM, limits these GEMMs once the A rows are re-read from L2.
+template <int BN>
+struct TcShape {
+    static constexpr int B_BYTES = BN * TC_BK * 2;
+    static constexpr int STAGE = A_TILE_BYTES + B_BYTES;
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+};
 
 struct TensorMaps {
     CUtensorMap xp;       // A of gate/up: [Tmax*K + Tmax][H]
     CUtensorMap h;        // A of down:    [Tmax*K + Tmax][Fmax]
-    CUtensorMap gate;     // [E*F][H], box 64 rows
+    CUtensorMap gate;     // [E*F][H], box TC_BN_UP / 2 rows
     CUtensorMap up;       // [E*F][H]
-    CUtensorMap down;     // [E*H][F], box 128 rows
+    CUtensorMap down;     // [E*H][F], box TC_BN_DOWN rows
     CUtensorMap sh_gate;  // [Fs][H]
     CUtensorMap sh_up;    // [Fs][H]
     CUtensorMap sh_down;  // [H][Fs]
@@ -53,8 +62,9 @@ struct TensorMaps {
 };
 
 // A operand, then the B operand(s) of the routed experts and of the shared
-// expert; the gate/up GEMM loads two 64-row B boxes (gate rows, up rows), the
-// down GEMM one 128-row box (b1 / sb1 unused).
+// expert; the gate/up GEMM loads two B boxes of TC_BN_UP / 2 rows (gate rows,
+// up rows), the down GEMM one box of TC_BN_DOWN rows (b1 / sb1 unused), the
+// router GEMM one of 128 rows.
 struct TcMaps {
     CUtensorMap a, b0, b1, sb0, sb1;
 };
@@ -139,9 +149,14 @@ __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, 
     return ti.m0 >= 0 && ti.m0 < ti.rows && ti.n0 >= 0;
 }
 
-template <int EPI, typename Maps>
+template <int EPI, int BN, typename Maps>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ Maps maps, const TcArgs a)
 {
+    using Sh = TcShape<BN>;
+    constexpr int TC_STAGES = Sh::STAGES;
+    constexpr int STAGE_BYTES = Sh::STAGE;
+    constexpr int B_TILE_BYTES = Sh::B_BYTES;
+    constexpr int TMEM_COLS = Sh::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + TC_STAGES * STAGE_BYTES);
@@ -241,7 +256,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, 128);
+            constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -259,7 +274,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(b * 128);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
                 for (int kb = 0; kb < ti.nk; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag)) {
                         record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
@@ -307,13 +322,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 break;
             }
             tc_fence_after();
-            const uint32_t tbase = tmem_base + lane_addr + (uint32_t)(b * 128);
+            const uint32_t tbase = tmem_base + lane_addr + (uint32_t)(b * BN);
             const int j = ti.m0 + r;              // row within the group
             const bool valid = j < ti.rows;
             if (EPI == EPI_ROUTER) {
                 // logits[t][n] (+ router bias), fp32; R need not be a multiple of 4
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 16) {
+                for (int c = 0; c < BN; c += 16) {
                     uint32_t v[16];
                     tmem_ld16(tbase + c, v);
                     tmem_ld_wait();
@@ -330,15 +345,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 }
             } else if (EPI == EPI_UP) {
                 const int fd = ti.shared ? a.Fs : a.F;
-                (void)fd;
+                const int hcols = min(BN / 2, fd - ti.n0);  // a multiple of 64 (fd is)
                 const float *bg = (!ti.shared && a.gate_b) ? a.gate_b + (size_t)ti.g * a.F + ti.n0 : nullptr;
                 const float *bu = (!ti.shared && a.up_b) ? a.up_b + (size_t)ti.g * a.F + ti.n0 : nullptr;
                 __nv_bfloat16 *hrow = a.h + (size_t)(ti.a_row0 + j) * a.Fmax + ti.n0;
 #pragma unroll 1
-                for (int c = 0; c < 64; c += 16) {
+                for (int c = 0; c < BN / 2; c += 16) {
+                    if (c >= hcols) break;
                     uint32_t g[16], u[16];
                     tmem_ld16(tbase + c, g);
-                    tmem_ld16(tbase + 64 + c, u);
+                    tmem_ld16(tbase + BN / 2 + c, u);
                     tmem_ld_wait();
                     uint32_t packed[8];
 #pragma unroll
@@ -374,9 +390,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 }
                 const float *bd = (!ti.shared && a.down_b) ? a.down_b + (size_t)ti.g * a.H + ti.n0 : nullptr;
                 __nv_bfloat16 *yrow = a.ys + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n0;
-                const int ncols = min(128, a.H - ti.n0);
+                const int ncols = min(BN, a.H - ti.n0);
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 16) {
+                for (int c = 0; c < BN; c += 16) {
                     uint32_t v[16];
                     tmem_ld16(tbase + c, v);
                     tmem_ld_wait();
@@ -465,25 +481,26 @@ int tc_prepare(Layer &L)
     if (!m) return -1;
     const uint64_t rows_all = (uint64_t)L.Tmax * L.K + L.Tmax;
     bool ok = encode_2d(&m->xp, L.xp, L.H, rows_all, TC_BM) && encode_2d(&m->h, L.h, L.Fmax, rows_all, TC_BM) &&
-              encode_2d(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
-              encode_2d(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, 64) &&
-              encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, 128) &&
+              encode_2d(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, TC_BN_UP / 2) &&
+              encode_2d(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, TC_BN_UP / 2) &&
+              encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, TC_BN_DOWN) &&
               encode_2d(&m->router, L.router_w, L.H, (uint64_t)L.R, 128);
     if (ok && L.Fs) {
-        ok = encode_2d(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, 64) && encode_2d(&m->sh_up, L.sh_up_w, L.H, L.Fs, 64) &&
-             encode_2d(&m->sh_down, L.sh_down_w, L.Fs, L.H, 128);
+        ok = encode_2d(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, TC_BN_UP / 2) &&
+             encode_2d(&m->sh_up, L.sh_up_w, L.H, L.Fs, TC_BN_UP / 2) &&
+             encode_2d(&m->sh_down, L.sh_down_w, L.Fs, L.H, TC_BN_DOWN);
     } else if (ok) {
         m->sh_gate = m->gate;
         m->sh_up = m->up;
         m->sh_down = m->down;
     }
     if (!ok) { delete m; return -1; }
-    if (cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TC_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TC_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_ROUTER, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TC_SMEM) != cudaSuccess) {
+    if (cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<TC_BN_UP>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<TC_BN_DOWN>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_ROUTER, 128, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<128>::SMEM) != cudaSuccess) {
         delete m;
         return -1;
     }
@@ -522,10 +539,10 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
     const int grid = L.num_sms;
     if (which == 1) {
         TcMaps mu{m.xp, m.gate, m.up, m.sh_gate, m.sh_up};
-        tc_gemm_kernel<EPI_UP, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(mu, a);
+        tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_UP>::SMEM, s>>>(mu, a);
     } else {
         TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down};
-        tc_gemm_kernel<EPI_DOWN, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(md, a);
+        tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_DOWN>::SMEM, s>>>(md, a);
     }
     return 1;
 }
@@ -545,7 +562,7 @@ int launch_tc_router(const Layer &L, const void *x, int T, cudaStream_t s)
     a.router_nt = (L.R + 127) / 128;
     const int tiles = ((T + TC_BM - 1) / TC_BM) * a.router_nt;
     const int grid = tiles < L.num_sms ? tiles : L.num_sms;
-    tc_gemm_kernel<EPI_ROUTER, TcMaps><<<grid, TC_THREADS, TC_SMEM, s>>>(mr, a);
+    tc_gemm_kernel<EPI_ROUTER, 128, TcMaps><<<grid, TC_THREADS, TcShape<128>::SMEM, s>>>(mr, a);
     return 1;
 }
 

@@ -422,8 +422,8 @@ constexpr int MAX_LAUNCHES_PER_FORWARD = 8;
 
 // tile geometry of the tensor-core path (used by the grouping kernel)
 constexpr int TC_BM = 128;       // token rows per tile
-constexpr int TC_BN_UP = 128;    // gate/up tile: 64 gate + 64 up columns -> 64 h columns
-constexpr int TC_BN_DOWN = 128;  // down tile: output columns
+constexpr int TC_BN_UP = 256;    // gate/up tile: 128 gate + 128 up columns -> 128 h columns
+constexpr int TC_BN_DOWN = 256;  // down tile: output columns
 constexpr int TC_BK = 64;        // K elements per pipeline stage (128 bytes of bf16)
 
 }  // namespace moe

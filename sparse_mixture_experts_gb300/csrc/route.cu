@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
         for (int g = gb; g < ge; ++g) {
             const bool shared = g >= n_act;
             const int mt = ((shared ? a.T : s_cnt[s_act[g]]) + TC_BM - 1) / TC_BM;
-            cu += mt * ((shared ? a.Fs : a.F) / (TC_BN_UP / 2));
+            cu += mt * (((shared ? a.Fs : a.F) + TC_BN_UP / 2 - 1) / (TC_BN_UP / 2));
             cd += mt * n_dn;
         }
         int fu = block_exclusive_scan(cu, &n_up);
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
             gx[g] = shared ? E : s_act[g];
             gr[g] = rows;
             g0[g] = shared ? a.T * a.K : __ldcg(&a.offsets[s_act[g]]);
-            fu += mt * ((shared ? a.Fs : a.F) / (TC_BN_UP / 2));
+            fu += mt * (((shared ? a.Fs : a.F) + TC_BN_UP / 2 - 1) / (TC_BN_UP / 2));
             fd += mt * n_dn;
         }
         if (tid == 0) { gu[n_groups] = n_up; gd[n_groups] = n_down; }
