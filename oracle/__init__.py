@@ -80,12 +80,61 @@ def _get():
             for fn in ("orc_check_config", "orc_router_logits", "orc_select", "orc_weights_for_selection",
                        "orc_expert", "orc_shared", "orc_token_output", "orc_forward", "orc_max_threads"):
                 getattr(lib, fn).restype = ctypes.c_int
+            lib.orc_e2m1_value.argtypes = [ctypes.c_uint]
+            lib.orc_e2m1_value.restype = ctypes.c_double
+            lib.orc_e8m0_scale.argtypes = [ctypes.c_uint]
+            lib.orc_e8m0_scale.restype = ctypes.c_double
+            lib.orc_mxfp4_dequant.argtypes = [VP, VP, ctypes.c_int64, I, VP]
+            lib.orc_mxfp4_dequant.restype = ctypes.c_int
             _lib = lib
     return _lib
 
 
 def _p(a):
     return None if a is None else a.ctypes.data
+
+
+def e2m1_value(code: int) -> float:
+    """Value of one E2M1 code (see moe_oracle.h)."""
+    return _get().orc_e2m1_value(int(code))
+
+
+def e8m0_scale(e: int) -> float:
+    """Scale of one E8M0 byte: 2^(e - 127)."""
+    return _get().orc_e8m0_scale(int(e))
+
+
+def mxfp4_dequant(blocks: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """[..., cols/32, 16] uint8 blocks and [..., cols/32] uint8 scales ->
+    [..., cols] float32 (exact)."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    if blocks.shape[-1] != 16 or blocks.shape[:-1] != scales.shape:
+        raise ValueError("blocks must be [..., nb, 16] and scales [..., nb]")
+    nb = scales.shape[-1]
+    rows = int(np.prod(scales.shape[:-1]))
+    out = np.empty(scales.shape[:-1] + (nb * 32,), dtype=np.float32)
+    if _get().orc_mxfp4_dequant(_p(blocks), _p(scales), rows, nb * 32, _p(out)) != 0:
+        raise ValueError("bad MXFP4 tensor")
+    return out
+
+
+def _bf16_to_f32(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+def dense_weights_of_mxfp4(weights: dict) -> dict:
+    """The float32 weights an MXFP4 layer stands for: the routed experts
+    dequantised, every bf16 tensor widened (both exact)."""
+    w = {}
+    for n, a in weights.items():
+        if n in ("gate_up_blocks", "gate_up_scales", "down_blocks", "down_scales"):
+            continue
+        w[n] = _bf16_to_f32(a)
+    w["gate_up_w"] = mxfp4_dequant(weights["gate_up_blocks"], weights["gate_up_scales"])
+    w["down_w"] = mxfp4_dequant(weights["down_blocks"], weights["down_scales"])
+    return w
 
 
 class Oracle:
@@ -104,12 +153,16 @@ class Oracle:
         c.act_alpha, c.act_limit = float(spec.act_alpha), float(spec.act_limit)
         c.has_bias = int(spec.has_bias)
         c.gate_up_interleaved = int(spec.gate_up_interleaved)
-        c.w_dtype = DTYPES[spec.dtype]
+        mx = getattr(spec, "expert_format", "dense") == "mxfp4"
+        if mx:
+            # MXFP4 experts: the layer is evaluated on its exact float32 expansion
+            weights = dense_weights_of_mxfp4(weights)
+        c.w_dtype = DTYPES["f32" if mx else spec.dtype]
         c.x_dtype = DTYPES[spec.dtype]
         self._c = c
         self._keep = {}
         w = _Weights()
-        wdt = np.uint16 if spec.dtype == "bf16" else np.float32
+        wdt = np.float32 if mx else (np.uint16 if spec.dtype == "bf16" else np.float32)
         for n in _WNAMES:
             a = weights.get(n)
             if a is not None:

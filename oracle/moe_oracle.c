@@ -323,3 +323,34 @@ int orc_forward(const orc_config *c, const orc_weights *w, const void *x,
     (void)n_threads;
     return failed ? -3 : 0;
 }
+
+/* ---- MXFP4 expert weights (see moe_oracle.h) ---- */
+double orc_e2m1_value(unsigned code)
+{
+    const unsigned sign = (code >> 3) & 1u, ex = (code >> 1) & 3u, man = code & 1u;
+    const double mag = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, (int)ex - 1);
+    return sign ? -mag : mag;
+}
+
+double orc_e8m0_scale(unsigned e8m0)
+{
+    return e8m0 == 255u ? NAN : ldexp(1.0, (int)e8m0 - 127);
+}
+
+int orc_mxfp4_dequant(const uint8_t *blocks, const uint8_t *scales, int64_t rows, int cols, float *out)
+{
+    if (!blocks || !scales || !out || rows < 0 || cols <= 0 || cols % 32) return -1;
+    const int nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int b = 0; b < nb; ++b) {
+            const double sc = orc_e8m0_scale(scales[r * nb + b]);
+            const uint8_t *blk = blocks + (r * nb + b) * 16;
+            for (int j = 0; j < 32; ++j) {
+                const unsigned byte = blk[j / 2];
+                const unsigned code = (j & 1) ? (byte >> 4) : (byte & 15u);
+                out[r * cols + b * 32 + j] = (float)(orc_e2m1_value(code) * sc);
+            }
+        }
+    }
+    return 0;
+}

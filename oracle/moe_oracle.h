@@ -125,6 +125,24 @@ int orc_forward(const orc_config *c, const orc_weights *w, const void *x,
 /* Number of OpenMP threads the library would use (1 without OpenMP). */
 int orc_max_threads(void);
 
+/* MXFP4 expert weights ("Phase 19: MoE -- gpt-oss-20b", the MXFP4 packing
+ * note under the measured tensor layout, and section 3, MXFP4 dequantisation):
+ * each row of an [out][in] matrix is stored as in/32 blocks of 16 bytes = 32
+ * four-bit E2M1 codes (low nibble = even element, high nibble = odd element),
+ * blocks running along the input dimension, with one E8M0 byte per block;
+ * value = e2m1(code) * 2^(e8m0 - 127).  E2M1 (OCP Microscaling formats): bit 3
+ * sign, bits 2..1 exponent with bias 1, bit 0 mantissa; exponent 0 encodes
+ * 0 or 0.5 (subnormal), otherwise 1.m * 2^(exponent - 1).  E8M0 255 is NaN.
+ *
+ * orc_e2m1_value: the value of one code (0..15).
+ * orc_e8m0_scale: the scale of one E8M0 byte.
+ * orc_mxfp4_dequant: out[rows][cols] (float; every value is exact in float)
+ *   from blocks [rows][cols/32][16] and scales [rows][cols/32]; cols must be
+ *   a positive multiple of 32.  Returns 0, or -1 on a bad argument. */
+double orc_e2m1_value(unsigned code);
+double orc_e8m0_scale(unsigned e8m0);
+int orc_mxfp4_dequant(const uint8_t *blocks, const uint8_t *scales, int64_t rows, int cols, float *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -152,6 +152,7 @@ class LayerSpec:
     dtype: str = "bf16"                    # weights and activations: "f32" / "bf16"
     router_init: str = "normal"            # "normal" / "uniform" / "zipf"
     zipf_s: float = 1.1
+    expert_format: str = "dense"           # "dense" (dtype) or "mxfp4" (routed experts; rest bf16)
 
     def replace(self, **kw) -> "LayerSpec":
         return dataclasses.replace(self, **kw)
@@ -164,6 +165,8 @@ QWEN_ZIPF = QWEN.replace(name="qwen35moe-shaped, Zipf s=1.1 expert load (H=2048,
 GPTOSS = LayerSpec("gpt-oss-20b-shaped (H=2880, E=32, top-4, F=2880, biases, clamped GLU)", 2880, 32, 4, 2880,
                    router_mode="topk_softmax", act="clamp_glu", has_bias=True, gate_up_interleaved=True)
 MIXTRAL = LayerSpec("mixtral-shaped (H=4096, E=8, top-2, F=14336)", 4096, 8, 2, 14336, router_init="uniform")
+GPTOSS_MXFP4 = GPTOSS.replace(name="gpt-oss-20b-shaped, MXFP4 experts (H=2880, E=32, top-4, F=2880, biases)",
+                              expert_format="mxfp4")
 
 # workload -> token counts exercised
 WORKLOADS = {
@@ -172,11 +175,13 @@ WORKLOADS = {
     "qwen_prefill_zipf": (QWEN_ZIPF, (4096,)),
     "gptoss": (GPTOSS, (1, 64, 2048)),
     "mixtral": (MIXTRAL, (1, 16, 256, 4096, 16384)),
+    "gptoss_mxfp4": (GPTOSS_MXFP4, (1, 4, 16, 64)),
 }
 
 # stream ids, one per tensor
 _S = dict(router_w=1, router_b=2, gate_w=3, up_w=4, gate_up_w=5, gate_up_b=6, down_w=7, down_b=8,
-          sh_gate_w=9, sh_up_w=10, sh_down_w=11, sh_gate_inp=12, zipf_perm=20, zipf_dir=21, x=100)
+          sh_gate_w=9, sh_up_w=10, sh_down_w=11, sh_gate_inp=12, zipf_perm=20, zipf_dir=21,
+          gate_up_blocks=30, gate_up_scales=31, down_blocks=32, down_scales=33, x=100)
 _ZIPF_ALPHA = 8.0
 _BIAS_STD = math.sqrt(0.02)
 
@@ -195,11 +200,32 @@ def _zipf_parts(spec: LayerSpec, seed: int):
     return logp, u
 
 
+def _mxfp4(rows_shape, cols: int, seed: int, blocks_stream: int, scales_stream: int):
+    """MXFP4 tensor [*rows_shape][cols]: blocks [..][cols/32][16] of uniformly
+    drawn bytes (every E2M1 code equally likely) and one E8M0 scale per block
+    drawn from {119, 120, 121}: |code value| has RMS 2.93, so the values have
+    RMS near 1/sqrt(cols) for cols around 2880, like the dense layers."""
+    nb = cols // 32
+    n_rows = int(np.prod(rows_shape))
+    raw = u64((n_rows * nb * 16 + 7) // 8, seed, blocks_stream)
+    blocks = raw.view(np.uint8)[: n_rows * nb * 16].reshape(tuple(rows_shape) + (nb, 16)).copy()
+    sc = u64(n_rows * nb, seed, scales_stream)
+    scales = (119 + (sc % np.uint64(3))).astype(np.uint8).reshape(tuple(rows_shape) + (nb,))
+    return blocks, scales
+
+
 def make_weights(spec: LayerSpec, seed: int = 0) -> dict:
     """All weight/bias tensors of one layer as numpy arrays (float32, or
-    uint16 bf16 bit patterns when spec.dtype == "bf16")."""
+    uint16 bf16 bit patterns when spec.dtype == "bf16").  With
+    expert_format == "mxfp4" the routed experts come as MXFP4 blocks and
+    scales (uint8): gate_up_blocks [E][2F][H/32][16] (rows interleaved gate,
+    up), gate_up_scales [E][2F][H/32], down_blocks [E][H][F/32][16],
+    down_scales [E][H][F/32]; router, biases and activations stay bf16."""
     H, E, F, Fs, dt = spec.hidden, spec.n_expert, spec.expert_ff, spec.shared_ff, spec.dtype
     w = {}
+    if spec.expert_format == "mxfp4":
+        if dt != "bf16" or not spec.gate_up_interleaved or Fs or H % 32 or F % 32:
+            raise ValueError("mxfp4 layers: bf16, interleaved gate_up, no shared expert, H and F multiples of 32")
     if spec.router_init == "uniform":
         a = math.sqrt(3.0 / H)
         w["router_w"] = uniform((E, H), -a, a, seed, _S["router_w"], dt)
@@ -214,6 +240,11 @@ def make_weights(spec: LayerSpec, seed: int = 0) -> dict:
         w["router_b"] = normal((E,), _BIAS_STD, seed, _S["router_b"], dt)
         w["gate_up_b"] = normal((E, 2 * F), _BIAS_STD, seed, _S["gate_up_b"], dt)
         w["down_b"] = normal((E, H), _BIAS_STD, seed, _S["down_b"], dt)
+    if spec.expert_format == "mxfp4":
+        w["gate_up_blocks"], w["gate_up_scales"] = _mxfp4((E, 2 * F), H, seed, _S["gate_up_blocks"],
+                                                          _S["gate_up_scales"])
+        w["down_blocks"], w["down_scales"] = _mxfp4((E, H), F, seed, _S["down_blocks"], _S["down_scales"])
+        return w
     if spec.gate_up_interleaved:
         w["gate_up_w"] = normal((E, 2 * F, H), 1.0 / math.sqrt(H), seed, _S["gate_up_w"], dt)
     else:
@@ -243,6 +274,9 @@ def make_x(spec: LayerSpec, n_tokens: int, seed: int = 0, first_token: int = 0) 
 
 def weight_bytes_per_expert(spec: LayerSpec) -> int:
     """Bytes of one routed expert's weights (and biases) as stored."""
+    if spec.expert_format == "mxfp4":
+        n = 3 * spec.hidden * spec.expert_ff  # codes: half a byte each; a scale byte per 32
+        return n // 2 + n // 32 + (2 * spec.expert_ff + spec.hidden) * 2
     el = 2 if spec.dtype == "bf16" else 4
     n = 3 * spec.hidden * spec.expert_ff
     if spec.has_bias:

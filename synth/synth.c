@@ -108,6 +108,9 @@ void synth_uniform_bf16(uint64_t seed, uint64_t stream, uint64_t offset, int64_t
 void synth_u64(uint64_t seed, uint64_t stream, uint64_t offset, int64_t n, uint64_t *out)
 {
     uint64_t key = stream_key(seed, stream);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t i = 0; i < n; ++i)
         out[i] = draw(key, offset + (uint64_t)i);
 }

@@ -435,3 +435,98 @@ def test_invalid_configs_are_rejected():
         oracle.Oracle(synth.LayerSpec("bad", 8, 4, 5, 4, dtype="f32"), {})
     with pytest.raises(ValueError):
         oracle.Oracle(synth.LayerSpec("bad", 8, 4, 0, 4, dtype="f32"), {})
+
+
+# ----------------------------------------------------------------------------
+# MXFP4 expert weights ("Phase 19: MoE -- gpt-oss-20b": MXFP4 packing note and
+# section 3, dequantisation; E2M1 values from the OCP Microscaling formats)
+# ----------------------------------------------------------------------------
+
+# the sixteen E2M1 values as the OCP definition lists them
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def test_e2m1_code_table():
+    vals = [oracle.e2m1_value(c) for c in range(16)]
+    assert vals == E2M1_TABLE
+    # sign bit 3, magnitudes of 0..7 strictly increasing from 0, largest 6
+    for c in range(8):
+        assert vals[c + 8] == -vals[c] and math.copysign(1.0, vals[c + 8]) == -1.0
+    assert all(vals[c] < vals[c + 1] for c in range(7)) and max(vals) == 6.0
+
+
+def test_e8m0_scale():
+    assert oracle.e8m0_scale(127) == 1.0
+    assert oracle.e8m0_scale(128) == 2.0 and oracle.e8m0_scale(126) == 0.5
+    assert oracle.e8m0_scale(0) == 2.0 ** -127 and oracle.e8m0_scale(254) == 2.0 ** 127
+    assert math.isnan(oracle.e8m0_scale(255))
+
+
+def test_mxfp4_nibble_order_and_block_direction():
+    # one row of 64 elements = two blocks along the input dimension
+    blocks = np.zeros((1, 2, 16), dtype=np.uint8)
+    scales = np.array([[127, 129]], dtype=np.uint8)
+    blocks[0, 0, 0] = 0x21   # element 0 = code 1 (low nibble), element 1 = code 2 (high nibble)
+    blocks[0, 1, 15] = 0xF7  # element 32 + 30 = code 7, element 32 + 31 = code 15
+    v = oracle.mxfp4_dequant(blocks, scales)[0]
+    assert v[0] == 0.5 and v[1] == 1.0
+    assert v[62] == 6.0 * 4 and v[63] == -6.0 * 4
+    assert np.count_nonzero(v) == 4
+
+
+def _numpy_dequant(blocks, scales):
+    """The same definition restated with numpy bit operations (table lookup)."""
+    lo, hi = blocks & 0x0F, blocks >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(blocks.shape[:-1] + (32,))
+    vals = np.array(E2M1_TABLE)[codes] * np.ldexp(1.0, scales.astype(np.int64) - 127)[..., None]
+    return vals.reshape(scales.shape[:-1] + (scales.shape[-1] * 32,))
+
+
+def test_mxfp4_dequant_matches_table_restatement():
+    spec = synth.GPTOSS_MXFP4.replace(hidden=96, n_expert=3, expert_ff=64, top_k=2)
+    w = synth.make_weights(spec, seed=3)
+    for b, s in (("gate_up_blocks", "gate_up_scales"), ("down_blocks", "down_scales")):
+        np.testing.assert_array_equal(oracle.mxfp4_dequant(w[b], w[s]), _numpy_dequant(w[b], w[s]))
+
+
+def test_hand_example_mxfp4(golden_dir):
+    with open(os.path.join(golden_dir, "hand_example_mxfp4.json")) as f:
+        g = json.load(f)
+    spec = _spec_from(g["layer"])
+    H, E, F = spec.hidden, spec.n_expert, spec.expert_ff
+    w = {
+        "router_w": synth.to_bf16(np.zeros((E, H), np.float32)),
+        "router_b": synth.to_bf16(np.array(g["router_b"], np.float32)),
+        "gate_up_b": synth.to_bf16(np.zeros((E, 2 * F), np.float32)),
+        "down_b": synth.to_bf16(np.zeros((E, H), np.float32)),
+        "gate_up_blocks": np.zeros((E, 2 * F, H // 32, 16), np.uint8),
+        "gate_up_scales": np.full((E, 2 * F, H // 32), g["scales_default"], np.uint8),
+        "down_blocks": np.zeros((E, H, F // 32, 16), np.uint8),
+        "down_scales": np.full((E, H, F // 32), g["scales_default"], np.uint8),
+    }
+    for nz in g["nonzero_bytes"]:
+        w[nz["tensor"]][nz["expert"], nz["row"], 0, nz["byte"]] = int(nz["value"], 16)
+    for so in g["scale_overrides"]:
+        w[so["tensor"]][so["expert"], so["row"], so["block"]] = so["value"]
+    x = np.zeros((1, H), np.float32)
+    x[0, :len(g["x"])] = g["x"]
+    out, idx, wt = oracle.Oracle(spec, w).forward(synth.to_bf16(x))
+    assert idx[0].tolist() == [0] and wt[0].tolist() == [1.0]
+    exp = [_ev(v) for v in g["expected_out_first2"]]
+    np.testing.assert_allclose(out[0, :2], exp, rtol=1e-13, atol=0)
+    assert np.count_nonzero(out[0, 2:]) == 0
+
+
+def test_mxfp4_layer_equals_dense_layer_of_its_values():
+    # the MXFP4 layer is the dense layer whose weights are the dequantised values
+    spec = synth.GPTOSS_MXFP4.replace(hidden=64, n_expert=4, expert_ff=64, top_k=2)
+    w = synth.make_weights(spec, seed=5)
+    dense = {k: synth.bf16_to_f32(v) for k, v in w.items() if v.dtype == np.uint16}
+    dense["gate_up_w"] = _numpy_dequant(w["gate_up_blocks"], w["gate_up_scales"]).astype(np.float32)
+    dense["down_w"] = _numpy_dequant(w["down_blocks"], w["down_scales"]).astype(np.float32)
+    x = synth.make_x(spec, 5, seed=2)
+    out_mx, idx_mx, _ = oracle.Oracle(spec, w).forward(x)
+    dspec = spec.replace(dtype="f32", expert_format="dense")
+    out_d, idx_d, _ = oracle.Oracle(dspec, dense).forward(synth.bf16_to_f32(x))
+    np.testing.assert_array_equal(idx_mx, idx_d)
+    np.testing.assert_array_equal(out_mx, out_d)
