@@ -52,6 +52,7 @@ WORKLOADS = {
     "gptoss_prefill": (synth.GPTOSS, 2048, (), 3),
     "mixtral_decode": (synth.MIXTRAL, 1, (16, 256), 3),
     "mixtral_prefill": (synth.MIXTRAL, 4096, (16384,), 2),
+    "gptoss_mxfp4_decode": (synth.GPTOSS_MXFP4, 1, (4, 16), 6),
 }
 N_BATCHES = 16  # distinct token batches cycled through
 
@@ -181,6 +182,8 @@ def oracle_rate(spec, w, budget_s: float = 12.0, max_tokens: int = 1 << 16, seed
 
 
 def _spec_dtype(spec):
+    if spec.expert_format == "mxfp4":
+        return "mxfp4-f16"  # MXFP4 expert weights widened to f16 for the MMA, fp32 accumulation
     return "bf16" if spec.dtype == "bf16" else "f32"
 
 
@@ -271,6 +274,10 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
     for k, v in w.items():
         t = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16) if v.dtype == np.uint16 else torch.from_numpy(v)
         wt[k] = t.to(dev)
+    mxfp4 = spec.expert_format == "mxfp4"
+    if mxfp4:  # the ABI takes the MXFP4 blocks in the gate_up_w / down_w slots
+        wt["gate_up_w"] = wt.pop("gate_up_blocks")
+        wt["down_w"] = wt.pop("down_blocks")
     cfg = moe.MoEConfig(
         hidden=spec.hidden, n_expert=spec.n_expert, top_k=spec.top_k, expert_ff=spec.expert_ff,
         shared_ff=spec.shared_ff,
@@ -278,7 +285,7 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
         norm_topk_prob=spec.norm_topk_prob, weights_scale=spec.weights_scale,
         act=moe.ACT_SWIGLU if spec.act == "swiglu" else moe.ACT_CLAMP_GLU, act_alpha=spec.act_alpha,
         act_limit=spec.act_limit, has_bias=spec.has_bias, gate_up_interleaved=spec.gate_up_interleaved,
-        w_dtype=moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32,
+        w_dtype=moe.DT_MXFP4 if mxfp4 else (moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32),
         act_dtype=moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32, out_dtype=moe.DT_F32, max_tokens=Tmax)
     layers = [moe.MoELayer(cfg, wt, device=dev) for _ in range(n_layers)]
     del wt
@@ -351,8 +358,11 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
     batches_used = [i % N_BATCHES for i in range(args.steps)]
     d_avg = float(np.mean([distinct[b] for b in batches_used]))
     H, F, Fs, E = spec.hidden, spec.expert_ff, spec.shared_ff, spec.n_expert
-    per_expert_up = 2 * F * H * eb + (2 * F * 4 if spec.has_bias else 0)
-    per_expert_down = H * F * eb + (H * 4 if spec.has_bias else 0)
+    # weight bytes a step reads per selected expert (MXFP4: half a byte per code
+    # and a scale byte per 32 codes; biases are fp32 in the layer)
+    wel = (0.5 + 1.0 / 32) if mxfp4 else eb
+    per_expert_up = 2 * F * H * wel + (2 * F * 4 if spec.has_bias else 0)
+    per_expert_down = H * F * wel + (H * 4 if spec.has_bias else 0)
     router_bytes = (E + (1 if Fs else 0)) * H * eb
     shared_bytes = 3 * Fs * H * eb
     step_bytes = d_avg * (per_expert_up + per_expert_down) + router_bytes + shared_bytes + T * H * (eb + 4)
@@ -375,7 +385,7 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
     total_k = sum(ms for ms, _ in ktimes.values())
     kernel_share = {k: (ms / total_k if total_k else None) for k, (ms, _) in ktimes.items()}
     top = max((k for k in ktimes if ktimes[k][1]), key=lambda k: ktimes[k][0])
-    if ktimes.get("experts", (0, 0))[1]:
+    if ktimes.get("experts", (0, 0))[1] or ktimes.get("experts_mxfp4", (0, 0))[1]:
         path = "weight-streaming tensor-core"
     elif ktimes.get("fused", (0, 0))[1]:
         path = "fused"
@@ -385,9 +395,9 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
         path = "stream"
     decode_like = path != "tensor-core"
     up_rows = T * spec.top_k
-    if top in ("fused", "experts"):
+    if top in ("fused", "experts", "experts_mxfp4"):
         # all expert weights of the step stream through this one kernel
-        alg = step_bytes - (router_bytes if top == "experts" else 0)
+        alg = step_bytes - (router_bytes if top != "fused" else 0)
         bound, unit, peak = "hbm", "GB/s", hbm_peak
         achieved = alg / (kernel_avg_us[top] * 1e-6) / 1e9
     elif top in ("up", "down"):

@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
     MOE_OK = 0,
@@ -62,7 +62,30 @@ typedef enum {
     MOE_ERR_DEVICE_TIMEOUT = -6   /* a bounded device-side wait gave up */
 } moe_status;
 
-typedef enum { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
+typedef enum {
+    MOE_DT_F32 = 0,
+    MOE_DT_BF16 = 1,
+    /* w_dtype only: the routed experts' weights in MXFP4 ("Phase 19: MoE --
+     * gpt-oss-20b", MXFP4 packing note under the measured tensor layout, and
+     * section 3, MXFP4 dequantisation).  Each [out][in] matrix row is in/32
+     * blocks of 16 bytes = 32 E2M1 codes (low nibble = even element, high
+     * nibble = odd element; E2M1 as in the OCP Microscaling formats), blocks
+     * along the input dimension, plus one E8M0 byte per block; an element is
+     * e2m1(code) * 2^(e8m0 - 127).  gate_up_w / down_w then hold the blocks
+     * ([E][2F][H/32][16] and [E][H][F/32][16] bytes) and gate_up_scales /
+     * down_scales the scales ([E][2F][H/32], [E][H][F/32]); the router and the
+     * biases are bf16 and act_dtype must be bf16.  Requires
+     * gate_up_interleaved = 1, shared_ff = 0 and H, F multiples of 64.
+     * moe_create also keeps the experts dequantised to bf16 (exact: every
+     * E2M1 code times a power of two fits bf16), which the prefill paths
+     * read.  The decode path (T <= 16 on the tensor-core path) streams the
+     * codes and scales themselves and widens them to f16 on chip; that is
+     * exact when every E8M0 byte is in 113..140, so a layer with a scale
+     * outside that range decodes from the bf16 copy instead.  Either way the
+     * result equals the bf16 layer built from the dequantised weights, up to
+     * rounding order. */
+    MOE_DT_MXFP4 = 2
+} moe_dtype;
 
 typedef enum {
     /* softmax over all experts -> top-k -> (renormalise) -> * weights_scale
@@ -94,8 +117,8 @@ typedef struct {
     float act_limit;             /* MOE_ACT_CLAMP_GLU: 7.0 */
     int32_t has_bias;            /* router [E], gate_up [E][2F], down [E][H] biases */
     int32_t gate_up_interleaved; /* 1: one [E][2F][H] gate_up tensor, gate = even rows */
-    int32_t w_dtype;             /* moe_dtype of every weight and bias */
-    int32_t act_dtype;           /* moe_dtype of x; must equal w_dtype */
+    int32_t w_dtype;             /* moe_dtype of every weight and bias (MOE_DT_MXFP4: see moe_dtype) */
+    int32_t act_dtype;           /* moe_dtype of x; must equal w_dtype (bf16 with MOE_DT_MXFP4) */
     int32_t out_dtype;           /* moe_dtype of out */
     int32_t max_tokens;          /* workspace is sized once for this many tokens */
 } moe_config;
@@ -118,6 +141,8 @@ typedef struct {
     const void *sh_up_w;     /* [Fs][H] */
     const void *sh_down_w;   /* [H][Fs] */
     const void *sh_gate_inp; /* [H] scalar-gate vector */
+    const void *gate_up_scales; /* [E][2F][H/32] E8M0 bytes (w_dtype MOE_DT_MXFP4 only) */
+    const void *down_scales;    /* [E][H][F/32] E8M0 bytes (w_dtype MOE_DT_MXFP4 only) */
 } moe_weights;
 
 typedef struct moe_layer moe_layer;
@@ -197,7 +222,8 @@ typedef enum {
     MOE_KERNEL_FUSED = 7,    /* whole layer in one kernel (fused decode path) */
     MOE_KERNEL_EXPERTS = 8,  /* selection, gate/up and down in one persistent kernel
                                 (weight-streaming tensor-core decode path) */
-    MOE_KERNEL_COUNT = 9
+    MOE_KERNEL_EXPERTS_MXFP4 = 9, /* the same kernel streaming MXFP4 codes and scales */
+    MOE_KERNEL_COUNT = 10
 } moe_kernel_kind;
 
 /* Synchronises the device, then writes, per kernel kind, the summed device

@@ -21,11 +21,12 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OOM, ERR_CUDA, ERR_TOO_MANY_TOKENS, ERR_DEVICE_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 _STATUS_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CUDA", -5: "TOO_MANY_TOKENS",
                  -6: "DEVICE_TIMEOUT"}
-DT_F32, DT_BF16 = 0, 1
+DT_F32, DT_BF16, DT_MXFP4 = 0, 1, 2
 ROUTER_SOFTMAX_TOPK, ROUTER_TOPK_SOFTMAX = 0, 1
 ACT_SWIGLU, ACT_CLAMP_GLU = 0, 1
 PATH_AUTO, PATH_STREAM, PATH_TC, PATH_FUSED, PATH_DECODE_TC = 0, 1, 2, 3, 4
-KERNEL_KINDS = ("router", "select", "group", "up", "down", "combine", "gather", "fused", "experts")
+KERNEL_KINDS = ("router", "select", "group", "up", "down", "combine", "gather", "fused", "experts",
+                "experts_mxfp4")
 
 _DT = {"f32": DT_F32, "bf16": DT_BF16}
 _TORCH_DT = {DT_F32: torch.float32, DT_BF16: torch.bfloat16}
@@ -47,7 +48,7 @@ class _Config(ctypes.Structure):
 
 
 WEIGHT_NAMES = ("router_w", "router_b", "gate_w", "up_w", "gate_up_w", "gate_up_b", "down_w", "down_b",
-                "sh_gate_w", "sh_up_w", "sh_down_w", "sh_gate_inp")
+                "sh_gate_w", "sh_up_w", "sh_down_w", "sh_gate_inp", "gate_up_scales", "down_scales")
 
 
 class _Weights(ctypes.Structure):
@@ -134,7 +135,9 @@ def _stream_handle(stream) -> int:
 class MoELayer:
     """A created layer.  ``weights`` maps the names in ``WEIGHT_NAMES`` to
     tensors (device or host) in the config's weight dtype; they are copied at
-    creation."""
+    creation.  With ``w_dtype == DT_MXFP4`` the expert weights are uint8
+    tensors: gate_up_w / down_w the MXFP4 blocks, gate_up_scales /
+    down_scales the E8M0 scales (the rest bf16; see include/moe.h)."""
 
     def __init__(self, config: MoEConfig, weights: dict, device: Optional[torch.device] = None):
         lib = load_library()
@@ -154,6 +157,7 @@ class MoELayer:
             _check(lib.moe_layer_create(ctypes.byref(config._c()), ctypes.byref(w), ctypes.byref(handle)))
         self._h = handle
         self.out_dtype = _TORCH_DT[config.out_dtype]
+        self.mxfp4 = config.w_dtype == DT_MXFP4
         self.x_dtype = _TORCH_DT[config.act_dtype]
 
     # ------------------------------------------------------------------

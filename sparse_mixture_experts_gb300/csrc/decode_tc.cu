@@ -47,7 +47,7 @@ namespace moe {
 
 constexpr int DT_TOK = 16;                      // N: token columns
 constexpr int DT_STAGES = 8;
-constexpr int DT_THREADS = 192;
+constexpr int DT_THREADS = 192;                 // bf16 weights: producer, MMA, 4 epilogue warps
 constexpr int DT_A_BYTES = 128 * 64 * 2;        // 16 KB weight tile
 constexpr int DT_B_BYTES = DT_TOK * 64 * 2;     // 2 KB token tile
 constexpr int DT_STAGE_BYTES = DT_A_BYTES + DT_B_BYTES;
@@ -56,7 +56,34 @@ constexpr int DT_TMEM_COLS = DT_ACC * DT_TOK;   // 16 fp32 columns each
 constexpr int DT_EP_LD = DT_TOK + 1;            // row pitch (floats) of the epilogue's accumulator copy
 constexpr int DT_XCH_BYTES = 128 * DT_EP_LD * 4; // the accumulator tile in shared memory
 constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
-constexpr size_t DT_SMEM = (size_t)DT_STAGES * DT_STAGE_BYTES + 1024 + DT_XCH_BYTES + 1024;
+// MXFP4 weights: a stage's raw data (token tile, codes, scales) is a third of a
+// bf16 stage, so the producer's ring is deeper (DT_FP4_RS stages, about the
+// bytes in flight of the bf16 ring) and 4 more warps dequantise each raw stage
+// into a shallow ring of f16 operand slots (DT_FP4_AS), each an A tile with the
+// stage's token tile copied behind it.  The dequantising warps release the raw
+// stage themselves, so the MMA thread commits once per stage (to the slot): at
+// N = 16 the MMA thread's issue rate, not the tensor pipe, bounds this loop,
+// and every tcgen05.commit costs about as much as an MMA.
+constexpr int DT_FP4_CODES = 128 * 32;          // 128 rows x 64 four-bit codes
+constexpr int DT_FP4_SCALES = 128 * 2;          // 128 rows x 2 E8M0 bytes
+constexpr int DT_FP4_RS = 18;                   // raw stages
+constexpr int DT_FP4_AS = 4;                    // operand slots (f16 A tile + token tile)
+constexpr int DT_FP4_SLOT = DT_A_BYTES + DT_B_BYTES;  // a multiple of 1024 (128-byte swizzle atoms)
+
+template <bool FP4>
+struct DtShape {
+    static constexpr int THREADS = FP4 ? DT_THREADS + 128 : DT_THREADS;
+    static constexpr int RS = FP4 ? DT_FP4_RS : DT_STAGES;   // producer ring
+    // smem: bf16 [RS][A | B]; MXFP4 [AS][A | B] [RS][B] [RS][codes] [RS][scales]
+    static constexpr int B_OFF = FP4 ? DT_FP4_AS * DT_FP4_SLOT : DT_A_BYTES;      // first (raw) B tile
+    static constexpr int B_STRIDE = FP4 ? DT_B_BYTES : DT_STAGE_BYTES;
+    static constexpr int A_STRIDE = FP4 ? DT_FP4_SLOT : DT_STAGE_BYTES;
+    static constexpr int CODES_OFF = B_OFF + RS * DT_B_BYTES;                      // MXFP4 only
+    static constexpr int SCALES_OFF = CODES_OFF + RS * DT_FP4_CODES;
+    static constexpr int RING = FP4 ? (SCALES_OFF + RS * DT_FP4_SCALES + 1023) / 1024 * 1024
+                                    : DT_STAGES * DT_STAGE_BYTES;
+    static constexpr size_t SMEM = (size_t)RING + 1024 + DT_XCH_BYTES + 1024;
+};
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
 constexpr int DT_SATURATING_CTAS = 128;         // CTAs streaming at once that saturate HBM
 constexpr int DT_UP_MIN_KB = 8;                 // smallest gate/up split, in 64-wide K blocks
@@ -86,7 +113,9 @@ struct DecArgs {
     int *active;
     RouteMeta *meta;
     const float *gate_b, *up_b, *down_b;
-    __nv_bfloat16 *hp;    // [groups_max*16][Fmax]
+    void *hp;             // [groups_max*16][Fmax], bf16 (f16 for MXFP4 weights)
+    const uint8_t *gu_codes, *gu_scales, *dn_codes, *dn_scales;  // MXFP4 weights, packed (see Layer)
+    int ot;               // down output tiles of 128 rows
     float *partials;      // [gate/up, down][units][T][128]
     int *counters;        // tickets, group completion, work counter
     void *out;
@@ -104,6 +133,7 @@ struct DecArgs {
 // ---------------------------------------------------------------------------
 struct DecRouteArgs {
     const __nv_bfloat16 *x;
+    __half *x16;          // MXFP4 weights: f16 copy of x for the token operand (else null)
     const __nv_bfloat16 *router_w;
     const float *router_b;
     float *logits;
@@ -121,6 +151,12 @@ __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
         // kernel 2 of the previous forward has finished (stream order)
         for (int i = threadIdx.x; i < a.n_reset; i += 256) a.counters[DT_GROUP_DONE + i * DT_DONE_STRIDE] = 0;
         if (threadIdx.x == 0) a.counters[DT_NEXT_UNIT] = 0;
+    }
+    if (a.x16) {
+        // the blocks share the conversion of x (exact for |x| in the f16 range)
+        const size_t n = (size_t)a.T * H, per = (n + gridDim.x - 1) / gridDim.x;
+        const size_t i0 = (size_t)blockIdx.x * per, i1 = min(n, i0 + per);
+        for (size_t i = i0 + threadIdx.x; i < i1; i += 256) a.x16[i] = __float2half_rn(__bfloat162float(a.x[i]));
     }
     __shared__ float s_part[8][DT_TOK];
     const int r = blockIdx.x;
@@ -342,6 +378,49 @@ __device__ __forceinline__ void sum_partials(const float *pt, int S, int T, int 
     }
 }
 
+// MXFP4 -> f16: the four bytes of w hold eight E2M1 codes (low nibble = even
+// element); each byte widens to an f16 pair (hardware conversion)
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t (&h)[4])
+{
+    asm("{ .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
+}
+
+// 2^(e8m0 - 127) as an f16 pair; the layer checks at creation that every
+// scale is in 113..140, where this and every code times it are exact f16
+__device__ __forceinline__ __half2 e8m0_half2(uint32_t e8m0)
+{
+    const uint32_t b = (e8m0 - 127u + 15u) << 10;
+    const uint32_t v = b | (b << 16);
+    return *reinterpret_cast<const __half2 *>(&v);
+}
+
+// One row of an A tile from a raw stage's MXFP4 codes and scales: row r's 64
+// elements (two 32-element blocks) to f16, written in the 128-byte swizzled
+// K-major layout the MMA reads (16-byte chunk q of row r at q ^ (r & 7)).
+__device__ __forceinline__ void fp4_dequant_row(uint8_t *a_tile, const uint8_t *codes, const uint8_t *scales, int r)
+{
+    const uint4 *c = reinterpret_cast<const uint4 *>(codes + r * 32);
+    const uint4 c0 = c[0], c1 = c[1];
+    const uint8_t *sc = scales + r * 2;
+    const __half2 s0 = e8m0_half2(sc[0]), s1 = e8m0_half2(sc[1]);
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    uint8_t *row = a_tile + r * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        uint32_t h[4];
+        e2m1x8_to_f16(words[q], h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 v = __hmul2(*reinterpret_cast<__half2 *>(&h[i]), q < 4 ? s0 : s1);
+            h[i] = *reinterpret_cast<uint32_t *>(&v);
+        }
+        *reinterpret_cast<uint4 *>(row + ((q ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
 // routing weight of token t for group g (0 when t is not routed to it)
 __device__ __forceinline__ float group_weight(int g, int t, int n_act, int K, const int *s_act, const int *s_idx,
                                               const float *s_w, const float *s_gsh)
@@ -357,18 +436,24 @@ __device__ __forceinline__ float group_weight(int g, int t, int n_act, int K, co
 // ---------------------------------------------------------------------------
 // kernel 2: selection + gate/up + down, persistent, dynamic work claiming
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid_constant__ DecMaps maps,
-                                                                     const DecArgs a)
+template <bool FP4>
+__global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(const __grid_constant__ DecMaps maps,
+                                                                               const DecArgs a)
 {
+    using Sh = DtShape<FP4>;
+    constexpr int THREADS = Sh::THREADS;
+    constexpr int RS = Sh::RS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *xch = reinterpret_cast<float *>(smem + DT_STAGES * DT_STAGE_BYTES);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + DT_STAGES * DT_STAGE_BYTES + DT_XCH_BYTES);
-    uint64_t *empty = full + DT_STAGES;
-    uint64_t *acc_full = empty + DT_STAGES;   // [DT_ACC]
+    float *xch = reinterpret_cast<float *>(smem + Sh::RING);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Sh::RING + DT_XCH_BYTES);  // [RS] raw stage landed
+    uint64_t *empty = full + RS;              // [RS] raw stage consumed
+    uint64_t *acc_full = empty + RS;          // [DT_ACC]
     uint64_t *uq_full = acc_full + DT_ACC;    // [DT_ACC] unit handed out
     uint64_t *uq_empty = uq_full + DT_ACC;    // [DT_ACC] unit finished, slot and accumulator free
-    int *uq = reinterpret_cast<int *>(uq_empty + DT_ACC);  // [DT_ACC]
+    uint64_t *deq = uq_empty + DT_ACC;        // [DT_FP4_AS] MXFP4: the A tile is dequantised
+    uint64_t *a_empty = deq + DT_FP4_AS;      // [DT_FP4_AS] MXFP4: the A tile has been read by the MMA
+    int *uq = reinterpret_cast<int *>(a_empty + DT_FP4_AS);  // [DT_ACC]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(uq + DT_ACC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *bcast = reinterpret_cast<int *>(tmem_slot + 2);  // [4]
@@ -389,9 +474,9 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     const int T = a.T, K = a.K, E = a.E;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < DT_STAGES; ++s) {
+        for (int s = 0; s < RS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], FP4 ? 4 : 1);  // MXFP4: one arrival per dequantising warp
         }
         mbar_init(&s_bnd_bar, 1);
         for (int b = 0; b < DT_ACC; ++b) {
@@ -399,6 +484,11 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             mbar_init(&uq_full[b], 1);
             mbar_init(&uq_empty[b], 1);
         }
+        if (FP4)
+            for (int s = 0; s < DT_FP4_AS; ++s) {
+                mbar_init(&deq[s], 4);
+                mbar_init(&a_empty[s], 1);
+            }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -414,7 +504,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
         tmap_prefetch(&maps.down);
         tmap_prefetch(&maps.hp);
     }
-    for (int e = threadIdx.x; e < E; e += DT_THREADS) s_cnt[e] = 0;
+    for (int e = threadIdx.x; e < E; e += THREADS) s_cnt[e] = 0;
     if (threadIdx.x < 32) s_mask[threadIdx.x] = 0u;
     tc_fence_before();
     __syncthreads();
@@ -434,7 +524,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     // ---- routing, the same in every CTA ----
     // two tokens per warp at a time, so their load latencies and dependent
     // reductions overlap
-    constexpr int NW = DT_THREADS / 32;
+    constexpr int NW = THREADS / 32;
     for (int t = warp; t < T; t += 2 * NW) {
         const int t2 = t + NW;
         const bool two = t2 < T;
@@ -470,7 +560,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     const int nwords = (E + 31) / 32;
     int n_act = 0;
     for (int wd = 0; wd < nwords; ++wd) n_act += __popc(s_mask[wd]);
-    for (int e = threadIdx.x; e < E; e += DT_THREADS) {
+    for (int e = threadIdx.x; e < E; e += THREADS) {
         const uint32_t m = s_mask[e >> 5];
         if ((m >> (e & 31)) & 1u) {
             int r = __popc(m & ((1u << (e & 31)) - 1u));
@@ -480,14 +570,14 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
     }
     __syncthreads();
     if (blockIdx.x == 0) {
-        for (int p = threadIdx.x; p < P; p += DT_THREADS) {
+        for (int p = threadIdx.x; p < P; p += THREADS) {
             a.topk_idx[p] = s_idx[p];
             a.topk_w[p] = s_w[p];
         }
-        for (int e = threadIdx.x; e < E; e += DT_THREADS) a.counts[e] = s_cnt[e];
-        for (int g = threadIdx.x; g < n_act; g += DT_THREADS) a.active[g] = s_act[g];
+        for (int e = threadIdx.x; e < E; e += THREADS) a.counts[e] = s_cnt[e];
+        for (int g = threadIdx.x; g < n_act; g += THREADS) a.active[g] = s_act[g];
         if (a.Fs > 0)
-            for (int t = threadIdx.x; t < T; t += DT_THREADS) a.sh_gate[t] = s_gsh[t];
+            for (int t = threadIdx.x; t < T; t += THREADS) a.sh_gate[t] = s_gsh[t];
         if (threadIdx.x == 0) {
             a.meta->n_active = n_act;
             a.meta->n_pairs = P;
@@ -551,11 +641,12 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 bool claimed = false;
                 // one segment per group the unit's K blocks fall in (gate/up: one)
                 while (seg_k < seg_end && ok) {
-                    int kb0, kb1, arow, brow;
+                    int kb0, kb1, arow, brow, wexp;  // wexp: the segment's expert (MXFP4 weights)
                     const CUtensorMap *ma, *mb = nullptr;
                     if (is_up) {
                         kb0 = seg_k; kb1 = seg_end;
                         seg_k = seg_end;
+                        wexp = ux.shared ? 0 : s_act[ux.g];
                         if (ux.shared) { ma = &maps.sh_gate; mb = &maps.sh_up; arow = ux.ft * 64; }
                         else { ma = &maps.gate; mb = &maps.up; arow = s_act[ux.g] * a.F + ux.ft * 64; }
                         brow = 0;
@@ -567,6 +658,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                         const int n = min(fd / 64 - local, seg_end - seg_k);
                         kb0 = local; kb1 = local + n;
                         seg_k += n;
+                        wexp = shared ? 0 : s_act[gi];
                         if (shared) { ma = &maps.sh_down; arow = dn.tile * 128; }
                         else { ma = &maps.down; arow = s_act[gi] * a.H + dn.tile * 128; }
                         brow = gi * DT_TOK;
@@ -601,21 +693,34 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                             ok = false;
                             break;
                         }
-                        uint8_t *sa = smem + stage * DT_STAGE_BYTES;
-                        uint8_t *sb = sa + DT_A_BYTES;
-                        mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
+                        uint8_t *sa = smem + stage * Sh::A_STRIDE;  // bf16 only
+                        uint8_t *sb = smem + Sh::B_OFF + stage * Sh::B_STRIDE;
                         const int kc = kb * 64;
-                        if (is_up) {
+                        if (FP4) {
+                            // packed codes and scales of this (row block, K block), the token tile by TMA
+                            mbar_arrive_expect_tx(&full[stage], DT_B_BYTES + DT_FP4_CODES + DT_FP4_SCALES);
+                            const size_t blk = is_up ? ((size_t)wexp * (a.F / 64) + ux.ft) * (a.H / 64) + kb
+                                                     : ((size_t)wexp * a.ot + dn.tile) * (a.F / 64) + kb;
+                            bulk_load(smem + Sh::CODES_OFF + stage * DT_FP4_CODES,
+                                      (is_up ? a.gu_codes : a.dn_codes) + blk * DT_FP4_CODES, DT_FP4_CODES,
+                                      &full[stage]);
+                            bulk_load(smem + Sh::SCALES_OFF + stage * DT_FP4_SCALES,
+                                      (is_up ? a.gu_scales : a.dn_scales) + blk * DT_FP4_SCALES, DT_FP4_SCALES,
+                                      &full[stage]);
+                            tma_load_2d(sb, is_up ? &maps.x : &maps.hp, &full[stage], kc, brow);
+                        } else if (is_up) {
+                            mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
                             tma_load_2d(sa, ma, &full[stage], kc, arow);
                             tma_load_2d(sa + DT_A_BYTES / 2, mb, &full[stage], kc, arow);
                             tma_load_2d(sb, &maps.x, &full[stage], kc, brow);
                         } else {
+                            mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
                             tma_load_2d(sa, ma, &full[stage], kc, arow);
                             tma_load_2d(sb, &maps.hp, &full[stage], kc, brow);
                         }
                         used |= 1u << stage;
                         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
-                        if (++stage == DT_STAGES) stage = 0, phase ^= 1;
+                        if (++stage == RS) stage = 0, phase ^= 1;
                     }
                 }
                 if (!claimed) u_next = atomicAdd(next_unit, 1);
@@ -629,15 +734,15 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 }
             }
             volatile int never = 0;
-            for (int s = 0; s < DT_STAGES; ++s)
+            for (int s = 0; s < RS; ++s)
                 if ((used >> s) & 1u) mbar_wait(&full[s], (last_phase >> s) & 1u, &never);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(128, DT_TOK);
-            int stage = 0;
-            uint32_t phase = 0;
+            constexpr uint32_t idesc = FP4 ? idesc_f16_f32(128, DT_TOK) : idesc_bf16_f32(128, DT_TOK);
+            int stage = 0, ast = 0;      // raw stage; MXFP4: A tile
+            uint32_t phase = 0, aph = 0;
             int qi = 0;
             uint32_t qph = 0;
             int last_acc = -1;
@@ -662,21 +767,27 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 }
                 bool ok = true;
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                    // MXFP4: the slot holds both operands once it is dequantised
+                    if (FP4 ? !mbar_wait(&deq[ast], aph, abort_flag) : !mbar_wait(&full[stage], phase, abort_flag)) {
                         record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
                         *abort_flag = 1;
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * DT_STAGE_BYTES);
-                    const uint32_t sb = sa + DT_A_BYTES;
+                    const uint32_t sa = smem_u32(smem + (FP4 ? ast : stage) * Sh::A_STRIDE);
+                    const uint32_t sb = FP4 ? sa + DT_A_BYTES : smem_u32(smem + Sh::B_OFF + stage * Sh::B_STRIDE);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
                                  (kb | k) != 0);
-                    mma_commit(&empty[stage]);
-                    if (++stage == DT_STAGES) stage = 0, phase ^= 1;
+                    if (FP4) {
+                        mma_commit(&a_empty[ast]);
+                        if (++ast == DT_FP4_AS) ast = 0, aph ^= 1;
+                    } else {
+                        mma_commit(&empty[stage]);
+                        if (++stage == RS) stage = 0, phase ^= 1;
+                    }
                 }
                 if (!ok) break;
                 mma_commit(&acc_full[qi]);
@@ -689,7 +800,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                 mbar_wait(&acc_full[last_acc], last_acc_phase, &never);
             }
         }
-    } else {
+    } else if (warp < 6) {
         // ------------------------------ epilogue (warps 2..5) ------------------------------
         const int q = warp & 3;
         const int r = q * 32 + lane;                // accumulator row = weight row of the tile
@@ -787,7 +898,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                     const float bg = (!ux.shared && a.gate_b) ? a.gate_b[(size_t)e * a.F + f] : 0.0f;
                     const float bu = (!ux.shared && a.up_b) ? a.up_b[(size_t)e * a.F + f] : 0.0f;
                     const bool swiglu = ux.shared || a.act == MOE_ACT_SWIGLU;
-                    __nv_bfloat16 *dst = a.hp + (size_t)ux.g * DT_TOK * a.Fmax + f;
+                    const size_t hbase = (size_t)ux.g * DT_TOK * a.Fmax + f;
 #pragma unroll 1
                     for (int t = 0; t < DT_TOK; ++t) {
                         float hval = 0.0f;
@@ -797,7 +908,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
                                           : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
                             hval *= s_wt[t];
                         }
-                        dst[(size_t)t * a.Fmax] = __float2bfloat16_rn(hval);
+                        if (FP4) reinterpret_cast<__half *>(a.hp)[hbase + (size_t)t * a.Fmax] = __float2half_rn(hval);
+                        else reinterpret_cast<__nv_bfloat16 *>(a.hp)[hbase + (size_t)t * a.Fmax] = __float2bfloat16_rn(hval);
                     }
                 }
                 // publish: h' of this tile is written (generic proxy) and will be
@@ -826,6 +938,66 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
             if (et == 0) mbar_arrive(&uq_empty[qi]);
             if (++qi == DT_ACC) qi = 0, qph ^= 1;
         }
+    } else if (FP4) {
+        // ------------------------------ MXFP4 dequantisation (warps 6..9) ------------------------------
+        // Follows the units in queue order like the MMA role; thread r converts
+        // row r of every stage once its codes have landed, then the stage is
+        // released to the MMA (128 arrivals).  After a failed wait the loop
+        // keeps going without work (every later wait fails fast on the abort
+        // flag) until the producer's end marker, so the named barrier below
+        // always sees all 128 threads.
+        __shared__ int s_dq[2];
+        const int r = threadIdx.x - DT_THREADS;
+        int qi = 0, stage = 0, ast = 0;
+        uint32_t qph = 0, phase = 0, aph = 0;
+        for (;;) {
+            if (r == 0) {
+                int go = 1;
+                if (!mbar_wait(&uq_full[qi], qph, abort_flag)) go = 0;
+                else if (uq[qi] < 0) go = 2;
+                if (go == 0) {
+                    record_error(a.status, DEV_TIMEOUT_ACCUM_BARRIER);
+                    *abort_flag = 1;
+                }
+                s_dq[0] = go;
+                s_dq[1] = go == 1 ? uq[qi] : -1;
+            }
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            const int go = s_dq[0], u = s_dq[1];
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (go != 1) break;
+            int nk;
+            if (u < sc.up_units) {
+                const UpUnit x = up_unit(sc, u, a.F);
+                nk = x.kb1 - x.kb0;
+            } else {
+                const DnUnit d = dn_unit(sc, u - sc.up_units, s_dnb);
+                nk = d.kb1 - d.kb0;
+            }
+            for (int kb = 0; kb < nk; ++kb) {
+                // raw stage landed, and the A tile it goes to has been read
+                if (mbar_wait(&full[stage], phase, abort_flag) && mbar_wait(&a_empty[ast], aph ^ 1, abort_flag)) {
+                    uint8_t *slot = smem + ast * DT_FP4_SLOT;
+                    fp4_dequant_row(slot, smem + Sh::CODES_OFF + stage * DT_FP4_CODES,
+                                    smem + Sh::SCALES_OFF + stage * DT_FP4_SCALES, r);
+                    // the token tile moves with its swizzle: both tiles are 1024-byte aligned
+                    reinterpret_cast<uint4 *>(slot + DT_A_BYTES)[r] =
+                        reinterpret_cast<const uint4 *>(smem + Sh::B_OFF + stage * DT_B_BYTES)[r];
+                    fence_proxy_async_shared();  // generic-proxy writes, read by the MMA (async proxy)
+                } else if (!*abort_flag) {
+                    record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                    *abort_flag = 1;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&empty[stage]);  // the raw stage is consumed
+                    mbar_arrive(&deq[ast]);
+                }
+                if (++stage == RS) stage = 0, phase ^= 1;
+                if (++ast == DT_FP4_AS) ast = 0, aph ^= 1;
+            }
+            if (++qi == DT_ACC) qi = 0, qph ^= 1;
+        }
     }
 
     tc_fence_before();
@@ -840,7 +1012,8 @@ __global__ void __launch_bounds__(DT_THREADS, 1) dec_experts_kernel(const __grid
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-static bool dec_encode(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows)
+static bool dec_encode(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+                       bool f16 = false)
 {
     static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     if (!enc) {
@@ -855,7 +1028,8 @@ static bool dec_encode(CUtensorMap *m, const void *base, uint64_t inner, uint64_
     cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {64, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+    return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
+               dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -888,7 +1062,7 @@ int dectc_prepare(Layer &L)
     bool ok = dec_encode(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
               dec_encode(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, 64) &&
               dec_encode(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, 128) &&
-              dec_encode(&m->hp, L.dec_hp, L.Fmax, (uint64_t)dectc_groups_max(L) * DT_TOK, DT_TOK);
+              dec_encode(&m->hp, L.dec_hp, L.Fmax, (uint64_t)dectc_groups_max(L) * DT_TOK, DT_TOK, L.fp4_decode);
     if (ok && L.Fs) {
         ok = dec_encode(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, 64) && dec_encode(&m->sh_up, L.sh_up_w, L.H, L.Fs, 64) &&
              dec_encode(&m->sh_down, L.sh_down_w, L.Fs, L.H, 128);
@@ -898,8 +1072,10 @@ int dectc_prepare(Layer &L)
         m->sh_down = m->down;
     }
     if (ok)
-        ok = cudaFuncSetAttribute(dec_experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DT_SMEM) ==
-             cudaSuccess;
+        ok = cudaFuncSetAttribute(dec_experts_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)DtShape<false>::SMEM) == cudaSuccess &&
+             cudaFuncSetAttribute(dec_experts_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)DtShape<true>::SMEM) == cudaSuccess;
     if (!ok) { delete m; return -1; }
     L.dectc = m;
     return 0;
@@ -917,6 +1093,7 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     if (which == 0) {
         DecRouteArgs r;
         r.x = (const __nv_bfloat16 *)x;
+        r.x16 = L.fp4_decode ? (__half *)L.dec_x16 : nullptr;
         r.router_w = (const __nv_bfloat16 *)L.router_w;
         r.router_b = L.router_b;
         r.logits = L.logits;
@@ -927,13 +1104,20 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
         return 1;
     }
     DecMaps m = *L.dectc;
-    if (!dec_encode(&m.x, x, L.H, (uint64_t)T, DT_TOK)) return -1;
+    if (L.fp4_decode) {
+        if (!dec_encode(&m.x, L.dec_x16, L.H, (uint64_t)T, DT_TOK, true)) return -1;
+    } else if (!dec_encode(&m.x, x, L.H, (uint64_t)T, DT_TOK)) {
+        return -1;
+    }
     DecArgs a;
     a.logits = L.logits;
     a.topk_idx = L.topk_idx; a.topk_w = L.topk_w; a.sh_gate = L.sh_gate; a.counts = L.counts; a.active = L.active;
     a.meta = L.meta;
     a.gate_b = L.gate_b; a.up_b = L.up_b; a.down_b = L.down_b;
-    a.hp = (__nv_bfloat16 *)L.dec_hp;
+    a.hp = L.dec_hp;
+    a.gu_codes = L.fp4_gu_codes; a.gu_scales = L.fp4_gu_scales;
+    a.dn_codes = L.fp4_dn_codes; a.dn_scales = L.fp4_dn_scales;
+    a.ot = (L.H + 127) / 128;
     a.partials = L.dec_partials;
     a.counters = L.dec_tickets;
     a.out = out;
@@ -946,15 +1130,82 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     a.max_units = L.num_sms * DT_UNITS_PER_CTA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.num_sms);
-    cfg.blockDim = dim3(DT_THREADS);
-    cfg.dynamicSmemBytes = DT_SMEM;
+    cfg.blockDim = dim3(L.fp4_decode ? DtShape<true>::THREADS : DtShape<false>::THREADS);
+    cfg.dynamicSmemBytes = L.fp4_decode ? DtShape<true>::SMEM : DtShape<false>::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, dec_experts_kernel, m, a) == cudaSuccess ? 1 : -1;
+    const cudaError_t e = L.fp4_decode ? cudaLaunchKernelEx(&cfg, dec_experts_kernel<true>, m, a)
+                                       : cudaLaunchKernelEx(&cfg, dec_experts_kernel<false>, m, a);
+    return e == cudaSuccess ? 1 : -1;
+}
+
+// ---------------------------------------------------------------------------
+// MXFP4 packing for the decode kernel: each (row block, 64-wide K block) of a
+// matrix becomes one contiguous run of 128 rows x 32 code bytes and one of
+// 128 rows x 2 scale bytes (a row's two 16-byte blocks are adjacent in the
+// source, so a row copies 32 bytes).  gate/up: 64 gate rows then the 64
+// matching up rows of the de-interleaved gate_up; down: 128 output rows, rows
+// past H zero (code 0 is the value 0).
+// ---------------------------------------------------------------------------
+__global__ void pack_fp4_gate_up_kernel(const uint8_t *blocks, const uint8_t *scales, int E, int F, int H,
+                                        uint8_t *codes, uint8_t *sc)
+{
+    const int nkb = H / 64, nb = H / 32;
+    const size_t n = (size_t)E * 2 * F * nkb;  // one (source row, K block) each
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / nkb;               // interleaved row of [E][2F]
+        const int kb = (int)(i - row * nkb);
+        const int e = (int)(row / (2 * F)), rr = (int)(row - (size_t)e * 2 * F);
+        const int f = rr >> 1, up = rr & 1;
+        const size_t blk = ((size_t)e * (F / 64) + f / 64) * nkb + kb;
+        const int trow = up * 64 + (f & 63);
+        const uint4 *src = reinterpret_cast<const uint4 *>(blocks + (row * nb + 2 * kb) * 16);
+        uint4 *dst = reinterpret_cast<uint4 *>(codes + blk * DT_FP4_CODES + trow * 32);
+        dst[0] = src[0];
+        dst[1] = src[1];
+        sc[blk * DT_FP4_SCALES + trow * 2] = scales[row * nb + 2 * kb];
+        sc[blk * DT_FP4_SCALES + trow * 2 + 1] = scales[row * nb + 2 * kb + 1];
+    }
+}
+
+__global__ void pack_fp4_down_kernel(const uint8_t *blocks, const uint8_t *scales, int E, int F, int H, uint8_t *codes,
+                                     uint8_t *sc)
+{
+    const int nkb = F / 64, nb = F / 32, ot = (H + 127) / 128;
+    const size_t n = (size_t)E * ot * 128 * nkb;  // one (padded output row, K block) each
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t prow = i / nkb;               // [E][ot*128]
+        const int kb = (int)(i - prow * nkb);
+        const int e = (int)(prow / ((size_t)ot * 128)), h = (int)(prow - (size_t)e * ot * 128);
+        const size_t blk = ((size_t)e * ot + h / 128) * nkb + kb;
+        const int trow = h & 127;
+        uint4 *dst = reinterpret_cast<uint4 *>(codes + blk * DT_FP4_CODES + trow * 32);
+        if (h < H) {
+            const size_t row = (size_t)e * H + h;
+            const uint4 *src = reinterpret_cast<const uint4 *>(blocks + (row * nb + 2 * kb) * 16);
+            dst[0] = src[0];
+            dst[1] = src[1];
+            sc[blk * DT_FP4_SCALES + trow * 2] = scales[row * nb + 2 * kb];
+            sc[blk * DT_FP4_SCALES + trow * 2 + 1] = scales[row * nb + 2 * kb + 1];
+        } else {
+            dst[0] = dst[1] = make_uint4(0, 0, 0, 0);
+            sc[blk * DT_FP4_SCALES + trow * 2] = sc[blk * DT_FP4_SCALES + trow * 2 + 1] = 127;
+        }
+    }
+}
+
+int dectc_pack_fp4(Layer &L, const uint8_t *gu_blocks, const uint8_t *gu_scales, const uint8_t *dn_blocks,
+                   const uint8_t *dn_scales)
+{
+    pack_fp4_gate_up_kernel<<<4 * L.num_sms, 256>>>(gu_blocks, gu_scales, L.E, L.F, L.H, L.fp4_gu_codes,
+                                                     L.fp4_gu_scales);
+    pack_fp4_down_kernel<<<4 * L.num_sms, 256>>>(dn_blocks, dn_scales, L.E, L.F, L.H, L.fp4_dn_codes,
+                                                  L.fp4_dn_scales);
+    return cudaDeviceSynchronize() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace moe

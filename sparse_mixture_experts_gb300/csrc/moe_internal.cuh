@@ -82,6 +82,7 @@ struct Layer {
     void *h = nullptr;         // [Tmax*K + Tmax][Fmax] activations (routed rows sorted by expert, then shared)
     void *xp = nullptr;        // [Tmax*K + Tmax][H] x rows gathered in expert order, then x (tensor-core path)
     void *ys = nullptr;        // [Tmax][K+1][H] weighted expert outputs per (token, slot), weight dtype
+    bool mxfp4 = false;        // routed experts given in MXFP4 (gate_w/up_w/down_w hold their bf16 values)
     int *gfirst = nullptr;     // [5][E + 2] per group: first gate/up tile (and the total), first down tile
                                // (and the total), expert (E = shared), rows, first row in the sorted buffers
     int *status = nullptr;     // DeviceError
@@ -96,6 +97,15 @@ struct Layer {
     float *dec_partials = nullptr;   // split-K partial sums
     float *dec_wtab = nullptr;       // [groups_max][16] routing weight of token t for group g
     int *dec_tickets = nullptr;      // per-tile arrival counters
+    // MXFP4 weight-streaming decode: the routed experts' codes and scales
+    // packed per (row block, 64-wide K block) so a pipeline stage is one
+    // contiguous copy of each; x in f16 for the token operand
+    bool fp4_decode = false;         // MXFP4 layer whose scales fit the f16 operand path
+    uint8_t *fp4_gu_codes = nullptr; // [E][F/64][H/64][128 rows: 64 gate, 64 up][32 B]
+    uint8_t *fp4_gu_scales = nullptr;// [E][F/64][H/64][128][2]
+    uint8_t *fp4_dn_codes = nullptr; // [E][ceil(H/128)][F/64][128][32 B]
+    uint8_t *fp4_dn_scales = nullptr;// [E][ceil(H/128)][F/64][128][2]
+    void *dec_x16 = nullptr;         // [16][H] f16 copy of the decode batch
 
     // per-kernel timing (moe_timing_enable / moe_timing_read)
     int timing_max = 0;         // forwards recorded per window; 0 = off
@@ -406,6 +416,10 @@ int launch_decode(const Layer &L, const void *x, int T, void *out, cudaStream_t 
 bool dectc_supported(const Layer &L, int T);
 size_t dectc_workspace(const Layer &L, size_t &hp_bytes, size_t &part_bytes, size_t &tab_bytes, size_t &ticket_bytes);
 int dectc_prepare(Layer &L);
+// MXFP4 layers: pack the expert codes and scales for the decode kernel (from the
+// caller's blocks and scales already on the device); 0 on success
+int dectc_pack_fp4(Layer &L, const uint8_t *gu_blocks, const uint8_t *gu_scales, const uint8_t *dn_blocks,
+                   const uint8_t *dn_scales);
 void dectc_release(Layer &L);
 // which: 0 = router logits, 1 = selection + gate/up + down (writes out)
 int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s);

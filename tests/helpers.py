@@ -33,7 +33,9 @@ def moe_config(spec: synth.LayerSpec, max_tokens: int, out_dtype: str = "f32"):
         norm_topk_prob=spec.norm_topk_prob, weights_scale=spec.weights_scale,
         act=moe.ACT_SWIGLU if spec.act == "swiglu" else moe.ACT_CLAMP_GLU,
         act_alpha=spec.act_alpha, act_limit=spec.act_limit, has_bias=spec.has_bias,
-        gate_up_interleaved=spec.gate_up_interleaved, w_dtype=dt[spec.dtype], act_dtype=dt[spec.dtype],
+        gate_up_interleaved=spec.gate_up_interleaved,
+        w_dtype=moe.DT_MXFP4 if getattr(spec, "expert_format", "dense") == "mxfp4" else dt[spec.dtype],
+        act_dtype=dt[spec.dtype],
         out_dtype=dt[out_dtype], max_tokens=max_tokens)
 
 
@@ -42,6 +44,8 @@ def to_torch(a: np.ndarray, device="cuda"):
     import torch
     if a.dtype == np.uint16:
         t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    elif a.dtype == np.uint8:
+        t = torch.from_numpy(np.ascontiguousarray(a))
     else:
         t = torch.from_numpy(a)
     return t.to(device) if device != "cpu" else t
@@ -50,6 +54,10 @@ def to_torch(a: np.ndarray, device="cuda"):
 def make_layer(spec, weights: dict, max_tokens: int, out_dtype: str = "f32", path: int = 0):
     import sparse_mixture_experts_gb300 as moe
     w = {k: to_torch(v) for k, v in weights.items()}
+    if getattr(spec, "expert_format", "dense") == "mxfp4":
+        # the ABI takes the MXFP4 blocks in the gate_up_w / down_w slots
+        w["gate_up_w"] = w.pop("gate_up_blocks")
+        w["down_w"] = w.pop("down_blocks")
     layer = moe.MoELayer(moe_config(spec, max_tokens, out_dtype), w)
     if path:
         layer.set_path(path)

@@ -43,14 +43,14 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
 
 
 def test_config_struct_layout_matches_header():
     import sparse_mixture_experts_gb300 as moe
     # 17 four-byte fields, no padding
     assert ctypes.sizeof(moe._Config) == 17 * 4
-    assert ctypes.sizeof(moe._Weights) == 12 * ctypes.sizeof(ctypes.c_void_p)
+    assert ctypes.sizeof(moe._Weights) == 14 * ctypes.sizeof(ctypes.c_void_p)
 
 
 @pytest.mark.parametrize("bad", [
@@ -61,6 +61,8 @@ def test_config_struct_layout_matches_header():
     dict(router_mode=7),
     dict(act=5),
     dict(w_dtype=3),
+    dict(w_dtype=2, act_dtype=1, gate_up_interleaved=0),  # MXFP4 needs the interleaved gate_up
+    dict(w_dtype=2, act_dtype=0, gate_up_interleaved=1),  # MXFP4 needs bf16 activations
     dict(act_dtype=1, w_dtype=0),  # mixed activation / weight dtype
     dict(max_tokens=-1),
 ])

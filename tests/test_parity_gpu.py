@@ -30,6 +30,8 @@ CASES = [
     ("qwen_prefill_zipf", 4096, 160),
     ("gptoss", 1, 1), ("gptoss", 64, 64), ("gptoss", 2048, 64),
     ("mixtral", 1, 1), ("mixtral", 16, 16), ("mixtral", 256, 40), ("mixtral", 4096, 24), ("mixtral", 16384, 24),
+    # MXFP4 experts: the decode path reads the codes and scales; the others the layer's bf16 values
+    ("gptoss_mxfp4", 1, 1), ("gptoss_mxfp4", 4, 4), ("gptoss_mxfp4", 16, 16), ("gptoss_mxfp4", 64, 32),
 ]
 
 # CUDA-core flops budget for the streaming path in a test (it is the decode path)
@@ -292,3 +294,47 @@ def test_paths_agree_on_decode_batch():
         np.testing.assert_array_equal(outs[(path, "idx")], outs[(PATHS[0], "idx")])
         ref = outs[PATHS[0]]
         assert np.linalg.norm(outs[path] - ref) <= 1e-2 * np.linalg.norm(ref)
+
+
+MXFP4_SMALL = synth.GPTOSS_MXFP4.replace(name="gpt-oss-like, MXFP4 experts, small", hidden=256, n_expert=8, top_k=2,
+                                         expert_ff=192)
+
+
+@pytest.mark.parametrize("low_scale", [False, True], ids=["codes", "bf16-copy"])
+def test_mxfp4_decode_kernel_choice(low_scale):
+    """A decode batch on MXFP4 experts runs the kernel that streams the codes
+    and scales (timed as its own kind) while every E8M0 scale is in 113..140,
+    where its f16 operands are exact; one scale below that range sends the
+    layer to the bf16 copy.  Both agree with the oracle on the same weights."""
+    spec, T = MXFP4_SMALL, 5
+    w = synth.make_weights(spec, seed=5)
+    if low_scale:
+        s = w["down_scales"].copy()
+        s.flat[37] = 112
+        w["down_scales"] = s
+    x = synth.make_x(spec, T, seed=5)
+    layer = helpers.make_layer(spec, w, 16)
+    layer.set_path(moe.PATH_DECODE_TC)
+    layer.timing_enable(4)
+    out = layer.forward(helpers.to_torch(x)).float().cpu().numpy()
+    kinds = layer.timing_read()
+    idx, _ = layer.routing(T)
+    idx = idx.cpu().numpy()
+    layer.status()
+    layer.close()
+    want, other = ("experts", "experts_mxfp4") if low_scale else ("experts_mxfp4", "experts")
+    assert kinds[want][1] == 1 and kinds[other][1] == 0, kinds
+    orc = oracle.Oracle(spec, w)
+    mism, ties, invalid, _ = helpers.index_parity_all(orc, x, idx)
+    assert not mism and not invalid
+    rep = helpers.compare(orc, x, np.arange(T), out, idx)
+    assert rep.ok(spec.dtype), str(rep)
+
+
+@pytest.mark.parametrize("T", [1, 7, 16])
+def test_mxfp4_small_layer_all_paths_agree(T):
+    """Ragged decode batches on a small MXFP4 layer: the MXFP4 decode kernel
+    and the bf16-copy paths give the oracle's result."""
+    for path in PATHS:
+        rep = _small_case(MXFP4_SMALL, T, path, seed=9)
+        assert rep.ok(MXFP4_SMALL.dtype), (path, str(rep))
