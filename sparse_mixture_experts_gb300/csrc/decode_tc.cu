@@ -52,36 +52,41 @@ constexpr int DT_A_BYTES = 128 * 64 * 2;        // 16 KB weight tile
 constexpr int DT_B_BYTES = DT_TOK * 64 * 2;     // 2 KB token tile
 constexpr int DT_STAGE_BYTES = DT_A_BYTES + DT_B_BYTES;
 constexpr int DT_ACC = 8;                       // unit queue slots = TMEM accumulators
-constexpr int DT_TMEM_COLS = DT_ACC * DT_TOK;   // 16 fp32 columns each
 constexpr int DT_EP_LD = DT_TOK + 1;            // row pitch (floats) of the epilogue's accumulator copy
 constexpr int DT_XCH_BYTES = 128 * DT_EP_LD * 4; // the accumulator tile in shared memory
 constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
-// MXFP4 weights: a stage's raw data (token tile, codes, scales) is a third of a
-// bf16 stage, so the producer's ring is deeper (DT_FP4_RS stages, about the
-// bytes in flight of the bf16 ring) and 4 more warps dequantise each raw stage
-// into a shallow ring of f16 operand slots (DT_FP4_AS), each an A tile with the
-// stage's token tile copied behind it.  The dequantising warps release the raw
-// stage themselves, so the MMA thread commits once per stage (to the slot): at
-// N = 16 the MMA thread's issue rate, not the tensor pipe, bounds this loop,
-// and every tcgen05.commit costs about as much as an MMA.
-constexpr int DT_FP4_CODES = 128 * 32;          // 128 rows x 64 four-bit codes
-constexpr int DT_FP4_SCALES = 128 * 2;          // 128 rows x 2 E8M0 bytes
-constexpr int DT_FP4_RS = 18;                   // raw stages
-constexpr int DT_FP4_AS = 4;                    // operand slots (f16 A tile + token tile)
-constexpr int DT_FP4_SLOT = DT_A_BYTES + DT_B_BYTES;  // a multiple of 1024 (128-byte swizzle atoms)
+// MXFP4 weights: a stage is the token tile and one packed block of codes and
+// scales (DT_FP4_BLK bytes for 128 rows x 64 K), a third of a bf16 stage, so
+// the producer's ring is deeper (DT_FP4_RS stages).  Eight more warps widen
+// each block to f16 and store it straight into tensor memory, where the MMA
+// reads its A operand (DT_FP4_AS tiles of 32 columns): the f16 tile never
+// touches shared memory, whose bandwidth would otherwise bound the stage rate.
+// Two MMA warps take alternate stages into accumulators of their own (an MMA
+// costs its issuing thread about as much at N = 16 as at N = 256, so one
+// thread's issue rate would bound the stream), and the epilogue adds the two.
+constexpr int DT_FP4_BLK = 128 * 32 + 128 * 2;  // codes [2 halves][128 rows][16 B], scales [2 halves][128 rows]
+constexpr int DT_FP4_RS = 24;                   // raw stages
+constexpr int DT_FP4_AS = 8;                    // A tiles in tensor memory
+constexpr int DT_FP4_DQW = 8;                   // dequantising warps
+constexpr int DT_FP4_NM = 2;                    // MMA warps
+constexpr int DT_FP4_NP = 4;                    // producer threads
+constexpr int DT_FP4_DQG = 2;                   // dequantising groups of 4 warps, taking alternate stages
+constexpr int DT_FP4_A_COL = 256;               // first A-tile column (accumulators use 0..255)
+constexpr int DT_FP4_TMEM_COLS = 512;
 
 template <bool FP4>
 struct DtShape {
-    static constexpr int THREADS = FP4 ? DT_THREADS + 128 : DT_THREADS;
+    // bf16: producer, MMA, 4 epilogue warps; MXFP4: + 8 dequantising warps, a second MMA warp and a
+    // warp of three more producer threads
+    static constexpr int THREADS = FP4 ? DT_THREADS + 32 * (DT_FP4_DQW + 2) : DT_THREADS;
     static constexpr int RS = FP4 ? DT_FP4_RS : DT_STAGES;   // producer ring
-    // smem: bf16 [RS][A | B]; MXFP4 [AS][A | B] [RS][B] [RS][codes] [RS][scales]
-    static constexpr int B_OFF = FP4 ? DT_FP4_AS * DT_FP4_SLOT : DT_A_BYTES;      // first (raw) B tile
+    static constexpr int TMEM_COLS = FP4 ? DT_FP4_TMEM_COLS : DT_ACC * DT_TOK;
+    // smem: bf16 [RS][A | B]; MXFP4 [RS][B] [RS][block]
+    static constexpr int B_OFF = FP4 ? 0 : DT_A_BYTES;      // first B tile
     static constexpr int B_STRIDE = FP4 ? DT_B_BYTES : DT_STAGE_BYTES;
-    static constexpr int A_STRIDE = FP4 ? DT_FP4_SLOT : DT_STAGE_BYTES;
-    static constexpr int CODES_OFF = B_OFF + RS * DT_B_BYTES;                      // MXFP4 only
-    static constexpr int SCALES_OFF = CODES_OFF + RS * DT_FP4_CODES;
-    static constexpr int RING = FP4 ? (SCALES_OFF + RS * DT_FP4_SCALES + 1023) / 1024 * 1024
-                                    : DT_STAGES * DT_STAGE_BYTES;
+    static constexpr int A_STRIDE = DT_STAGE_BYTES;         // bf16 only
+    static constexpr int BLK_OFF = RS * DT_B_BYTES;         // MXFP4 only
+    static constexpr int RING = FP4 ? (BLK_OFF + RS * DT_FP4_BLK + 1023) / 1024 * 1024 : DT_STAGES * DT_STAGE_BYTES;
     static constexpr size_t SMEM = (size_t)RING + 1024 + DT_XCH_BYTES + 1024;
 };
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
@@ -114,7 +119,7 @@ struct DecArgs {
     RouteMeta *meta;
     const float *gate_b, *up_b, *down_b;
     void *hp;             // [groups_max*16][Fmax], bf16 (f16 for MXFP4 weights)
-    const uint8_t *gu_codes, *gu_scales, *dn_codes, *dn_scales;  // MXFP4 weights, packed (see Layer)
+    const uint8_t *gu_fp4, *dn_fp4;  // MXFP4 weights, packed blocks (see Layer)
     int ot;               // down output tiles of 128 rows
     float *partials;      // [gate/up, down][units][T][128]
     int *counters;        // tickets, group completion, work counter
@@ -397,27 +402,23 @@ __device__ __forceinline__ __half2 e8m0_half2(uint32_t e8m0)
     return *reinterpret_cast<const __half2 *>(&v);
 }
 
-// One row of an A tile from a raw stage's MXFP4 codes and scales: row r's 64
-// elements (two 32-element blocks) to f16, written in the 128-byte swizzled
-// K-major layout the MMA reads (16-byte chunk q of row r at q ^ (r & 7)).
-__device__ __forceinline__ void fp4_dequant_row(uint8_t *a_tile, const uint8_t *codes, const uint8_t *scales, int r)
+// Half h (elements 32h .. 32h+31, one E8M0 scale) of row r of a packed
+// MXFP4 block, widened and scaled to 16 f16 pairs: v[c] holds elements
+// 32h + 2c (low half) and 32h + 2c + 1, as A-tile column 16h + c in tensor memory.
+__device__ __forceinline__ void fp4_dequant_half(const uint8_t *blk, int h, int r, uint32_t (&v)[16])
 {
-    const uint4 *c = reinterpret_cast<const uint4 *>(codes + r * 32);
-    const uint4 c0 = c[0], c1 = c[1];
-    const uint8_t *sc = scales + r * 2;
-    const __half2 s0 = e8m0_half2(sc[0]), s1 = e8m0_half2(sc[1]);
-    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    uint8_t *row = a_tile + r * 128;
+    const uint4 c = *reinterpret_cast<const uint4 *>(blk + (h * 128 + r) * 16);
+    const __half2 s = e8m0_half2(blk[128 * 32 + h * 128 + r]);
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        uint32_t h[4];
-        e2m1x8_to_f16(words[q], h);
+    for (int q = 0; q < 4; ++q) {
+        uint32_t hq[4];
+        e2m1x8_to_f16(words[q], hq);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            __half2 v = __hmul2(*reinterpret_cast<__half2 *>(&h[i]), q < 4 ? s0 : s1);
-            h[i] = *reinterpret_cast<uint32_t *>(&v);
+            __half2 x = __hmul2(*reinterpret_cast<__half2 *>(&hq[i]), s);
+            v[q * 4 + i] = *reinterpret_cast<uint32_t *>(&x);
         }
-        *reinterpret_cast<uint4 *>(row + ((q ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
     }
 }
 
@@ -451,9 +452,9 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
     uint64_t *acc_full = empty + RS;          // [DT_ACC]
     uint64_t *uq_full = acc_full + DT_ACC;    // [DT_ACC] unit handed out
     uint64_t *uq_empty = uq_full + DT_ACC;    // [DT_ACC] unit finished, slot and accumulator free
-    uint64_t *deq = uq_empty + DT_ACC;        // [DT_FP4_AS] MXFP4: the A tile is dequantised
-    uint64_t *a_empty = deq + DT_FP4_AS;      // [DT_FP4_AS] MXFP4: the A tile has been read by the MMA
-    int *uq = reinterpret_cast<int *>(a_empty + DT_FP4_AS);  // [DT_ACC]
+    uint64_t *deq = uq_empty + DT_ACC;        // [DT_FP4_AS] MXFP4: the A tile is in tensor memory
+    uint64_t *drain = deq + DT_FP4_AS;        // [2] an MMA thread's own completion, after an abort
+    int *uq = reinterpret_cast<int *>(drain + 2);  // [DT_ACC]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(uq + DT_ACC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *bcast = reinterpret_cast<int *>(tmem_slot + 2);  // [4]
@@ -476,25 +477,23 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
     if (threadIdx.x == 0) {
         for (int s = 0; s < RS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], FP4 ? 4 : 1);  // MXFP4: one arrival per dequantising warp
+            mbar_init(&empty[s], 1);
         }
         mbar_init(&s_bnd_bar, 1);
         for (int b = 0; b < DT_ACC; ++b) {
-            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_full[b], FP4 ? DT_FP4_NM : 1);
             mbar_init(&uq_full[b], 1);
-            mbar_init(&uq_empty[b], 1);
+            mbar_init(&uq_empty[b], FP4 ? DT_FP4_NP : 1);  // MXFP4: the epilogue and the following producers
         }
         if (FP4)
-            for (int s = 0; s < DT_FP4_AS; ++s) {
-                mbar_init(&deq[s], 4);
-                mbar_init(&a_empty[s], 1);
-            }
+            for (int s = 0; s < DT_FP4_AS; ++s) mbar_init(&deq[s], DT_FP4_DQW / DT_FP4_DQG);
+        for (int m = 0; m < 2; ++m) mbar_init(&drain[m], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(DT_TMEM_COLS));
+                     "r"(Sh::TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (warp == 0 && lane == 0) {
@@ -588,36 +587,55 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
     int *group_done = a.counters + DT_GROUP_DONE;
     int *next_unit = a.counters + DT_NEXT_UNIT;
 
-    if (warp == 0) {
-        // ------------------------------ producer ------------------------------
-        if (lane == 0) {
+    if (warp == 0 || (FP4 && warp == 7 + DT_FP4_DQW)) {
+        // ------------------------------ producer(s) ------------------------------
+        // Producer 0 claims the units and hands them out.  MXFP4: three more
+        // producer threads follow the queue, and producer p issues the stages
+        // whose index in the stream is p mod 4, since one thread's issue rate
+        // bounds the small stages.
+        constexpr int NP = FP4 ? DT_FP4_NP : 1;
+        const int pw = warp == 0 ? (lane == 0 ? 0 : NP) : (lane < NP - 1 ? 1 + lane : NP);
+        if (pw < NP) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t used = 0, last_phase = 0;  // per stage: loads issued, parity of the last
+            uint32_t gs = 0;                    // index of the next stage in the stream
             int qi = 0;
             uint32_t qph = 0;
             bool ok = true;
             int u_next = first_unit;
             bool bounds = false;
             while (ok) {
-                int u = u_next;
-                if (u >= sc.up_units) {
-                    // the down split count is computed off the critical path (epilogue role)
-                    if (!bounds && !mbar_wait(&s_bnd_bar, 0, abort_flag)) {
-                        record_error(a.status, DEV_TIMEOUT_ACCUM_BARRIER);
-                        *abort_flag = 1;
-                        u = -1;
+                int u;
+                if (pw == 0) {
+                    u = u_next;
+                    if (u >= sc.up_units) {
+                        // the down split count is computed off the critical path (epilogue role)
+                        if (!bounds && !mbar_wait(&s_bnd_bar, 0, abort_flag)) {
+                            record_error(a.status, DEV_TIMEOUT_ACCUM_BARRIER);
+                            *abort_flag = 1;
+                            u = -1;
+                        }
+                        bounds = true;
+                        if (u >= sc.up_units + sc.ot * s_sdn) u = -1;
                     }
-                    bounds = true;
-                    if (u >= sc.up_units + sc.ot * s_sdn) u = -1;
+                    if (!mbar_wait(&uq_empty[qi], qph ^ 1, abort_flag)) {
+                        record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    uq[qi] = u;
+                    mbar_arrive(&uq_full[qi]);
+                } else {
+                    if (!mbar_wait(&uq_full[qi], qph, abort_flag)) {
+                        record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    u = uq[qi];
+                    // the slot may be handed out again only once this thread has read it
+                    mbar_arrive(&uq_empty[qi]);
                 }
-                if (!mbar_wait(&uq_empty[qi], qph ^ 1, abort_flag)) {
-                    record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
-                    *abort_flag = 1;
-                    break;
-                }
-                uq[qi] = u;
-                mbar_arrive(&uq_full[qi]);
                 if (++qi == DT_ACC) qi = 0, qph ^= 1;
                 if (u < 0) break;
                 const bool is_up = u < sc.up_units;
@@ -638,7 +656,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                 // the counter's round trip overlaps this unit's loads.  Claims stay
                 // in order: a CTA holds at most one unclaimed-ahead unit, and a
                 // down unit only waits for gate/up units, which never wait.
-                bool claimed = false;
+                bool claimed = pw != 0;  // only producer 0 claims
                 // one segment per group the unit's K blocks fall in (gate/up: one)
                 while (seg_k < seg_end && ok) {
                     int kb0, kb1, arow, brow, wexp;  // wexp: the segment's expert (MXFP4 weights)
@@ -663,9 +681,10 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         else { ma = &maps.down; arow = s_act[gi] * a.H + dn.tile * 128; }
                         brow = gi * DT_TOK;
                         // h'[gi] is complete once every gate/up tile of the group is
+                        // (only waited for by a producer with a stage in the segment)
                         const int need = fd / 64;
                         int *done = group_done + gi * DT_DONE_STRIDE;
-                        if (ld_acquire(done) < need) {
+                        if ((n >= NP || (int)(((uint32_t)pw + NP - gs % NP) % NP) < n) && ld_acquire(done) < need) {
                             // poll with a short back-off: many producers may wait on
                             // the same counter, and the increment must get through
                             const unsigned long long t0 = globaltimer();
@@ -682,50 +701,48 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         fence_proxy_async_global();
                         if (!ok) break;
                     }
-                    for (int kb = kb0; kb < kb1; ++kb, --left) {
+                    for (int kb = kb0; kb < kb1; ++kb, --left, ++gs) {
                         if (!claimed && left <= DT_CLAIM_AHEAD) {
                             u_next = atomicAdd(next_unit, 1);
                             claimed = true;
                         }
-                        if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
-                            record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
-                            *abort_flag = 1;
-                            ok = false;
-                            break;
+                        if ((int)(gs % NP) == pw) {
+                            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                                record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
+                                *abort_flag = 1;
+                                ok = false;
+                                break;
+                            }
+                            uint8_t *sa = smem + stage * Sh::A_STRIDE;  // bf16 only
+                            uint8_t *sb = smem + Sh::B_OFF + stage * Sh::B_STRIDE;
+                            const int kc = kb * 64;
+                            if (FP4) {
+                                // the packed block of this (row block, K block), the token tile by TMA
+                                mbar_arrive_expect_tx(&full[stage], DT_B_BYTES + DT_FP4_BLK);
+                                const size_t blk = is_up ? ((size_t)wexp * (a.F / 64) + ux.ft) * (a.H / 64) + kb
+                                                         : ((size_t)wexp * a.ot + dn.tile) * (a.F / 64) + kb;
+                                bulk_load(smem + Sh::BLK_OFF + stage * DT_FP4_BLK,
+                                          (is_up ? a.gu_fp4 : a.dn_fp4) + blk * DT_FP4_BLK, DT_FP4_BLK, &full[stage]);
+                                tma_load_2d(sb, is_up ? &maps.x : &maps.hp, &full[stage], kc, brow);
+                            } else if (is_up) {
+                                mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
+                                tma_load_2d(sa, ma, &full[stage], kc, arow);
+                                tma_load_2d(sa + DT_A_BYTES / 2, mb, &full[stage], kc, arow);
+                                tma_load_2d(sb, &maps.x, &full[stage], kc, brow);
+                            } else {
+                                mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
+                                tma_load_2d(sa, ma, &full[stage], kc, arow);
+                                tma_load_2d(sb, &maps.hp, &full[stage], kc, brow);
+                            }
+                            used |= 1u << stage;
+                            last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                         }
-                        uint8_t *sa = smem + stage * Sh::A_STRIDE;  // bf16 only
-                        uint8_t *sb = smem + Sh::B_OFF + stage * Sh::B_STRIDE;
-                        const int kc = kb * 64;
-                        if (FP4) {
-                            // packed codes and scales of this (row block, K block), the token tile by TMA
-                            mbar_arrive_expect_tx(&full[stage], DT_B_BYTES + DT_FP4_CODES + DT_FP4_SCALES);
-                            const size_t blk = is_up ? ((size_t)wexp * (a.F / 64) + ux.ft) * (a.H / 64) + kb
-                                                     : ((size_t)wexp * a.ot + dn.tile) * (a.F / 64) + kb;
-                            bulk_load(smem + Sh::CODES_OFF + stage * DT_FP4_CODES,
-                                      (is_up ? a.gu_codes : a.dn_codes) + blk * DT_FP4_CODES, DT_FP4_CODES,
-                                      &full[stage]);
-                            bulk_load(smem + Sh::SCALES_OFF + stage * DT_FP4_SCALES,
-                                      (is_up ? a.gu_scales : a.dn_scales) + blk * DT_FP4_SCALES, DT_FP4_SCALES,
-                                      &full[stage]);
-                            tma_load_2d(sb, is_up ? &maps.x : &maps.hp, &full[stage], kc, brow);
-                        } else if (is_up) {
-                            mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
-                            tma_load_2d(sa, ma, &full[stage], kc, arow);
-                            tma_load_2d(sa + DT_A_BYTES / 2, mb, &full[stage], kc, arow);
-                            tma_load_2d(sb, &maps.x, &full[stage], kc, brow);
-                        } else {
-                            mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
-                            tma_load_2d(sa, ma, &full[stage], kc, arow);
-                            tma_load_2d(sb, &maps.hp, &full[stage], kc, brow);
-                        }
-                        used |= 1u << stage;
-                        last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                         if (++stage == RS) stage = 0, phase ^= 1;
                     }
                 }
                 if (!claimed) u_next = atomicAdd(next_unit, 1);
             }
-            if (*abort_flag) {
+            if (pw == 0 && *abort_flag) {
                 // let the other roles leave: hand out the end-of-work marker
                 for (int i = 0; i < DT_ACC; ++i) {
                     uq[qi] = -1;
@@ -737,12 +754,18 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
             for (int s = 0; s < RS; ++s)
                 if ((used >> s) & 1u) mbar_wait(&full[s], (last_phase >> s) & 1u, &never);
         }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer ------------------------------
+    } else if (warp == 1 || (FP4 && warp == 6 + DT_FP4_DQW)) {
+        // ------------------------------ MMA issuer(s) ------------------------------
+        // bf16: one thread issues every stage.  MXFP4: two threads take
+        // alternate stages (by their index in the stream) into accumulators of
+        // their own, with A the tile the dequantising warps left in tensor memory.
+        constexpr int NM = FP4 ? DT_FP4_NM : 1;
+        const int mw = warp == 1 ? 0 : 1;
         if (lane == 0) {
             constexpr uint32_t idesc = FP4 ? idesc_f16_f32(128, DT_TOK) : idesc_bf16_f32(128, DT_TOK);
-            int stage = 0, ast = 0;      // raw stage; MXFP4: A tile
+            int stage = 0, ast = 0;  // raw stage; MXFP4: A tile
             uint32_t phase = 0, aph = 0;
+            uint32_t gs = 0;         // index of the next stage in the stream
             int qi = 0;
             uint32_t qph = 0;
             int last_acc = -1;
@@ -756,7 +779,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                 const int u = uq[qi];
                 if (u < 0) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(qi * DT_TOK);
+                const uint32_t d_tmem = tmem_base + (uint32_t)((qi * NM + mw) * DT_TOK);
                 int nk;
                 if (u < sc.up_units) {
                     const UpUnit x = up_unit(sc, u, a.F);
@@ -765,39 +788,48 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                     const DnUnit d = dn_unit(sc, u - sc.up_units, s_dnb);
                     nk = d.kb1 - d.kb0;
                 }
-                bool ok = true;
-                for (int kb = 0; kb < nk; ++kb) {
-                    // MXFP4: the slot holds both operands once it is dequantised
-                    if (FP4 ? !mbar_wait(&deq[ast], aph, abort_flag) : !mbar_wait(&full[stage], phase, abort_flag)) {
-                        record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + (FP4 ? ast : stage) * Sh::A_STRIDE);
-                    const uint32_t sb = FP4 ? sa + DT_A_BYTES : smem_u32(smem + Sh::B_OFF + stage * Sh::B_STRIDE);
+                bool ok = true, first = true;
+                for (int kb = 0; kb < nk; ++kb, ++gs) {
+                    if (!FP4 || (int)(gs % NM) == mw) {
+                        // MXFP4: the A tile is in tensor memory once the block it came
+                        // from has landed, so the token tile has too
+                        if (FP4 ? !mbar_wait(&deq[ast], aph, abort_flag) : !mbar_wait(&full[stage], phase, abort_flag)) {
+                            record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sb = smem_u32(smem + Sh::B_OFF + stage * Sh::B_STRIDE);
+                        if (FP4) {
+                            const uint32_t at = tmem_base + (uint32_t)(DT_FP4_A_COL + ast * 32);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
-                                 (kb | k) != 0);
-                    if (FP4) {
-                        mma_commit(&a_empty[ast]);
-                        if (++ast == DT_FP4_AS) ast = 0, aph ^= 1;
-                    } else {
-                        mma_commit(&empty[stage]);
-                        if (++stage == RS) stage = 0, phase ^= 1;
+                            for (int k = 0; k < 4; ++k)
+                                mma_f16_ta(d_tmem, at + k * 8, smem_desc_sw128(sb + k * 32), idesc, !first || k != 0);
+                        } else {
+                            const uint32_t sa = smem_u32(smem + stage * Sh::A_STRIDE);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
+                                         (kb | k) != 0);
+                        }
+                        mma_commit(&empty[stage]);  // the raw stage (and MXFP4: the A tile) is free
+                        first = false;
                     }
+                    if (++stage == RS) stage = 0, phase ^= 1;
+                    if (FP4 && ++ast == DT_FP4_AS) ast = 0, aph ^= 1;
                 }
                 if (!ok) break;
-                mma_commit(&acc_full[qi]);
+                mma_commit(&acc_full[qi]);  // MXFP4: also when this thread had no stage of the unit
                 last_acc = qi;
                 last_acc_phase = qph;
                 if (++qi == DT_ACC) qi = 0, qph ^= 1;
             }
             if (*abort_flag && last_acc >= 0) {
+                // no MMA of this thread may still write tensor memory at teardown
                 volatile int never = 0;
-                mbar_wait(&acc_full[last_acc], last_acc_phase, &never);
+                mma_commit(&drain[mw]);
+                mbar_wait(&drain[mw], 0, &never);
             }
         }
     } else if (warp < 6) {
@@ -816,6 +848,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
         }
         int qi = 0;
         uint32_t qph = 0;
+        uint32_t e_gs = 0;  // MXFP4: index in the stream of the unit's first stage
         for (;;) {
             // one thread waits (bounded) and tells the others, so that all 128
             // leave together and no named barrier below can hang
@@ -835,21 +868,37 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
             const int u = uq[qi];
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (go != 1) break;
-            tc_fence_after();
-            uint32_t raw[16];
-            tmem_ld16(tmem_base + lane_addr + (uint32_t)(qi * DT_TOK), raw);
-            tmem_ld_wait();
-            float v[DT_TOK];
-#pragma unroll
-            for (int t = 0; t < DT_TOK; ++t) v[t] = __uint_as_float(raw[t]);
             const bool is_up = u < sc.up_units;
             UpUnit ux;
             DnUnit dx;
-            int tile, S, tbase, pslot;
-            if (is_up) { ux = up_unit(sc, u, a.F); tile = ux.tile; S = ux.S; tbase = 0; pslot = ux.pslot; }
+            int tile, S, tbase, pslot, nk;
+            if (is_up) { ux = up_unit(sc, u, a.F); tile = ux.tile; S = ux.S; tbase = 0; pslot = ux.pslot; nk = ux.kb1 - ux.kb0; }
             else {
                 dx = dn_unit(sc, u - sc.up_units, s_dnb);
-                tile = dx.tile; S = s_sdn; tbase = DT_TICKET_DOWN; pslot = a.max_units + tile * S;
+                tile = dx.tile; S = s_sdn; tbase = DT_TICKET_DOWN; pslot = a.max_units + tile * S; nk = dx.kb1 - dx.kb0;
+            }
+            tc_fence_after();
+            uint32_t raw[16];
+            float v[DT_TOK];
+            if (FP4) {
+                // the two MMA threads' accumulators; one that got no stage of the
+                // unit (a single-stage unit) holds nothing
+#pragma unroll
+                for (int t = 0; t < DT_TOK; ++t) v[t] = 0.0f;
+#pragma unroll
+                for (int m = 0; m < DT_FP4_NM; ++m) {
+                    if (nk < DT_FP4_NM && (int)(e_gs % DT_FP4_NM) != m) continue;
+                    tmem_ld16(tmem_base + lane_addr + (uint32_t)((qi * DT_FP4_NM + m) * DT_TOK), raw);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int t = 0; t < DT_TOK; ++t) v[t] += __uint_as_float(raw[t]);
+                }
+                e_gs += (uint32_t)nk;
+            } else {
+                tmem_ld16(tmem_base + lane_addr + (uint32_t)(qi * DT_TOK), raw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int t = 0; t < DT_TOK; ++t) v[t] = __uint_as_float(raw[t]);
             }
 
             bool finalize = true;
@@ -939,19 +988,27 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
             if (++qi == DT_ACC) qi = 0, qph ^= 1;
         }
     } else if (FP4) {
-        // ------------------------------ MXFP4 dequantisation (warps 6..9) ------------------------------
-        // Follows the units in queue order like the MMA role; thread r converts
-        // row r of every stage once its codes have landed, then the stage is
-        // released to the MMA (128 arrivals).  After a failed wait the loop
-        // keeps going without work (every later wait fails fast on the abort
-        // flag) until the producer's end marker, so the named barrier below
-        // always sees all 128 threads.
+        // ------------------------------ MXFP4 dequantisation (warps 6..13) ------------------------------
+        // Follows the units in queue order like the MMA threads.  Two groups of
+        // four warps take alternate stages (by their index in the stream); in a
+        // group, warp w widens the rows of its 32-lane quadrant w % 4, lane =
+        // row, straight into the A tile in tensor memory (a warp reaches only
+        // its own quadrant's lanes).  A tile is rewritten once the MMA
+        // DT_FP4_AS stages back, its last reader, has completed (that stage's
+        // release of its raw stage).  After a failed wait the loop keeps going
+        // without work (every later wait fails fast on the abort flag) until the
+        // producer's end marker, so the named barrier below always sees all the
+        // warps.
         __shared__ int s_dq[2];
-        const int r = threadIdx.x - DT_THREADS;
-        int qi = 0, stage = 0, ast = 0;
-        uint32_t qph = 0, phase = 0, aph = 0;
+        const int dr = threadIdx.x - DT_THREADS;  // 0 .. 32 * DT_FP4_DQW - 1
+        const int q = warp & 3, grp = (warp - 6) >> 2;
+        const int row = q * 32 + lane;
+        const uint32_t t_a = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)DT_FP4_A_COL;
+        int qi = 0, stage = 0, ast = 0, ps = 0;   // ps: raw stage of the stage DT_FP4_AS back
+        uint32_t qph = 0, phase = 0, pph = 0;
+        uint32_t gs = 0;
         for (;;) {
-            if (r == 0) {
+            if (dr == 0) {
                 int go = 1;
                 if (!mbar_wait(&uq_full[qi], qph, abort_flag)) go = 0;
                 else if (uq[qi] < 0) go = 2;
@@ -962,9 +1019,9 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                 s_dq[0] = go;
                 s_dq[1] = go == 1 ? uq[qi] : -1;
             }
-            asm volatile("bar.sync 2, 128;" ::: "memory");
+            asm volatile("bar.sync 2, %0;" ::"n"(32 * DT_FP4_DQW) : "memory");
             const int go = s_dq[0], u = s_dq[1];
-            asm volatile("bar.sync 2, 128;" ::: "memory");
+            asm volatile("bar.sync 2, %0;" ::"n"(32 * DT_FP4_DQW) : "memory");
             if (go != 1) break;
             int nk;
             if (u < sc.up_units) {
@@ -974,27 +1031,30 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                 const DnUnit d = dn_unit(sc, u - sc.up_units, s_dnb);
                 nk = d.kb1 - d.kb0;
             }
-            for (int kb = 0; kb < nk; ++kb) {
-                // raw stage landed, and the A tile it goes to has been read
-                if (mbar_wait(&full[stage], phase, abort_flag) && mbar_wait(&a_empty[ast], aph ^ 1, abort_flag)) {
-                    uint8_t *slot = smem + ast * DT_FP4_SLOT;
-                    fp4_dequant_row(slot, smem + Sh::CODES_OFF + stage * DT_FP4_CODES,
-                                    smem + Sh::SCALES_OFF + stage * DT_FP4_SCALES, r);
-                    // the token tile moves with its swizzle: both tiles are 1024-byte aligned
-                    reinterpret_cast<uint4 *>(slot + DT_A_BYTES)[r] =
-                        reinterpret_cast<const uint4 *>(smem + Sh::B_OFF + stage * DT_B_BYTES)[r];
-                    fence_proxy_async_shared();  // generic-proxy writes, read by the MMA (async proxy)
-                } else if (!*abort_flag) {
-                    record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
-                    *abort_flag = 1;
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&empty[stage]);  // the raw stage is consumed
-                    mbar_arrive(&deq[ast]);
+            for (int kb = 0; kb < nk; ++kb, ++gs) {
+                if ((int)(gs % DT_FP4_DQG) == grp) {
+                    bool ok = mbar_wait(&full[stage], phase, abort_flag);
+                    if (ok && gs >= (uint32_t)DT_FP4_AS) ok = mbar_wait(&empty[ps], pph, abort_flag);
+                    if (ok) {
+                        tc_fence_after();
+                        const uint8_t *blk = smem + Sh::BLK_OFF + stage * DT_FP4_BLK;
+                        uint32_t v0[16], v1[16];
+                        fp4_dequant_half(blk, 0, row, v0);
+                        fp4_dequant_half(blk, 1, row, v1);
+                        tmem_st16(t_a + (uint32_t)(ast * 32), v0);
+                        tmem_st16(t_a + (uint32_t)(ast * 32 + 16), v1);
+                        tmem_st_wait();
+                    } else if (!*abort_flag) {
+                        record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                        *abort_flag = 1;
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&deq[ast]);
                 }
                 if (++stage == RS) stage = 0, phase ^= 1;
-                if (++ast == DT_FP4_AS) ast = 0, aph ^= 1;
+                if (++ast == DT_FP4_AS) ast = 0;
+                if (gs >= (uint32_t)DT_FP4_AS && ++ps == RS) ps = 0, pph ^= 1;
             }
             if (++qi == DT_ACC) qi = 0, qph ^= 1;
         }
@@ -1005,7 +1065,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(DT_TMEM_COLS));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(Sh::TMEM_COLS));
     }
 }
 
@@ -1115,8 +1175,8 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     a.meta = L.meta;
     a.gate_b = L.gate_b; a.up_b = L.up_b; a.down_b = L.down_b;
     a.hp = L.dec_hp;
-    a.gu_codes = L.fp4_gu_codes; a.gu_scales = L.fp4_gu_scales;
-    a.dn_codes = L.fp4_dn_codes; a.dn_scales = L.fp4_dn_scales;
+    a.gu_fp4 = L.fp4_gu;
+    a.dn_fp4 = L.fp4_dn;
     a.ot = (L.H + 127) / 128;
     a.partials = L.dec_partials;
     a.counters = L.dec_tickets;
@@ -1145,14 +1205,26 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
 
 // ---------------------------------------------------------------------------
 // MXFP4 packing for the decode kernel: each (row block, 64-wide K block) of a
-// matrix becomes one contiguous run of 128 rows x 32 code bytes and one of
-// 128 rows x 2 scale bytes (a row's two 16-byte blocks are adjacent in the
-// source, so a row copies 32 bytes).  gate/up: 64 gate rows then the 64
-// matching up rows of the de-interleaved gate_up; down: 128 output rows, rows
-// past H zero (code 0 is the value 0).
+// matrix becomes one contiguous block of DT_FP4_BLK bytes, the codes as
+// [2 halves][128 rows][16 B] (half h = the row's 32-element source block
+// 2 kb + h) and then the scales as [2 halves][128 rows], so that a warp
+// reading one half of 32 consecutive rows reads 512 contiguous bytes.
+// gate/up: 64 gate rows then the 64 matching up rows of the de-interleaved
+// gate_up; down: 128 output rows, rows past H zero (code 0 is the value 0).
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void fp4_pack_row(uint8_t *blk, int trow, const uint8_t *src_blocks,
+                                             const uint8_t *src_scales)
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        reinterpret_cast<uint4 *>(blk + (h * 128 + trow) * 16)[0] =
+            src_blocks ? reinterpret_cast<const uint4 *>(src_blocks)[h] : make_uint4(0, 0, 0, 0);
+        blk[128 * 32 + h * 128 + trow] = src_scales ? src_scales[h] : 127;
+    }
+}
+
 __global__ void pack_fp4_gate_up_kernel(const uint8_t *blocks, const uint8_t *scales, int E, int F, int H,
-                                        uint8_t *codes, uint8_t *sc)
+                                        uint8_t *out)
 {
     const int nkb = H / 64, nb = H / 32;
     const size_t n = (size_t)E * 2 * F * nkb;  // one (source row, K block) each
@@ -1162,18 +1234,12 @@ __global__ void pack_fp4_gate_up_kernel(const uint8_t *blocks, const uint8_t *sc
         const int e = (int)(row / (2 * F)), rr = (int)(row - (size_t)e * 2 * F);
         const int f = rr >> 1, up = rr & 1;
         const size_t blk = ((size_t)e * (F / 64) + f / 64) * nkb + kb;
-        const int trow = up * 64 + (f & 63);
-        const uint4 *src = reinterpret_cast<const uint4 *>(blocks + (row * nb + 2 * kb) * 16);
-        uint4 *dst = reinterpret_cast<uint4 *>(codes + blk * DT_FP4_CODES + trow * 32);
-        dst[0] = src[0];
-        dst[1] = src[1];
-        sc[blk * DT_FP4_SCALES + trow * 2] = scales[row * nb + 2 * kb];
-        sc[blk * DT_FP4_SCALES + trow * 2 + 1] = scales[row * nb + 2 * kb + 1];
+        fp4_pack_row(out + blk * DT_FP4_BLK, up * 64 + (f & 63), blocks + (row * nb + 2 * kb) * 16,
+                     scales + row * nb + 2 * kb);
     }
 }
 
-__global__ void pack_fp4_down_kernel(const uint8_t *blocks, const uint8_t *scales, int E, int F, int H, uint8_t *codes,
-                                     uint8_t *sc)
+__global__ void pack_fp4_down_kernel(const uint8_t *blocks, const uint8_t *scales, int E, int F, int H, uint8_t *out)
 {
     const int nkb = F / 64, nb = F / 32, ot = (H + 127) / 128;
     const size_t n = (size_t)E * ot * 128 * nkb;  // one (padded output row, K block) each
@@ -1182,29 +1248,23 @@ __global__ void pack_fp4_down_kernel(const uint8_t *blocks, const uint8_t *scale
         const int kb = (int)(i - prow * nkb);
         const int e = (int)(prow / ((size_t)ot * 128)), h = (int)(prow - (size_t)e * ot * 128);
         const size_t blk = ((size_t)e * ot + h / 128) * nkb + kb;
-        const int trow = h & 127;
-        uint4 *dst = reinterpret_cast<uint4 *>(codes + blk * DT_FP4_CODES + trow * 32);
-        if (h < H) {
-            const size_t row = (size_t)e * H + h;
-            const uint4 *src = reinterpret_cast<const uint4 *>(blocks + (row * nb + 2 * kb) * 16);
-            dst[0] = src[0];
-            dst[1] = src[1];
-            sc[blk * DT_FP4_SCALES + trow * 2] = scales[row * nb + 2 * kb];
-            sc[blk * DT_FP4_SCALES + trow * 2 + 1] = scales[row * nb + 2 * kb + 1];
-        } else {
-            dst[0] = dst[1] = make_uint4(0, 0, 0, 0);
-            sc[blk * DT_FP4_SCALES + trow * 2] = sc[blk * DT_FP4_SCALES + trow * 2 + 1] = 127;
-        }
+        const size_t row = (size_t)e * H + h;
+        fp4_pack_row(out + blk * DT_FP4_BLK, h & 127, h < H ? blocks + (row * nb + 2 * kb) * 16 : nullptr,
+                     h < H ? scales + row * nb + 2 * kb : nullptr);
     }
+}
+
+size_t dectc_fp4_bytes(const Layer &L, bool gate_up)
+{
+    const size_t ot = (L.H + 127) / 128;
+    return gate_up ? (size_t)L.E * (L.F / 64) * (L.H / 64) * DT_FP4_BLK : (size_t)L.E * ot * (L.F / 64) * DT_FP4_BLK;
 }
 
 int dectc_pack_fp4(Layer &L, const uint8_t *gu_blocks, const uint8_t *gu_scales, const uint8_t *dn_blocks,
                    const uint8_t *dn_scales)
 {
-    pack_fp4_gate_up_kernel<<<4 * L.num_sms, 256>>>(gu_blocks, gu_scales, L.E, L.F, L.H, L.fp4_gu_codes,
-                                                     L.fp4_gu_scales);
-    pack_fp4_down_kernel<<<4 * L.num_sms, 256>>>(dn_blocks, dn_scales, L.E, L.F, L.H, L.fp4_dn_codes,
-                                                  L.fp4_dn_scales);
+    pack_fp4_gate_up_kernel<<<4 * L.num_sms, 256>>>(gu_blocks, gu_scales, L.E, L.F, L.H, L.fp4_gu);
+    pack_fp4_down_kernel<<<4 * L.num_sms, 256>>>(dn_blocks, dn_scales, L.E, L.F, L.H, L.fp4_dn);
     return cudaDeviceSynchronize() == cudaSuccess ? 0 : -1;
 }
 

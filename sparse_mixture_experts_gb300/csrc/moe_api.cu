@@ -348,11 +348,8 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
             // operands hold every code times 2^(e8m0 - 127) exactly for e8m0 in 113..140
             L.fp4_decode = gu4.min_scale >= 113 && dn4.min_scale >= 113 && gu4.max_scale <= 140 && dn4.max_scale <= 140;
             if (L.fp4_decode) {
-                const size_t ot = (H + 127) / 128;
-                if ((st = dev_alloc_t(L, &L.fp4_gu_codes, E * 2 * F * H / 2))) return st;
-                if ((st = dev_alloc_t(L, &L.fp4_gu_scales, E * 2 * F * H / 32))) return st;
-                if ((st = dev_alloc_t(L, &L.fp4_dn_codes, E * ot * 128 * F / 2))) return st;
-                if ((st = dev_alloc_t(L, &L.fp4_dn_scales, E * ot * 128 * F / 32))) return st;
+                if ((st = dev_alloc_t(L, &L.fp4_gu, dectc_fp4_bytes(L, true)))) return st;
+                if ((st = dev_alloc_t(L, &L.fp4_dn, dectc_fp4_bytes(L, false)))) return st;
                 if ((st = dev_alloc(L, &L.dec_x16, 16 * H * 2))) return st;
                 if (dectc_pack_fp4(L, gu4.blocks, gu4.scales, dn4.blocks, dn4.scales) != 0)
                     return fail(MOE_ERR_CUDA, "MXFP4 packing failed");

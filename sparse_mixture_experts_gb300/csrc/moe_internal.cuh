@@ -101,10 +101,8 @@ struct Layer {
     // packed per (row block, 64-wide K block) so a pipeline stage is one
     // contiguous copy of each; x in f16 for the token operand
     bool fp4_decode = false;         // MXFP4 layer whose scales fit the f16 operand path
-    uint8_t *fp4_gu_codes = nullptr; // [E][F/64][H/64][128 rows: 64 gate, 64 up][32 B]
-    uint8_t *fp4_gu_scales = nullptr;// [E][F/64][H/64][128][2]
-    uint8_t *fp4_dn_codes = nullptr; // [E][ceil(H/128)][F/64][128][32 B]
-    uint8_t *fp4_dn_scales = nullptr;// [E][ceil(H/128)][F/64][128][2]
+    uint8_t *fp4_gu = nullptr;       // [E][F/64][H/64] packed blocks (128 rows: 64 gate, 64 up; codes, scales)
+    uint8_t *fp4_dn = nullptr;       // [E][ceil(H/128)][F/64] packed blocks
     void *dec_x16 = nullptr;         // [16][H] f16 copy of the decode batch
 
     // per-kernel timing (moe_timing_enable / moe_timing_read)
@@ -418,6 +416,7 @@ size_t dectc_workspace(const Layer &L, size_t &hp_bytes, size_t &part_bytes, siz
 int dectc_prepare(Layer &L);
 // MXFP4 layers: pack the expert codes and scales for the decode kernel (from the
 // caller's blocks and scales already on the device); 0 on success
+size_t dectc_fp4_bytes(const Layer &L, bool gate_up);  // packed MXFP4 bytes of gate/up or down
 int dectc_pack_fp4(Layer &L, const uint8_t *gu_blocks, const uint8_t *gu_scales, const uint8_t *dn_blocks,
                    const uint8_t *dn_scales);
 void dectc_release(Layer &L);
