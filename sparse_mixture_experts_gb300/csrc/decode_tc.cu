@@ -35,8 +35,9 @@
 //             All gate/up units are claimed before any down unit, so a waiting
 //             down unit only depends on work that CTAs already hold.
 // The producer hands each claimed unit to the MMA and epilogue roles through a
-// queue of 8 slots; slot i also owns TMEM accumulator i.  All waits are bounded
-// (about a second); results are deterministic.
+// queue of 8 slots.  Two MMA threads take alternate stages of the stream, each
+// into its own TMEM accumulator of the unit's slot, and the epilogue adds the
+// two.  All waits are bounded (about a second); results are deterministic.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -47,28 +48,29 @@ namespace moe {
 
 constexpr int DT_TOK = 16;                      // N: token columns
 constexpr int DT_STAGES = 8;
-constexpr int DT_THREADS = 192;                 // bf16 weights: producer, MMA, 4 epilogue warps
+constexpr int DT_THREADS = 192;                 // producer, MMA, 4 epilogue warps (then the second MMA warp)
 constexpr int DT_A_BYTES = 128 * 64 * 2;        // 16 KB weight tile
 constexpr int DT_B_BYTES = DT_TOK * 64 * 2;     // 2 KB token tile
 constexpr int DT_STAGE_BYTES = DT_A_BYTES + DT_B_BYTES;
-constexpr int DT_ACC = 8;                       // unit queue slots = TMEM accumulators
+constexpr int DT_ACC = 8;                       // unit queue slots (each owns an accumulator per MMA warp)
 constexpr int DT_EP_LD = DT_TOK + 1;            // row pitch (floats) of the epilogue's accumulator copy
 constexpr int DT_XCH_BYTES = 128 * DT_EP_LD * 4; // the accumulator tile in shared memory
 constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
-// MXFP4 weights: a stage is the token tile and one packed block of codes and
-// scales (DT_FP4_BLK bytes for 128 rows x 64 K), a third of a bf16 stage, so
-// the producer's ring is deeper (DT_FP4_RS stages).  Eight more warps widen
+// MXFP4 weights: a stage is DT_FP4_KPS 64-wide K blocks, each a token tile and
+// one packed block of codes and scales (DT_FP4_BLK bytes for 128 rows x 64 K);
+// with two blocks per stage a unit's odd last block makes a one-block stage and
+// the blocks of a stage may come from different groups (down units).  Two
+// blocks per stage measured no faster than one (the per-stage hand-offs are not
+// what bounds this loop), so one is used.  The producer's ring holds
+// DT_FP4_RS stages.  Eight more warps widen
 // each block to f16 and store it straight into tensor memory, where the MMA
-// reads its A operand (DT_FP4_AS tiles of 32 columns): the f16 tile never
+// reads its A operand (DT_FP4_AS tiles of 64 columns): the f16 tile never
 // touches shared memory, whose bandwidth would otherwise bound the stage rate.
-// Two MMA warps take alternate stages into accumulators of their own (an MMA
-// costs its issuing thread about as much at N = 16 as at N = 256, so one
-// thread's issue rate would bound the stream), and the epilogue adds the two.
 constexpr int DT_FP4_BLK = 128 * 32 + 128 * 2;  // codes [2 halves][128 rows][16 B], scales [2 halves][128 rows]
+constexpr int DT_FP4_KPS = 1;                   // K blocks per stage (1 or 2)
 constexpr int DT_FP4_RS = 24;                   // raw stages
-constexpr int DT_FP4_AS = 8;                    // A tiles in tensor memory
+constexpr int DT_FP4_AS = 8;                    // A tiles (stages) in tensor memory, 32 columns per K block
 constexpr int DT_FP4_DQW = 8;                   // dequantising warps
-constexpr int DT_FP4_NM = 2;                    // MMA warps
 constexpr int DT_FP4_NP = 4;                    // producer threads
 constexpr int DT_FP4_DQG = 2;                   // dequantising groups of 4 warps, taking alternate stages
 constexpr int DT_FP4_A_COL = 256;               // first A-tile column (accumulators use 0..255)
@@ -78,17 +80,26 @@ template <bool FP4>
 struct DtShape {
     // bf16: producer, MMA, 4 epilogue warps; MXFP4: + 8 dequantising warps, a second MMA warp and a
     // warp of three more producer threads
-    static constexpr int THREADS = FP4 ? DT_THREADS + 32 * (DT_FP4_DQW + 2) : DT_THREADS;
+    static constexpr int THREADS = FP4 ? DT_THREADS + 32 * (DT_FP4_DQW + 2) : DT_THREADS + 32;
+    static constexpr int NM = 2;                                    // MMA warps
+    static constexpr int MMA2_WARP = FP4 ? 6 + DT_FP4_DQW : 6;      // the second one
     static constexpr int RS = FP4 ? DT_FP4_RS : DT_STAGES;   // producer ring
-    static constexpr int TMEM_COLS = FP4 ? DT_FP4_TMEM_COLS : DT_ACC * DT_TOK;
-    // smem: bf16 [RS][A | B]; MXFP4 [RS][B] [RS][block]
+    static constexpr int TMEM_COLS = FP4 ? DT_FP4_TMEM_COLS : DT_ACC * 2 * DT_TOK;
+    static constexpr int KPS = FP4 ? DT_FP4_KPS : 1;        // K blocks per stage
+    // smem: bf16 [RS][A | B]; MXFP4 [RS][KPS][B] [RS][KPS][block]
     static constexpr int B_OFF = FP4 ? 0 : DT_A_BYTES;      // first B tile
-    static constexpr int B_STRIDE = FP4 ? DT_B_BYTES : DT_STAGE_BYTES;
+    static constexpr int B_STRIDE = FP4 ? KPS * DT_B_BYTES : DT_STAGE_BYTES;
     static constexpr int A_STRIDE = DT_STAGE_BYTES;         // bf16 only
-    static constexpr int BLK_OFF = RS * DT_B_BYTES;         // MXFP4 only
-    static constexpr int RING = FP4 ? (BLK_OFF + RS * DT_FP4_BLK + 1023) / 1024 * 1024 : DT_STAGES * DT_STAGE_BYTES;
+    static constexpr int BLK_OFF = RS * KPS * DT_B_BYTES;   // MXFP4 only
+    static constexpr int BLK_STRIDE = KPS * DT_FP4_BLK;
+    static constexpr int RING = FP4 ? (BLK_OFF + RS * BLK_STRIDE + 1023) / 1024 * 1024 : DT_STAGES * DT_STAGE_BYTES;
     static constexpr size_t SMEM = (size_t)RING + 1024 + DT_XCH_BYTES + 1024;
 };
+static_assert(DT_FP4_KPS == 1 || DT_FP4_KPS == 2, "one or two K blocks per MXFP4 stage");
+static_assert(DT_ACC * 2 * DT_TOK <= DT_FP4_A_COL && DT_FP4_A_COL + DT_FP4_AS * DT_FP4_KPS * 32 <= DT_FP4_TMEM_COLS,
+              "MXFP4 accumulators and A tiles fit the tensor memory allocation");
+static_assert(DT_FP4_RS <= 32 && DT_STAGES <= 32, "the producer's per-stage masks are 32 bits");
+static_assert(DtShape<true>::SMEM + 11 * 1024 <= 227 * 1024, "MXFP4 ring and static shared memory fit a CTA");
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
 constexpr int DT_SATURATING_CTAS = 128;         // CTAs streaming at once that saturate HBM
 constexpr int DT_UP_MIN_KB = 8;                 // smallest gate/up split, in 64-wide K blocks
@@ -481,7 +492,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
         }
         mbar_init(&s_bnd_bar, 1);
         for (int b = 0; b < DT_ACC; ++b) {
-            mbar_init(&acc_full[b], FP4 ? DT_FP4_NM : 1);
+            mbar_init(&acc_full[b], Sh::NM);
             mbar_init(&uq_full[b], 1);
             mbar_init(&uq_empty[b], FP4 ? DT_FP4_NP : 1);  // MXFP4: the epilogue and the following producers
         }
@@ -652,6 +663,9 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                     seg_end = dn.kb1;
                 }
                 int left = seg_end - seg_k;
+                const int unit_nk = left;
+                int pos = 0;          // K block of the unit
+                bool merged = false;  // MXFP4: this stage's second block came with the first
                 // the next unit is claimed a few stages before this one ends, so
                 // the counter's round trip overlaps this unit's loads.  Claims stay
                 // in order: a CTA holds at most one unclaimed-ahead unit, and a
@@ -681,10 +695,12 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         else { ma = &maps.down; arow = s_act[gi] * a.H + dn.tile * 128; }
                         brow = gi * DT_TOK;
                         // h'[gi] is complete once every gate/up tile of the group is
-                        // (only waited for by a producer with a stage in the segment)
+                        // (only waited for by a producer with a stage in the segment:
+                        // its stages are those of stream index gs .. gs + ns - 1)
                         const int need = fd / 64;
                         int *done = group_done + gi * DT_DONE_STRIDE;
-                        if ((n >= NP || (int)(((uint32_t)pw + NP - gs % NP) % NP) < n) && ld_acquire(done) < need) {
+                        const int ns = (pos % Sh::KPS + n + Sh::KPS - 1) / Sh::KPS;
+                        if ((ns >= NP || (int)(((uint32_t)pw + NP - gs % NP) % NP) < ns) && ld_acquire(done) < need) {
                             // poll with a short back-off: many producers may wait on
                             // the same counter, and the increment must get through
                             const unsigned long long t0 = globaltimer();
@@ -701,43 +717,58 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         fence_proxy_async_global();
                         if (!ok) break;
                     }
-                    for (int kb = kb0; kb < kb1; ++kb, --left, ++gs) {
+                    for (int kb = kb0; kb < kb1; ++kb, --left, ++pos) {
                         if (!claimed && left <= DT_CLAIM_AHEAD) {
                             u_next = atomicAdd(next_unit, 1);
                             claimed = true;
                         }
+                        const int sub = pos % Sh::KPS;  // K block within the stage
                         if ((int)(gs % NP) == pw) {
-                            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
-                                record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
-                                *abort_flag = 1;
-                                ok = false;
-                                break;
+                            if (sub == 0) {
+                                if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                                    record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
+                                    *abort_flag = 1;
+                                    ok = false;
+                                    break;
+                                }
+                                // the one arrival of the stage's full barrier, with every byte its
+                                // copies below complete (bf16: A and the token tile; MXFP4: per K
+                                // block a packed block and a token tile)
+                                const int nkb = min(Sh::KPS, unit_nk - pos);
+                                mbar_arrive_expect_tx(&full[stage], FP4 ? nkb * (DT_B_BYTES + DT_FP4_BLK) : DT_STAGE_BYTES);
                             }
                             uint8_t *sa = smem + stage * Sh::A_STRIDE;  // bf16 only
-                            uint8_t *sb = smem + Sh::B_OFF + stage * Sh::B_STRIDE;
+                            uint8_t *sb = smem + Sh::B_OFF + stage * Sh::B_STRIDE + sub * DT_B_BYTES;
                             const int kc = kb * 64;
                             if (FP4) {
-                                // the packed block of this (row block, K block), the token tile by TMA
-                                mbar_arrive_expect_tx(&full[stage], DT_B_BYTES + DT_FP4_BLK);
+                                // the packed block(s) of this (row block, K block): one copy for
+                                // both blocks of a stage when they are adjacent (the same segment);
+                                // the token tile by TMA
                                 const size_t blk = is_up ? ((size_t)wexp * (a.F / 64) + ux.ft) * (a.H / 64) + kb
                                                          : ((size_t)wexp * a.ot + dn.tile) * (a.F / 64) + kb;
-                                bulk_load(smem + Sh::BLK_OFF + stage * DT_FP4_BLK,
-                                          (is_up ? a.gu_fp4 : a.dn_fp4) + blk * DT_FP4_BLK, DT_FP4_BLK, &full[stage]);
+                                if (sub == 0 || !merged) {
+                                    merged = sub == 0 && Sh::KPS == 2 && kb + 1 < kb1;  // (KPS <= 2)
+                                    const uint32_t nb = merged ? 2 : 1;
+                                    bulk_load(smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * DT_FP4_BLK,
+                                              (is_up ? a.gu_fp4 : a.dn_fp4) + blk * DT_FP4_BLK, nb * DT_FP4_BLK,
+                                              &full[stage]);
+                                }
                                 tma_load_2d(sb, is_up ? &maps.x : &maps.hp, &full[stage], kc, brow);
                             } else if (is_up) {
-                                mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
                                 tma_load_2d(sa, ma, &full[stage], kc, arow);
                                 tma_load_2d(sa + DT_A_BYTES / 2, mb, &full[stage], kc, arow);
                                 tma_load_2d(sb, &maps.x, &full[stage], kc, brow);
                             } else {
-                                mbar_arrive_expect_tx(&full[stage], DT_STAGE_BYTES);
                                 tma_load_2d(sa, ma, &full[stage], kc, arow);
                                 tma_load_2d(sb, &maps.hp, &full[stage], kc, brow);
                             }
                             used |= 1u << stage;
                             last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                         }
-                        if (++stage == RS) stage = 0, phase ^= 1;
+                        if (sub == Sh::KPS - 1 || pos == unit_nk - 1) {  // the stage is complete
+                            if (++stage == RS) stage = 0, phase ^= 1;
+                            ++gs;
+                        }
                     }
                 }
                 if (!claimed) u_next = atomicAdd(next_unit, 1);
@@ -754,12 +785,14 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
             for (int s = 0; s < RS; ++s)
                 if ((used >> s) & 1u) mbar_wait(&full[s], (last_phase >> s) & 1u, &never);
         }
-    } else if (warp == 1 || (FP4 && warp == 6 + DT_FP4_DQW)) {
-        // ------------------------------ MMA issuer(s) ------------------------------
-        // bf16: one thread issues every stage.  MXFP4: two threads take
-        // alternate stages (by their index in the stream) into accumulators of
-        // their own, with A the tile the dequantising warps left in tensor memory.
-        constexpr int NM = FP4 ? DT_FP4_NM : 1;
+    } else if (warp == 1 || warp == Sh::MMA2_WARP) {
+        // ------------------------------ MMA issuers ------------------------------
+        // Two threads take alternate stages (by their index in the stream) into
+        // accumulators of their own, which the epilogue adds: at N = 16 an MMA
+        // costs its issuing thread about as much as at N = 256, so one thread's
+        // issue rate would bound the stream.  MXFP4: A is the tile the
+        // dequantising warps left in tensor memory.
+        constexpr int NM = Sh::NM;
         const int mw = warp == 1 ? 0 : 1;
         if (lane == 0) {
             constexpr uint32_t idesc = FP4 ? idesc_f16_f32(128, DT_TOK) : idesc_bf16_f32(128, DT_TOK);
@@ -789,8 +822,8 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                     nk = d.kb1 - d.kb0;
                 }
                 bool ok = true, first = true;
-                for (int kb = 0; kb < nk; ++kb, ++gs) {
-                    if (!FP4 || (int)(gs % NM) == mw) {
+                for (int j = 0; j * Sh::KPS < nk; ++j, ++gs) {
+                    if ((int)(gs % NM) == mw) {
                         // MXFP4: the A tile is in tensor memory once the block it came
                         // from has landed, so the token tile has too
                         if (FP4 ? !mbar_wait(&deq[ast], aph, abort_flag) : !mbar_wait(&full[stage], phase, abort_flag)) {
@@ -802,16 +835,20 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         tc_fence_after();
                         const uint32_t sb = smem_u32(smem + Sh::B_OFF + stage * Sh::B_STRIDE);
                         if (FP4) {
-                            const uint32_t at = tmem_base + (uint32_t)(DT_FP4_A_COL + ast * 32);
+                            const int nkb = min(Sh::KPS, nk - j * Sh::KPS);
+                            const uint32_t at = tmem_base + (uint32_t)(DT_FP4_A_COL + ast * 32 * Sh::KPS);
+                            for (int sub = 0; sub < nkb; ++sub)
 #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                mma_f16_ta(d_tmem, at + k * 8, smem_desc_sw128(sb + k * 32), idesc, !first || k != 0);
+                                for (int k = 0; k < 4; ++k)
+                                    mma_f16_ta(d_tmem, at + sub * 32 + k * 8,
+                                               smem_desc_sw128(sb + sub * DT_B_BYTES + k * 32), idesc,
+                                               !first || sub != 0 || k != 0);
                         } else {
                             const uint32_t sa = smem_u32(smem + stage * Sh::A_STRIDE);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
-                                         (kb | k) != 0);
+                                         !first || k != 0);
                         }
                         mma_commit(&empty[stage]);  // the raw stage (and MXFP4: the A tile) is free
                         first = false;
@@ -880,25 +917,21 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
             tc_fence_after();
             uint32_t raw[16];
             float v[DT_TOK];
-            if (FP4) {
+            {
                 // the two MMA threads' accumulators; one that got no stage of the
                 // unit (a single-stage unit) holds nothing
 #pragma unroll
                 for (int t = 0; t < DT_TOK; ++t) v[t] = 0.0f;
+                const int nst = (nk + Sh::KPS - 1) / Sh::KPS;  // stages of the unit
 #pragma unroll
-                for (int m = 0; m < DT_FP4_NM; ++m) {
-                    if (nk < DT_FP4_NM && (int)(e_gs % DT_FP4_NM) != m) continue;
-                    tmem_ld16(tmem_base + lane_addr + (uint32_t)((qi * DT_FP4_NM + m) * DT_TOK), raw);
+                for (int m = 0; m < Sh::NM; ++m) {
+                    if (nst < Sh::NM && (int)(e_gs % Sh::NM) != m) continue;
+                    tmem_ld16(tmem_base + lane_addr + (uint32_t)((qi * Sh::NM + m) * DT_TOK), raw);
                     tmem_ld_wait();
 #pragma unroll
                     for (int t = 0; t < DT_TOK; ++t) v[t] += __uint_as_float(raw[t]);
                 }
-                e_gs += (uint32_t)nk;
-            } else {
-                tmem_ld16(tmem_base + lane_addr + (uint32_t)(qi * DT_TOK), raw);
-                tmem_ld_wait();
-#pragma unroll
-                for (int t = 0; t < DT_TOK; ++t) v[t] = __uint_as_float(raw[t]);
+                e_gs += (uint32_t)nst;
             }
 
             bool finalize = true;
@@ -987,7 +1020,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
             if (et == 0) mbar_arrive(&uq_empty[qi]);
             if (++qi == DT_ACC) qi = 0, qph ^= 1;
         }
-    } else if (FP4) {
+    } else if (FP4 && warp < 6 + DT_FP4_DQW) {
         // ------------------------------ MXFP4 dequantisation (warps 6..13) ------------------------------
         // Follows the units in queue order like the MMA threads.  Two groups of
         // four warps take alternate stages (by their index in the stream); in a
@@ -1031,18 +1064,22 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                 const DnUnit d = dn_unit(sc, u - sc.up_units, s_dnb);
                 nk = d.kb1 - d.kb0;
             }
-            for (int kb = 0; kb < nk; ++kb, ++gs) {
+            for (int j = 0; j * DT_FP4_KPS < nk; ++j, ++gs) {
                 if ((int)(gs % DT_FP4_DQG) == grp) {
                     bool ok = mbar_wait(&full[stage], phase, abort_flag);
                     if (ok && gs >= (uint32_t)DT_FP4_AS) ok = mbar_wait(&empty[ps], pph, abort_flag);
                     if (ok) {
                         tc_fence_after();
-                        const uint8_t *blk = smem + Sh::BLK_OFF + stage * DT_FP4_BLK;
-                        uint32_t v0[16], v1[16];
-                        fp4_dequant_half(blk, 0, row, v0);
-                        fp4_dequant_half(blk, 1, row, v1);
-                        tmem_st16(t_a + (uint32_t)(ast * 32), v0);
-                        tmem_st16(t_a + (uint32_t)(ast * 32 + 16), v1);
+                        const int nkb = min(DT_FP4_KPS, nk - j * DT_FP4_KPS);
+                        for (int sub = 0; sub < nkb; ++sub) {
+                            const uint8_t *blk = smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * DT_FP4_BLK;
+                            uint32_t v0[16], v1[16];
+                            fp4_dequant_half(blk, 0, row, v0);
+                            fp4_dequant_half(blk, 1, row, v1);
+                            const uint32_t col = (uint32_t)((ast * DT_FP4_KPS + sub) * 32);
+                            tmem_st16(t_a + col, v0);
+                            tmem_st16(t_a + col + 16, v1);
+                        }
                         tmem_st_wait();
                     } else if (!*abort_flag) {
                         record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
