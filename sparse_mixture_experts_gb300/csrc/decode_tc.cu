@@ -973,23 +973,25 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                 asm volatile("bar.sync 1, 128;" ::: "memory");
             }
             if (finalize && is_up) {
-                // rows 0..63 are gate projections, rows 64..127 the matching up projections
-                if (r < 64) {
-                    const int f = ux.ft * 64 + r;
+                // rows 0..63 are gate projections, rows 64..127 the matching up
+                // projections.  All 128 threads: feature r % 64 for every other
+                // token from r / 64.  Only the T real token rows of h' are written:
+                // a row t >= T feeds only column t of the down accumulator, which
+                // nothing reads.
+                {
+                    const int fr = r & 63;
+                    const int f = ux.ft * 64 + fr;
                     const int e = ux.shared ? -1 : s_act[ux.g];
                     const float bg = (!ux.shared && a.gate_b) ? a.gate_b[(size_t)e * a.F + f] : 0.0f;
                     const float bu = (!ux.shared && a.up_b) ? a.up_b[(size_t)e * a.F + f] : 0.0f;
                     const bool swiglu = ux.shared || a.act == MOE_ACT_SWIGLU;
                     const size_t hbase = (size_t)ux.g * DT_TOK * a.Fmax + f;
 #pragma unroll 1
-                    for (int t = 0; t < DT_TOK; ++t) {
-                        float hval = 0.0f;
-                        if (t < T) {
-                            const float gv = xch[r * DT_EP_LD + t] + bg, uv = xch[(r + 64) * DT_EP_LD + t] + bu;
-                            hval = swiglu ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
-                                          : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
-                            hval *= s_wt[t];
-                        }
+                    for (int t = r >> 6; t < T; t += 2) {
+                        const float gv = xch[fr * DT_EP_LD + t] + bg, uv = xch[(fr + 64) * DT_EP_LD + t] + bu;
+                        float hval = swiglu ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
+                                            : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
+                        hval *= s_wt[t];
                         if (FP4) reinterpret_cast<__half *>(a.hp)[hbase + (size_t)t * a.Fmax] = __float2half_rn(hval);
                         else reinterpret_cast<__nv_bfloat16 *>(a.hp)[hbase + (size_t)t * a.Fmax] = __float2bfloat16_rn(hval);
                     }
