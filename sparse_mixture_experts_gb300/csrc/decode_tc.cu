@@ -60,12 +60,14 @@ constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
 // one packed block of codes and scales (DT_FP4_BLK bytes for 128 rows x 64 K);
 // with two blocks per stage a unit's odd last block makes a one-block stage and
 // the blocks of a stage may come from different groups (down units).  Two
-// blocks per stage measured no faster than one (the per-stage hand-offs are not
-// what bounds this loop), so one is used.  The producer's ring holds
-// DT_FP4_RS stages.  Eight more warps widen
-// each block to f16 and store it straight into tensor memory, where the MMA
-// reads its A operand (DT_FP4_AS tiles of 64 columns): the f16 tile never
+// blocks per stage measured no faster than one, so one is used.  The
+// producer's ring holds DT_FP4_RS stages.  Eight more warps widen each block to
+// f16 and store it straight into tensor memory, where the MMA reads its A
+// operand (DT_FP4_AS tiles of 32 columns per K block): the f16 tile never
 // touches shared memory, whose bandwidth would otherwise bound the stage rate.
+// What bounds this pipeline instead is the length of each role's per-stage
+// instruction path (one warp or thread per stage), hence several producer
+// threads, two dequantising groups and two MMA threads taking stages in turn.
 constexpr int DT_FP4_BLK = 128 * 32 + 128 * 2;  // codes [2 halves][128 rows][16 B], scales [2 halves][128 rows]
 constexpr int DT_FP4_KPS = 1;                   // K blocks per stage (1 or 2)
 constexpr int DT_FP4_RS = 24;                   // raw stages
