@@ -230,6 +230,13 @@ EDGE_SPECS = [
     # fp32 layer larger than the tiny one, unnormalised weights with a scale
     ("f32_unnormalised", synth.LayerSpec("f32 mid", 96, 12, 3, 40, shared_ff=24, norm_topk_prob=False,
                                          weights_scale=2.5, dtype="f32"), 70),
+    # MXFP4 experts: every expert selected, a single expert, a ragged tail
+    ("mxfp4_k_equals_E", synth.GPTOSS_MXFP4.replace(name="mxfp4 k=E", hidden=128, n_expert=4, top_k=4,
+                                                    expert_ff=64), 37),
+    ("mxfp4_single_expert", synth.GPTOSS_MXFP4.replace(name="mxfp4 E=1", hidden=192, n_expert=1, top_k=1,
+                                                       expert_ff=128), 45),
+    ("mxfp4_ragged", synth.GPTOSS_MXFP4.replace(name="mxfp4 small", hidden=192, n_expert=8, top_k=4,
+                                                expert_ff=128), 133),
 ]
 
 
@@ -300,14 +307,22 @@ MXFP4_SMALL = synth.GPTOSS_MXFP4.replace(name="gpt-oss-like, MXFP4 experts, smal
                                          expert_ff=192)
 
 
-@pytest.mark.parametrize("low_scale", [False, True], ids=["codes", "bf16-copy"])
-def test_mxfp4_decode_kernel_choice(low_scale):
+@pytest.mark.parametrize("scales", ["synthetic", "range_edges", "below_range"])
+def test_mxfp4_decode_kernel_choice(scales):
     """A decode batch on MXFP4 experts runs the kernel that streams the codes
     and scales (timed as its own kind) while every E8M0 scale is in 113..140,
-    where its f16 operands are exact; one scale below that range sends the
-    layer to the bf16 copy.  Both agree with the oracle on the same weights."""
+    where its f16 operands are exact (the edges included: 2^-14 and 2^13);
+    one scale below that range sends the layer to the bf16 copy.  Each agrees
+    with the oracle on the same weights."""
     spec, T = MXFP4_SMALL, 5
     w = synth.make_weights(spec, seed=5)
+    low_scale = scales == "below_range"
+    if scales == "range_edges":
+        for name in ("gate_up_scales", "down_scales"):
+            s = w[name].copy()
+            s.flat[3::97] = 113
+            s.flat[11::89] = 140
+            w[name] = s
     if low_scale:
         s = w["down_scales"].copy()
         s.flat[37] = 112
