@@ -26,9 +26,43 @@ constexpr int NOALLOC_MAX_DEVICES = 64;
 
 static __device__ __align__(256) float g_noalloc_logits[NOALLOC_MAX_LOGITS];
 
-// device address of g_noalloc_logits, per device, taken once with that device current
-static float *g_noalloc_ptr[NOALLOC_MAX_DEVICES];
+// Device address of g_noalloc_logits, per device, looked up with that device
+// current and kept together with the unique id of the CUDA context it belongs
+// to.  A device reset (or a switch to another context) loads the module again
+// at another address; the id then differs and the address is looked up anew.
+struct NoallocScratch {
+    unsigned long long ctx_id = 0;
+    float *ptr = nullptr;
+};
+static NoallocScratch g_noalloc_scratch[NOALLOC_MAX_DEVICES];
 static std::mutex g_noalloc_mutex;
+
+typedef int (*PfnCtxGetCurrent)(void **ctx);
+typedef int (*PfnCtxGetId)(void *ctx, unsigned long long *id);
+
+// unique id of the calling thread's current CUDA context (0 if unavailable)
+static unsigned long long current_context_id()
+{
+    static PfnCtxGetCurrent get_current = nullptr;
+    static PfnCtxGetId get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PfnCtxGetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PfnCtxGetId>(p);
+        looked_up = true;
+    }
+    void *ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+    return id;
+}
 
 template <typename TW> __device__ __forceinline__ float load_scalar(const TW *p);
 template <> __device__ __forceinline__ float load_scalar<float>(const float *p) { return *p; }
@@ -80,13 +114,9 @@ __global__ void __launch_bounds__(256) noalloc_logits_kernel(const TW *__restric
     }
 }
 
-__device__ __forceinline__ bool na_better(float v, int i, float bv, int bi)
-{
-    return v > bv || (v == bv && i < bi);
-}
-
-// one warp per token: top-k (ties to the lower index, descending order),
-// routing weights, and the token's contribution to the per-expert counts
+// one warp per token: top-k (ties to the lower index, descending order) and
+// routing weights by the same warp routine the layer's selection kernels use,
+// and the token's contribution to the per-expert counts
 __global__ void __launch_bounds__(256) noalloc_select_kernel(const float *__restrict__ logits, int T, int E, int K,
                                                              int mode, int norm, float scale, int *__restrict__ idx,
                                                              float *__restrict__ wout, int *__restrict__ counts)
@@ -94,45 +124,9 @@ __global__ void __launch_bounds__(256) noalloc_select_kernel(const float *__rest
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
-    const float *l = logits + (size_t)t * E;
-    float mx = -INFINITY;
-    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    int sel_i = -1;
-    float sel_v = 0.0f;
-    unsigned taken = 0;  // bit q: expert lane + 32 q already selected
-    for (int j = 0; j < K; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        int q = 0;
-        for (int e = lane; e < E; e += 32, ++q) {
-            if (taken & (1u << q)) continue;
-            const float v = l[e];
-            if (bi == 0x7fffffff || na_better(v, e, bv, bi)) { bv = v; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || na_better(ov, oi, bv, bi))) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) { sel_i = bi; sel_v = bv; }
-    }
-    float w;
-    if (mode == MOE_ROUTER_SOFTMAX_TOPK) {
-        float z = 0.0f;
-        for (int e = lane; e < E; e += 32) z += __expf(l[e] - mx);
-        z = warp_sum(z);
-        const float p = (lane < K) ? __expf(sel_v - mx) / z : 0.0f;
-        const float ps = warp_sum(p);
-        w = (norm ? p / ps : p) * scale;
-    } else {
-        const float m0 = __shfl_sync(0xffffffffu, sel_v, 0);
-        const float ex = (lane < K) ? __expf(sel_v - m0) : 0.0f;
-        w = ex / warp_sum(ex);
-    }
+    int sel_i;
+    float sel_v, w;
+    warp_select_any(logits + (size_t)t * E, E, K, mode, norm, scale, lane, sel_i, sel_v, w);
     if (lane < K) {
         idx[(size_t)t * K + lane] = sel_i;
         wout[(size_t)t * K + lane] = w;
@@ -178,17 +172,21 @@ extern "C" moe_status moe_route_noalloc(const void *x, const void *router_w, con
     if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return na_fail(MOE_ERR_UNSUPPORTED, "device ordinal >= 64");
     float *scratch;
     {
-        // first call on a device: look up the array's device address with that
-        // device current (a host-side use of the symbol itself is not a device
-        // address)
+        // first call on a device (or in a new context on it): look up the
+        // array's device address with that device current; a host-side use of
+        // the symbol itself is not a device address
         std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-        if (!g_noalloc_ptr[dev]) {
+        NoallocScratch &c = g_noalloc_scratch[dev];
+        const unsigned long long id = current_context_id();
+        if (!c.ptr || id == 0 || id != c.ctx_id) {
             float *p = nullptr;
             e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_noalloc_logits);
             if (e != cudaSuccess || !p) return na_fail(MOE_ERR_CUDA, "cudaGetSymbolAddress of the routing scratch failed");
-            g_noalloc_ptr[dev] = p;
+            c.ptr = p;
+            // the lookup makes the device's context current if none was
+            c.ctx_id = current_context_id();
         }
-        scratch = g_noalloc_ptr[dev];
+        scratch = c.ptr;
     }
 
     cudaStream_t s = (cudaStream_t)stream;
