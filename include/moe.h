@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum {
     MOE_OK = 0,
@@ -187,6 +187,33 @@ moe_status moe_get_logits(moe_layer *layer, float *logits, float *sh_logit, void
  * counts[E] int32 (device pointer).  Asynchronous on `stream`. */
 moe_status moe_get_expert_counts(moe_layer *layer, int32_t *counts, void *stream);
 
+/* Intermediates of the last forward, for checking each step against a
+ * reference ("Engine" (cherenkov), section "Prefill": tokens grouped by
+ * expert, gathered, projected and scattered back).  Kept only by the grouped
+ * paths (MOE_PATH_TC and MOE_PATH_STREAM); after a decode-path forward a
+ * non-NULL dst returns UNSUPPORTED.  n = that forward's n_tokens, k = top_k.
+ *   MOE_INTER_OFFSETS  int32 [E + 1]: exclusive prefix sum of the per-expert
+ *                      row counts (expert e's rows start at offsets[e])
+ *   MOE_INTER_PERM     int32 [n k]: the pair ids p = t k + slot in expert
+ *                      order (a stable sort by expert: ascending p within one)
+ *   MOE_INTER_H        [n k (+ n)][max(F, Fs)] in the weight dtype: the
+ *                      activation act(gate, up) of each routed row in the
+ *                      order of MOE_INTER_PERM, then the shared expert's rows
+ *                      (token order) when the layer has one
+ *   MOE_INTER_YS       fp32 [n][k + 1][H]: w_slot (W_down h + b_down) of every
+ *                      (token, slot), and in slot k the gated shared-expert
+ *                      output (zeros-free only when the layer has one)
+ * *size (if non-NULL) receives the byte count; dst NULL only queries it.
+ * dst is a device pointer of `capacity` bytes.  Asynchronous on `stream`. */
+typedef enum {
+    MOE_INTER_OFFSETS = 0,
+    MOE_INTER_PERM = 1,
+    MOE_INTER_H = 2,
+    MOE_INTER_YS = 3
+} moe_intermediate;
+moe_status moe_get_intermediate(moe_layer *layer, int32_t which, void *dst, size_t capacity, size_t *size,
+                                void *stream);
+
 /* Kernel-path selection, for tests and benchmarks. */
 typedef enum {
     MOE_PATH_AUTO = 0,     /* default: DECODE_TC, else FUSED, else TC, else STREAM (first that applies) */
@@ -252,8 +279,11 @@ void moe_destroy(moe_layer *layer);
  * cudaMalloc (an application that owns all device memory through its own pool,
  * a process whose allocator is frozen after start-up, a real-time loop where
  * an allocation and the synchronisation it can bring are not allowed).  The
- * pages have no counterpart of this entry point; it computes the same routing
- * as moe_forward (moe_get_routing / moe_get_expert_counts) without a layer.
+ * pages have no counterpart of this entry point; it computes the routing that
+ * moe_forward reports (moe_get_routing / moe_get_expert_counts) without a
+ * layer, with the same selection routine: the logits are fp32 dot products
+ * whose rounding order may differ from the layer's router kernels, so a token
+ * whose k-th and (k+1)-th logits nearly tie may pick differently.
  *
  * x [n_tokens][hidden], router_w [n_expert][hidden] and the optional router_b
  * [n_expert] are device pointers in `dtype` (x and router_w 16-byte aligned);
@@ -268,7 +298,9 @@ void moe_destroy(moe_layer *layer);
  * on a device share that array and it keeps the last call's contents, so calls
  * that overlap on the GPU race; order them (one stream, or events).  The first
  * call on each device looks the array's address up (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  Other
+ * that device current, and looks it up again when the device's CUDA context
+ * has changed since (after cudaDeviceReset, say); make that first call before
+ * any stream capture.  Other
  * errors: INVALID_ARG (NULL or misaligned pointer, bad size, mode or dtype),
  * UNSUPPORTED (top_k > 32, n_expert > 1024, hidden not a multiple of 8, device
  * ordinal >= 64), CUDA. */

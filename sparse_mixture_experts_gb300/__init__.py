@@ -25,6 +25,7 @@ DT_F32, DT_BF16, DT_MXFP4 = 0, 1, 2
 ROUTER_SOFTMAX_TOPK, ROUTER_TOPK_SOFTMAX = 0, 1
 ACT_SWIGLU, ACT_CLAMP_GLU = 0, 1
 PATH_AUTO, PATH_STREAM, PATH_TC, PATH_FUSED, PATH_DECODE_TC = 0, 1, 2, 3, 4
+INTER_OFFSETS, INTER_PERM, INTER_H, INTER_YS = 0, 1, 2, 3
 KERNEL_KINDS = ("router", "select", "group", "up", "down", "combine", "gather", "fused", "experts",
                 "experts_mxfp4")
 
@@ -85,6 +86,7 @@ def load_library(path: str = LIB_PATH):
         "moe_abi_version": ([], I32),
         "moe_route_noalloc": ([VP, VP, VP, I32, I32, I32, I32, I32, I32, ctypes.c_float, I32, VP, VP, VP, VP],
                               ctypes.c_int),
+        "moe_get_intermediate": ([VP, I32, VP, ctypes.c_size_t, P(ctypes.c_size_t), VP], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -195,6 +197,17 @@ class MoELayer:
         c = torch.empty((self.config.n_expert,), dtype=torch.int32, device=self.device)
         _check(_lib.moe_get_expert_counts(self._h, c.data_ptr(), _stream_handle(stream)))
         return c
+
+    def intermediate(self, which: int, stream=None) -> torch.Tensor:
+        """A grouped-path intermediate of the last forward as a flat uint8
+        device tensor (see moe_get_intermediate in include/moe.h)."""
+        n = ctypes.c_size_t()
+        _check(_lib.moe_get_intermediate(self._h, int(which), None, 0, ctypes.byref(n), _stream_handle(stream)))
+        buf = torch.empty((n.value,), dtype=torch.uint8, device=self.device)
+        if n.value:
+            _check(_lib.moe_get_intermediate(self._h, int(which), buf.data_ptr(), n.value, None,
+                                             _stream_handle(stream)))
+        return buf
 
     def set_path(self, path: int) -> None:
         _check(_lib.moe_set_path(self._h, int(path)))

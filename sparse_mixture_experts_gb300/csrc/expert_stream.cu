@@ -30,7 +30,7 @@ struct StreamArgs {
     const void *sh_gate_w, *sh_up_w, *sh_down_w;
     const float *topk_w, *sh_gate;
     void *h;
-    void *ys;          // weight dtype
+    float *ys;         // [T][K+1][H] fp32
     float alpha, limit;
 };
 
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(256) expert_down_stream_kernel(StreamArgs a)
                         t = p / a.K; slot = p - t * a.K; wgt = a.topk_w[p];
                     }
                     const float y = mine + (bd ? bd[row] : 0.0f);
-                    store_out((TW *)a.ys + ((size_t)t * S + slot) * a.H + row, wgt * y);
+                    a.ys[((size_t)t * S + slot) * a.H + row] = wgt * y;
                 }
             }
         }
@@ -255,17 +255,12 @@ int launch_experts_stream(const Layer &L, const void *x, int T, int which, cudaS
 
 // ---------------------------------------------------------------------------
 // combine: out[t][i] = sum_{slot < K} ys[t][slot][i] (+ ys[t][K][i]); ys holds the
-// weighted per-slot outputs in the weight dtype (bf16 for bf16 layers)
+// weighted per-slot outputs in fp32
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float4 load4_stream(const float *p) { return __ldcs(reinterpret_cast<const float4 *>(p)); }
-__device__ __forceinline__ float4 load4_stream(const __nv_bfloat16 *p)
-{
-    const uint2 u = __ldcs(reinterpret_cast<const uint2 *>(p));
-    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-}
 
-template <typename TY, typename TO>
-__global__ void __launch_bounds__(256) combine_kernel(const TY *__restrict__ ys, int T, int K, int H, int has_shared,
+template <typename TO>
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ ys, int T, int K, int H, int has_shared,
                                                       TO *__restrict__ out)
 {
     const int S = K + 1;
@@ -274,7 +269,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const TY *__restrict__ ys,
     for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4; q += (size_t)gridDim.x * blockDim.x) {
         const size_t e = q * 4;
         const size_t t = e / H, i = e - t * H;
-        const TY *p = ys + t * S * H + i;
+        const float *p = ys + t * S * H + i;
         float4 acc = load4_stream(p);
         for (int sl = 1; sl < nslots; ++sl) {
             const float4 v = load4_stream(p + (size_t)sl * H);
@@ -294,12 +289,9 @@ int launch_combine(const Layer &L, int T, void *out, cudaStream_t s)
     size_t want = (n4 + 255) / 256, cap = (size_t)L.num_sms * 8;
     int blocks = (int)(want < cap ? want : cap);
     blocks = max(blocks, 1);
-    const bool ybf = L.cfg.w_dtype == MOE_DT_BF16, obf = L.cfg.out_dtype == MOE_DT_BF16;
     const int hs = L.Fs > 0;
-    if (ybf && obf) combine_kernel<<<blocks, 256, 0, s>>>((const __nv_bfloat16 *)L.ys, T, L.K, L.H, hs, (__nv_bfloat16 *)out);
-    else if (ybf) combine_kernel<<<blocks, 256, 0, s>>>((const __nv_bfloat16 *)L.ys, T, L.K, L.H, hs, (float *)out);
-    else if (obf) combine_kernel<<<blocks, 256, 0, s>>>((const float *)L.ys, T, L.K, L.H, hs, (__nv_bfloat16 *)out);
-    else combine_kernel<<<blocks, 256, 0, s>>>((const float *)L.ys, T, L.K, L.H, hs, (float *)out);
+    if (L.cfg.out_dtype == MOE_DT_BF16) combine_kernel<<<blocks, 256, 0, s>>>(L.ys, T, L.K, L.H, hs, (__nv_bfloat16 *)out);
+    else combine_kernel<<<blocks, 256, 0, s>>>(L.ys, T, L.K, L.H, hs, (float *)out);
     return 1;
 }
 

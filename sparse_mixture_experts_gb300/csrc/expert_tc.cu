@@ -82,7 +82,7 @@ struct TcArgs {
     const float *gate_b, *up_b, *down_b;
     const float *topk_w, *sh_gate;
     __nv_bfloat16 *h;   // EPI_UP output
-    __nv_bfloat16 *ys;  // EPI_DOWN output (bf16 weighted per-slot outputs)
+    float *ys;          // EPI_DOWN output: weighted per-slot outputs [T][K+1][H], fp32
     float *logits;      // EPI_ROUTER output [T][R]
     const float *router_b;
     int R, router_nt;   // router rows, router N tiles
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     }
                 }
                 const float *bd = (!ti.shared && a.down_b) ? a.down_b + (size_t)ti.g * a.H + ti.n0 : nullptr;
-                __nv_bfloat16 *yrow = a.ys + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n0;
+                float *yrow = a.ys + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n0;
                 const int ncols = min(BN, a.H - ti.n0);
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 16) {
@@ -404,16 +404,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                             if (bd && c + i < ncols) y += bd[c + i];
                             o[i] = wgt * y;
                         }
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            __nv_bfloat162 p2 = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
-                            pk[i] = *reinterpret_cast<uint32_t *>(&p2);
-                        }
                         // H is a multiple of 64, so a 16-column chunk is either fully in or fully out
-                        uint4 *dst = reinterpret_cast<uint4 *>(yrow + c);
-                        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        float4 *dst = reinterpret_cast<float4 *>(yrow + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                     }
                 }
             }
@@ -523,7 +517,7 @@ static TcArgs make_tc_args(const Layer &L, int T)
     a.gate_b = L.gate_b; a.up_b = L.up_b; a.down_b = L.down_b;
     a.topk_w = L.topk_w; a.sh_gate = L.sh_gate;
     a.h = (__nv_bfloat16 *)L.h;
-    a.ys = (__nv_bfloat16 *)L.ys;
+    a.ys = L.ys;
     a.status = L.status;
     a.T = T; a.K = L.K; a.E = L.E; a.H = L.H; a.F = L.F; a.Fs = L.Fs; a.Fmax = L.Fmax; a.Tmax = L.Tmax;
     a.act = L.cfg.act;

@@ -325,7 +325,7 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     if ((st = dev_alloc_t(L, &L.active, E))) return st;
     if ((st = dev_alloc_t(L, &L.meta, 1))) return st;
     if ((st = dev_alloc(L, &L.h, (T * K + T) * (size_t)L.Fmax * eb))) return st;
-    if ((st = dev_alloc(L, &L.ys, T * (K + 1) * H * eb))) return st;
+    if ((st = dev_alloc_t(L, &L.ys, T * (K + 1) * H))) return st;
     if ((st = dev_alloc_t(L, &L.status, 1))) return st;
     if ((st = dev_alloc_t(L, &L.gbar, 2))) return st;
     if ((st = dev_alloc(L, &L.x_stage, T * H * eb))) return st;
@@ -426,6 +426,7 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
         if (bad || e != cudaSuccess) return cuda_fail(e != cudaSuccess ? e : cudaErrorLaunchFailure, "decode launch");
         L.last_T = T;
         L.last_launches = n;
+        L.last_grouped = 0;
         return MOE_OK;
     }
     if (route == Route::Fused) {
@@ -440,6 +441,7 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
         if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
         L.last_T = T;
         L.last_launches = n;
+        L.last_grouped = 0;
         return MOE_OK;
     }
     int router_bad = 0;
@@ -466,6 +468,7 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     L.last_T = T;
     L.last_launches = n;
+    L.last_grouped = 1;
     return MOE_OK;
 }
 
@@ -553,6 +556,31 @@ moe_status moe_get_expert_counts(moe_layer *layer, int32_t *counts, void *stream
     if (!layer || !counts) return fail(MOE_ERR_INVALID_ARG, "layer and counts must be non-NULL");
     const Layer &L = *layer;
     CUDA_TRY(cudaMemcpyAsync(counts, L.counts, L.E * sizeof(int32_t), cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_get_intermediate(moe_layer *layer, int32_t which, void *dst, size_t capacity, size_t *size,
+                                void *stream)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    const Layer &L = *layer;
+    const size_t T = (size_t)L.last_T, K = (size_t)L.K;
+    const size_t rows = T * K + (L.Fs > 0 ? T : 0);
+    const void *src = nullptr;
+    size_t bytes = 0;
+    switch (which) {
+    case MOE_INTER_OFFSETS: src = L.offsets; bytes = T ? ((size_t)L.E + 1) * sizeof(int32_t) : 0; break;
+    case MOE_INTER_PERM: src = L.expert_rows; bytes = T * K * sizeof(int32_t); break;
+    case MOE_INTER_H: src = L.h; bytes = rows * (size_t)L.Fmax * L.wbytes; break;
+    case MOE_INTER_YS: src = L.ys; bytes = T * (K + 1) * (size_t)L.H * sizeof(float); break;
+    default: return fail(MOE_ERR_INVALID_ARG, "unknown intermediate");
+    }
+    if (size) *size = bytes;
+    if (bytes == 0 || !dst) return MOE_OK;
+    if (!L.last_grouped)
+        return fail(MOE_ERR_UNSUPPORTED, "the last forward ran a decode path, which keeps no grouped intermediates");
+    if (capacity < bytes) return fail(MOE_ERR_INVALID_ARG, "destination too small");
+    CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
     return MOE_OK;
 }
 

@@ -81,7 +81,7 @@ struct Layer {
     RouteMeta *meta = nullptr;
     void *h = nullptr;         // [Tmax*K + Tmax][Fmax] activations (routed rows sorted by expert, then shared)
     void *xp = nullptr;        // [Tmax*K + Tmax][H] x rows gathered in expert order, then x (tensor-core path)
-    void *ys = nullptr;        // [Tmax][K+1][H] weighted expert outputs per (token, slot), weight dtype
+    float *ys = nullptr;       // [Tmax][K+1][H] weighted expert outputs per (token, slot), fp32
     bool mxfp4 = false;        // routed experts given in MXFP4 (gate_w/up_w/down_w hold their bf16 values)
     int *gfirst = nullptr;     // [5][E + 2] per group: first gate/up tile (and the total), first down tile
                                // (and the total), expert (E = shared), rows, first row in the sorted buffers
@@ -116,6 +116,7 @@ struct Layer {
     size_t device_bytes = 0;
     int last_T = 0;
     int last_launches = 0;
+    int last_grouped = 0;       // 1: the last forward ran a grouped path (tensor-core or CUDA-core stream)
 };
 
 // ---------------------------------------------------------------------------

@@ -353,3 +353,84 @@ def test_mxfp4_small_layer_all_paths_agree(T):
     for path in PATHS:
         rep = _small_case(MXFP4_SMALL, T, path, seed=9)
         assert rep.ok(MXFP4_SMALL.dtype), (path, str(rep))
+
+
+def _bf16_bits_to_f32(a):
+    return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+INTER_CASES = [
+    # name, tokens, path, routed rows sampled, shared rows sampled
+    ("tiny", 16, moe.PATH_STREAM, 32, 0),
+    ("qwen_prefill_zipf", 4096, moe.PATH_TC, 48, 8),
+    ("qwen_prefill_zipf", 300, moe.PATH_STREAM, 32, 8),
+    ("gptoss", 64, moe.PATH_TC, 24, 0),
+    ("mixtral", 256, moe.PATH_TC, 12, 0),
+    ("gptoss_mxfp4", 64, moe.PATH_TC, 16, 0),
+]
+
+
+@pytest.mark.parametrize("name,T,path,n_routed,n_shared", INTER_CASES,
+                         ids=[f"{c[0]}-T{c[1]}-{'tc' if c[2] == moe.PATH_TC else 'stream'}" for c in INTER_CASES])
+def test_intermediates_match_oracle(name, T, path, n_routed, n_shared):
+    """Each grouped-path intermediate against the oracle: the expert offsets
+    and the pair permutation bit-exact with a stable sort of the selection by
+    expert; the activations h of sampled routed rows (and shared-expert rows)
+    against the oracle's expert evaluation at the parity tolerance; and, where
+    the path keeps them, the weighted per-slot outputs."""
+    wl = workload(name)
+    spec = wl.spec
+    wl.layer.set_path(path)
+    x = wl.x[:T]
+    wl.layer.forward(wl.x_dev[:T])
+    idx, wt = wl.layer.routing(T)
+    torch.cuda.synchronize()
+    wl.layer.status()
+    idx, wt = idx.cpu().numpy(), wt.cpu().numpy()
+    E, K, H, F, Fs = spec.n_expert, spec.top_k, spec.hidden, spec.expert_ff, spec.shared_ff
+    Fmax = max(F, Fs)
+    mism, ties, invalid, logits = helpers.index_parity_all(wl.orc, x, idx)
+    assert not mism and not invalid
+    # the grouping of the selection (the oracle's, which equals the GPU's off near ties)
+    sel = idx if ties else np.stack([wl.orc.select(logits[t])[0] for t in range(T)])
+    offsets = wl.layer.intermediate(moe.INTER_OFFSETS).cpu().numpy().view(np.int32)
+    perm = wl.layer.intermediate(moe.INTER_PERM).cpu().numpy().view(np.int32)
+    counts = np.bincount(sel.reshape(-1), minlength=E)
+    np.testing.assert_array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+    np.testing.assert_array_equal(perm, np.argsort(sel.reshape(-1), kind="stable"))
+
+    raw = wl.layer.intermediate(moe.INTER_H).cpu().numpy()
+    rows = T * K + (T if Fs else 0)
+    h = (_bf16_bits_to_f32(raw.view(np.uint16)) if spec.dtype == "bf16" else raw.view(np.float32)).reshape(rows, Fmax)
+    xf = synth.as_f32(np.ascontiguousarray(x), spec.dtype).astype(np.float64)
+    pick = helpers.sample_rows(T * K, n_routed, seed=7)
+    got, ref, yref, ykey = [], [], [], []
+    for j in pick:
+        p = int(perm[j])
+        t, slot = divmod(p, K)
+        hr, yr = wl.orc.expert(int(idx[t, slot]), xf[t])
+        got.append(h[j, :F])
+        ref.append(hr)
+        w_ref = wl.orc.weights_for_selection(logits[t], idx[t])
+        yref.append(w_ref[slot] * yr)
+        ykey.append((t, slot))
+    for t in (helpers.sample_rows(T, n_shared, seed=8) if Fs else []):
+        hr, yr, g = wl.orc.shared(xf[t])
+        got.append(h[T * K + t, :Fs])
+        ref.append(hr)
+        yref.append(g * yr)
+        ykey.append((int(t), K))
+    got, ref = np.concatenate(got).astype(np.float64), np.concatenate(ref)
+    tol = helpers.REL_L2[spec.dtype]
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= tol, f"h rel-L2 {rel:.3e}"
+    assert np.abs(got - ref).max() <= helpers.MAX_ABS_FRAC * np.abs(ref).max()
+
+    if path == moe.PATH_STREAM:
+        ys = wl.layer.intermediate(moe.INTER_YS).cpu().numpy().view(np.float32).reshape(T, K + 1, H)
+        gy = np.concatenate([ys[t, s] for t, s in ykey]).astype(np.float64)
+        ry = np.concatenate(yref)
+        rel = np.linalg.norm(gy - ry) / np.linalg.norm(ry)
+        assert rel <= tol, f"Ys rel-L2 {rel:.3e}"
+        assert np.abs(gy - ry).max() <= helpers.MAX_ABS_FRAC * np.abs(ry).max()
+    wl.layer.set_path(moe.PATH_AUTO)
