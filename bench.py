@@ -379,8 +379,8 @@ class Model:
             return self.router + T * H * eb + T * (s.n_expert + (1 if Fs else 0)) * 4, 2.0 * T * H * s.n_expert
         if kind == "combine":
             return T * (K + 1) * H * 4 + T * H * 4, 0.0
-        if kind == "gather":
-            return rows * H * eb + T * H * eb, 0.0
+        if kind == "gather":  # the routed rows (the shared expert reads x itself)
+            return T * K * H * eb + T * H * eb, 0.0
         return None, None
 
 
@@ -683,7 +683,7 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
             "e2e": e2e,
             "gpu_launches": head["gpu_launches_per_step"] * args.steps,
             "clocks": head["clocks"],
-            "other_token_counts": {k: {"tokens_per_s": v["tokens_per_s"], "ms_per_step": v["ms_per_step"],
+            "other_token_counts": {k: {"tokens_per_s": v["tokens_per_s"], "ms_per_step": v["ms_per_step"], "kernels": v["kernels"],
                                        "distinct_experts": v["distinct_experts"],
                                        "hbm_frac": v["step_roofline"]["hbm_frac"],
                                        "roofline": v["roofline"]} for k, v in extra.items()},

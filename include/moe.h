@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 typedef enum {
     MOE_OK = 0,
@@ -261,8 +261,30 @@ typedef enum {
 moe_status moe_timing_read(moe_layer *layer, float *total_ms, int32_t *launches);
 
 /* Synchronises the device and reports a device-side error recorded by the
- * layer's kernels (MOE_ERR_DEVICE_TIMEOUT), then clears it.  MOE_OK if none. */
+ * layer's kernels (MOE_ERR_DEVICE_TIMEOUT), then clears it and resets the
+ * layer's inter-block counters so that the next forward starts clean (the
+ * output of the forward that failed is not valid).  MOE_OK if none. */
 moe_status moe_get_status(moe_layer *layer);
+
+/* Bound, in nanoseconds, of every wait of the layer's kernels on work of
+ * another thread block (a grid barrier, another block's activations, the
+ * injected wait below); ns <= 0 restores the default of one second, values
+ * under 1000 become 1000.  A wait that runs out records
+ * MOE_ERR_DEVICE_TIMEOUT for moe_get_status, and the kernel stops issuing
+ * work, waits for its own copies and tensor-core operations in flight and
+ * returns.  Waits inside one block's pipeline keep the one-second bound.
+ * Takes effect at the next forward.  Errors: INVALID_ARG (ns above 10 s). */
+moe_status moe_set_wait_limit(moe_layer *layer, int64_t ns);
+
+/* Test-only fault injection ("Qwen3.5-MoE Model Implementation", Gotchas and
+ * Fragile Spots: failures must not be silent).  While on, every forward makes
+ * its kernels wait for a condition that nothing satisfies -- a grid barrier
+ * one arrival short (fused decode path), a group's activations one tile short
+ * (weight-streaming decode path), a device word that stays zero (tensor-core
+ * GEMMs) -- so that the wait runs out after the wait limit, the output is not
+ * valid and moe_get_status reports MOE_ERR_DEVICE_TIMEOUT.  No GPU fault is
+ * involved.  Off by default. */
+moe_status moe_set_fault_injection(moe_layer *layer, int32_t on);
 
 /* Number of kernel launches the last forward issued. */
 int32_t moe_last_launch_count(const moe_layer *layer);

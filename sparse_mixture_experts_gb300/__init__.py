@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH):
         "moe_route_noalloc": ([VP, VP, VP, I32, I32, I32, I32, I32, I32, ctypes.c_float, I32, VP, VP, VP, VP],
                               ctypes.c_int),
         "moe_get_intermediate": ([VP, I32, VP, ctypes.c_size_t, P(ctypes.c_size_t), VP], ctypes.c_int),
+        "moe_set_wait_limit": ([VP, ctypes.c_int64], ctypes.c_int),
+        "moe_set_fault_injection": ([VP, I32], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -208,6 +210,15 @@ class MoELayer:
             _check(_lib.moe_get_intermediate(self._h, int(which), buf.data_ptr(), n.value, None,
                                              _stream_handle(stream)))
         return buf
+
+    def set_wait_limit(self, ns: int) -> None:
+        """Bound of the kernels' waits on other thread blocks (0 = default 1 s)."""
+        _check(_lib.moe_set_wait_limit(self._h, int(ns)))
+
+    def set_fault_injection(self, on: bool) -> None:
+        """Test only: the next forwards wait for what never happens and report
+        MOE_ERR_DEVICE_TIMEOUT through status()."""
+        _check(_lib.moe_set_fault_injection(self._h, int(bool(on))))
 
     def set_path(self, path: int) -> None:
         _check(_lib.moe_set_path(self._h, int(path)))

@@ -22,7 +22,8 @@
 //   summed in slot order (deterministic), written straight to `out`.
 //
 // Each weight row is read once per forward with 16-byte loads; the grid
-// barriers spin with a one-second bound and record an error on timeout.
+// barriers spin with a bound (a second by default) and, on timeout, record an
+// error and end the kernel.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -33,7 +34,6 @@ constexpr int DEC_TMAX = 8;       // tokens
 constexpr int DEC_PAIRS = 256;    // max tokens * top_k
 constexpr int DEC_FR = 16;        // ff rows per phase-B item
 constexpr int DEC_RC_MAX = 16;    // output rows per phase-C item
-constexpr unsigned long long DEC_WAIT_NS = 1000000000ull;
 
 struct DecodeArgs {
     const void *x;
@@ -54,6 +54,8 @@ struct DecodeArgs {
     void *h;
     unsigned *gbar;  // [0] arrivals, [1] generation
     int *status;
+    unsigned long long wait_ns;  // bound of a grid-barrier wait
+    int inject;                  // test-only: barriers that never complete
     int rc;           // output rows per phase-C item
     int prefetch;     // prefetch phase-C rows into L2 during phase B
 };
@@ -65,16 +67,22 @@ __device__ __forceinline__ unsigned long long dec_timer()
     return t;
 }
 
-// Grid-wide barrier for a cooperative launch; bounded spin.
-__device__ __forceinline__ void grid_barrier(unsigned *gbar, int *status)
+// Grid-wide barrier for a cooperative launch; the spin is bounded by wait_ns.
+// Returns false (in every thread of the block) when the wait ran out: the
+// error is recorded and the caller returns, since other blocks' results are
+// not all there.  `extra` (test-only fault injection) raises the arrival
+// count the last block must see, so that no block ever completes the barrier.
+__device__ __forceinline__ bool grid_barrier(unsigned *gbar, int *status, unsigned long long wait_ns, int extra)
 {
+    __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
+        int ok = 1;
         volatile unsigned *gen = gbar + 1;
         const unsigned g = *gen;
         __threadfence();
         const unsigned arrived = atomicAdd(gbar, 1u);
-        if (arrived == gridDim.x - 1) {
+        if (arrived == gridDim.x - 1 + (unsigned)extra) {
             gbar[0] = 0;
             __threadfence();
             atomicExch(gbar + 1, g + 1);
@@ -82,15 +90,18 @@ __device__ __forceinline__ void grid_barrier(unsigned *gbar, int *status)
             const unsigned long long t0 = dec_timer();
             unsigned it = 0;
             while (*gen == g) {
-                if ((++it & 63) == 0 && dec_timer() - t0 > DEC_WAIT_NS) {
+                if ((++it & 63) == 0 && dec_timer() - t0 > wait_ns) {
                     record_error(status, DEV_TIMEOUT_GRID_BARRIER);
+                    ok = 0;
                     break;
                 }
             }
         }
         __threadfence();
+        s_ok = ok;
     }
     __syncthreads();
+    return s_ok != 0;
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
@@ -234,7 +245,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) moe_decode_kernel(const Decode
             }
         }
     }
-    grid_barrier(a.gbar, a.status);
+    if (!grid_barrier(a.gbar, a.status, a.wait_ns, a.inject)) return;
 
     // ------------------------------ phase B ------------------------------
     for (int t = warp; t < T; t += DEC_WARPS) {
@@ -373,7 +384,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2) moe_decode_kernel(const Decode
             }
         }
     }
-    grid_barrier(a.gbar, a.status);
+    if (!grid_barrier(a.gbar, a.status, a.wait_ns, a.inject)) return;
 
     // ------------------------------ phase C ------------------------------
     {
@@ -488,6 +499,8 @@ int launch_decode(const Layer &L, const void *x, int T, void *out, cudaStream_t 
     a.logits = L.logits; a.topk_idx = L.topk_idx; a.topk_w = L.topk_w; a.sh_gate = L.sh_gate; a.counts = L.counts;
     a.h = L.h;
     a.gbar = L.gbar;
+    a.wait_ns = L.wait_ns;
+    a.inject = L.inject;
     a.status = L.status;
     const int G = L.decode_grid;
     int rc = (L.H + G - 1) / G;

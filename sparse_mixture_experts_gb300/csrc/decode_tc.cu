@@ -144,6 +144,8 @@ struct DecArgs {
     int act, out_bf16;
     float alpha, limit;
     int max_units;
+    unsigned long long wait_ns;  // bound of a wait on another CTA's activations
+    int inject;                  // test-only: dependency waits that never complete
 };
 
 // ---------------------------------------------------------------------------
@@ -351,30 +353,6 @@ __device__ __forceinline__ int dn_group(const Sched &s, int kb, int &local)
     }
     local = kb - s.kb_routed;
     return s.n_act;
-}
-
-__device__ __forceinline__ int ld_acquire(const int *p)
-{
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
-
-// counter increment that releases this thread's earlier writes (and, through
-// the preceding named barrier, its group's) to the GPU; no value comes back
-__device__ __forceinline__ void red_release_add(int *p, int v)
-{
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// ticket: releases the group's partial sums and acquires the other arrivals'
-__device__ __forceinline__ int atom_acq_rel_add(int *p, int v)
-{
-    int old;
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
 }
 
 // v[t] += the S split partials of row r, in split order; U splits' loads are
@@ -699,7 +677,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         // h'[gi] is complete once every gate/up tile of the group is
                         // (only waited for by a producer with a stage in the segment:
                         // its stages are those of stream index gs .. gs + ns - 1)
-                        const int need = fd / 64;
+                        const int need = fd / 64 + a.inject;  // (never reached under fault injection)
                         int *done = group_done + gi * DT_DONE_STRIDE;
                         const int ns = (pos % Sh::KPS + n + Sh::KPS - 1) / Sh::KPS;
                         if ((ns >= NP || (int)(((uint32_t)pw + NP - gs % NP) % NP) < ns) && ld_acquire(done) < need) {
@@ -708,8 +686,8 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                             const unsigned long long t0 = globaltimer();
                             while (ld_acquire(done) < need) {
                                 __nanosleep(128);
-                                if (*abort_flag || globaltimer() - t0 > WAIT_LIMIT_NS) {
-                                    record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                                if (*abort_flag || globaltimer() - t0 > a.wait_ns) {
+                                    record_error(a.status, DEV_TIMEOUT_DEPENDENCY);
                                     *abort_flag = 1;
                                     ok = false;
                                     break;
@@ -803,8 +781,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
             uint32_t gs = 0;         // index of the next stage in the stream
             int qi = 0;
             uint32_t qph = 0;
-            int last_acc = -1;
-            uint32_t last_acc_phase = 0;
+            bool issued = false;  // any MMA of this thread
             for (;;) {
                 if (!mbar_wait(&uq_full[qi], qph, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_ACCUM_FREE);
@@ -854,17 +831,16 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         }
                         mma_commit(&empty[stage]);  // the raw stage (and MXFP4: the A tile) is free
                         first = false;
+                        issued = true;
                     }
                     if (++stage == RS) stage = 0, phase ^= 1;
                     if (FP4 && ++ast == DT_FP4_AS) ast = 0, aph ^= 1;
                 }
                 if (!ok) break;
                 mma_commit(&acc_full[qi]);  // MXFP4: also when this thread had no stage of the unit
-                last_acc = qi;
-                last_acc_phase = qph;
                 if (++qi == DT_ACC) qi = 0, qph ^= 1;
             }
-            if (*abort_flag && last_acc >= 0) {
+            if (issued) {
                 // no MMA of this thread may still write tensor memory at teardown
                 volatile int never = 0;
                 mma_commit(&drain[mw]);
@@ -1229,6 +1205,8 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     a.out_bf16 = L.cfg.out_dtype == MOE_DT_BF16;
     a.alpha = L.cfg.act_alpha; a.limit = L.cfg.act_limit;
     a.max_units = L.num_sms * DT_UNITS_PER_CTA;
+    a.wait_ns = L.wait_ns;
+    a.inject = L.inject;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.num_sms);
     cfg.blockDim = dim3(L.fp4_decode ? DtShape<true>::THREADS : DtShape<false>::THREADS);

@@ -46,7 +46,10 @@ struct TcShape {
     static constexpr int STAGE = A_TILE_BYTES + B_BYTES;
     static constexpr int STAGES = BN == 256 ? 4 : 6;
     static constexpr int TMEM_COLS = 2 * BN;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+    // after the ring: barriers, then the epilogue's staging (4 warps x 32 rows x 16 fp32)
+    static constexpr int STAGING_OFF = STAGES * STAGE + 256;
+    static constexpr int STAGING_BYTES = 4 * 32 * 16 * 4;
+    static constexpr size_t SMEM = (size_t)STAGING_OFF + STAGING_BYTES + 1024 /*align*/;
 };
 
 struct TensorMaps {
@@ -67,6 +70,7 @@ struct TensorMaps {
 // router GEMM one of 128 rows.
 struct TcMaps {
     CUtensorMap a, b0, b1, sb0, sb1;
+    CUtensorMap sa;  // A of the shared expert's gate/up tiles: x itself (its rows are all tokens in order)
 };
 
 // ---------------------------------------------------------------------------
@@ -83,10 +87,13 @@ struct TcArgs {
     const float *topk_w, *sh_gate;
     __nv_bfloat16 *h;   // EPI_UP output
     float *ys;          // EPI_DOWN output: weighted per-slot outputs [T][K+1][H], fp32
-    float *logits;      // EPI_ROUTER output [T][R]
+    float *logits;      // EPI_ROUTER output [T][R] (router_S == 1)
+    float *rparts;      // EPI_ROUTER output [router_S][T][R] partial sums over K ranges (router_S > 1)
     const float *router_b;
-    int R, router_nt;   // router rows, router N tiles
+    int R, router_nt, router_S, router_bn;  // router rows, router N tiles, K splits, tile width
     int *status;
+    const volatile int *stall;   // test-only fault injection: a word nothing sets, waited for (else null)
+    unsigned long long wait_ns;  // bound of that wait
     int T, K, E, H, F, Fs, Fmax, Tmax;
     int act;
     float alpha, limit;
@@ -96,7 +103,8 @@ struct TileInfo {
     int g, m0, n0;
     int rows;     // rows of the group
     int a_row0;   // first row of the group in the A tensor
-    int nk;       // K blocks
+    int kb0, nk;  // first K block, K blocks
+    int split;    // router: K range of the tile
     bool shared;
 };
 
@@ -116,16 +124,24 @@ template <int EPI>
 __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, const GroupTab &gt, int &gcur)
 {
     if (EPI == EPI_ROUTER) {
-        // dense: every 128-token tile against every 128-row tile of the router
+        // dense: every 128-token tile against every 128-row tile of the router,
+        // K split in router_S ranges (so that the small GEMM covers the GPU)
+        const int per = a.router_nt * a.router_S;
+        const int rem = t % per;
         ti.g = 0;
-        ti.m0 = (t / a.router_nt) * TC_BM;
-        ti.n0 = (t % a.router_nt) * 128;
+        ti.m0 = (t / per) * TC_BM;
+        ti.n0 = (rem / a.router_S) * a.router_bn;
+        ti.split = rem % a.router_S;
         ti.shared = false;
         ti.rows = a.T;
         ti.a_row0 = 0;
-        ti.nk = a.H / TC_BK;
-        return true;
+        const int nkb = a.H / TC_BK;
+        ti.kb0 = nkb * ti.split / a.router_S;
+        ti.nk = nkb * (ti.split + 1) / a.router_S - ti.kb0;
+        return ti.nk > 0;
     }
+    ti.kb0 = 0;
+    ti.split = 0;
     // the group of tile t: the last one whose first tile is <= t; within a
     // group the tiles run (n, m) with m fastest
     if (gt.n <= 0 || t < 0 || t >= gt.first[gt.n]) return false;
@@ -163,11 +179,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     uint64_t *empty = full + TC_STAGES;
     uint64_t *acc_full = empty + TC_STAGES;   // [2]
     uint64_t *acc_empty = acc_full + 2;       // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *drain = acc_empty + 2;          // the MMA thread's own completion, after an abort
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = EPI == EPI_ROUTER ? ((a.T + TC_BM - 1) / TC_BM) * a.router_nt
+    const int n_tiles = EPI == EPI_ROUTER ? ((a.T + TC_BM - 1) / TC_BM) * a.router_nt * a.router_S
                                           : (EPI == EPI_UP ? a.meta->n_up_tiles : a.meta->n_down_tiles);
 
     if (threadIdx.x == 0) {
@@ -179,6 +196,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 128);
         }
+        mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -212,6 +230,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             tmap_prefetch(&maps.a);
+            if (EPI == EPI_UP) tmap_prefetch(&maps.sa);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t used = 0, last_phase = 0;  // per stage: loads issued, parity of the last
@@ -233,8 +252,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     uint8_t *sa = smem + stage * STAGE_BYTES;
                     uint8_t *sb = sa + A_TILE_BYTES;
                     mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-                    const int kc = kb * TC_BK;
-                    tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
+                    const int kc = (ti.kb0 + kb) * TC_BK;
+                    if (EPI == EPI_UP && ti.shared) tma_load_2d(sa, &maps.sa, &full[stage], kc, ti.m0);
+                    else tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
                     if (EPI == EPI_UP) {
                         const int brow = ti.shared ? ti.n0 : ti.g * a.F + ti.n0;
                         tma_load_2d(sb, ti.shared ? &maps.sb0 : &maps.b0, &full[stage], kc, brow);
@@ -261,8 +281,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            int last_acc = -1;
-            uint32_t last_acc_phase = 0;
+            bool issued = false;  // any MMA of this thread
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
                 TileInfo ti;
                 if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
@@ -292,17 +311,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                                  (kb | k) != 0);
                     }
                     mma_commit(&empty[stage]);
+                    issued = true;
                     if (++stage == TC_STAGES) stage = 0, phase ^= 1;
                 }
                 if (!ok) break;
                 mma_commit(&acc_full[b]);
-                last_acc = b;
-                last_acc_phase = acc_phase;
             }
-            // on abort, let the MMAs already issued finish before TMEM is freed
-            if (*abort_flag && last_acc >= 0) {
+            // every MMA this thread issued completes before the shared memory it
+            // reads and the tensor memory it writes are released: after an abort
+            // the epilogue may not wait for the accumulators (and a tile's last
+            // MMAs may not be committed to one)
+            if (issued) {
                 volatile int never = 0;
-                mbar_wait(&acc_full[last_acc], last_acc_phase, &never);
+                mma_commit(drain);
+                mbar_wait(drain, 0, &never);
             }
         }
     } else {
@@ -311,7 +333,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         const int r = q * 32 + lane;        // accumulator row (tile row) of this thread
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         int it = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+        bool run = true;
+        if (a.stall) {
+            // test-only fault injection: every epilogue thread waits (bounded) for
+            // a word that nothing sets; when the wait runs out the CTA aborts
+            // with the MMA and the copies in flight, which then drain
+            const unsigned long long t0 = globaltimer();
+            while (*a.stall == 0) {
+                __nanosleep(256);
+                if (*abort_flag || globaltimer() - t0 > a.wait_ns) break;
+            }
+            if (*a.stall == 0) {
+                record_error(a.status, DEV_TIMEOUT_INJECTED);
+                *abort_flag = 1;
+                run = false;
+            }
+        }
+        for (int t = blockIdx.x; run && t < n_tiles; t += gridDim.x, ++it) {
             TileInfo ti;
             if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
             const int b = it & 1;
@@ -326,9 +364,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             const int j = ti.m0 + r;              // row within the group
             const bool valid = j < ti.rows;
             if (EPI == EPI_ROUTER) {
-                // logits[t][n] (+ router bias), fp32; R need not be a multiple of 4
+                // logits[t][n] (+ router bias), fp32, or with K split the partial
+                // sum of this K range (the bias in the first); R need not be a
+                // multiple of 4
+                float *dst = a.router_S > 1 ? a.rparts + (size_t)ti.split * a.T * a.R : a.logits;
+                const bool with_bias = a.router_b && ti.split == 0;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 16) {
+                    if (ti.n0 + c >= a.R) break;  // the same for the whole warp
                     uint32_t v[16];
                     tmem_ld16(tbase + c, v);
                     tmem_ld_wait();
@@ -337,8 +380,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         for (int i = 0; i < 16; ++i) {
                             const int n = ti.n0 + c + i;
                             if (n < a.R) {
-                                const float b = (a.router_b && n < a.E) ? a.router_b[n] : 0.0f;
-                                a.logits[(size_t)j * a.R + n] = __uint_as_float(v[i]) + b;
+                                const float b = (with_bias && n < a.E) ? a.router_b[n] : 0.0f;
+                                dst[(size_t)j * a.R + n] = __uint_as_float(v[i]) + b;
                             }
                         }
                     }
@@ -389,26 +432,38 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     }
                 }
                 const float *bd = (!ti.shared && a.down_b) ? a.down_b + (size_t)ti.g * a.H + ti.n0 : nullptr;
-                float *yrow = a.ys + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n0;
-                const int ncols = min(BN, a.H - ti.n0);
+                // this thread's fp32 row of the per-slot buffer (0: a row past the group's end)
+                const unsigned long long yrow =
+                    valid ? reinterpret_cast<unsigned long long>(a.ys + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n0)
+                          : 0ull;
+                const int ncols = min(BN, a.H - ti.n0);  // the same for the whole tile; a multiple of 64 (H is)
+                // Each thread holds one row; the warp's 32 rows x 16 columns go
+                // through shared memory so that each store instruction writes 8
+                // rows x 64 contiguous bytes (whole sectors) instead of 32 rows x
+                // 16 bytes.  Row r's float4 q sits at r * 4 + (q ^ ((r >> 1) & 3)):
+                // no bank conflicts for the row-wise writes or the column-wise reads.
+                float4 *stg = reinterpret_cast<float4 *>(smem + Sh::STAGING_OFF) + q * 128;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
+                for (int c = 0; c < ncols; c += 16) {
                     uint32_t v[16];
                     tmem_ld16(tbase + c, v);
                     tmem_ld_wait();
-                    if (valid && c < ncols) {
-                        float o[16];
+                    float o[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float y = __uint_as_float(v[i]);
-                            if (bd && c + i < ncols) y += bd[c + i];
-                            o[i] = wgt * y;
-                        }
-                        // H is a multiple of 64, so a 16-column chunk is either fully in or fully out
-                        float4 *dst = reinterpret_cast<float4 *>(yrow + c);
+                    for (int i = 0; i < 16; ++i) o[i] = wgt * (__uint_as_float(v[i]) + (bd ? bd[c + i] : 0.0f));
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i)
+                        stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =
+                            make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int f = i * 32 + lane, rr = f >> 2, qq = f & 3;
+                        const float4 val = stg[rr * 4 + (qq ^ ((rr >> 1) & 3))];
+                        const unsigned long long dst = __shfl_sync(0xffffffffu, yrow, rr);
+                        if (dst) reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + c)[qq] = val;
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -519,10 +574,12 @@ static TcArgs make_tc_args(const Layer &L, int T)
     a.h = (__nv_bfloat16 *)L.h;
     a.ys = L.ys;
     a.status = L.status;
+    a.stall = L.inject ? L.never : nullptr;
+    a.wait_ns = L.wait_ns;
     a.T = T; a.K = L.K; a.E = L.E; a.H = L.H; a.F = L.F; a.Fs = L.Fs; a.Fmax = L.Fmax; a.Tmax = L.Tmax;
     a.act = L.cfg.act;
     a.alpha = L.cfg.act_alpha; a.limit = L.cfg.act_limit;
-    a.logits = nullptr; a.router_b = nullptr; a.R = L.R; a.router_nt = 1;
+    a.logits = nullptr; a.rparts = nullptr; a.router_b = nullptr; a.R = L.R; a.router_nt = 1; a.router_S = 1; a.router_bn = 128;
     return a;
 }
 
@@ -532,16 +589,33 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
     TcArgs a = make_tc_args(L, T);
     const int grid = L.num_sms;
     if (which == 1) {
-        TcMaps mu{m.xp, m.gate, m.up, m.sh_gate, m.sh_up};
+        TcMaps mu{m.xp, m.gate, m.up, m.sh_gate, m.sh_up, m.xp};
+        if (L.Fs > 0 && !encode_2d(&mu.sa, x, L.H, (uint64_t)T, TC_BM)) return -1;
         tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_UP>::SMEM, s>>>(mu, a);
     } else {
-        TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down};
+        TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down, m.h};
         tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_DOWN>::SMEM, s>>>(md, a);
     }
     return 1;
 }
 
-// router logits on the tensor cores: logits[T][R] = x Wr^T (+ b); the x
+// K ranges of the router GEMM.  With fewer (token, router-row) tiles than half
+// the SMs (few router rows, or few tokens), K is split so that about one tile
+// runs per SM, each range at least four 64-wide K blocks, at most
+// TC_ROUTER_MAX_SPLITS; the selection kernel then adds the partial sums.
+// (Measured on the qwen35moe-, gpt-oss- and mixtral-shaped layers: splits cut
+// the router from 25-28 to 15-18 us where it had 16-32 tiles, and cost more
+// in the selection kernel than they saved where it had 96 or more.)
+int tc_router_splits(const Layer &L, int T)
+{
+    const int mn = ((T + TC_BM - 1) / TC_BM) * ((L.R + 127) / 128);
+    if (2 * mn >= L.num_sms) return 1;  // enough tiles: the partial sums would cost more than they save
+    const int S = min((L.num_sms + mn - 1) / mn, min(TC_ROUTER_MAX_SPLITS, (L.H / TC_BK) / 4));
+    return max(S, 1);
+}
+
+// router logits on the tensor cores: logits[T][R] = x Wr^T (+ b), or with K
+// split, partial sums that the selection kernel adds in split order; the x
 // tensor map is encoded for this forward's x pointer
 int launch_tc_router(const Layer &L, const void *x, int T, cudaStream_t s)
 {
@@ -554,7 +628,10 @@ int launch_tc_router(const Layer &L, const void *x, int T, cudaStream_t s)
     a.router_b = L.router_b;
     a.R = L.R;
     a.router_nt = (L.R + 127) / 128;
-    const int tiles = ((T + TC_BM - 1) / TC_BM) * a.router_nt;
+    a.router_S = tc_router_splits(L, T);
+    a.router_bn = 128;
+    a.rparts = L.router_parts;
+    const int tiles = ((T + TC_BM - 1) / TC_BM) * a.router_nt * a.router_S;
     const int grid = tiles < L.num_sms ? tiles : L.num_sms;
     tc_gemm_kernel<EPI_ROUTER, 128, TcMaps><<<grid, TC_THREADS, TcShape<128>::SMEM, s>>>(mr, a);
     return 1;

@@ -327,6 +327,8 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     if ((st = dev_alloc(L, &L.h, (T * K + T) * (size_t)L.Fmax * eb))) return st;
     if ((st = dev_alloc_t(L, &L.ys, T * (K + 1) * H))) return st;
     if ((st = dev_alloc_t(L, &L.status, 1))) return st;
+    if ((st = dev_alloc_t(L, &L.never, 1))) return st;
+    CUDA_TRY(cudaMemset(L.never, 0, sizeof(int)));
     if ((st = dev_alloc_t(L, &L.gbar, 2))) return st;
     if ((st = dev_alloc(L, &L.x_stage, T * H * eb))) return st;
     if ((st = dev_alloc(L, &L.out_stage, T * H * (c.out_dtype == MOE_DT_BF16 ? 2 : 4)))) return st;
@@ -342,6 +344,7 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
         // routed rows (T*K, expert-sorted) then the shared expert's rows (T)
         if ((st = dev_alloc(L, &L.xp, (T * K + T) * H * eb))) return st;
         if ((st = dev_alloc_t(L, &L.gfirst, 5 * (E + 2)))) return st;
+        if ((st = dev_alloc_t(L, &L.router_parts, (size_t)TC_ROUTER_MAX_SPLITS * T * L.R))) return st;
         if (tc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "tensor map creation failed");
         if (L.mxfp4) {
             // the MXFP4 decode kernel reads the codes and scales themselves; its f16
@@ -452,11 +455,18 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
         return r < 0 ? 0 : r;
     });
     if (router_bad) return fail(MOE_ERR_CUDA, "tensor map for x could not be encoded");
-    run(MOE_KERNEL_SELECT, [&] { return launch_select(L, T, s); });
+    const int splits = tc ? tc_router_splits(L, T) : 1;
+    run(MOE_KERNEL_SELECT, [&] { return launch_select(L, T, splits, s); });
     run(MOE_KERNEL_GROUP, [&] { return launch_group(L, T, tc, s); });
     run(MOE_KERNEL_GATHER, [&] { return launch_scatter(L, x, T, tc, s); });
     if (tc) {
-        run(MOE_KERNEL_UP, [&] { return launch_experts_tc(L, x, T, 1, s); });
+        int up_bad = 0;
+        run(MOE_KERNEL_UP, [&] {
+            const int r = launch_experts_tc(L, x, T, 1, s);
+            up_bad = r < 0;
+            return r < 0 ? 0 : r;
+        });
+        if (up_bad) return fail(MOE_ERR_CUDA, "tensor map for x could not be encoded");
         run(MOE_KERNEL_DOWN, [&] { return launch_experts_tc(L, x, T, 2, s); });
     } else {
         run(MOE_KERNEL_UP, [&] { return launch_experts_stream(L, x, T, 0, s); });
@@ -649,11 +659,37 @@ moe_status moe_get_status(moe_layer *layer)
     int code = 0;
     CUDA_TRY(cudaMemcpy(&code, layer->status, sizeof(int), cudaMemcpyDeviceToHost));
     if (code != 0) {
+        // a kernel that gave up may have left its inter-block counters mid-count:
+        // start the next forward from zero
+        Layer &L = *layer;
+        CUDA_TRY(cudaMemset(L.gbar, 0, 2 * sizeof(unsigned)));
+        CUDA_TRY(cudaMemset(L.meta, 0, sizeof(RouteMeta)));
+        if (L.dec_tickets) {
+            size_t hp_b, part_b, tab_b, tick_b;
+            dectc_workspace(L, hp_b, part_b, tab_b, tick_b);
+            CUDA_TRY(cudaMemset(L.dec_tickets, 0, tick_b));
+        }
+        CUDA_TRY(cudaDeviceSynchronize());
         CUDA_TRY(cudaMemset(layer->status, 0, sizeof(int)));
         char buf[96];
         snprintf(buf, sizeof buf, "device-side error %d recorded by a kernel", code);
         return fail(code == DEV_BAD_TILE ? MOE_ERR_CUDA : MOE_ERR_DEVICE_TIMEOUT, buf);
     }
+    return MOE_OK;
+}
+
+moe_status moe_set_wait_limit(moe_layer *layer, int64_t ns)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (ns > 10000000000LL) return fail(MOE_ERR_INVALID_ARG, "wait limit above 10 s");
+    layer->wait_ns = ns <= 0 ? 1000000000ull : (unsigned long long)(ns < 1000 ? 1000 : ns);
+    return MOE_OK;
+}
+
+moe_status moe_set_fault_injection(moe_layer *layer, int32_t on)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    layer->inject = on ? 1 : 0;
     return MOE_OK;
 }
 

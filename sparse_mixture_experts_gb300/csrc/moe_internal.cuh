@@ -24,6 +24,8 @@ enum DeviceError : int {
     DEV_TIMEOUT_ACCUM_FREE = 4,     // epilogue->MMA accumulator never released
     DEV_BAD_TILE = 5,               // a tile descriptor outside the problem
     DEV_TIMEOUT_GRID_BARRIER = 6,   // a block of the cooperative decode kernel never arrived
+    DEV_TIMEOUT_DEPENDENCY = 7,     // a group's activations never completed (weight-streaming decode kernel)
+    DEV_TIMEOUT_INJECTED = 8,       // the test-only injected wait ran out (tensor-core GEMMs)
 };
 
 // Groups of rows a grouped kernel walks over: the routed experts that
@@ -68,6 +70,7 @@ struct Layer {
 
     // workspace, sized for Tmax tokens
     float *logits = nullptr;   // [Tmax][R]
+    float *router_parts = nullptr;  // [TC_ROUTER_MAX_SPLITS][Tmax][R] partial logits of the split router GEMM
     int *topk_idx = nullptr;   // [Tmax][K]
     float *topk_w = nullptr;   // [Tmax][K]
     float *sh_gate = nullptr;  // [Tmax]
@@ -86,6 +89,9 @@ struct Layer {
     int *gfirst = nullptr;     // [5][E + 2] per group: first gate/up tile (and the total), first down tile
                                // (and the total), expert (E = shared), rows, first row in the sorted buffers
     int *status = nullptr;     // DeviceError
+    int *never = nullptr;      // a device word that stays 0 (what fault injection waits for)
+    unsigned long long wait_ns = 1000000000ull;  // bound of a wait on another block (moe_set_wait_limit)
+    int inject = 0;            // test-only: the next forwards wait for what never happens
     unsigned *gbar = nullptr;  // [2] grid-barrier arrivals / generation (decode kernel)
     int decode_grid = 0;       // blocks of the cooperative decode kernel (0 = unavailable)
     void *x_stage = nullptr;   // [Tmax][H] for moe_forward_host
@@ -398,7 +404,8 @@ void set_last_error(const char *msg);
 // host-side launchers (each returns the number of kernels it launched, or -1)
 // ---------------------------------------------------------------------------
 int launch_router(const Layer &L, const void *x, int T, cudaStream_t s);
-int launch_select(const Layer &L, int T, cudaStream_t s);
+// with splits > 1, first adds the router's partial logits in split order
+int launch_select(const Layer &L, int T, int splits, cudaStream_t s);
 int launch_group(const Layer &L, int T, bool build_tiles, cudaStream_t s);
 // positions of the picks in expert order; with rows, also gathers x into xp
 int launch_scatter(const Layer &L, const void *x, int T, bool rows, cudaStream_t s);
@@ -431,6 +438,7 @@ void tc_release(Layer &L);
 // which: 1 = gate/up GEMM + activation, 2 = down GEMM + weight (the token rows are gathered by launch_scatter)
 int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStream_t s);
 int launch_tc_router(const Layer &L, const void *x, int T, cudaStream_t s);
+int tc_router_splits(const Layer &L, int T);  // K ranges the tensor-core router uses for T tokens
 
 constexpr int MAX_LAUNCHES_PER_FORWARD = 8;
 
@@ -439,5 +447,6 @@ constexpr int TC_BM = 128;       // token rows per tile
 constexpr int TC_BN_UP = 256;    // gate/up tile: 128 gate + 128 up columns -> 128 h columns
 constexpr int TC_BN_DOWN = 256;  // down tile: output columns
 constexpr int TC_BK = 64;        // K elements per pipeline stage (128 bytes of bf16)
+constexpr int TC_ROUTER_MAX_SPLITS = 4;  // K ranges of the tensor-core router GEMM
 
 }  // namespace moe

@@ -98,7 +98,8 @@ int launch_router(const Layer &L, const void *x, int T, cudaStream_t s)
 // pick, how many earlier tokens of the chunk picked the same expert (its rank
 // within the chunk).  Both come from one SEL_TOK-bit token mask per expert.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(SEL_TOK * 32) select_kernel(const float *__restrict__ logits, int T, int E, int R,
+__global__ void __launch_bounds__(SEL_TOK * 32) select_kernel(float *__restrict__ logits, const float *__restrict__ parts,
+                                                              int splits, int T, int E, int R,
                                                               int K, int mode, int norm, float scale, int has_shared,
                                                               int *__restrict__ topk_idx, float *__restrict__ topk_w,
                                                               float *__restrict__ sh_gate, int hist_pitch,
@@ -110,6 +111,21 @@ __global__ void __launch_bounds__(SEL_TOK * 32) select_kernel(const float *__res
     __syncthreads();
     const int t = blockIdx.x * SEL_TOK + warp;
     int sel_i = -1;
+    if (t < T && splits > 1) {
+        // the router GEMM split K: its partial sums, added in split order, are the logits
+        for (int e = lane; e < R; e += 32) {
+            float p[TC_ROUTER_MAX_SPLITS];
+#pragma unroll
+            for (int sp = 0; sp < TC_ROUTER_MAX_SPLITS; ++sp)
+                p[sp] = sp < splits ? __ldcg(parts + ((size_t)sp * T + t) * R + e) : 0.0f;
+            float v = p[0];
+#pragma unroll
+            for (int sp = 1; sp < TC_ROUTER_MAX_SPLITS; ++sp)
+                if (sp < splits) v += p[sp];
+            logits[(size_t)t * R + e] = v;
+        }
+        __syncwarp();
+    }
     if (t < T) {
         const float *l = logits + (size_t)t * R;
         float sel_v, w;
@@ -127,12 +143,12 @@ __global__ void __launch_bounds__(SEL_TOK * 32) select_kernel(const float *__res
     if (t < T && lane < K) pair_rank[(size_t)t * K + lane] = __popc(s_tm[sel_i] & ((1u << warp) - 1u));
 }
 
-int launch_select(const Layer &L, int T, cudaStream_t s)
+int launch_select(const Layer &L, int T, int splits, cudaStream_t s)
 {
     const moe_config &c = L.cfg;
     select_kernel<<<(T + SEL_TOK - 1) / SEL_TOK, SEL_TOK * 32, 0, s>>>(
-        L.logits, T, L.E, L.R, L.K, c.router_mode, c.norm_topk_prob, c.weights_scale, L.Fs > 0, L.topk_idx, L.topk_w,
-        L.sh_gate, L.hist_pitch, L.chunk_hist, L.pair_rank);
+        L.logits, L.router_parts, splits, T, L.E, L.R, L.K, c.router_mode, c.norm_topk_prob, c.weights_scale,
+        L.Fs > 0, L.topk_idx, L.topk_w, L.sh_gate, L.hist_pitch, L.chunk_hist, L.pair_rank);
     return 1;
 }
 
@@ -302,8 +318,8 @@ int launch_group(const Layer &L, int T, bool build_tiles, cudaStream_t s)
 // offsets[e] + (start of t's chunk among e's picks) + (its rank in the chunk):
 // ascending token order within each expert.  expert_rows[position] = p; with
 // rows, also the gather of the token rows into the expert-sorted activation
-// buffer (one warp per row; the shared expert's rows, all tokens in order,
-// follow the T*K routed rows).
+// buffer (one warp per row).  The shared expert's rows are all tokens in
+// order: the gate/up GEMM reads them from x itself.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) scatter_kernel(const __nv_bfloat16 *__restrict__ x, int T, int K, int H,
                                                       int has_shared, int hist_pitch, const int *__restrict__ topk_idx,
@@ -323,18 +339,11 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __nv_bfloat16 *__res
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + warp;
-    const int n_rows = P + (has_shared ? T : 0);
-    if (r >= n_rows) return;
-    int tok, dst;
-    if (r < P) {
-        const int e = topk_idx[r];
-        tok = r / K;
-        dst = offsets[e] + chunk_start[(size_t)e * hist_pitch + tok / SEL_TOK] + pair_rank[r];
-        if (lane == 0) expert_rows[dst] = r;
-    } else {
-        tok = r - P;
-        dst = r;
-    }
+    if (r >= P) return;
+    const int e = topk_idx[r];
+    const int tok = r / K;
+    const int dst = offsets[e] + chunk_start[(size_t)e * hist_pitch + tok / SEL_TOK] + pair_rank[r];
+    if (lane == 0) expert_rows[dst] = r;
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)tok * H);
     uint4 *d = reinterpret_cast<uint4 *>(xp + (size_t)dst * H);
     for (int c = lane; c < H / 8; c += 32) d[c] = __ldg(src + c);
@@ -348,8 +357,7 @@ int launch_scatter(const Layer &L, const void *x, int T, bool rows, cudaStream_t
                                                        L.pair_rank, L.chunk_hist, L.offsets, L.expert_rows, nullptr);
         return 1;
     }
-    const int n_rows = P + (L.Fs > 0 ? T : 0);
-    scatter_kernel<<<(n_rows + 7) / 8, 256, 0, s>>>((const __nv_bfloat16 *)x, T, L.K, L.H, L.Fs > 0, L.hist_pitch,
+    scatter_kernel<<<(P + 7) / 8, 256, 0, s>>>((const __nv_bfloat16 *)x, T, L.K, L.H, L.Fs > 0, L.hist_pitch,
                                                     L.topk_idx, L.pair_rank, L.chunk_hist, L.offsets, L.expert_rows,
                                                     (__nv_bfloat16 *)L.xp);
     return 1;

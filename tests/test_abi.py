@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.moe_abi_version() == 3
+    assert lib.moe_abi_version() == 4
 
 
 def test_config_struct_layout_matches_header():
@@ -95,3 +95,10 @@ def test_binding_does_not_import_the_oracle():
             "print(bad); sys.exit(1 if bad else 0)")
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_settings_reject_a_null_layer(lib):
+    import sparse_mixture_experts_gb300 as moe
+    assert lib.moe_set_wait_limit(None, 1000) == moe.ERR_INVALID_ARG
+    assert lib.moe_set_fault_injection(None, 1) == moe.ERR_INVALID_ARG
+    assert lib.moe_get_intermediate(None, 0, None, 0, None, None) == moe.ERR_INVALID_ARG
