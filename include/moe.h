@@ -331,6 +331,34 @@ moe_status moe_route_noalloc(const void *x, const void *router_w, const void *ro
                              int32_t norm_topk_prob, float weights_scale, int32_t dtype, int32_t *idx, float *w,
                              int32_t *counts, void *stream);
 
+/* Expert parallelism: index arithmetic (host pointers, int32; no device work).
+ * The pages list expert parallelism as not done ("Phase 19: MoE --
+ * gpt-oss-20b", section 6); the split builds on the grouping step ("Engine"
+ * (cherenkov), section "Prefill").  n_ranks ranks, rank g owns the experts
+ * [first_expert[g], first_expert[g+1]) (ascending, first_expert[0] = 0,
+ * first_expert[n_ranks] = n_expert).  Each rank routes its own tokens and
+ * orders its (token, slot) pairs by expert (MOE_INTER_PERM), which groups them
+ * by owning rank.
+ *
+ * moe_ep_send_plan: counts[n_expert] = the local pairs per expert ->
+ *   send_counts[g], send_displs[g]: the rows of the expert-ordered pairs that
+ *   go to rank g (one all-to-all of token rows dispatches them).
+ * moe_ep_recv_plan: counts_from[n_ranks][n_local] = what each rank sends this
+ *   one per local expert (an all-to-all of the count rows) -> recv_counts[g],
+ *   recv_displs[g] of the arriving rows (source-major), order[n_recv]: the
+ *   arriving row at position i of the local expert-major order (expert
+ *   ascending, then source rank, then the source's order), group_offsets
+ *   [n_local + 1] of each local expert in that order.  The experts' outputs go
+ *   back in arrival order (the inverse all-to-all), so each source gets them in
+ *   its own expert order and scatters them to (token, slot) for the fixed
+ *   slot-order combine.
+ * Errors: INVALID_ARG (NULL pointer, bad ranges, negative counts, more than
+ * 2^31 - 1 rows). */
+moe_status moe_ep_send_plan(int32_t n_expert, int32_t n_ranks, const int32_t *first_expert, const int32_t *counts,
+                            int32_t *send_counts, int32_t *send_displs);
+moe_status moe_ep_recv_plan(int32_t n_ranks, int32_t n_local, const int32_t *counts_from, int32_t *recv_counts,
+                            int32_t *recv_displs, int32_t *order, int32_t *group_offsets);
+
 /* Description of the last error on this thread ("" if none). */
 const char *moe_last_error(void);
 

@@ -89,6 +89,8 @@ def load_library(path: str = LIB_PATH):
         "moe_get_intermediate": ([VP, I32, VP, ctypes.c_size_t, P(ctypes.c_size_t), VP], ctypes.c_int),
         "moe_set_wait_limit": ([VP, ctypes.c_int64], ctypes.c_int),
         "moe_set_fault_injection": ([VP, I32], ctypes.c_int),
+        "moe_ep_send_plan": ([I32, I32, VP, VP, VP, VP], ctypes.c_int),
+        "moe_ep_recv_plan": ([I32, I32, VP, VP, VP, VP, VP], ctypes.c_int),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
