@@ -263,7 +263,7 @@ def cpu_baselines(spec, w, budget_all: float, budget_one: float):
 
 def _spec_dtype(spec):
     if spec.expert_format == "mxfp4":
-        return "mxfp4-f16"  # MXFP4 expert weights widened to f16 for the MMA, fp32 accumulation
+        return "mxfp4-bf16"  # MXFP4 expert weights widened to bf16 on chip for the MMA, fp32 accumulation
     return "bf16" if spec.dtype == "bf16" else "f32"
 
 

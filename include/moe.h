@@ -76,14 +76,15 @@ typedef enum {
      * down_scales the scales ([E][2F][H/32], [E][H][F/32]); the router and the
      * biases are bf16 and act_dtype must be bf16.  Requires
      * gate_up_interleaved = 1, shared_ff = 0 and H, F multiples of 64.
-     * moe_create also keeps the experts dequantised to bf16 (exact: every
-     * E2M1 code times a power of two fits bf16), which the prefill paths
-     * read.  The decode path (T <= 16 on the tensor-core path) streams the
-     * codes and scales themselves and widens them to f16 on chip; that is
-     * exact when every E8M0 byte is in 113..140, so a layer with a scale
-     * outside that range decodes from the bf16 copy instead.  Either way the
-     * result equals the bf16 layer built from the dequantised weights, up to
-     * rounding order. */
+     * The layer keeps only the codes and scales (repacked per 128-row,
+     * 64-wide K block); both tensor-core paths (weight-streaming decode for up
+     * to 16 tokens, grouped GEMMs above) widen them to bf16 on chip, exactly
+     * for every E8M0 byte (an E2M1 value times a power of two has at most two
+     * significant bits; products beyond the fp32 range are infinite, byte 255
+     * is NaN).  The result equals the bf16 layer built from the dequantised
+     * weights, up to rounding order.  MOE_PATH_STREAM and MOE_PATH_FUSED are
+     * UNSUPPORTED for such a layer, and create is UNSUPPORTED on a device
+     * without the tensor-core kernels. */
     MOE_DT_MXFP4 = 2
 } moe_dtype;
 

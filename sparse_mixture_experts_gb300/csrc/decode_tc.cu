@@ -42,6 +42,7 @@
 #include <cudaTypedefs.h>
 
 #include "moe_internal.cuh"
+#include "mxfp4.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -62,9 +63,11 @@ constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
 // the blocks of a stage may come from different groups (down units).  Two
 // blocks per stage measured no faster than one, so one is used.  The
 // producer's ring holds DT_FP4_RS stages.  Eight more warps widen each block to
-// f16 and store it straight into tensor memory, where the MMA reads its A
-// operand (DT_FP4_AS tiles of 32 columns per K block): the f16 tile never
-// touches shared memory, whose bandwidth would otherwise bound the stage rate.
+// bf16 (exactly, for every scale byte: a table lookup per code, see mxfp4.cuh)
+// and store it straight into tensor memory, where the MMA reads its A operand
+// (DT_FP4_AS tiles of 32 columns per K block); the token operand is x and h'
+// in bf16 as for bf16 weights.  The widened tile never touches shared memory,
+// whose bandwidth would otherwise bound the stage rate.
 // What bounds this pipeline instead is the length of each role's per-stage
 // instruction path (one warp or thread per stage), hence several producer
 // threads, two dequantising groups and two MMA threads taking stages in turn.
@@ -95,13 +98,14 @@ struct DtShape {
     static constexpr int BLK_OFF = RS * KPS * DT_B_BYTES;   // MXFP4 only
     static constexpr int BLK_STRIDE = KPS * DT_FP4_BLK;
     static constexpr int RING = FP4 ? (BLK_OFF + RS * BLK_STRIDE + 1023) / 1024 * 1024 : DT_STAGES * DT_STAGE_BYTES;
-    static constexpr size_t SMEM = (size_t)RING + 1024 + DT_XCH_BYTES + 1024;
+    static constexpr int TAB_BYTES = FP4 ? 256 * (int)sizeof(Fp4Table) : 0;  // MXFP4 -> bf16 tables, one per scale byte
+    static constexpr size_t SMEM = (size_t)RING + 1024 + DT_XCH_BYTES + 1024 + TAB_BYTES;
 };
 static_assert(DT_FP4_KPS == 1 || DT_FP4_KPS == 2, "one or two K blocks per MXFP4 stage");
 static_assert(DT_ACC * 2 * DT_TOK <= DT_FP4_A_COL && DT_FP4_A_COL + DT_FP4_AS * DT_FP4_KPS * 32 <= DT_FP4_TMEM_COLS,
               "MXFP4 accumulators and A tiles fit the tensor memory allocation");
 static_assert(DT_FP4_RS <= 32 && DT_STAGES <= 32, "the producer's per-stage masks are 32 bits");
-static_assert(DtShape<true>::SMEM + 11 * 1024 <= 227 * 1024, "MXFP4 ring and static shared memory fit a CTA");
+static_assert(DtShape<true>::SMEM + 11 * 1024 <= 227 * 1024, "MXFP4 ring, tables and static shared memory fit a CTA");
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
 constexpr int DT_SATURATING_CTAS = 128;         // CTAs streaming at once that saturate HBM
 constexpr int DT_UP_MIN_KB = 8;                 // smallest gate/up split, in 64-wide K blocks
@@ -131,7 +135,7 @@ struct DecArgs {
     int *active;
     RouteMeta *meta;
     const float *gate_b, *up_b, *down_b;
-    void *hp;             // [groups_max*16][Fmax], bf16 (f16 for MXFP4 weights)
+    void *hp;             // [groups_max*16][Fmax], bf16
     const uint8_t *gu_fp4, *dn_fp4;  // MXFP4 weights, packed blocks (see Layer)
     int ot;               // down output tiles of 128 rows
     float *partials;      // [gate/up, down][units][T][128]
@@ -153,7 +157,6 @@ struct DecArgs {
 // ---------------------------------------------------------------------------
 struct DecRouteArgs {
     const __nv_bfloat16 *x;
-    __half *x16;          // MXFP4 weights: f16 copy of x for the token operand (else null)
     const __nv_bfloat16 *router_w;
     const float *router_b;
     float *logits;
@@ -171,12 +174,6 @@ __global__ void __launch_bounds__(256) dec_route_kernel(const DecRouteArgs a)
         // kernel 2 of the previous forward has finished (stream order)
         for (int i = threadIdx.x; i < a.n_reset; i += 256) a.counters[DT_GROUP_DONE + i * DT_DONE_STRIDE] = 0;
         if (threadIdx.x == 0) a.counters[DT_NEXT_UNIT] = 0;
-    }
-    if (a.x16) {
-        // the blocks share the conversion of x (exact for |x| in the f16 range)
-        const size_t n = (size_t)a.T * H, per = (n + gridDim.x - 1) / gridDim.x;
-        const size_t i0 = (size_t)blockIdx.x * per, i1 = min(n, i0 + per);
-        for (size_t i = i0 + threadIdx.x; i < i1; i += 256) a.x16[i] = __float2half_rn(__bfloat162float(a.x[i]));
     }
     __shared__ float s_part[8][DT_TOK];
     const int r = blockIdx.x;
@@ -374,42 +371,22 @@ __device__ __forceinline__ void sum_partials(const float *pt, int S, int T, int 
     }
 }
 
-// MXFP4 -> f16: the four bytes of w hold eight E2M1 codes (low nibble = even
-// element); each byte widens to an f16 pair (hardware conversion)
-__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t (&h)[4])
-{
-    asm("{ .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3; }"
-        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(w));
-}
-
-// 2^(e8m0 - 127) as an f16 pair; the layer checks at creation that every
-// scale is in 113..140, where this and every code times it are exact f16
-__device__ __forceinline__ __half2 e8m0_half2(uint32_t e8m0)
-{
-    const uint32_t b = (e8m0 - 127u + 15u) << 10;
-    const uint32_t v = b | (b << 16);
-    return *reinterpret_cast<const __half2 *>(&v);
-}
-
-// Half h (elements 32h .. 32h+31, one E8M0 scale) of row r of a packed
-// MXFP4 block, widened and scaled to 16 f16 pairs: v[c] holds elements
-// 32h + 2c (low half) and 32h + 2c + 1, as A-tile column 16h + c in tensor memory.
-__device__ __forceinline__ void fp4_dequant_half(const uint8_t *blk, int h, int r, uint32_t (&v)[16])
+// Half h (elements 32h .. 32h+31, one E8M0 scale) of row r of a packed MXFP4
+// block, widened exactly to 16 bf16 pairs: v[c] holds elements 32h + 2c (low
+// half) and 32h + 2c + 1, as A-tile column 16h + c in tensor memory.  tabs:
+// the conversion tables of the 256 scale bytes (in shared memory).
+__device__ __forceinline__ void fp4_dequant_half(const uint8_t *blk, int h, int r, const Fp4Table *tabs,
+                                                 uint32_t (&v)[16])
 {
     const uint4 c = *reinterpret_cast<const uint4 *>(blk + (h * 128 + r) * 16);
-    const __half2 s = e8m0_half2(blk[128 * 32 + h * 128 + r]);
+    const Fp4Table t = tabs[blk[128 * 32 + h * 128 + r]];
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t hq[4];
-        e2m1x8_to_f16(words[q], hq);
+        uint32_t o[4];
+        mxfp4_to_bf16x8(words[q], t, o);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            __half2 x = __hmul2(*reinterpret_cast<__half2 *>(&hq[i]), s);
-            v[q * 4 + i] = *reinterpret_cast<uint32_t *>(&x);
-        }
+        for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
     }
 }
 
@@ -438,6 +415,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *xch = reinterpret_cast<float *>(smem + Sh::RING);
+    Fp4Table *fp4tab = reinterpret_cast<Fp4Table *>(smem + Sh::RING + DT_XCH_BYTES + 1024);  // MXFP4 only
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Sh::RING + DT_XCH_BYTES);  // [RS] raw stage landed
     uint64_t *empty = full + RS;              // [RS] raw stage consumed
     uint64_t *acc_full = empty + RS;          // [DT_ACC]
@@ -496,6 +474,8 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
     }
     for (int e = threadIdx.x; e < E; e += THREADS) s_cnt[e] = 0;
     if (threadIdx.x < 32) s_mask[threadIdx.x] = 0u;
+    if constexpr (FP4)
+        for (int i = threadIdx.x; i < 256; i += THREADS) fp4tab[i] = mxfp4_table((uint32_t)i);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -775,7 +755,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
         constexpr int NM = Sh::NM;
         const int mw = warp == 1 ? 0 : 1;
         if (lane == 0) {
-            constexpr uint32_t idesc = FP4 ? idesc_f16_f32(128, DT_TOK) : idesc_bf16_f32(128, DT_TOK);
+            constexpr uint32_t idesc = idesc_bf16_f32(128, DT_TOK);
             int stage = 0, ast = 0;  // raw stage; MXFP4: A tile
             uint32_t phase = 0, aph = 0;
             uint32_t gs = 0;         // index of the next stage in the stream
@@ -819,7 +799,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                             for (int sub = 0; sub < nkb; ++sub)
 #pragma unroll
                                 for (int k = 0; k < 4; ++k)
-                                    mma_f16_ta(d_tmem, at + sub * 32 + k * 8,
+                                    mma_ta(d_tmem, at + sub * 32 + k * 8,
                                                smem_desc_sw128(sb + sub * DT_B_BYTES + k * 32), idesc,
                                                !first || sub != 0 || k != 0);
                         } else {
@@ -970,8 +950,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         float hval = swiglu ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
                                             : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
                         hval *= s_wt[t];
-                        if (FP4) reinterpret_cast<__half *>(a.hp)[hbase + (size_t)t * a.Fmax] = __float2half_rn(hval);
-                        else reinterpret_cast<__nv_bfloat16 *>(a.hp)[hbase + (size_t)t * a.Fmax] = __float2bfloat16_rn(hval);
+                        reinterpret_cast<__nv_bfloat16 *>(a.hp)[hbase + (size_t)t * a.Fmax] = __float2bfloat16_rn(hval);
                     }
                 }
                 // publish: h' of this tile is written (generic proxy) and will be
@@ -1053,12 +1032,13 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         const int nkb = min(DT_FP4_KPS, nk - j * DT_FP4_KPS);
                         for (int sub = 0; sub < nkb; ++sub) {
                             const uint8_t *blk = smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * DT_FP4_BLK;
-                            uint32_t v0[16], v1[16];
-                            fp4_dequant_half(blk, 0, row, v0);
-                            fp4_dequant_half(blk, 1, row, v1);
                             const uint32_t col = (uint32_t)((ast * DT_FP4_KPS + sub) * 32);
-                            tmem_st16(t_a + col, v0);
-                            tmem_st16(t_a + col + 16, v1);
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {  // one half at a time: 16 words live
+                                uint32_t v[16];
+                                fp4_dequant_half(blk, h, row, fp4tab, v);
+                                tmem_st16(t_a + col + 16 * h, v);
+                            }
                         }
                         tmem_st_wait();
                     } else if (!*abort_flag) {
@@ -1136,10 +1116,15 @@ int dectc_prepare(Layer &L)
     if ((long long)dectc_groups_max(L) * DT_DONE_STRIDE > DT_NEXT_UNIT - DT_GROUP_DONE) return -1;
     DecMaps *m = new (std::nothrow) DecMaps();
     if (!m) return -1;
-    bool ok = dec_encode(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
-              dec_encode(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, 64) &&
-              dec_encode(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, 128) &&
-              dec_encode(&m->hp, L.dec_hp, L.Fmax, (uint64_t)dectc_groups_max(L) * DT_TOK, DT_TOK, L.fp4_decode);
+    bool ok = dec_encode(&m->hp, L.dec_hp, L.Fmax, (uint64_t)dectc_groups_max(L) * DT_TOK, DT_TOK);
+    if (L.mxfp4) {
+        // the experts stream as packed MXFP4 blocks (bulk copies), not through tensor maps
+        m->gate = m->up = m->down = m->hp;
+    } else {
+        ok = ok && dec_encode(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
+             dec_encode(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, 64) &&
+             dec_encode(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, 128);
+    }
     if (ok && L.Fs) {
         ok = dec_encode(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, 64) && dec_encode(&m->sh_up, L.sh_up_w, L.H, L.Fs, 64) &&
              dec_encode(&m->sh_down, L.sh_down_w, L.Fs, L.H, 128);
@@ -1170,7 +1155,6 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     if (which == 0) {
         DecRouteArgs r;
         r.x = (const __nv_bfloat16 *)x;
-        r.x16 = L.fp4_decode ? (__half *)L.dec_x16 : nullptr;
         r.router_w = (const __nv_bfloat16 *)L.router_w;
         r.router_b = L.router_b;
         r.logits = L.logits;
@@ -1181,11 +1165,7 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
         return 1;
     }
     DecMaps m = *L.dectc;
-    if (L.fp4_decode) {
-        if (!dec_encode(&m.x, L.dec_x16, L.H, (uint64_t)T, DT_TOK, true)) return -1;
-    } else if (!dec_encode(&m.x, x, L.H, (uint64_t)T, DT_TOK)) {
-        return -1;
-    }
+    if (!dec_encode(&m.x, x, L.H, (uint64_t)T, DT_TOK)) return -1;
     DecArgs a;
     a.logits = L.logits;
     a.topk_idx = L.topk_idx; a.topk_w = L.topk_w; a.sh_gate = L.sh_gate; a.counts = L.counts; a.active = L.active;
@@ -1209,15 +1189,15 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     a.inject = L.inject;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.num_sms);
-    cfg.blockDim = dim3(L.fp4_decode ? DtShape<true>::THREADS : DtShape<false>::THREADS);
-    cfg.dynamicSmemBytes = L.fp4_decode ? DtShape<true>::SMEM : DtShape<false>::SMEM;
+    cfg.blockDim = dim3(L.mxfp4 ? DtShape<true>::THREADS : DtShape<false>::THREADS);
+    cfg.dynamicSmemBytes = L.mxfp4 ? DtShape<true>::SMEM : DtShape<false>::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = L.fp4_decode ? cudaLaunchKernelEx(&cfg, dec_experts_kernel<true>, m, a)
+    const cudaError_t e = L.mxfp4 ? cudaLaunchKernelEx(&cfg, dec_experts_kernel<true>, m, a)
                                        : cudaLaunchKernelEx(&cfg, dec_experts_kernel<false>, m, a);
     return e == cudaSuccess ? 1 : -1;
 }

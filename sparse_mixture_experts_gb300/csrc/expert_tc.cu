@@ -29,27 +29,36 @@
 #include <cudaTypedefs.h>
 
 #include "moe_internal.cuh"
+#include "mxfp4.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
 
 constexpr int TC_THREADS = 192;
 constexpr int A_TILE_BYTES = TC_BM * TC_BK * 2;        // 16 KB
+constexpr int TC_FP4_BLK = 128 * 32 + 128 * 2;         // packed MXFP4 block: 128 rows x 64 K (codes, scales)
 
 // Per tile width BN (the MMA's N): the B tile, the stage, the ring depth and
 // the TMEM columns (two accumulators of BN fp32 columns).  N = 256 halves the
 // A bytes staged per weight byte, which matters because a CTA's TMA stream,
 // not HBM, limits these GEMMs once the A rows are re-read from L2.
-template <int BN>
+template <int BN, bool FP4 = false>
 struct TcShape {
     static constexpr int B_BYTES = BN * TC_BK * 2;
-    static constexpr int STAGE = A_TILE_BYTES + B_BYTES;
-    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    // MXFP4 weights: two packed blocks (codes and scales of 2 x 128 rows x 64 K)
+    // land next to the tiles; dequantising warps write the bf16 B tile from them
+    static constexpr int RAW_BYTES = FP4 ? 2 * TC_FP4_BLK : 0;
+    static constexpr int STAGE = (A_TILE_BYTES + B_BYTES + RAW_BYTES + 1023) / 1024 * 1024;
+    static constexpr int STAGES = FP4 ? 3 : (BN == 256 ? 4 : 6);
     static constexpr int TMEM_COLS = 2 * BN;
-    // after the ring: barriers, then the epilogue's staging (4 warps x 32 rows x 16 fp32)
+    // after the ring: barriers, then the epilogue's staging (4 warps x 32 rows x
+    // 16 fp32), then (MXFP4) the conversion tables of the 256 scale bytes
     static constexpr int STAGING_OFF = STAGES * STAGE + 256;
     static constexpr int STAGING_BYTES = 4 * 32 * 16 * 4;
-    static constexpr size_t SMEM = (size_t)STAGING_OFF + STAGING_BYTES + 1024 /*align*/;
+    static constexpr int TAB_OFF = STAGING_OFF + STAGING_BYTES;
+    static constexpr int TAB_BYTES = FP4 ? 256 * (int)sizeof(Fp4Table) : 0;
+    static constexpr size_t SMEM = (size_t)TAB_OFF + TAB_BYTES + 1024 /*align*/;
+    static constexpr int THREADS = FP4 ? TC_THREADS + 128 : TC_THREADS;  // + 4 dequantising warps
 };
 
 struct TensorMaps {
@@ -92,6 +101,7 @@ struct TcArgs {
     const float *router_b;
     int R, router_nt, router_S, router_bn;  // router rows, router N tiles, K splits, tile width
     int *status;
+    const uint8_t *fp4;          // MXFP4 weights: packed blocks of gate/up ([E][F/64][H/64]) or down ([E][H/128][F/64])
     const volatile int *stall;   // test-only fault injection: a word nothing sets, waited for (else null)
     unsigned long long wait_ns;  // bound of that wait
     int T, K, E, H, F, Fs, Fmax, Tmax;
@@ -165,10 +175,11 @@ __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, 
     return ti.m0 >= 0 && ti.m0 < ti.rows && ti.n0 >= 0;
 }
 
-template <int EPI, int BN, typename Maps>
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ Maps maps, const TcArgs a)
+template <int EPI, int BN, typename Maps, bool FP4 = false>
+__global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ Maps maps,
+                                                                               const TcArgs a)
 {
-    using Sh = TcShape<BN>;
+    using Sh = TcShape<BN, FP4>;
     constexpr int TC_STAGES = Sh::STAGES;
     constexpr int STAGE_BYTES = Sh::STAGE;
     constexpr int B_TILE_BYTES = Sh::B_BYTES;
@@ -180,7 +191,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     uint64_t *acc_full = empty + TC_STAGES;   // [2]
     uint64_t *acc_empty = acc_full + 2;       // [2]
     uint64_t *drain = acc_empty + 2;          // the MMA thread's own completion, after an abort
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *bready = drain + 1;             // [TC_STAGES] MXFP4: the B tile is dequantised
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bready + TC_STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -197,6 +209,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             mbar_init(&acc_empty[b], 128);
         }
         mbar_init(drain, 1);
+        if (FP4)
+            for (int st = 0; st < TC_STAGES; ++st) mbar_init(&bready[st], 128);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -214,13 +228,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         gt.n = n_act + (a.Fs > 0 ? 1 : 0);
         const int P = a.E + 2;
         const int *gf = a.gfirst + (EPI == EPI_UP ? 0 : P);
-        for (int i = threadIdx.x; i <= gt.n; i += TC_THREADS) s_gfirst[i] = gf[i];
-        for (int i = threadIdx.x; i < gt.n; i += TC_THREADS) {
+        for (int i = threadIdx.x; i <= gt.n; i += Sh::THREADS) s_gfirst[i] = gf[i];
+        for (int i = threadIdx.x; i < gt.n; i += Sh::THREADS) {
             s_gexp[i] = a.gfirst[2 * P + i];
             s_grows[i] = a.gfirst[3 * P + i];
             s_grow0[i] = a.gfirst[4 * P + i];
         }
     }
+    Fp4Table *fp4tab = reinterpret_cast<Fp4Table *>(smem + Sh::TAB_OFF);
+    if constexpr (FP4)
+        for (int i = threadIdx.x; i < 256; i += Sh::THREADS) fp4tab[i] = mxfp4_table((uint32_t)i);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -251,8 +268,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     }
                     uint8_t *sa = smem + stage * STAGE_BYTES;
                     uint8_t *sb = sa + A_TILE_BYTES;
-                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                     const int kc = (ti.kb0 + kb) * TC_BK;
+                    if constexpr (FP4) {
+                        // the A tile, and the packed blocks of the tile's 2 x 128 weight rows
+                        // (gate/up: features n0 .. n0+127 as two blocks of 64 gate + 64 up
+                        // rows; down: output rows n0 .. n0+255); a block past the matrix is
+                        // not copied (its rows are written as zeros)
+                        const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
+                        const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
+                        const int nvalid = min(2, nb - b0);
+                        const int nkbt = EPI == EPI_UP ? a.H / TC_BK : a.F / TC_BK;
+                        mbar_arrive_expect_tx(&full[stage], A_TILE_BYTES + nvalid * TC_FP4_BLK);
+                        tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
+                        for (int q = 0; q < nvalid; ++q) {
+                            const size_t blk = ((size_t)ti.g * nb + b0 + q) * nkbt + ti.kb0 + kb;
+                            bulk_load(sb + B_TILE_BYTES + q * TC_FP4_BLK, a.fp4 + blk * TC_FP4_BLK, TC_FP4_BLK,
+                                      &full[stage]);
+                        }
+                        used |= 1u << stage;
+                        last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+                        if (++stage == TC_STAGES) stage = 0, phase ^= 1;
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
                     if (EPI == EPI_UP && ti.shared) tma_load_2d(sa, &maps.sa, &full[stage], kc, ti.m0);
                     else tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
                     if (EPI == EPI_UP) {
@@ -295,7 +333,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
                 for (int kb = 0; kb < ti.nk; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                    if (!mbar_wait(&full[stage], phase, abort_flag) ||
+                        (FP4 && !mbar_wait(&bready[stage], phase, abort_flag))) {
                         record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
                         *abort_flag = 1;
                         ok = false;
@@ -325,6 +364,68 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 volatile int never = 0;
                 mma_commit(drain);
                 mbar_wait(drain, 0, &never);
+            }
+        }
+    } else if (FP4 && warp >= 6) {
+        // ------------------------------ MXFP4 dequantisation (warps 6..9) ------------------------------
+        // Per stage: the 256 rows of the B tile, two per thread, each 64 codes
+        // widened exactly to bf16 and written as eight 16-byte chunks at their
+        // 128-byte-swizzle positions (chunk j of row r at r * 128 + ((j ^ (r & 7)) << 4),
+        // the layout the TMA would have written).  Then the writes are made
+        // visible to the tensor cores' reads and the stage is released to the MMA.
+        const int dt = threadIdx.x - TC_THREADS;  // 0 .. 127
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            TileInfo ti;
+            if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
+            const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
+            const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
+            for (int kb = 0; kb < ti.nk; ++kb) {
+                if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                    record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                uint8_t *bt = smem + stage * STAGE_BYTES + A_TILE_BYTES;
+                const uint8_t *raw = bt + B_TILE_BYTES;
+#pragma unroll
+                for (int rr0 = 0; rr0 < 256; rr0 += 128) {
+                    const int rr = rr0 + dt;
+                    int q, brow;  // packed block of the tile, row in it
+                    if (EPI == EPI_UP) {
+                        const int f = rr & 127;
+                        q = f >> 6;
+                        brow = (rr < 128 ? 0 : 64) + (f & 63);
+                    } else {
+                        q = rr >> 7;
+                        brow = rr & 127;
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(bt + rr * 128);
+                    if (b0 + q >= nb) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) dst[j ^ (rr & 7)] = make_uint4(0, 0, 0, 0);
+                        continue;
+                    }
+                    const uint8_t *pb = raw + q * TC_FP4_BLK;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 c = *reinterpret_cast<const uint4 *>(pb + (h * 128 + brow) * 16);
+                        const Fp4Table tb = fp4tab[pb[128 * 32 + h * 128 + brow]];
+                        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t o[4];
+                            mxfp4_to_bf16x8(words[w], tb, o);
+                            dst[(h * 4 + w) ^ (rr & 7)] = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+                fence_proxy_async_shared();
+                mbar_arrive(&bready[stage]);
+                if (++stage == TC_STAGES) stage = 0, phase ^= 1;
             }
         }
     } else {
@@ -530,10 +631,15 @@ int tc_prepare(Layer &L)
     if (!m) return -1;
     const uint64_t rows_all = (uint64_t)L.Tmax * L.K + L.Tmax;
     bool ok = encode_2d(&m->xp, L.xp, L.H, rows_all, TC_BM) && encode_2d(&m->h, L.h, L.Fmax, rows_all, TC_BM) &&
-              encode_2d(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, TC_BN_UP / 2) &&
-              encode_2d(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, TC_BN_UP / 2) &&
-              encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, TC_BN_DOWN) &&
               encode_2d(&m->router, L.router_w, L.H, (uint64_t)L.R, 128);
+    if (L.mxfp4) {
+        // the experts' B operand is dequantised from the packed blocks in the kernel
+        m->gate = m->up = m->down = m->router;
+    } else {
+        ok = ok && encode_2d(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, TC_BN_UP / 2) &&
+             encode_2d(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, TC_BN_UP / 2) &&
+             encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, TC_BN_DOWN);
+    }
     if (ok && L.Fs) {
         ok = encode_2d(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, TC_BN_UP / 2) &&
              encode_2d(&m->sh_up, L.sh_up_w, L.H, L.Fs, TC_BN_UP / 2) &&
@@ -549,7 +655,13 @@ int tc_prepare(Layer &L)
         cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)TcShape<TC_BN_DOWN>::SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<EPI_ROUTER, 128, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<128>::SMEM) != cudaSuccess) {
+                             (int)TcShape<128>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<TC_BN_UP, true>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<TC_BN_DOWN, true>::SMEM) != cudaSuccess) {
         delete m;
         return -1;
     }
@@ -574,6 +686,7 @@ static TcArgs make_tc_args(const Layer &L, int T)
     a.h = (__nv_bfloat16 *)L.h;
     a.ys = L.ys;
     a.status = L.status;
+    a.fp4 = nullptr;
     a.stall = L.inject ? L.never : nullptr;
     a.wait_ns = L.wait_ns;
     a.T = T; a.K = L.K; a.E = L.E; a.H = L.H; a.F = L.F; a.Fs = L.Fs; a.Fmax = L.Fmax; a.Tmax = L.Tmax;
@@ -591,10 +704,22 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
     if (which == 1) {
         TcMaps mu{m.xp, m.gate, m.up, m.sh_gate, m.sh_up, m.xp};
         if (L.Fs > 0 && !encode_2d(&mu.sa, x, L.H, (uint64_t)T, TC_BM)) return -1;
-        tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_UP>::SMEM, s>>>(mu, a);
+        if (L.mxfp4) {
+            a.fp4 = L.fp4_gu;
+            using Sh = TcShape<TC_BN_UP, true>;
+            tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, true><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
+        } else {
+            tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_UP>::SMEM, s>>>(mu, a);
+        }
     } else {
         TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down, m.h};
-        tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_DOWN>::SMEM, s>>>(md, a);
+        if (L.mxfp4) {
+            a.fp4 = L.fp4_dn;
+            using Sh = TcShape<TC_BN_DOWN, true>;
+            tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, true><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
+        } else {
+            tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_DOWN>::SMEM, s>>>(md, a);
+        }
     }
     return 1;
 }

@@ -112,61 +112,22 @@ __global__ void split_bias_kernel(const void *src, int dtype, int E, int F, int 
     }
 }
 
-// MXFP4 [rows][cols/32][16] codes + [rows][cols/32] E8M0 scales -> bf16
-// [rows][cols]; with `odd` set, even rows go to `even` and odd rows to `odd`
-// (row r / 2), which de-interleaves gpt-oss's gate_up.  The E2M1 pair of a
-// byte is widened by the hardware conversion (low nibble = even element) and
-// scaled by a power of two, so every value is exact in bf16.
-__global__ void mxfp4_to_bf16_kernel(const uint8_t *blocks, const uint8_t *scales, size_t rows, int cols,
-                                     __nv_bfloat162 *even, __nv_bfloat162 *odd)
-{
-    const size_t half = (size_t)cols / 2, n = rows * half;
-    const int nb = cols / 32;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const size_t r = i / half, c2 = i - r * half;  // elements 2 c2, 2 c2 + 1
-        const size_t b = r * nb + c2 / 16;
-        const uint16_t byte = blocks[b * 16 + c2 % 16];
-        uint32_t h2;
-        asm("{ .reg .b8 t; cvt.u8.u16 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "h"(byte));
-        const float2 v = __half22float2(*reinterpret_cast<__half2 *>(&h2));
-        const int e = scales[b];
-        const float lo = e == 255 ? __int_as_float(0x7fc00000) : ldexpf(v.x, e - 127);
-        const float hi = e == 255 ? __int_as_float(0x7fc00000) : ldexpf(v.y, e - 127);
-        const __nv_bfloat162 o = __floats2bfloat162_rn(lo, hi);
-        if (odd) ((r & 1) ? odd : even)[(r >> 1) * half + c2] = o;
-        else even[r * half + c2] = o;
-    }
-}
-
-// an MXFP4 tensor copied to the device (freed by the caller, cudaFree), its
-// bf16 values written to even / odd, and the range of its E8M0 scales
+// an MXFP4 tensor copied to the device for packing (freed by the caller, cudaFree)
 struct Fp4Staged {
     uint8_t *blocks = nullptr, *scales = nullptr;
-    int min_scale = 255, max_scale = 0;
     void release() { if (blocks) cudaFree(blocks); if (scales) cudaFree(scales); blocks = scales = nullptr; }
 };
 
-moe_status upload_mxfp4(Layer &L, const void *blocks, const void *scales, size_t rows, size_t cols,
-                        void *even, void *odd, const char *name, Fp4Staged &st)
+moe_status stage_mxfp4(const void *blocks, const void *scales, size_t rows, size_t cols, const char *name,
+                       Fp4Staged &st)
 {
     if (!blocks || !scales) return fail(MOE_ERR_INVALID_ARG, std::string("missing MXFP4 weight: ") + name);
     const size_t nb = cols / 32;
-    std::vector<uint8_t> hs(rows * nb);
     cudaError_t e = cudaMalloc((void **)&st.blocks, rows * nb * 16);
     if (e == cudaSuccess) e = cudaMalloc((void **)&st.scales, rows * nb);
     if (e == cudaSuccess) e = cudaMemcpy(st.blocks, blocks, rows * nb * 16, cudaMemcpyDefault);
-    if (e == cudaSuccess) e = cudaMemcpy(hs.data(), scales, rows * nb, cudaMemcpyDefault);
-    if (e == cudaSuccess) e = cudaMemcpy(st.scales, hs.data(), rows * nb, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) {
-        mxfp4_to_bf16_kernel<<<4 * L.num_sms, 256>>>(st.blocks, st.scales, rows, (int)cols, (__nv_bfloat162 *)even,
-                                                     (__nv_bfloat162 *)odd);
-        e = cudaDeviceSynchronize();
-    }
+    if (e == cudaSuccess) e = cudaMemcpy(st.scales, scales, rows * nb, cudaMemcpyDefault);
     if (e != cudaSuccess) return cuda_fail(e, name);
-    for (uint8_t v : hs) {
-        st.min_scale = v < st.min_scale ? v : st.min_scale;
-        st.max_scale = v > st.max_scale ? v : st.max_scale;
-    }
     return MOE_OK;
 }
 
@@ -256,16 +217,21 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     if ((st = dev_alloc(L, &L.router_w, (size_t)L.R * H * eb))) return st;
     if ((st = upload(L.router_w, w->router_w, E * H * eb, "router_w"))) return st;
     if (Fs && (st = upload((char *)L.router_w + E * H * eb, w->sh_gate_inp, H * eb, "sh_gate_inp"))) return st;
-    if ((st = dev_alloc(L, &L.gate_w, E * F * H * eb))) return st;
-    if ((st = dev_alloc(L, &L.up_w, E * F * H * eb))) return st;
-    Fp4Staged gu4, dn4;  // the MXFP4 tensors on the device until the decode packing below
+    Fp4Staged gu4, dn4;  // the MXFP4 tensors on the device until the packing below
     struct Release {
         Fp4Staged &a, &b;
         ~Release() { a.release(); b.release(); }
     } release_fp4{gu4, dn4};
     if (L.mxfp4) {
-        if ((st = upload_mxfp4(L, w->gate_up_w, w->gate_up_scales, E * 2 * F, H, L.gate_w, L.up_w, "gate_up_w", gu4)))
-            return st;
+        // the routed experts stay MXFP4: the tensor-core kernels widen them on chip
+        if ((st = stage_mxfp4(w->gate_up_w, w->gate_up_scales, E * 2 * F, H, "gate_up_w", gu4))) return st;
+        if ((st = stage_mxfp4(w->down_w, w->down_scales, E * H, F, "down_w", dn4))) return st;
+    } else {
+        if ((st = dev_alloc(L, &L.gate_w, E * F * H * eb))) return st;
+        if ((st = dev_alloc(L, &L.up_w, E * F * H * eb))) return st;
+    }
+    if (L.mxfp4) {
+        // nothing more: the packed blocks are built below
     } else if (c.gate_up_interleaved) {
         void *tmp = nullptr;
         CUDA_TRY(cudaMalloc(&tmp, E * 2 * F * H * eb));
@@ -281,11 +247,9 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
         if ((st = upload(L.gate_w, w->gate_w, E * F * H * eb, "gate_w"))) return st;
         if ((st = upload(L.up_w, w->up_w, E * F * H * eb, "up_w"))) return st;
     }
-    if ((st = dev_alloc(L, &L.down_w, E * H * F * eb))) return st;
-    if (L.mxfp4) {
-        if ((st = upload_mxfp4(L, w->down_w, w->down_scales, E * H, F, L.down_w, nullptr, "down_w", dn4))) return st;
-    } else if ((st = upload(L.down_w, w->down_w, E * H * F * eb, "down_w"))) {
-        return st;
+    if (!L.mxfp4) {
+        if ((st = dev_alloc(L, &L.down_w, E * H * F * eb))) return st;
+        if ((st = upload(L.down_w, w->down_w, E * H * F * eb, "down_w"))) return st;
     }
     if (c.has_bias) {
         if ((st = upload_f32(L, &L.router_b, w->router_b, E, "router_b"))) return st;
@@ -340,6 +304,10 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
 
     std::string why;
     L.tc_capable = tc_supported(L, why);
+    if (L.mxfp4) {
+        L.decode_grid = 0;  // the CUDA-core paths read bf16 or fp32 weights only
+        if (!L.tc_capable) return fail(MOE_ERR_UNSUPPORTED, "MXFP4 experts need the tensor-core kernels: " + why);
+    }
     if (L.tc_capable) {
         // routed rows (T*K, expert-sorted) then the shared expert's rows (T)
         if ((st = dev_alloc(L, &L.xp, (T * K + T) * H * eb))) return st;
@@ -347,16 +315,12 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
         if ((st = dev_alloc_t(L, &L.router_parts, (size_t)TC_ROUTER_MAX_SPLITS * T * L.R))) return st;
         if (tc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "tensor map creation failed");
         if (L.mxfp4) {
-            // the MXFP4 decode kernel reads the codes and scales themselves; its f16
-            // operands hold every code times 2^(e8m0 - 127) exactly for e8m0 in 113..140
-            L.fp4_decode = gu4.min_scale >= 113 && dn4.min_scale >= 113 && gu4.max_scale <= 140 && dn4.max_scale <= 140;
-            if (L.fp4_decode) {
-                if ((st = dev_alloc_t(L, &L.fp4_gu, dectc_fp4_bytes(L, true)))) return st;
-                if ((st = dev_alloc_t(L, &L.fp4_dn, dectc_fp4_bytes(L, false)))) return st;
-                if ((st = dev_alloc(L, &L.dec_x16, 16 * H * 2))) return st;
-                if (dectc_pack_fp4(L, gu4.blocks, gu4.scales, dn4.blocks, dn4.scales) != 0)
-                    return fail(MOE_ERR_CUDA, "MXFP4 packing failed");
-            }
+            // one contiguous block per (row block, 64-wide K block) for both
+            // tensor-core paths
+            if ((st = dev_alloc_t(L, &L.fp4_gu, dectc_fp4_bytes(L, true)))) return st;
+            if ((st = dev_alloc_t(L, &L.fp4_dn, dectc_fp4_bytes(L, false)))) return st;
+            if (dectc_pack_fp4(L, gu4.blocks, gu4.scales, dn4.blocks, dn4.scales) != 0)
+                return fail(MOE_ERR_CUDA, "MXFP4 packing failed");
         }
         size_t hp_b, part_b, tab_b, tick_b;
         dectc_workspace(L, hp_b, part_b, tab_b, tick_b);
@@ -423,7 +387,7 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
     if (route == Route::DecodeTC) {
         int bad = 0;
         run(MOE_KERNEL_ROUTER, [&] { int r = launch_dectc(L, x, T, out, 0, s); bad |= r < 0; return r < 0 ? 0 : r; });
-        run(L.fp4_decode ? MOE_KERNEL_EXPERTS_MXFP4 : MOE_KERNEL_EXPERTS, [&] { int r = launch_dectc(L, x, T, out, 1, s); bad |= r < 0; return r < 0 ? 0 : r; });
+        run(L.mxfp4 ? MOE_KERNEL_EXPERTS_MXFP4 : MOE_KERNEL_EXPERTS, [&] { int r = launch_dectc(L, x, T, out, 1, s); bad |= r < 0; return r < 0 ? 0 : r; });
         if (rec) ++L.timing_recorded;
         cudaError_t e = cudaGetLastError();
         if (bad || e != cudaSuccess) return cuda_fail(e != cudaSuccess ? e : cudaErrorLaunchFailure, "decode launch");
@@ -601,7 +565,10 @@ moe_status moe_set_path(moe_layer *layer, int32_t path)
     if (path == MOE_PATH_DECODE_TC && !layer->dectc)
         return fail(MOE_ERR_UNSUPPORTED, "weight-streaming tensor-core path unavailable (needs the tensor-core path)");
     if (path == MOE_PATH_FUSED && layer->decode_grid == 0)
-        return fail(MOE_ERR_UNSUPPORTED, "cooperative launch unavailable on this device");
+        return fail(MOE_ERR_UNSUPPORTED, layer->mxfp4 ? "MXFP4 experts run on the tensor-core paths only"
+                                                      : "cooperative launch unavailable on this device");
+    if (path == MOE_PATH_STREAM && layer->mxfp4)
+        return fail(MOE_ERR_UNSUPPORTED, "MXFP4 experts run on the tensor-core paths only");
     if (path == MOE_PATH_TC && !layer->tc_capable) {
         std::string why;
         tc_supported(*layer, why);

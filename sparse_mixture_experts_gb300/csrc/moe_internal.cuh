@@ -85,7 +85,7 @@ struct Layer {
     void *h = nullptr;         // [Tmax*K + Tmax][Fmax] activations (routed rows sorted by expert, then shared)
     void *xp = nullptr;        // [Tmax*K + Tmax][H] x rows gathered in expert order, then x (tensor-core path)
     float *ys = nullptr;       // [Tmax][K+1][H] weighted expert outputs per (token, slot), fp32
-    bool mxfp4 = false;        // routed experts given in MXFP4 (gate_w/up_w/down_w hold their bf16 values)
+    bool mxfp4 = false;        // routed experts in MXFP4 (fp4_gu / fp4_dn; gate_w, up_w, down_w unused)
     int *gfirst = nullptr;     // [5][E + 2] per group: first gate/up tile (and the total), first down tile
                                // (and the total), expert (E = shared), rows, first row in the sorted buffers
     int *status = nullptr;     // DeviceError
@@ -103,13 +103,11 @@ struct Layer {
     float *dec_partials = nullptr;   // split-K partial sums
     float *dec_wtab = nullptr;       // [groups_max][16] routing weight of token t for group g
     int *dec_tickets = nullptr;      // per-tile arrival counters
-    // MXFP4 weight-streaming decode: the routed experts' codes and scales
-    // packed per (row block, 64-wide K block) so a pipeline stage is one
-    // contiguous copy of each; x in f16 for the token operand
-    bool fp4_decode = false;         // MXFP4 layer whose scales fit the f16 operand path
+    // MXFP4 experts: codes and scales packed per (row block, 64-wide K block)
+    // so that a pipeline stage is one contiguous copy; both tensor-core paths
+    // widen them to bf16 on chip
     uint8_t *fp4_gu = nullptr;       // [E][F/64][H/64] packed blocks (128 rows: 64 gate, 64 up; codes, scales)
     uint8_t *fp4_dn = nullptr;       // [E][ceil(H/128)][F/64] packed blocks
-    void *dec_x16 = nullptr;         // [16][H] f16 copy of the decode batch
 
     // per-kernel timing (moe_timing_enable / moe_timing_read)
     int timing_max = 0;         // forwards recorded per window; 0 = off

@@ -132,7 +132,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
 
 // the same with A in tensor memory: a_tmem addresses row i of A at lane i, its
 // K elements packed two 16-bit values per 32-bit column (even element low)
-__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void mma_ta(uint32_t tmem_d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
                                            uint32_t accumulate)
 {
     asm volatile(

@@ -307,29 +307,35 @@ MXFP4_SMALL = synth.GPTOSS_MXFP4.replace(name="gpt-oss-like, MXFP4 experts, smal
                                          expert_ff=192)
 
 
-@pytest.mark.parametrize("scales", ["synthetic", "range_edges", "below_range"])
-def test_mxfp4_decode_kernel_choice(scales):
-    """A decode batch on MXFP4 experts runs the kernel that streams the codes
-    and scales (timed as its own kind) while every E8M0 scale is in 113..140,
-    where its f16 operands are exact (the edges included: 2^-14 and 2^13);
-    one scale below that range sends the layer to the bf16 copy.  Each agrees
-    with the oracle on the same weights."""
-    spec, T = MXFP4_SMALL, 5
+@pytest.mark.parametrize("scales", ["synthetic", "spread_100_150", "edges"])
+@pytest.mark.parametrize("T", [5, 200])
+def test_mxfp4_scales_take_the_packed_path(scales, T):
+    """MXFP4 experts stay packed for every scale byte: a decode batch runs the
+    kernel that streams the codes and scales (timed as its own kind) and a
+    prefill batch the grouped GEMMs that widen them, and both agree with the
+    oracle on the same weights -- with the synthetic scales, with scales
+    spread over 100..150, and with the edge bytes 1 (subnormal products), 113
+    and 140, and 254 on blocks whose codes are all zero (so that no product
+    leaves the fp32 range)."""
+    spec = MXFP4_SMALL
     w = synth.make_weights(spec, seed=5)
-    low_scale = scales == "below_range"
-    if scales == "range_edges":
+    if scales == "spread_100_150":
         for name in ("gate_up_scales", "down_scales"):
-            s = w[name].copy()
-            s.flat[3::97] = 113
-            s.flat[11::89] = 140
-            w[name] = s
-    if low_scale:
-        s = w["down_scales"].copy()
-        s.flat[37] = 112
-        w["down_scales"] = s
+            r = synth.u64(w[name].size, 5, 77 if name == "down_scales" else 76)
+            w[name] = (100 + (r % np.uint64(51))).astype(np.uint8).reshape(w[name].shape)
+    if scales == "edges":
+        for name, blocks in (("gate_up_scales", "gate_up_blocks"), ("down_scales", "down_blocks")):
+            sc = w[name].copy()
+            sc.flat[3::97] = 113
+            sc.flat[11::89] = 140
+            sc.flat[5::53] = 1
+            b = w[blocks].copy().reshape(-1, 16)
+            zero = np.arange(sc.size)[7::61]
+            sc.flat[zero] = 254
+            b[zero] = 0
+            w[name], w[blocks] = sc, b.reshape(w[blocks].shape)
     x = synth.make_x(spec, T, seed=5)
-    layer = helpers.make_layer(spec, w, 16)
-    layer.set_path(moe.PATH_DECODE_TC)
+    layer = helpers.make_layer(spec, w, T)
     layer.timing_enable(4)
     out = layer.forward(helpers.to_torch(x)).float().cpu().numpy()
     kinds = layer.timing_read()
@@ -337,8 +343,10 @@ def test_mxfp4_decode_kernel_choice(scales):
     idx = idx.cpu().numpy()
     layer.status()
     layer.close()
-    want, other = ("experts", "experts_mxfp4") if low_scale else ("experts_mxfp4", "experts")
-    assert kinds[want][1] == 1 and kinds[other][1] == 0, kinds
+    if T <= DECODE_TC_MAX_TOKENS:
+        assert kinds["experts_mxfp4"][1] == 1 and kinds["experts"][1] == 0, kinds
+    else:
+        assert kinds["up"][1] == 1 and kinds["down"][1] == 1, kinds
     orc = oracle.Oracle(spec, w)
     mism, ties, invalid, _ = helpers.index_parity_all(orc, x, idx)
     assert not mism and not invalid
@@ -346,13 +354,37 @@ def test_mxfp4_decode_kernel_choice(scales):
     assert rep.ok(spec.dtype), str(rep)
 
 
+def test_mxfp4_layer_keeps_only_the_packed_experts():
+    """An MXFP4 gpt-oss-shaped layer holds its experts as codes and scales:
+    its device bytes are the packed experts plus the rest of the layer and the
+    workspace, far below the bf16 experts' 1.6 GB."""
+    spec = synth.GPTOSS_MXFP4
+    w = synth.make_weights(spec, seed=0)
+    layer = helpers.make_layer(spec, w, 16)
+    nbytes = layer.device_bytes
+    layer.close()
+    E, H, F = spec.n_expert, spec.hidden, spec.expert_ff
+    packed = E * 3 * H * F * (0.5 + 1 / 32)          # 423 MB
+    bf16_experts = E * 3 * H * F * 2                 # 1.59 GB
+    assert packed <= nbytes <= packed + 0.1e9, (nbytes, packed)
+    assert nbytes < 0.3 * bf16_experts
+
+
 @pytest.mark.parametrize("T", [1, 7, 16])
-def test_mxfp4_small_layer_all_paths_agree(T):
-    """Ragged decode batches on a small MXFP4 layer: the MXFP4 decode kernel
-    and the bf16-copy paths give the oracle's result."""
-    for path in PATHS:
+def test_mxfp4_small_layer_paths_agree(T):
+    """Ragged batches on a small MXFP4 layer: both tensor-core paths (the
+    weight-streaming decode kernel and the grouped GEMMs) give the oracle's
+    result; the CUDA-core paths, which read bf16 or fp32 weights only, are
+    refused."""
+    for path in (moe.PATH_DECODE_TC, moe.PATH_TC):
         rep = _small_case(MXFP4_SMALL, T, path, seed=9)
         assert rep.ok(MXFP4_SMALL.dtype), (path, str(rep))
+    layer = helpers.make_layer(MXFP4_SMALL, synth.make_weights(MXFP4_SMALL, seed=9), T)
+    for path in (moe.PATH_STREAM, moe.PATH_FUSED):
+        with pytest.raises(moe.MoEError) as ei:
+            layer.set_path(path)
+        assert ei.value.status == moe.ERR_UNSUPPORTED
+    layer.close()
 
 
 def _bf16_bits_to_f32(a):
