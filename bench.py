@@ -64,6 +64,7 @@ WORKLOADS = {
     "mixtral_decode": (synth.MIXTRAL, 1, (16, 256), 3),
     "mixtral_prefill": (synth.MIXTRAL, 4096, (16384,), 2),
     "gptoss_mxfp4_decode": (synth.GPTOSS_MXFP4, 1, (4, 16), 6),
+    "gptoss_mxfp4_prefill": (synth.GPTOSS_MXFP4, 2048, (64,), 3),
     "tiny": (synth.TINY, 16, (), 1),
 }
 

@@ -58,7 +58,8 @@ struct TcShape {
     static constexpr int TAB_OFF = STAGING_OFF + STAGING_BYTES;
     static constexpr int TAB_BYTES = FP4 ? 256 * (int)sizeof(Fp4Table) : 0;
     static constexpr size_t SMEM = (size_t)TAB_OFF + TAB_BYTES + 1024 /*align*/;
-    static constexpr int THREADS = FP4 ? TC_THREADS + 128 : TC_THREADS;  // + 4 dequantising warps
+    static constexpr int DQ_THREADS = FP4 ? 256 : 0;                     // dequantising warps: one B row each
+    static constexpr int THREADS = TC_THREADS + DQ_THREADS;
 };
 
 struct TensorMaps {
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(c
         }
         mbar_init(drain, 1);
         if (FP4)
-            for (int st = 0; st < TC_STAGES; ++st) mbar_init(&bready[st], 128);
+            for (int st = 0; st < TC_STAGES; ++st) mbar_init(&bready[st], Sh::DQ_THREADS);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -367,13 +368,13 @@ __global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(c
             }
         }
     } else if (FP4 && warp >= 6) {
-        // ------------------------------ MXFP4 dequantisation (warps 6..9) ------------------------------
-        // Per stage: the 256 rows of the B tile, two per thread, each 64 codes
+        // ------------------------------ MXFP4 dequantisation (warps 6..13) ------------------------------
+        // Per stage: the 256 rows of the B tile, one per thread, each 64 codes
         // widened exactly to bf16 and written as eight 16-byte chunks at their
         // 128-byte-swizzle positions (chunk j of row r at r * 128 + ((j ^ (r & 7)) << 4),
         // the layout the TMA would have written).  Then the writes are made
         // visible to the tensor cores' reads and the stage is released to the MMA.
-        const int dt = threadIdx.x - TC_THREADS;  // 0 .. 127
+        const int rr = threadIdx.x - TC_THREADS;  // the B-tile row of this thread: 0 .. 255
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
@@ -391,25 +392,21 @@ __global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(c
                 }
                 uint8_t *bt = smem + stage * STAGE_BYTES + A_TILE_BYTES;
                 const uint8_t *raw = bt + B_TILE_BYTES;
+                int q, brow;  // the packed block of the tile holding row rr, and the row in it
+                if (EPI == EPI_UP) {
+                    const int f = rr & 127;
+                    q = f >> 6;
+                    brow = (rr < 128 ? 0 : 64) + (f & 63);
+                } else {
+                    q = rr >> 7;
+                    brow = rr & 127;
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(bt + rr * 128);
+                const uint8_t *pb = raw + q * TC_FP4_BLK;
+                if (b0 + q >= nb) {
 #pragma unroll
-                for (int rr0 = 0; rr0 < 256; rr0 += 128) {
-                    const int rr = rr0 + dt;
-                    int q, brow;  // packed block of the tile, row in it
-                    if (EPI == EPI_UP) {
-                        const int f = rr & 127;
-                        q = f >> 6;
-                        brow = (rr < 128 ? 0 : 64) + (f & 63);
-                    } else {
-                        q = rr >> 7;
-                        brow = rr & 127;
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(bt + rr * 128);
-                    if (b0 + q >= nb) {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) dst[j ^ (rr & 7)] = make_uint4(0, 0, 0, 0);
-                        continue;
-                    }
-                    const uint8_t *pb = raw + q * TC_FP4_BLK;
+                    for (int j = 0; j < 8; ++j) dst[j ^ (rr & 7)] = make_uint4(0, 0, 0, 0);
+                } else {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint4 c = *reinterpret_cast<const uint4 *>(pb + (h * 128 + brow) * 16);
