@@ -110,7 +110,7 @@ constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
 constexpr int DT_SATURATING_CTAS = 128;         // CTAs streaming at once that saturate HBM
 constexpr int DT_UP_MIN_KB = 8;                 // smallest gate/up split, in 64-wide K blocks
 constexpr int DT_DOWN_GUIDE = 1;                // down ranges: a round of units takes 1/GUIDE of the K blocks left
-constexpr int DT_DOWN_MIN_KB = 16;              // smallest down range, in 64-wide K blocks (but the last)
+constexpr int DT_DOWN_MIN_KB = 8;               // smallest down range, in 64-wide K blocks (but the last)
 constexpr int DT_MAX_DOWN_SPLITS = 64;
 constexpr int DT_CLAIM_AHEAD = 4;               // stages before a unit's end at which the next one is claimed
 constexpr int DT_TICKET_DOWN = 8192;            // offset of the down tiles' tickets
