@@ -10,6 +10,7 @@ from __future__ import annotations
 import ctypes
 import dataclasses
 import os
+import sys
 from typing import Optional
 
 import torch
@@ -254,6 +255,12 @@ class MoELayer:
             self._h = ctypes.c_void_p()
 
     def __del__(self):
+        # At interpreter shutdown the CUDA runtime may already be tearing down;
+        # destroying the layer then (it synchronises the device and frees
+        # memory) can crash the process, and process exit frees the memory
+        # anyway.  Layers closed explicitly are unaffected.
+        if sys.is_finalizing():
+            return
         try:
             self.close()
         except Exception:
