@@ -86,6 +86,10 @@ def _get():
             lib.orc_e8m0_scale.restype = ctypes.c_double
             lib.orc_mxfp4_dequant.argtypes = [VP, VP, ctypes.c_int64, I, VP]
             lib.orc_mxfp4_dequant.restype = ctypes.c_int
+            lib.orc_fp16_value.argtypes = [ctypes.c_uint]
+            lib.orc_fp16_value.restype = ctypes.c_double
+            lib.orc_q4_dequant.argtypes = [VP, ctypes.c_int64, I, VP]
+            lib.orc_q4_dequant.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -119,9 +123,41 @@ def mxfp4_dequant(blocks: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return out
 
 
+def fp16_value(h: int) -> float:
+    """Value of one binary16 bit pattern."""
+    return _get().orc_fp16_value(int(h))
+
+
+def q4_dequant(blocks: np.ndarray) -> np.ndarray:
+    """[..., cols/32, 18] uint8 Q4 blocks -> [..., cols] float32 (exact)."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    if blocks.shape[-1] != 18:
+        raise ValueError("blocks must be [..., nb, 18]")
+    nb = blocks.shape[-2]
+    rows = int(np.prod(blocks.shape[:-2]))
+    out = np.empty(blocks.shape[:-2] + (nb * 32,), dtype=np.float32)
+    if _get().orc_q4_dequant(_p(blocks), rows, nb * 32, _p(out)) != 0:
+        raise ValueError("bad Q4 tensor")
+    return out
+
+
 def _bf16_to_f32(a: np.ndarray) -> np.ndarray:
     a = np.ascontiguousarray(a, dtype=np.uint16)
     return (a.astype(np.uint32) << 16).view(np.float32)
+
+
+def dense_weights_of_q4(weights: dict) -> dict:
+    """The float32 weights a layer with Q4 expert records stands for: the
+    routed experts dequantised, every bf16 tensor widened (both exact)."""
+    w = {}
+    for n, a in weights.items():
+        if n.endswith("_q4"):
+            continue
+        w[n] = _bf16_to_f32(a)
+    for n in ("gate_up_w", "gate_w", "up_w", "down_w"):
+        if n + "_q4" in weights:
+            w[n] = q4_dequant(weights[n + "_q4"])
+    return w
 
 
 def dense_weights_of_mxfp4(weights: dict) -> dict:
@@ -153,10 +189,13 @@ class Oracle:
         c.act_alpha, c.act_limit = float(spec.act_alpha), float(spec.act_limit)
         c.has_bias = int(spec.has_bias)
         c.gate_up_interleaved = int(spec.gate_up_interleaved)
-        mx = getattr(spec, "expert_format", "dense") == "mxfp4"
-        if mx:
+        fmt = getattr(spec, "expert_format", "dense")
+        mx = fmt in ("mxfp4", "q4")
+        if fmt == "mxfp4":
             # MXFP4 experts: the layer is evaluated on its exact float32 expansion
             weights = dense_weights_of_mxfp4(weights)
+        elif fmt == "q4":
+            weights = dense_weights_of_q4(weights)
         c.w_dtype = DTYPES["f32" if mx else spec.dtype]
         c.x_dtype = DTYPES[spec.dtype]
         self._c = c

@@ -354,3 +354,39 @@ int orc_mxfp4_dequant(const uint8_t *blocks, const uint8_t *scales, int64_t rows
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Q4 records ("Engine" (cherenkov), section "Prefill": Q4 GEMMs with half
+ * weights and float accumulation; "Qwen3.5-MoE Model Implementation", KV
+ * Cache: ggml-Q4_0 rows).  A row is cols/32 blocks of 18 bytes: a half
+ * (IEEE binary16, little-endian) scale d, then 16 bytes of codes, byte j
+ * holding element j in its low nibble and element j + 16 in its high
+ * nibble; element = (code - 8) * d.
+ * ---------------------------------------------------------------------- */
+double orc_fp16_value(unsigned h)
+{
+    const int sign = (h >> 15) & 1, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)m, -24);                 /* zero and subnormals */
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+int orc_q4_dequant(const uint8_t *blocks, int64_t rows, int cols, float *out)
+{
+    if (!blocks || !out || rows < 0 || cols <= 0 || cols % 32) return -1;
+    const int nb = cols / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int b = 0; b < nb; ++b) {
+            const uint8_t *blk = blocks + (r * nb + b) * 18;
+            const double d = orc_fp16_value((unsigned)blk[0] | ((unsigned)blk[1] << 8));
+            for (int j = 0; j < 32; ++j) {
+                const unsigned byte = blk[2 + (j & 15)];
+                const unsigned code = j < 16 ? (byte & 15u) : (byte >> 4);
+                out[r * cols + b * 32 + j] = (float)(((double)code - 8.0) * d);  /* exact in float */
+            }
+        }
+    }
+    return 0;
+}

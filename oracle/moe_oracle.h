@@ -143,6 +143,17 @@ double orc_e2m1_value(unsigned code);
 double orc_e8m0_scale(unsigned e8m0);
 int orc_mxfp4_dequant(const uint8_t *blocks, const uint8_t *scales, int64_t rows, int cols, float *out);
 
+/* Q4 records ("Engine" (cherenkov), section "Prefill"; the ggml-Q4_0 rows of
+ * "Qwen3.5-MoE Model Implementation", KV Cache): a row of cols elements is
+ * cols/32 blocks of 18 bytes -- a binary16 scale d (little-endian), then 16
+ * bytes whose byte j holds element j (low nibble) and element j + 16 (high
+ * nibble); element = (code - 8) * d.
+ * orc_fp16_value: the value of one binary16 bit pattern (exact).
+ * orc_q4_dequant: out[rows][cols] (every value is exact in float: a 4-bit
+ * integer times an 11-bit significand). */
+double orc_fp16_value(unsigned h);
+int orc_q4_dequant(const uint8_t *blocks, int64_t rows, int cols, float *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -152,7 +152,7 @@ class LayerSpec:
     dtype: str = "bf16"                    # weights and activations: "f32" / "bf16"
     router_init: str = "normal"            # "normal" / "uniform" / "zipf"
     zipf_s: float = 1.1
-    expert_format: str = "dense"           # "dense" (dtype) or "mxfp4" (routed experts; rest bf16)
+    expert_format: str = "dense"           # "dense" (dtype), "mxfp4" or "q4" (routed experts; rest bf16)
 
     def replace(self, **kw) -> "LayerSpec":
         return dataclasses.replace(self, **kw)
@@ -168,6 +168,11 @@ MIXTRAL = LayerSpec("mixtral-shaped (H=4096, E=8, top-2, F=14336)", 4096, 8, 2, 
 GPTOSS_MXFP4 = GPTOSS.replace(name="gpt-oss-20b-shaped, MXFP4 experts (H=2880, E=32, top-4, F=2880, biases)",
                               expert_format="mxfp4")
 
+QWEN_Q4 = QWEN.replace(name="qwen35moe-shaped routed experts, Q4 records (H=2048, E=256, top-8, F=512)",
+                       shared_ff=0, expert_format="q4")
+GPTOSS_Q4 = GPTOSS.replace(name="gpt-oss-20b-shaped, Q4 expert records (H=2880, E=32, top-4, F=2880, biases)",
+                           expert_format="q4")
+
 # workload -> token counts exercised
 WORKLOADS = {
     "tiny": (TINY, (16,)),
@@ -176,12 +181,15 @@ WORKLOADS = {
     "gptoss": (GPTOSS, (1, 64, 2048)),
     "mixtral": (MIXTRAL, (1, 16, 256, 4096, 16384)),
     "gptoss_mxfp4": (GPTOSS_MXFP4, (1, 4, 16, 64)),
+    "qwen_q4": (QWEN_Q4, (1, 8, 300)),
+    "gptoss_q4": (GPTOSS_Q4, (1, 16, 2048)),
 }
 
 # stream ids, one per tensor
 _S = dict(router_w=1, router_b=2, gate_w=3, up_w=4, gate_up_w=5, gate_up_b=6, down_w=7, down_b=8,
           sh_gate_w=9, sh_up_w=10, sh_down_w=11, sh_gate_inp=12, zipf_perm=20, zipf_dir=21,
-          gate_up_blocks=30, gate_up_scales=31, down_blocks=32, down_scales=33, x=100)
+          gate_up_blocks=30, gate_up_scales=31, down_blocks=32, down_scales=33,
+          gate_up_q4=40, gate_q4=41, up_q4=42, down_q4=43, q4_scales=44, x=100)
 _ZIPF_ALPHA = 8.0
 _BIAS_STD = math.sqrt(0.02)
 
@@ -214,6 +222,25 @@ def _mxfp4(rows_shape, cols: int, seed: int, blocks_stream: int, scales_stream: 
     return blocks, scales
 
 
+def _q4(rows_shape, cols: int, seed: int, stream: int):
+    """Q4 records [*rows_shape][cols/32][18]: per block a binary16 scale d
+    (little-endian) and 16 bytes of uniformly drawn 4-bit codes.  The codes
+    minus 8 have RMS 4.64, so d = 2^u / (4.64 sqrt(cols)) with u uniform in
+    [-0.5, 0.5) per block gives values of RMS near 1/sqrt(cols), like the
+    dense layers."""
+    nb = cols // 32
+    n = int(np.prod(rows_shape)) * nb
+    raw = u64((n * 16 + 7) // 8, seed, stream)
+    codes = raw.view(np.uint8)[: n * 16].reshape(n, 16)
+    u = (u64(n, seed, _S["q4_scales"] * 1000 + stream) >> np.uint64(11)).astype(np.float64) / float(1 << 53)
+    d = (np.exp2(u - 0.5) / (4.64 * math.sqrt(cols))).astype(np.float16).view(np.uint16)
+    out = np.empty((n, 18), dtype=np.uint8)
+    out[:, 0] = (d & 0xFF).astype(np.uint8)
+    out[:, 1] = (d >> 8).astype(np.uint8)
+    out[:, 2:] = codes
+    return out.reshape(tuple(rows_shape) + (nb, 18))
+
+
 def make_weights(spec: LayerSpec, seed: int = 0) -> dict:
     """All weight/bias tensors of one layer as numpy arrays (float32, or
     uint16 bf16 bit patterns when spec.dtype == "bf16").  With
@@ -226,6 +253,9 @@ def make_weights(spec: LayerSpec, seed: int = 0) -> dict:
     if spec.expert_format == "mxfp4":
         if dt != "bf16" or not spec.gate_up_interleaved or Fs or H % 32 or F % 32:
             raise ValueError("mxfp4 layers: bf16, interleaved gate_up, no shared expert, H and F multiples of 32")
+    if spec.expert_format == "q4":
+        if dt != "bf16" or Fs or H % 32 or F % 32:
+            raise ValueError("q4 layers: bf16, no shared expert, H and F multiples of 32")
     if spec.router_init == "uniform":
         a = math.sqrt(3.0 / H)
         w["router_w"] = uniform((E, H), -a, a, seed, _S["router_w"], dt)
@@ -244,6 +274,14 @@ def make_weights(spec: LayerSpec, seed: int = 0) -> dict:
         w["gate_up_blocks"], w["gate_up_scales"] = _mxfp4((E, 2 * F), H, seed, _S["gate_up_blocks"],
                                                           _S["gate_up_scales"])
         w["down_blocks"], w["down_scales"] = _mxfp4((E, H), F, seed, _S["down_blocks"], _S["down_scales"])
+        return w
+    if spec.expert_format == "q4":
+        if spec.gate_up_interleaved:
+            w["gate_up_w_q4"] = _q4((E, 2 * F), H, seed, _S["gate_up_q4"])
+        else:
+            w["gate_w_q4"] = _q4((E, F), H, seed, _S["gate_q4"])
+            w["up_w_q4"] = _q4((E, F), H, seed, _S["up_q4"])
+        w["down_w_q4"] = _q4((E, H), F, seed, _S["down_q4"])
         return w
     if spec.gate_up_interleaved:
         w["gate_up_w"] = normal((E, 2 * F, H), 1.0 / math.sqrt(H), seed, _S["gate_up_w"], dt)
@@ -277,6 +315,9 @@ def weight_bytes_per_expert(spec: LayerSpec) -> int:
     if spec.expert_format == "mxfp4":
         n = 3 * spec.hidden * spec.expert_ff  # codes: half a byte each; a scale byte per 32
         return n // 2 + n // 32 + (2 * spec.expert_ff + spec.hidden) * 2
+    if spec.expert_format == "q4":
+        n = 3 * spec.hidden * spec.expert_ff  # 18 bytes per 32 elements
+        return n // 32 * 18 + ((2 * spec.expert_ff + spec.hidden) * 2 if spec.has_bias else 0)
     el = 2 if spec.dtype == "bf16" else 4
     n = 3 * spec.hidden * spec.expert_ff
     if spec.has_bias:

@@ -530,3 +530,80 @@ def test_mxfp4_layer_equals_dense_layer_of_its_values():
     out_d, idx_d, _ = oracle.Oracle(dspec, dense).forward(synth.bf16_to_f32(x))
     np.testing.assert_array_equal(idx_mx, idx_d)
     np.testing.assert_array_equal(out_mx, out_d)
+
+
+# ----------------------------------------------------------------------------
+# Q4 records: binary16 scale, 32 four-bit codes offset by 8, element j in the
+# low nibble of byte j and element j + 16 in its high nibble
+# ----------------------------------------------------------------------------
+
+def test_fp16_values():
+    assert oracle.fp16_value(0x3C00) == 1.0 and oracle.fp16_value(0xC000) == -2.0
+    assert oracle.fp16_value(0x3800) == 0.5 and oracle.fp16_value(0x3E00) == 1.5
+    assert oracle.fp16_value(0x7BFF) == 65504.0           # largest finite
+    assert oracle.fp16_value(0x0400) == 2.0 ** -14         # smallest normal
+    assert oracle.fp16_value(0x0001) == 2.0 ** -24         # smallest subnormal
+    assert oracle.fp16_value(0x0000) == 0.0 and math.copysign(1.0, oracle.fp16_value(0x8000)) == -1.0
+    assert math.isinf(oracle.fp16_value(0x7C00)) and math.isnan(oracle.fp16_value(0x7E00))
+    # every pattern agrees with numpy's binary16
+    pats = np.arange(1 << 16, dtype=np.uint16)
+    ref = pats.view(np.float16).astype(np.float64)
+    got = np.array([oracle.fp16_value(int(h)) for h in pats[::97]])
+    np.testing.assert_array_equal(got, ref[::97])
+
+
+def test_q4_block_hand_worked():
+    # d = 0.5; byte j holds code j (element j) and code 15 - j (element j + 16)
+    blk = np.zeros((1, 1, 18), np.uint8)
+    blk[0, 0, 0], blk[0, 0, 1] = 0x00, 0x38               # 0x3800 little-endian
+    for j in range(16):
+        blk[0, 0, 2 + j] = j | ((15 - j) << 4)
+    v = oracle.q4_dequant(blk)[0]
+    assert v[:16].tolist() == [(j - 8) * 0.5 for j in range(16)]      # -4.0 .. 3.5
+    assert v[16:].tolist() == [(15 - j - 8) * 0.5 for j in range(16)]  # 3.5 .. -4.0
+    assert v[8] == 0.0 and v[0] == -4.0                                # code 8 is zero
+
+
+def test_q4_block_direction_and_scale_per_block():
+    # two blocks along the input dimension, each with its own scale
+    blk = np.zeros((1, 2, 18), np.uint8)
+    blk[0, 0, :2] = [0x00, 0x3C]    # d = 1
+    blk[0, 1, :2] = [0x00, 0xC0]    # d = -2
+    blk[0, :, 2:] = 0x88            # every code 8 -> 0
+    blk[0, 0, 2] = 0x09             # element 0 = code 9 (+1), element 16 = code 0 (-8)
+    blk[0, 1, 17] = 0xF8            # element 32 + 15 = code 8 (0), element 32 + 31 = code 15 (+7)
+    v = oracle.q4_dequant(blk)[0]
+    assert v[0] == 1.0 and v[16] == -8.0 and v[63] == -14.0
+    assert np.count_nonzero(v) == 3
+
+
+def _numpy_q4(blocks):
+    """The same definition restated with numpy bit operations."""
+    d = (blocks[..., 0].astype(np.uint16) | (blocks[..., 1].astype(np.uint16) << 8)).view(np.float16)
+    q = blocks[..., 2:]
+    codes = np.concatenate([q & 0x0F, q >> 4], axis=-1).astype(np.float64) - 8.0
+    vals = codes * d.astype(np.float64)[..., None]
+    return vals.reshape(blocks.shape[:-2] + (blocks.shape[-2] * 32,))
+
+
+def test_q4_dequant_matches_numpy_restatement():
+    spec = synth.QWEN_Q4.replace(hidden=96, n_expert=3, expert_ff=64, top_k=2)
+    w = synth.make_weights(spec, seed=3)
+    for n in ("gate_w_q4", "up_w_q4", "down_w_q4"):
+        np.testing.assert_array_equal(oracle.q4_dequant(w[n]), _numpy_q4(w[n]))
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_q4_layer_equals_dense_layer_of_its_values(interleaved):
+    spec = synth.QWEN_Q4.replace(hidden=64, n_expert=4, expert_ff=64, top_k=2, gate_up_interleaved=interleaved)
+    w = synth.make_weights(spec, seed=5)
+    dense = {k: synth.bf16_to_f32(v) for k, v in w.items() if v.dtype == np.uint16}
+    for n in ("gate_up_w", "gate_w", "up_w", "down_w"):
+        if n + "_q4" in w:
+            dense[n] = _numpy_q4(w[n + "_q4"]).astype(np.float32)
+    x = synth.make_x(spec, 5, seed=2)
+    out_q, idx_q, _ = oracle.Oracle(spec, w).forward(x)
+    dspec = spec.replace(dtype="f32", expert_format="dense")
+    out_d, idx_d, _ = oracle.Oracle(dspec, dense).forward(synth.bf16_to_f32(x))
+    np.testing.assert_array_equal(idx_q, idx_d)
+    np.testing.assert_array_equal(out_q, out_d)
