@@ -65,6 +65,8 @@ WORKLOADS = {
     "mixtral_prefill": (synth.MIXTRAL, 4096, (16384,), 2),
     "gptoss_mxfp4_decode": (synth.GPTOSS_MXFP4, 1, (4, 16), 6),
     "gptoss_mxfp4_prefill": (synth.GPTOSS_MXFP4, 2048, (64,), 3),
+    "qwen_q4_decode": (synth.QWEN_Q4, 8, (1,), 8),
+    "gptoss_q4_prefill": (synth.GPTOSS_Q4, 2048, (16,), 3),
     "tiny": (synth.TINY, 16, (), 1),
 }
 
@@ -75,6 +77,8 @@ SWEEP = {
     "qwen35moe_prefill_zipf": (synth.QWEN_ZIPF, (4096,), 4),
     "gptoss20b": (synth.GPTOSS, (1, 64, 2048), 4),
     "gptoss20b_mxfp4": (synth.GPTOSS_MXFP4, (1, 4, 16, 64, 2048), 4),
+    "qwen35moe_q4": (synth.QWEN_Q4, (1, 8, 300), 8),
+    "gptoss20b_q4": (synth.GPTOSS_Q4, (1, 16, 2048), 4),
     "mixtral": (synth.MIXTRAL, (1, 16, 256, 4096, 16384), 2),
 }
 # the headline workload's sweep entry (measured once, reported in both places)
@@ -265,6 +269,8 @@ def cpu_baselines(spec, w, budget_all: float, budget_one: float):
 def _spec_dtype(spec):
     if spec.expert_format == "mxfp4":
         return "mxfp4-bf16"  # MXFP4 expert weights widened to bf16 on chip for the MMA, fp32 accumulation
+    if spec.expert_format == "q4":
+        return "q4-bf16"     # Q4 expert records widened (rounded) to bf16 on chip, fp32 accumulation
     return "bf16" if spec.dtype == "bf16" else "f32"
 
 
@@ -342,10 +348,11 @@ class Model:
 
     def __init__(self, spec):
         self.spec = spec
-        self.mx = spec.expert_format == "mxfp4"
+        self.mx = spec.expert_format in ("mxfp4", "q4")
         self.eb = 2 if spec.dtype == "bf16" else 4
         H, F, Fs, E = spec.hidden, spec.expert_ff, spec.shared_ff, spec.n_expert
-        wel = (0.5 + 1.0 / 32) if self.mx else self.eb  # MXFP4: half a byte per code, a scale byte per 32
+        # MXFP4: half a byte per code and a scale byte per 32; Q4: a two-byte scale per 32
+        wel = {"mxfp4": 0.5 + 1.0 / 32, "q4": 0.5 + 2.0 / 32}.get(spec.expert_format, self.eb)
         self.up_per_expert = 2 * F * H * wel + (2 * F * 4 if spec.has_bias else 0)
         self.down_per_expert = H * F * wel + (H * 4 if spec.has_bias else 0)
         self.router = (E + (1 if Fs else 0)) * H * self.eb
@@ -366,7 +373,7 @@ class Model:
         H, F, Fs, K = s.hidden, s.expert_ff, s.shared_ff, s.top_k
         rows = T * K + (T if Fs else 0)              # routed rows + the shared expert's
         hbytes = rows * max(F, Fs) * 2               # h, bf16
-        if kind in ("experts", "experts_mxfp4"):     # decode: the whole layer after the router
+        if kind in ("experts", "experts_mxfp4", "experts_q4"):  # decode: the whole layer after the router
             return self.step_bytes(T, d) - self.router, self.step_flops(T) - 2.0 * T * H * s.n_expert
         if kind == "fused":
             return self.step_bytes(T, d), self.step_flops(T)
@@ -426,6 +433,10 @@ class Runner:
         if self.mxfp4:  # the ABI takes the MXFP4 blocks in the gate_up_w / down_w slots
             wt["gate_up_w"] = wt.pop("gate_up_blocks")
             wt["down_w"] = wt.pop("down_blocks")
+        self.q4 = spec.expert_format == "q4"
+        if self.q4:  # and the Q4 records in the slots of the tensors they stand for
+            for k in [k for k in wt if k.endswith("_q4")]:
+                wt[k[:-3]] = wt.pop(k)
         cfg = moe.MoEConfig(
             hidden=spec.hidden, n_expert=spec.n_expert, top_k=spec.top_k, expert_ff=spec.expert_ff,
             shared_ff=spec.shared_ff,
@@ -433,7 +444,8 @@ class Runner:
             norm_topk_prob=spec.norm_topk_prob, weights_scale=spec.weights_scale,
             act=moe.ACT_SWIGLU if spec.act == "swiglu" else moe.ACT_CLAMP_GLU, act_alpha=spec.act_alpha,
             act_limit=spec.act_limit, has_bias=spec.has_bias, gate_up_interleaved=spec.gate_up_interleaved,
-            w_dtype=moe.DT_MXFP4 if self.mxfp4 else (moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32),
+            w_dtype=moe.DT_MXFP4 if self.mxfp4 else moe.DT_Q4 if self.q4 else (
+                moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32),
             act_dtype=moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32, out_dtype=moe.DT_F32, max_tokens=Tmax)
         self.layers = [moe.MoELayer(cfg, wt, device=dev) for _ in range(n_layers)]
         del wt
@@ -552,7 +564,7 @@ class Runner:
         tc, tc_kind = (self.tc_sustained, "sustained") if capped and self.tc_sustained else (self.tc_burst, "burst")
         t_hbm, t_tc = sb / (self.hbm * 1e9), sf / (tc * 1e12)
         floor = max(t_hbm, t_tc) if self.spec.dtype == "bf16" else t_hbm
-        if "experts" in kernels or "experts_mxfp4" in kernels:
+        if "experts" in kernels or "experts_mxfp4" in kernels or "experts_q4" in kernels:
             path = "weight-streaming tensor-core"
         elif "fused" in kernels:
             path = "fused"

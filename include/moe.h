@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 4
+#define MOE_ABI_VERSION 5
 
 typedef enum {
     MOE_OK = 0,
@@ -85,7 +85,27 @@ typedef enum {
      * weights, up to rounding order.  MOE_PATH_STREAM and MOE_PATH_FUSED are
      * UNSUPPORTED for such a layer, and create is UNSUPPORTED on a device
      * without the tensor-core kernels. */
-    MOE_DT_MXFP4 = 2
+    MOE_DT_MXFP4 = 2,
+    /* w_dtype only: the routed experts as Q4 records ("Engine" (cherenkov),
+     * section "Prefill": Q4 expert GEMMs with half weights and float
+     * accumulation; the record layout read as the ggml-Q4_0 rows named in
+     * "Qwen3.5-MoE Model Implementation", KV Cache).  A record covers 32 consecutive K elements of
+     * one row in 18 bytes: a little-endian binary16 scale d, then 16 bytes
+     * whose byte j holds element j in its low nibble and element j + 16 in
+     * its high nibble; element value = (code - 8) * d.  gate_up_w (or gate_w
+     * and up_w), and down_w, hold the records ([E][2F][H/32][18], or
+     * [E][F][H/32][18] each, and [E][H][F/32][18] bytes); the router and the
+     * biases are bf16 and act_dtype must be bf16.  Requires shared_ff = 0
+     * and H, F multiples of 64; gate_up_scales and down_scales stay NULL.
+     * The layer keeps only the records, repacked per 128-row, 64-wide K
+     * block (codes, then the scales); both tensor-core paths widen them on
+     * chip to bf16, each weight (code - 8) * d computed exactly in fp32 and
+     * rounded once to bf16 (round to nearest even), because the tensor
+     * cores multiply the bf16 activations with operands of the same type.
+     * The result equals the bf16 layer built from those rounded weights, up
+     * to rounding order.  The paths and devices supported are those of
+     * MOE_DT_MXFP4. */
+    MOE_DT_Q4 = 3
 } moe_dtype;
 
 typedef enum {
@@ -118,8 +138,8 @@ typedef struct {
     float act_limit;             /* MOE_ACT_CLAMP_GLU: 7.0 */
     int32_t has_bias;            /* router [E], gate_up [E][2F], down [E][H] biases */
     int32_t gate_up_interleaved; /* 1: one [E][2F][H] gate_up tensor, gate = even rows */
-    int32_t w_dtype;             /* moe_dtype of every weight and bias (MOE_DT_MXFP4: see moe_dtype) */
-    int32_t act_dtype;           /* moe_dtype of x; must equal w_dtype (bf16 with MOE_DT_MXFP4) */
+    int32_t w_dtype;             /* moe_dtype of every weight and bias (MOE_DT_MXFP4, MOE_DT_Q4: see moe_dtype) */
+    int32_t act_dtype;           /* moe_dtype of x; must equal w_dtype (bf16 with MOE_DT_MXFP4, MOE_DT_Q4) */
     int32_t out_dtype;           /* moe_dtype of out */
     int32_t max_tokens;          /* workspace is sized once for this many tokens */
 } moe_config;
@@ -251,7 +271,8 @@ typedef enum {
     MOE_KERNEL_EXPERTS = 8,  /* selection, gate/up and down in one persistent kernel
                                 (weight-streaming tensor-core decode path) */
     MOE_KERNEL_EXPERTS_MXFP4 = 9, /* the same kernel streaming MXFP4 codes and scales */
-    MOE_KERNEL_COUNT = 10
+    MOE_KERNEL_EXPERTS_Q4 = 10,   /* the same kernel streaming Q4 records */
+    MOE_KERNEL_COUNT = 11
 } moe_kernel_kind;
 
 /* Synchronises the device, then writes, per kernel kind, the summed device

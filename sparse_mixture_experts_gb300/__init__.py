@@ -22,13 +22,13 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OOM, ERR_CUDA, ERR_TOO_MANY_TOKENS, ERR_DEVICE_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 _STATUS_NAMES = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "OOM", -4: "CUDA", -5: "TOO_MANY_TOKENS",
                  -6: "DEVICE_TIMEOUT"}
-DT_F32, DT_BF16, DT_MXFP4 = 0, 1, 2
+DT_F32, DT_BF16, DT_MXFP4, DT_Q4 = 0, 1, 2, 3
 ROUTER_SOFTMAX_TOPK, ROUTER_TOPK_SOFTMAX = 0, 1
 ACT_SWIGLU, ACT_CLAMP_GLU = 0, 1
 PATH_AUTO, PATH_STREAM, PATH_TC, PATH_FUSED, PATH_DECODE_TC = 0, 1, 2, 3, 4
 INTER_OFFSETS, INTER_PERM, INTER_H, INTER_YS = 0, 1, 2, 3
 KERNEL_KINDS = ("router", "select", "group", "up", "down", "combine", "gather", "fused", "experts",
-                "experts_mxfp4")
+                "experts_mxfp4", "experts_q4")
 
 _DT = {"f32": DT_F32, "bf16": DT_BF16}
 _TORCH_DT = {DT_F32: torch.float32, DT_BF16: torch.bfloat16}
@@ -144,7 +144,9 @@ class MoELayer:
     tensors (device or host) in the config's weight dtype; they are copied at
     creation.  With ``w_dtype == DT_MXFP4`` the expert weights are uint8
     tensors: gate_up_w / down_w the MXFP4 blocks, gate_up_scales /
-    down_scales the E8M0 scales (the rest bf16; see include/moe.h)."""
+    down_scales the E8M0 scales; with ``w_dtype == DT_Q4`` gate_up_w (or
+    gate_w and up_w) and down_w are uint8 tensors of 18-byte Q4 records (the
+    rest bf16; see include/moe.h)."""
 
     def __init__(self, config: MoEConfig, weights: dict, device: Optional[torch.device] = None):
         lib = load_library()
@@ -165,6 +167,7 @@ class MoELayer:
         self._h = handle
         self.out_dtype = _TORCH_DT[config.out_dtype]
         self.mxfp4 = config.w_dtype == DT_MXFP4
+        self.q4 = config.w_dtype == DT_Q4
         self.x_dtype = _TORCH_DT[config.act_dtype]
 
     # ------------------------------------------------------------------

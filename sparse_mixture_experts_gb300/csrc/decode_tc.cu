@@ -42,7 +42,7 @@
 #include <cudaTypedefs.h>
 
 #include "moe_internal.cuh"
-#include "mxfp4.cuh"
+#include "lowbit.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -58,12 +58,12 @@ constexpr int DT_EP_LD = DT_TOK + 1;            // row pitch (floats) of the epi
 constexpr int DT_XCH_BYTES = 128 * DT_EP_LD * 4; // the accumulator tile in shared memory
 constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
 // MXFP4 weights: a stage is DT_FP4_KPS 64-wide K blocks, each a token tile and
-// one packed block of codes and scales (DT_FP4_BLK bytes for 128 rows x 64 K);
+// one packed block of codes and scales (128 rows x 64 K; see lowbit.cuh);
 // with two blocks per stage a unit's odd last block makes a one-block stage and
 // the blocks of a stage may come from different groups (down units).  Two
 // blocks per stage measured no faster than one, so one is used.  The
 // producer's ring holds DT_FP4_RS stages.  Eight more warps widen each block to
-// bf16 (exactly, for every scale byte: a table lookup per code, see mxfp4.cuh)
+// bf16 (exactly, for every scale byte: a table lookup per code, see lowbit.cuh)
 // and store it straight into tensor memory, where the MMA reads its A operand
 // (DT_FP4_AS tiles of 32 columns per K block); the token operand is x and h'
 // in bf16 as for bf16 weights.  The widened tile never touches shared memory,
@@ -71,7 +71,6 @@ constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
 // What bounds this pipeline instead is the length of each role's per-stage
 // instruction path (one warp or thread per stage), hence several producer
 // threads, two dequantising groups and two MMA threads taking stages in turn.
-constexpr int DT_FP4_BLK = 128 * 32 + 128 * 2;  // codes [2 halves][128 rows][16 B], scales [2 halves][128 rows]
 constexpr int DT_FP4_KPS = 1;                   // K blocks per stage (1 or 2)
 constexpr int DT_FP4_RS = 24;                   // raw stages
 constexpr int DT_FP4_AS = 8;                    // A tiles (stages) in tensor memory, 32 columns per K block
@@ -81,8 +80,12 @@ constexpr int DT_FP4_DQG = 2;                   // dequantising groups of 4 warp
 constexpr int DT_FP4_A_COL = 256;               // first A-tile column (accumulators use 0..255)
 constexpr int DT_FP4_TMEM_COLS = 512;
 
-template <bool FP4>
+// QF: the routed experts' format -- 0 bf16 (TMA tiles), 1 MXFP4, 2 Q4 (packed
+// low-bit blocks, widened to bf16 in tensor memory)
+template <int QF>
 struct DtShape {
+    static constexpr bool FP4 = QF != 0;  // packed low-bit weights (either format)
+    static constexpr int BLK = QF == 2 ? LOWBIT_BLK_Q4 : LOWBIT_BLK_MXFP4;  // bytes of a packed block
     // bf16: producer, MMA, 4 epilogue warps; MXFP4: + 8 dequantising warps, a second MMA warp and a
     // warp of three more producer threads
     static constexpr int THREADS = FP4 ? DT_THREADS + 32 * (DT_FP4_DQW + 2) : DT_THREADS + 32;
@@ -96,16 +99,17 @@ struct DtShape {
     static constexpr int B_STRIDE = FP4 ? KPS * DT_B_BYTES : DT_STAGE_BYTES;
     static constexpr int A_STRIDE = DT_STAGE_BYTES;         // bf16 only
     static constexpr int BLK_OFF = RS * KPS * DT_B_BYTES;   // MXFP4 only
-    static constexpr int BLK_STRIDE = KPS * DT_FP4_BLK;
+    static constexpr int BLK_STRIDE = KPS * BLK;
     static constexpr int RING = FP4 ? (BLK_OFF + RS * BLK_STRIDE + 1023) / 1024 * 1024 : DT_STAGES * DT_STAGE_BYTES;
-    static constexpr int TAB_BYTES = FP4 ? 256 * (int)sizeof(Fp4Table) : 0;  // MXFP4 -> bf16 tables, one per scale byte
+    static constexpr int TAB_BYTES = QF == 1 ? 256 * (int)sizeof(Fp4Table) : 0;  // MXFP4 -> bf16 tables, one per scale byte
     static constexpr size_t SMEM = (size_t)RING + 1024 + DT_XCH_BYTES + 1024 + TAB_BYTES;
 };
 static_assert(DT_FP4_KPS == 1 || DT_FP4_KPS == 2, "one or two K blocks per MXFP4 stage");
 static_assert(DT_ACC * 2 * DT_TOK <= DT_FP4_A_COL && DT_FP4_A_COL + DT_FP4_AS * DT_FP4_KPS * 32 <= DT_FP4_TMEM_COLS,
               "MXFP4 accumulators and A tiles fit the tensor memory allocation");
 static_assert(DT_FP4_RS <= 32 && DT_STAGES <= 32, "the producer's per-stage masks are 32 bits");
-static_assert(DtShape<true>::SMEM + 11 * 1024 <= 227 * 1024, "MXFP4 ring, tables and static shared memory fit a CTA");
+static_assert(DtShape<1>::SMEM + 11 * 1024 <= 227 * 1024, "MXFP4 ring, tables and static shared memory fit a CTA");
+static_assert(DtShape<2>::SMEM + 11 * 1024 <= 227 * 1024, "Q4 ring and static shared memory fit a CTA");
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
 constexpr int DT_SATURATING_CTAS = 128;         // CTAs streaming at once that saturate HBM
 constexpr int DT_UP_MIN_KB = 8;                 // smallest gate/up split, in 64-wide K blocks
@@ -371,25 +375,6 @@ __device__ __forceinline__ void sum_partials(const float *pt, int S, int T, int 
     }
 }
 
-// Half h (elements 32h .. 32h+31, one E8M0 scale) of row r of a packed MXFP4
-// block, widened exactly to 16 bf16 pairs: v[c] holds elements 32h + 2c (low
-// half) and 32h + 2c + 1, as A-tile column 16h + c in tensor memory.  tabs:
-// the conversion tables of the 256 scale bytes (in shared memory).
-__device__ __forceinline__ void fp4_dequant_half(const uint8_t *blk, int h, int r, const Fp4Table *tabs,
-                                                 uint32_t (&v)[16])
-{
-    const uint4 c = *reinterpret_cast<const uint4 *>(blk + (h * 128 + r) * 16);
-    const Fp4Table t = tabs[blk[128 * 32 + h * 128 + r]];
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t o[4];
-        mxfp4_to_bf16x8(words[q], t, o);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
-    }
-}
-
 // routing weight of token t for group g (0 when t is not routed to it)
 __device__ __forceinline__ float group_weight(int g, int t, int n_act, int K, const int *s_act, const int *s_idx,
                                               const float *s_w, const float *s_gsh)
@@ -405,11 +390,12 @@ __device__ __forceinline__ float group_weight(int g, int t, int n_act, int K, co
 // ---------------------------------------------------------------------------
 // kernel 2: selection + gate/up + down, persistent, dynamic work claiming
 // ---------------------------------------------------------------------------
-template <bool FP4>
-__global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(const __grid_constant__ DecMaps maps,
+template <int QF>
+__global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(const __grid_constant__ DecMaps maps,
                                                                                const DecArgs a)
 {
-    using Sh = DtShape<FP4>;
+    using Sh = DtShape<QF>;
+    constexpr bool FP4 = Sh::FP4;  // packed low-bit weights
     constexpr int THREADS = Sh::THREADS;
     constexpr int RS = Sh::RS;
     extern __shared__ uint8_t smem_raw[];
@@ -474,7 +460,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
     }
     for (int e = threadIdx.x; e < E; e += THREADS) s_cnt[e] = 0;
     if (threadIdx.x < 32) s_mask[threadIdx.x] = 0u;
-    if constexpr (FP4)
+    if constexpr (QF == 1)
         for (int i = threadIdx.x; i < 256; i += THREADS) fp4tab[i] = mxfp4_table((uint32_t)i);
     tc_fence_before();
     __syncthreads();
@@ -695,7 +681,7 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                                 // copies below complete (bf16: A and the token tile; MXFP4: per K
                                 // block a packed block and a token tile)
                                 const int nkb = min(Sh::KPS, unit_nk - pos);
-                                mbar_arrive_expect_tx(&full[stage], FP4 ? nkb * (DT_B_BYTES + DT_FP4_BLK) : DT_STAGE_BYTES);
+                                mbar_arrive_expect_tx(&full[stage], FP4 ? nkb * (DT_B_BYTES + Sh::BLK) : DT_STAGE_BYTES);
                             }
                             uint8_t *sa = smem + stage * Sh::A_STRIDE;  // bf16 only
                             uint8_t *sb = smem + Sh::B_OFF + stage * Sh::B_STRIDE + sub * DT_B_BYTES;
@@ -709,8 +695,8 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                                 if (sub == 0 || !merged) {
                                     merged = sub == 0 && Sh::KPS == 2 && kb + 1 < kb1;  // (KPS <= 2)
                                     const uint32_t nb = merged ? 2 : 1;
-                                    bulk_load(smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * DT_FP4_BLK,
-                                              (is_up ? a.gu_fp4 : a.dn_fp4) + blk * DT_FP4_BLK, nb * DT_FP4_BLK,
+                                    bulk_load(smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * Sh::BLK,
+                                              (is_up ? a.gu_fp4 : a.dn_fp4) + blk * Sh::BLK, nb * Sh::BLK,
                                               &full[stage]);
                                 }
                                 tma_load_2d(sb, is_up ? &maps.x : &maps.hp, &full[stage], kc, brow);
@@ -1031,12 +1017,12 @@ __global__ void __launch_bounds__(DtShape<FP4>::THREADS, 1) dec_experts_kernel(c
                         tc_fence_after();
                         const int nkb = min(DT_FP4_KPS, nk - j * DT_FP4_KPS);
                         for (int sub = 0; sub < nkb; ++sub) {
-                            const uint8_t *blk = smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * DT_FP4_BLK;
+                            const uint8_t *blk = smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * Sh::BLK;
                             const uint32_t col = (uint32_t)((ast * DT_FP4_KPS + sub) * 32);
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {  // one half at a time: 16 words live
                                 uint32_t v[16];
-                                fp4_dequant_half(blk, h, row, fp4tab, v);
+                                lowbit_dequant_half<QF>(blk, h, row, fp4tab, v);
                                 tmem_st16(t_a + col + 16 * h, v);
                             }
                         }
@@ -1117,8 +1103,8 @@ int dectc_prepare(Layer &L)
     DecMaps *m = new (std::nothrow) DecMaps();
     if (!m) return -1;
     bool ok = dec_encode(&m->hp, L.dec_hp, L.Fmax, (uint64_t)dectc_groups_max(L) * DT_TOK, DT_TOK);
-    if (L.mxfp4) {
-        // the experts stream as packed MXFP4 blocks (bulk copies), not through tensor maps
+    if (L.qfmt != QF_NONE) {
+        // the experts stream as packed low-bit blocks (bulk copies), not through tensor maps
         m->gate = m->up = m->down = m->hp;
     } else {
         ok = ok && dec_encode(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
@@ -1134,10 +1120,12 @@ int dectc_prepare(Layer &L)
         m->sh_down = m->down;
     }
     if (ok)
-        ok = cudaFuncSetAttribute(dec_experts_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)DtShape<false>::SMEM) == cudaSuccess &&
-             cudaFuncSetAttribute(dec_experts_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)DtShape<true>::SMEM) == cudaSuccess;
+        ok = cudaFuncSetAttribute(dec_experts_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)DtShape<0>::SMEM) == cudaSuccess &&
+             cudaFuncSetAttribute(dec_experts_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)DtShape<1>::SMEM) == cudaSuccess &&
+             cudaFuncSetAttribute(dec_experts_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)DtShape<2>::SMEM) == cudaSuccess;
     if (!ok) { delete m; return -1; }
     L.dectc = m;
     return 0;
@@ -1189,22 +1177,25 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     a.inject = L.inject;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.num_sms);
-    cfg.blockDim = dim3(L.mxfp4 ? DtShape<true>::THREADS : DtShape<false>::THREADS);
-    cfg.dynamicSmemBytes = L.mxfp4 ? DtShape<true>::SMEM : DtShape<false>::SMEM;
+    cfg.blockDim = dim3(L.qfmt == QF_Q4 ? DtShape<2>::THREADS : L.qfmt == QF_MXFP4 ? DtShape<1>::THREADS
+                                                                                    : DtShape<0>::THREADS);
+    cfg.dynamicSmemBytes = L.qfmt == QF_Q4 ? DtShape<2>::SMEM : L.qfmt == QF_MXFP4 ? DtShape<1>::SMEM
+                                                                                 : DtShape<0>::SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = L.mxfp4 ? cudaLaunchKernelEx(&cfg, dec_experts_kernel<true>, m, a)
-                                       : cudaLaunchKernelEx(&cfg, dec_experts_kernel<false>, m, a);
+    const cudaError_t e = L.qfmt == QF_Q4      ? cudaLaunchKernelEx(&cfg, dec_experts_kernel<2>, m, a)
+                          : L.qfmt == QF_MXFP4 ? cudaLaunchKernelEx(&cfg, dec_experts_kernel<1>, m, a)
+                                               : cudaLaunchKernelEx(&cfg, dec_experts_kernel<0>, m, a);
     return e == cudaSuccess ? 1 : -1;
 }
 
 // ---------------------------------------------------------------------------
 // MXFP4 packing for the decode kernel: each (row block, 64-wide K block) of a
-// matrix becomes one contiguous block of DT_FP4_BLK bytes, the codes as
+// matrix becomes one contiguous block of LOWBIT_BLK_MXFP4 bytes, the codes as
 // [2 halves][128 rows][16 B] (half h = the row's 32-element source block
 // 2 kb + h) and then the scales as [2 halves][128 rows], so that a warp
 // reading one half of 32 consecutive rows reads 512 contiguous bytes.
@@ -1233,7 +1224,7 @@ __global__ void pack_fp4_gate_up_kernel(const uint8_t *blocks, const uint8_t *sc
         const int e = (int)(row / (2 * F)), rr = (int)(row - (size_t)e * 2 * F);
         const int f = rr >> 1, up = rr & 1;
         const size_t blk = ((size_t)e * (F / 64) + f / 64) * nkb + kb;
-        fp4_pack_row(out + blk * DT_FP4_BLK, up * 64 + (f & 63), blocks + (row * nb + 2 * kb) * 16,
+        fp4_pack_row(out + blk * LOWBIT_BLK_MXFP4, up * 64 + (f & 63), blocks + (row * nb + 2 * kb) * 16,
                      scales + row * nb + 2 * kb);
     }
 }
@@ -1248,15 +1239,88 @@ __global__ void pack_fp4_down_kernel(const uint8_t *blocks, const uint8_t *scale
         const int e = (int)(prow / ((size_t)ot * 128)), h = (int)(prow - (size_t)e * ot * 128);
         const size_t blk = ((size_t)e * ot + h / 128) * nkb + kb;
         const size_t row = (size_t)e * H + h;
-        fp4_pack_row(out + blk * DT_FP4_BLK, h & 127, h < H ? blocks + (row * nb + 2 * kb) * 16 : nullptr,
+        fp4_pack_row(out + blk * LOWBIT_BLK_MXFP4, h & 127, h < H ? blocks + (row * nb + 2 * kb) * 16 : nullptr,
                      h < H ? scales + row * nb + 2 * kb : nullptr);
+    }
+}
+
+// Q4: the same block layout with a binary16 scale per row and half, and each
+// record's codes rearranged so that byte b holds elements 2b (low nibble) and
+// 2b + 1 (a record's byte j holds elements j and j + 16).  Rows past H get
+// scale 0 (value 0).
+__device__ __forceinline__ void q4_pack_row(uint8_t *blk, int trow, const uint8_t *rec0, const uint8_t *rec1)
+{
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint8_t *rec = h ? rec1 : rec0;
+        uint8_t codes[16];
+        uint16_t d = 0;
+        if (rec) {
+            d = (uint16_t)(rec[0] | (rec[1] << 8));
+#pragma unroll
+            for (int b = 0; b < 16; ++b) {
+                const int e0 = 2 * b, e1 = 2 * b + 1;
+                const uint32_t c0 = e0 < 16 ? (rec[2 + e0] & 15u) : (rec[2 + e0 - 16] >> 4);
+                const uint32_t c1 = e1 < 16 ? (rec[2 + e1] & 15u) : (rec[2 + e1 - 16] >> 4);
+                codes[b] = (uint8_t)(c0 | (c1 << 4));
+            }
+        } else {
+#pragma unroll
+            for (int b = 0; b < 16; ++b) codes[b] = 0x88;
+        }
+        uint8_t *dst = blk + (h * 128 + trow) * 16;
+#pragma unroll
+        for (int b = 0; b < 16; ++b) dst[b] = codes[b];
+        reinterpret_cast<uint16_t *>(blk + LOWBIT_CODE_BYTES)[h * 128 + trow] = d;
+    }
+}
+
+// gate/up rows come from an interleaved [E][2F] tensor (gate = even rows) or
+// from separate gate and up tensors [E][F]; records of H/32 blocks of 18 bytes
+__global__ void pack_q4_gate_up_kernel(const uint8_t *gate_up, const uint8_t *gate, const uint8_t *up, int E, int F,
+                                       int H, uint8_t *out)
+{
+    const int nkb = H / 64, nb = H / 32;
+    const size_t n = (size_t)E * 2 * F * nkb;  // one (gate/up row, K block) each
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t row = i / nkb;               // [E][2F]: (feature, gate / up) pairs
+        const int kb = (int)(i - row * nkb);
+        const int e = (int)(row / (2 * F)), rr = (int)(row - (size_t)e * 2 * F);
+        const int f = rr >> 1, isup = rr & 1;
+        const uint8_t *src = gate_up ? gate_up + ((size_t)e * 2 * F + 2 * f + isup) * nb * 18
+                                     : (isup ? up : gate) + ((size_t)e * F + f) * nb * 18;
+        const size_t blk = ((size_t)e * (F / 64) + f / 64) * nkb + kb;
+        q4_pack_row(out + blk * LOWBIT_BLK_Q4, isup * 64 + (f & 63), src + 2 * kb * 18, src + (2 * kb + 1) * 18);
+    }
+}
+
+__global__ void pack_q4_down_kernel(const uint8_t *down, int E, int F, int H, uint8_t *out)
+{
+    const int nkb = F / 64, nb = F / 32, ot = (H + 127) / 128;
+    const size_t n = (size_t)E * ot * 128 * nkb;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t prow = i / nkb;
+        const int kb = (int)(i - prow * nkb);
+        const int e = (int)(prow / ((size_t)ot * 128)), h = (int)(prow - (size_t)e * ot * 128);
+        const size_t blk = ((size_t)e * ot + h / 128) * nkb + kb;
+        const uint8_t *src = h < H ? down + ((size_t)e * H + h) * nb * 18 : nullptr;
+        q4_pack_row(out + blk * LOWBIT_BLK_Q4, h & 127, src ? src + 2 * kb * 18 : nullptr,
+                    src ? src + (2 * kb + 1) * 18 : nullptr);
     }
 }
 
 size_t dectc_fp4_bytes(const Layer &L, bool gate_up)
 {
     const size_t ot = (L.H + 127) / 128;
-    return gate_up ? (size_t)L.E * (L.F / 64) * (L.H / 64) * DT_FP4_BLK : (size_t)L.E * ot * (L.F / 64) * DT_FP4_BLK;
+    const size_t blk = L.qfmt == QF_Q4 ? LOWBIT_BLK_Q4 : LOWBIT_BLK_MXFP4;
+    return gate_up ? (size_t)L.E * (L.F / 64) * (L.H / 64) * blk : (size_t)L.E * ot * (L.F / 64) * blk;
+}
+
+int dectc_pack_q4(Layer &L, const uint8_t *gate_up, const uint8_t *gate, const uint8_t *up, const uint8_t *down)
+{
+    pack_q4_gate_up_kernel<<<4 * L.num_sms, 256>>>(gate_up, gate, up, L.E, L.F, L.H, L.fp4_gu);
+    pack_q4_down_kernel<<<4 * L.num_sms, 256>>>(down, L.E, L.F, L.H, L.fp4_dn);
+    return cudaDeviceSynchronize() == cudaSuccess ? 0 : -1;
 }
 
 int dectc_pack_fp4(Layer &L, const uint8_t *gu_blocks, const uint8_t *gu_scales, const uint8_t *dn_blocks,

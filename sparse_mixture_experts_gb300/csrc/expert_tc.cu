@@ -29,36 +29,37 @@
 #include <cudaTypedefs.h>
 
 #include "moe_internal.cuh"
-#include "mxfp4.cuh"
+#include "lowbit.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
 
 constexpr int TC_THREADS = 192;
 constexpr int A_TILE_BYTES = TC_BM * TC_BK * 2;        // 16 KB
-constexpr int TC_FP4_BLK = 128 * 32 + 128 * 2;         // packed MXFP4 block: 128 rows x 64 K (codes, scales)
 
 // Per tile width BN (the MMA's N): the B tile, the stage, the ring depth and
 // the TMEM columns (two accumulators of BN fp32 columns).  N = 256 halves the
 // A bytes staged per weight byte, which matters because a CTA's TMA stream,
 // not HBM, limits these GEMMs once the A rows are re-read from L2.
-template <int BN, bool FP4 = false>
+template <int BN, int QF = QF_NONE>
 struct TcShape {
+    static constexpr bool LOWBIT = QF != QF_NONE;
+    static constexpr int BLK = QF == QF_Q4 ? LOWBIT_BLK_Q4 : LOWBIT_BLK_MXFP4;
     static constexpr int B_BYTES = BN * TC_BK * 2;
-    // MXFP4 weights: two packed blocks (codes and scales of 2 x 128 rows x 64 K)
+    // low-bit weights: two packed blocks (codes and scales of 2 x 128 rows x 64 K)
     // land next to the tiles; dequantising warps write the bf16 B tile from them
-    static constexpr int RAW_BYTES = FP4 ? 2 * TC_FP4_BLK : 0;
+    static constexpr int RAW_BYTES = LOWBIT ? 2 * BLK : 0;
     static constexpr int STAGE = (A_TILE_BYTES + B_BYTES + RAW_BYTES + 1023) / 1024 * 1024;
-    static constexpr int STAGES = FP4 ? 3 : (BN == 256 ? 4 : 6);
+    static constexpr int STAGES = LOWBIT ? 3 : (BN == 256 ? 4 : 6);
     static constexpr int TMEM_COLS = 2 * BN;
     // after the ring: barriers, then the epilogue's staging (4 warps x 32 rows x
     // 16 fp32), then (MXFP4) the conversion tables of the 256 scale bytes
     static constexpr int STAGING_OFF = STAGES * STAGE + 256;
     static constexpr int STAGING_BYTES = 4 * 32 * 16 * 4;
     static constexpr int TAB_OFF = STAGING_OFF + STAGING_BYTES;
-    static constexpr int TAB_BYTES = FP4 ? 256 * (int)sizeof(Fp4Table) : 0;
+    static constexpr int TAB_BYTES = QF == QF_MXFP4 ? 256 * (int)sizeof(Fp4Table) : 0;
     static constexpr size_t SMEM = (size_t)TAB_OFF + TAB_BYTES + 1024 /*align*/;
-    static constexpr int DQ_THREADS = FP4 ? 256 : 0;                     // dequantising warps: one B row each
+    static constexpr int DQ_THREADS = LOWBIT ? 256 : 0;                    // dequantising warps: one B row each
     static constexpr int THREADS = TC_THREADS + DQ_THREADS;
 };
 
@@ -102,7 +103,7 @@ struct TcArgs {
     const float *router_b;
     int R, router_nt, router_S, router_bn;  // router rows, router N tiles, K splits, tile width
     int *status;
-    const uint8_t *fp4;          // MXFP4 weights: packed blocks of gate/up ([E][F/64][H/64]) or down ([E][H/128][F/64])
+    const uint8_t *fp4;          // low-bit weights: packed blocks of gate/up ([E][F/64][H/64]) or down ([E][H/128][F/64])
     const volatile int *stall;   // test-only fault injection: a word nothing sets, waited for (else null)
     unsigned long long wait_ns;  // bound of that wait
     int T, K, E, H, F, Fs, Fmax, Tmax;
@@ -176,11 +177,13 @@ __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, 
     return ti.m0 >= 0 && ti.m0 < ti.rows && ti.n0 >= 0;
 }
 
-template <int EPI, int BN, typename Maps, bool FP4 = false>
-__global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ Maps maps,
+template <int EPI, int BN, typename Maps, int QF = QF_NONE>
+__global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ Maps maps,
                                                                                const TcArgs a)
 {
-    using Sh = TcShape<BN, FP4>;
+    using Sh = TcShape<BN, QF>;
+    constexpr bool FP4 = Sh::LOWBIT;
+    constexpr int LB_BLK = Sh::BLK;
     constexpr int TC_STAGES = Sh::STAGES;
     constexpr int STAGE_BYTES = Sh::STAGE;
     constexpr int B_TILE_BYTES = Sh::B_BYTES;
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(c
     uint64_t *acc_full = empty + TC_STAGES;   // [2]
     uint64_t *acc_empty = acc_full + 2;       // [2]
     uint64_t *drain = acc_empty + 2;          // the MMA thread's own completion, after an abort
-    uint64_t *bready = drain + 1;             // [TC_STAGES] MXFP4: the B tile is dequantised
+    uint64_t *bready = drain + 1;             // [TC_STAGES] low-bit weights: the B tile is dequantised
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bready + TC_STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(c
         }
     }
     Fp4Table *fp4tab = reinterpret_cast<Fp4Table *>(smem + Sh::TAB_OFF);
-    if constexpr (FP4)
+    if constexpr (QF == QF_MXFP4)
         for (int i = threadIdx.x; i < 256; i += Sh::THREADS) fp4tab[i] = mxfp4_table((uint32_t)i);
     tc_fence_before();
     __syncthreads();
@@ -279,11 +282,11 @@ __global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(c
                         const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
                         const int nvalid = min(2, nb - b0);
                         const int nkbt = EPI == EPI_UP ? a.H / TC_BK : a.F / TC_BK;
-                        mbar_arrive_expect_tx(&full[stage], A_TILE_BYTES + nvalid * TC_FP4_BLK);
+                        mbar_arrive_expect_tx(&full[stage], A_TILE_BYTES + nvalid * LB_BLK);
                         tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
                         for (int q = 0; q < nvalid; ++q) {
                             const size_t blk = ((size_t)ti.g * nb + b0 + q) * nkbt + ti.kb0 + kb;
-                            bulk_load(sb + B_TILE_BYTES + q * TC_FP4_BLK, a.fp4 + blk * TC_FP4_BLK, TC_FP4_BLK,
+                            bulk_load(sb + B_TILE_BYTES + q * LB_BLK, a.fp4 + blk * LB_BLK, LB_BLK,
                                       &full[stage]);
                         }
                         used |= 1u << stage;
@@ -368,9 +371,9 @@ __global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(c
             }
         }
     } else if (FP4 && warp >= 6) {
-        // ------------------------------ MXFP4 dequantisation (warps 6..13) ------------------------------
+        // ------------------------------ low-bit dequantisation (warps 6..13) ------------------------------
         // Per stage: the 256 rows of the B tile, one per thread, each 64 codes
-        // widened exactly to bf16 and written as eight 16-byte chunks at their
+        // widened to bf16 (MXFP4 exactly, Q4 rounded once) and written as eight 16-byte chunks at their
         // 128-byte-swizzle positions (chunk j of row r at r * 128 + ((j ^ (r & 7)) << 4),
         // the layout the TMA would have written).  Then the writes are made
         // visible to the tensor cores' reads and the stage is released to the MMA.
@@ -402,22 +405,18 @@ __global__ void __launch_bounds__(TcShape<BN, FP4>::THREADS, 1) tc_gemm_kernel(c
                     brow = rr & 127;
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(bt + rr * 128);
-                const uint8_t *pb = raw + q * TC_FP4_BLK;
+                const uint8_t *pb = raw + q * LB_BLK;
                 if (b0 + q >= nb) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) dst[j ^ (rr & 7)] = make_uint4(0, 0, 0, 0);
                 } else {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint4 c = *reinterpret_cast<const uint4 *>(pb + (h * 128 + brow) * 16);
-                        const Fp4Table tb = fp4tab[pb[128 * 32 + h * 128 + brow]];
-                        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+                        uint32_t v[16];
+                        lowbit_dequant_half<QF>(pb, h, brow, fp4tab, v);
 #pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            uint32_t o[4];
-                            mxfp4_to_bf16x8(words[w], tb, o);
-                            dst[(h * 4 + w) ^ (rr & 7)] = make_uint4(o[0], o[1], o[2], o[3]);
-                        }
+                        for (int w = 0; w < 4; ++w)
+                            dst[(h * 4 + w) ^ (rr & 7)] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
                     }
                 }
                 fence_proxy_async_shared();
@@ -629,7 +628,7 @@ int tc_prepare(Layer &L)
     const uint64_t rows_all = (uint64_t)L.Tmax * L.K + L.Tmax;
     bool ok = encode_2d(&m->xp, L.xp, L.H, rows_all, TC_BM) && encode_2d(&m->h, L.h, L.Fmax, rows_all, TC_BM) &&
               encode_2d(&m->router, L.router_w, L.H, (uint64_t)L.R, 128);
-    if (L.mxfp4) {
+    if (L.qfmt != QF_NONE) {
         // the experts' B operand is dequantised from the packed blocks in the kernel
         m->gate = m->up = m->down = m->router;
     } else {
@@ -653,12 +652,18 @@ int tc_prepare(Layer &L)
                              (int)TcShape<TC_BN_DOWN>::SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<EPI_ROUTER, 128, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)TcShape<128>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, true>,
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, QF_MXFP4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_BN_UP, true>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, true>,
+                             (int)TcShape<TC_BN_UP, QF_MXFP4>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, QF_MXFP4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_BN_DOWN, true>::SMEM) != cudaSuccess) {
+                             (int)TcShape<TC_BN_DOWN, QF_MXFP4>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, QF_Q4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<TC_BN_UP, QF_Q4>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, QF_Q4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcShape<TC_BN_DOWN, QF_Q4>::SMEM) != cudaSuccess) {
         delete m;
         return -1;
     }
@@ -701,19 +706,27 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
     if (which == 1) {
         TcMaps mu{m.xp, m.gate, m.up, m.sh_gate, m.sh_up, m.xp};
         if (L.Fs > 0 && !encode_2d(&mu.sa, x, L.H, (uint64_t)T, TC_BM)) return -1;
-        if (L.mxfp4) {
+        if (L.qfmt == QF_MXFP4) {
             a.fp4 = L.fp4_gu;
-            using Sh = TcShape<TC_BN_UP, true>;
-            tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, true><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
+            using Sh = TcShape<TC_BN_UP, QF_MXFP4>;
+            tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, QF_MXFP4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
+        } else if (L.qfmt == QF_Q4) {
+            a.fp4 = L.fp4_gu;
+            using Sh = TcShape<TC_BN_UP, QF_Q4>;
+            tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, QF_Q4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
         } else {
             tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_UP>::SMEM, s>>>(mu, a);
         }
     } else {
         TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down, m.h};
-        if (L.mxfp4) {
+        if (L.qfmt == QF_MXFP4) {
             a.fp4 = L.fp4_dn;
-            using Sh = TcShape<TC_BN_DOWN, true>;
-            tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, true><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
+            using Sh = TcShape<TC_BN_DOWN, QF_MXFP4>;
+            tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, QF_MXFP4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
+        } else if (L.qfmt == QF_Q4) {
+            a.fp4 = L.fp4_dn;
+            using Sh = TcShape<TC_BN_DOWN, QF_Q4>;
+            tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, QF_Q4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
         } else {
             tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_DOWN>::SMEM, s>>>(md, a);
         }

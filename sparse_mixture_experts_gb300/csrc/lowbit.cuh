@@ -1,0 +1,216 @@
+// lowbit.cuh -- the low-bit expert formats, widened exactly (MXFP4) or
+// rounded once (Q4) to bf16 for the tensor-core kernels' weight operands, and
+// the packed block both kernels stream: per (128 weight rows, 64-wide K block)
+// the codes as [2 halves][128 rows][16 B] (half h = K elements 32h .. 32h+31,
+// byte b of a row's 16 = elements 2b (low nibble) and 2b + 1 (high nibble)),
+// then the scales as [2 halves][128 rows] (one E8M0 byte, or one binary16).
+//
+// MXFP4 ("Phase 19: MoE -- gpt-oss-20b", the MXFP4 packing note under the
+// measured tensor layout, and section 3 on MXFP4 dequantisation): an element
+// is e2m1(code) * 2^(e8m0 - 127); the low nibble of a byte is the even element.
+// E2M1 (sign, 2 exponent bits, 1 mantissa bit) has the magnitudes 0, 0.5, 1,
+// 1.5, 2, 3, 4, 6.  Every magnitude times a power of two has at most two
+// significant bits, so it is a bf16 number whenever it is an fp32 number: for
+// every scale byte 0..254 (2^-127 is the fp32 subnormal 0x00400000; products
+// beyond the fp32 range are infinite, as in IEEE arithmetic), and byte 255
+// (NaN) gives NaN.  Conversion: per scale byte, a 16-byte table of the eight
+// magnitudes' bf16 patterns (high bytes, then low bytes) computed with fp32
+// arithmetic; per eight codes (one 32-bit word), four byte-permutes look up
+// the high and low bytes of the magnitudes, two more place the sign bits into
+// the high bytes, and four interleave the bytes into bf16 pairs (even element
+// in the low half).
+//
+// Q4 ("Engine" (cherenkov), section "Prefill": Q4 GEMMs with half weights and
+// float accumulation; records as the ggml-Q4_0 rows named under "Qwen3.5-MoE
+// Model Implementation", KV Cache): 32 elements share a binary16 scale d, an
+// element is (code - 8) * d.  code - 8 is exact in fp32 (the code is placed in
+// the mantissa of 2^23 and 2^23 + 8 subtracted), and so is its product with d
+// (4 bits times 11); the product is rounded once to bf16, nearest even -- the
+// 16-bit ("half") weight of the pages, in the layer's activation type.
+//
+// The same code compiles for the host (the byte permute and the rounding
+// written out), which is how it is tested against the formats' definitions.
+#pragma once
+
+#include <stdint.h>
+#include <string.h>
+
+#if defined(__CUDACC__)
+#define MXFP4_HD __host__ __device__ __forceinline__
+#else
+#define MXFP4_HD inline
+#endif
+
+namespace moe {
+
+// the eight byte tables of one scale: magnitude m's bf16 pattern is
+// (hi[m] << 8) | lo[m]; hi[0..3] in ah, hi[4..7] in bh, likewise lo
+struct Fp4Table {
+    uint32_t ah, bh, al, bl;
+};
+
+MXFP4_HD float mxfp4_bits_float(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+MXFP4_HD uint32_t mxfp4_float_bits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return u;
+}
+
+// byte permute: result byte i = byte (c >> 4i) & 7 of the pair {a (bytes 0-3), b (bytes 4-7)}
+MXFP4_HD uint32_t mxfp4_prmt(uint32_t a, uint32_t b, uint32_t c)
+{
+#if defined(__CUDA_ARCH__)
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+#else
+    const uint64_t ab = ((uint64_t)b << 32) | a;
+    uint32_t d = 0;
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t sel = (c >> (4 * i)) & 0xfu;
+        uint32_t byte = (uint32_t)(ab >> (8 * (sel & 7u))) & 0xffu;
+        if (sel & 8u) byte = (byte & 0x80u) ? 0xffu : 0u;  // sign-replicate mode (unused here)
+        d |= byte << (8 * i);
+    }
+    return d;
+#endif
+}
+
+// the table of scale byte s (0..255)
+MXFP4_HD Fp4Table mxfp4_table(uint32_t s)
+{
+    // 2^(s - 127): the fp32 exponent field is s itself, except s = 0
+    // (2^-127, a subnormal) and s = 255 (NaN in E8M0)
+    const float scale = mxfp4_bits_float(s == 0 ? 0x00400000u : s == 255 ? 0x7fc00000u : (s << 23));
+    const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    uint32_t hi[8], lo[8];
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t v = mxfp4_float_bits(mag[m] * scale) >> 16;  // exact: at most two significant bits
+        hi[m] = v >> 8;
+        lo[m] = v & 0xffu;
+    }
+    Fp4Table t;
+    t.ah = hi[0] | hi[1] << 8 | hi[2] << 16 | hi[3] << 24;
+    t.bh = hi[4] | hi[5] << 8 | hi[6] << 16 | hi[7] << 24;
+    t.al = lo[0] | lo[1] << 8 | lo[2] << 16 | lo[3] << 24;
+    t.bl = lo[4] | lo[5] << 8 | lo[6] << 16 | lo[7] << 24;
+    return t;
+}
+
+// eight codes (nibble i = element i) -> four bf16 pairs: o[j] holds elements
+// 2j (low half) and 2j + 1
+MXFP4_HD void mxfp4_to_bf16x8(uint32_t w, const Fp4Table &t, uint32_t (&o)[4])
+{
+    const uint32_t idx = w & 0x77777777u;           // magnitudes
+    uint32_t hi0 = mxfp4_prmt(t.ah, t.bh, idx);       // high bytes of elements 0..3
+    uint32_t lo0 = mxfp4_prmt(t.al, t.bl, idx);
+    uint32_t hi1 = mxfp4_prmt(t.ah, t.bh, idx >> 16); // elements 4..7
+    uint32_t lo1 = mxfp4_prmt(t.al, t.bl, idx >> 16);
+    // sign of element i (bit 4i + 3) to bit 7 of high byte i
+    const uint32_t ev = (w << 4) & 0x80808080u;      // elements 0, 2, 4, 6 at bit 7 of bytes 0..3
+    const uint32_t od = w & 0x80808080u;             // elements 1, 3, 5, 7
+    hi0 |= mxfp4_prmt(ev, od, 0x5140u);
+    hi1 |= mxfp4_prmt(ev, od, 0x7362u);
+    o[0] = mxfp4_prmt(lo0, hi0, 0x5140u);
+    o[1] = mxfp4_prmt(lo0, hi0, 0x7362u);
+    o[2] = mxfp4_prmt(lo1, hi1, 0x5140u);
+    o[3] = mxfp4_prmt(lo1, hi1, 0x7362u);
+}
+
+// ---- Q4 ----
+
+// binary16 bit pattern -> float (exact)
+MXFP4_HD float q4_half_to_float(uint32_t h)
+{
+    const uint32_t sign = (h & 0x8000u) << 16, e = (h >> 10) & 31u, m = h & 1023u;
+    if (e == 0) {
+        // zero or subnormal: m * 2^-24, exact in fp32
+        const float v = (float)m * mxfp4_bits_float(0x33800000u);  // 2^-24
+        return sign ? -v : v;
+    }
+    if (e == 31) return mxfp4_bits_float(sign | 0x7f800000u | (m << 13));
+    return mxfp4_bits_float(sign | ((e + 112u) << 23) | (m << 13));
+}
+
+// two floats -> bf16 pair (a in the low half), round to nearest even
+MXFP4_HD uint32_t q4_pack_bf16x2(float a, float b)
+{
+#if defined(__CUDA_ARCH__)
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+    return d;
+#else
+    auto rne = [](float f) -> uint32_t {
+        const uint32_t u = mxfp4_float_bits(f);
+        if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x7fffffu)) return (u >> 16) | 0x40u;  // NaN stays NaN
+        return (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
+    };
+    return rne(a) | (rne(b) << 16);
+#endif
+}
+
+// (code - 8) as a float, exactly: code in the low mantissa bits of 2^23
+MXFP4_HD float q4_code_value(uint32_t code)
+{
+    return mxfp4_bits_float(0x4b000000u | code) - 8388616.0f;
+}
+
+// eight codes (nibble i = element i) with the block's scale d -> four bf16
+// pairs: o[j] holds elements 2j (low half) and 2j + 1
+MXFP4_HD void q4_to_bf16x8(uint32_t w, float d, uint32_t (&o)[4])
+{
+#if defined(__CUDACC__)
+#pragma unroll
+#endif
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t byte = (w >> (8 * j)) & 0xffu;
+        o[j] = q4_pack_bf16x2(q4_code_value(byte & 15u) * d, q4_code_value(byte >> 4) * d);
+    }
+}
+
+// bytes of one packed block: codes, then the scales
+constexpr int LOWBIT_CODE_BYTES = 128 * 32;
+constexpr int LOWBIT_BLK_MXFP4 = LOWBIT_CODE_BYTES + 128 * 2;      // an E8M0 byte per row and half
+constexpr int LOWBIT_BLK_Q4 = LOWBIT_CODE_BYTES + 128 * 2 * 2;     // a binary16 per row and half
+
+#if defined(__CUDACC__)
+// Half h (elements 32h .. 32h+31, one scale) of row r of a packed low-bit
+// block (QF 1: MXFP4, 2: Q4), widened to 16 bf16 pairs: v[c] holds elements
+// 32h + 2c (low half) and 32h + 2c + 1.  MXFP4: exact, by the scale byte's
+// table (tabs, in shared memory); Q4: (code - 8) * d rounded once to bf16.
+template <int QF>
+__device__ __forceinline__ void lowbit_dequant_half(const uint8_t *blk, int h, int r, const Fp4Table *tabs,
+                                                    uint32_t (&v)[16])
+{
+    const uint4 c = *reinterpret_cast<const uint4 *>(blk + (h * 128 + r) * 16);
+    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    if constexpr (QF == 1) {
+        const Fp4Table t = tabs[blk[LOWBIT_CODE_BYTES + h * 128 + r]];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t o[4];
+            mxfp4_to_bf16x8(words[q], t, o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
+        }
+    } else {
+        const float d = q4_half_to_float(reinterpret_cast<const uint16_t *>(blk + LOWBIT_CODE_BYTES)[h * 128 + r]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t o[4];
+            q4_to_bf16x8(words[q], d, o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
+        }
+    }
+}
+#endif
+
+}  // namespace moe

@@ -131,6 +131,16 @@ moe_status stage_mxfp4(const void *blocks, const void *scales, size_t rows, size
     return MOE_OK;
 }
 
+// a tensor of Q4 records copied to the device for packing (freed by the caller)
+moe_status stage_bytes(const void *src, size_t bytes, const char *name, uint8_t *&dst)
+{
+    if (!src) return fail(MOE_ERR_INVALID_ARG, std::string("missing Q4 weight: ") + name);
+    cudaError_t e = cudaMalloc((void **)&dst, bytes);
+    if (e == cudaSuccess) e = cudaMemcpy(dst, src, bytes, cudaMemcpyDefault);
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return MOE_OK;
+}
+
 moe_status upload(void *dst, const void *src, size_t bytes, const char *name)
 {
     if (!src) return fail(MOE_ERR_INVALID_ARG, std::string("missing weight: ") + name);
@@ -168,14 +178,16 @@ moe_status validate(const moe_config &c)
     if (c.act != MOE_ACT_SWIGLU && c.act != MOE_ACT_CLAMP_GLU) return fail(MOE_ERR_INVALID_ARG, "unknown act");
     for (int d : {c.act_dtype, c.out_dtype})
         if (d != MOE_DT_F32 && d != MOE_DT_BF16) return fail(MOE_ERR_INVALID_ARG, "unknown dtype");
-    if (c.w_dtype != MOE_DT_F32 && c.w_dtype != MOE_DT_BF16 && c.w_dtype != MOE_DT_MXFP4)
+    if (c.w_dtype != MOE_DT_F32 && c.w_dtype != MOE_DT_BF16 && c.w_dtype != MOE_DT_MXFP4 && c.w_dtype != MOE_DT_Q4)
         return fail(MOE_ERR_INVALID_ARG, "unknown dtype");
-    if (c.w_dtype == MOE_DT_MXFP4) {
-        if (c.act_dtype != MOE_DT_BF16) return fail(MOE_ERR_UNSUPPORTED, "MXFP4 experts need bf16 activations");
-        if (!c.gate_up_interleaved || c.shared_ff)
-            return fail(MOE_ERR_UNSUPPORTED, "MXFP4 experts need an interleaved gate_up and no shared expert");
+    if (c.w_dtype == MOE_DT_MXFP4 || c.w_dtype == MOE_DT_Q4) {
+        const std::string f = c.w_dtype == MOE_DT_MXFP4 ? "MXFP4" : "Q4";
+        if (c.act_dtype != MOE_DT_BF16) return fail(MOE_ERR_UNSUPPORTED, f + " experts need bf16 activations");
+        if (c.w_dtype == MOE_DT_MXFP4 && !c.gate_up_interleaved)
+            return fail(MOE_ERR_UNSUPPORTED, "MXFP4 experts need an interleaved gate_up");
+        if (c.shared_ff) return fail(MOE_ERR_UNSUPPORTED, f + " experts need a layer without a shared expert");
         if (c.hidden % 64 || c.expert_ff % 64)
-            return fail(MOE_ERR_UNSUPPORTED, "MXFP4 experts need hidden and expert_ff multiples of 64");
+            return fail(MOE_ERR_UNSUPPORTED, f + " experts need hidden and expert_ff multiples of 64");
     } else if (c.act_dtype != c.w_dtype) {
         return fail(MOE_ERR_UNSUPPORTED, "act_dtype must equal w_dtype");
     }
@@ -189,11 +201,11 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
 {
     moe_status st = validate(*cfg);
     if (st) return st;
-    // an MXFP4 layer keeps its routed experts dequantised to bf16 as well (the
-    // prefill paths run on those); every other tensor of it is bf16
-    L.mxfp4 = cfg->w_dtype == MOE_DT_MXFP4;
+    // a low-bit layer keeps its routed experts packed only; every other tensor
+    // of it is bf16
+    L.qfmt = cfg->w_dtype == MOE_DT_MXFP4 ? QF_MXFP4 : cfg->w_dtype == MOE_DT_Q4 ? QF_Q4 : QF_NONE;
     moe_config cb = *cfg;
-    if (L.mxfp4) cb.w_dtype = MOE_DT_BF16;
+    if (L.qfmt != QF_NONE) cb.w_dtype = MOE_DT_BF16;
     const moe_config &c = cb;
     L.cfg = c;
     CUDA_TRY(cudaGetDevice(&L.device));
@@ -218,19 +230,29 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     if ((st = upload(L.router_w, w->router_w, E * H * eb, "router_w"))) return st;
     if (Fs && (st = upload((char *)L.router_w + E * H * eb, w->sh_gate_inp, H * eb, "sh_gate_inp"))) return st;
     Fp4Staged gu4, dn4;  // the MXFP4 tensors on the device until the packing below
+    Fp4Staged q4a, q4b;  // Q4 records: (gate_up or gate, up), (down, -)
     struct Release {
-        Fp4Staged &a, &b;
-        ~Release() { a.release(); b.release(); }
-    } release_fp4{gu4, dn4};
-    if (L.mxfp4) {
+        Fp4Staged &a, &b, &c, &d;
+        ~Release() { a.release(); b.release(); c.release(); d.release(); }
+    } release_fp4{gu4, dn4, q4a, q4b};
+    if (L.qfmt == QF_MXFP4) {
         // the routed experts stay MXFP4: the tensor-core kernels widen them on chip
         if ((st = stage_mxfp4(w->gate_up_w, w->gate_up_scales, E * 2 * F, H, "gate_up_w", gu4))) return st;
         if ((st = stage_mxfp4(w->down_w, w->down_scales, E * H, F, "down_w", dn4))) return st;
+    } else if (L.qfmt == QF_Q4) {
+        // the routed experts stay Q4 records, 18 bytes per 32 elements of a row
+        if (c.gate_up_interleaved) {
+            if ((st = stage_bytes(w->gate_up_w, E * 2 * F * (H / 32) * 18, "gate_up_w", q4a.blocks))) return st;
+        } else {
+            if ((st = stage_bytes(w->gate_w, E * F * (H / 32) * 18, "gate_w", q4a.blocks))) return st;
+            if ((st = stage_bytes(w->up_w, E * F * (H / 32) * 18, "up_w", q4a.scales))) return st;
+        }
+        if ((st = stage_bytes(w->down_w, E * H * (F / 32) * 18, "down_w", q4b.blocks))) return st;
     } else {
         if ((st = dev_alloc(L, &L.gate_w, E * F * H * eb))) return st;
         if ((st = dev_alloc(L, &L.up_w, E * F * H * eb))) return st;
     }
-    if (L.mxfp4) {
+    if (L.qfmt != QF_NONE) {
         // nothing more: the packed blocks are built below
     } else if (c.gate_up_interleaved) {
         void *tmp = nullptr;
@@ -247,7 +269,7 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
         if ((st = upload(L.gate_w, w->gate_w, E * F * H * eb, "gate_w"))) return st;
         if ((st = upload(L.up_w, w->up_w, E * F * H * eb, "up_w"))) return st;
     }
-    if (!L.mxfp4) {
+    if (L.qfmt == QF_NONE) {
         if ((st = dev_alloc(L, &L.down_w, E * H * F * eb))) return st;
         if ((st = upload(L.down_w, w->down_w, E * H * F * eb, "down_w"))) return st;
     }
@@ -304,9 +326,9 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
 
     std::string why;
     L.tc_capable = tc_supported(L, why);
-    if (L.mxfp4) {
+    if (L.qfmt != QF_NONE) {
         L.decode_grid = 0;  // the CUDA-core paths read bf16 or fp32 weights only
-        if (!L.tc_capable) return fail(MOE_ERR_UNSUPPORTED, "MXFP4 experts need the tensor-core kernels: " + why);
+        if (!L.tc_capable) return fail(MOE_ERR_UNSUPPORTED, "low-bit experts need the tensor-core kernels: " + why);
     }
     if (L.tc_capable) {
         // routed rows (T*K, expert-sorted) then the shared expert's rows (T)
@@ -314,13 +336,17 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
         if ((st = dev_alloc_t(L, &L.gfirst, 5 * (E + 2)))) return st;
         if ((st = dev_alloc_t(L, &L.router_parts, (size_t)TC_ROUTER_MAX_SPLITS * T * L.R))) return st;
         if (tc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "tensor map creation failed");
-        if (L.mxfp4) {
+        if (L.qfmt != QF_NONE) {
             // one contiguous block per (row block, 64-wide K block) for both
             // tensor-core paths
             if ((st = dev_alloc_t(L, &L.fp4_gu, dectc_fp4_bytes(L, true)))) return st;
             if ((st = dev_alloc_t(L, &L.fp4_dn, dectc_fp4_bytes(L, false)))) return st;
-            if (dectc_pack_fp4(L, gu4.blocks, gu4.scales, dn4.blocks, dn4.scales) != 0)
+            if (L.qfmt == QF_MXFP4 && dectc_pack_fp4(L, gu4.blocks, gu4.scales, dn4.blocks, dn4.scales) != 0)
                 return fail(MOE_ERR_CUDA, "MXFP4 packing failed");
+            if (L.qfmt == QF_Q4 &&
+                dectc_pack_q4(L, c.gate_up_interleaved ? q4a.blocks : nullptr,
+                              c.gate_up_interleaved ? nullptr : q4a.blocks, q4a.scales, q4b.blocks) != 0)
+                return fail(MOE_ERR_CUDA, "Q4 packing failed");
         }
         size_t hp_b, part_b, tab_b, tick_b;
         dectc_workspace(L, hp_b, part_b, tab_b, tick_b);
@@ -387,7 +413,7 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
     if (route == Route::DecodeTC) {
         int bad = 0;
         run(MOE_KERNEL_ROUTER, [&] { int r = launch_dectc(L, x, T, out, 0, s); bad |= r < 0; return r < 0 ? 0 : r; });
-        run(L.mxfp4 ? MOE_KERNEL_EXPERTS_MXFP4 : MOE_KERNEL_EXPERTS, [&] { int r = launch_dectc(L, x, T, out, 1, s); bad |= r < 0; return r < 0 ? 0 : r; });
+        run(L.qfmt == QF_MXFP4 ? MOE_KERNEL_EXPERTS_MXFP4 : L.qfmt == QF_Q4 ? MOE_KERNEL_EXPERTS_Q4 : MOE_KERNEL_EXPERTS, [&] { int r = launch_dectc(L, x, T, out, 1, s); bad |= r < 0; return r < 0 ? 0 : r; });
         if (rec) ++L.timing_recorded;
         cudaError_t e = cudaGetLastError();
         if (bad || e != cudaSuccess) return cuda_fail(e != cudaSuccess ? e : cudaErrorLaunchFailure, "decode launch");
@@ -565,10 +591,10 @@ moe_status moe_set_path(moe_layer *layer, int32_t path)
     if (path == MOE_PATH_DECODE_TC && !layer->dectc)
         return fail(MOE_ERR_UNSUPPORTED, "weight-streaming tensor-core path unavailable (needs the tensor-core path)");
     if (path == MOE_PATH_FUSED && layer->decode_grid == 0)
-        return fail(MOE_ERR_UNSUPPORTED, layer->mxfp4 ? "MXFP4 experts run on the tensor-core paths only"
-                                                      : "cooperative launch unavailable on this device");
-    if (path == MOE_PATH_STREAM && layer->mxfp4)
-        return fail(MOE_ERR_UNSUPPORTED, "MXFP4 experts run on the tensor-core paths only");
+        return fail(MOE_ERR_UNSUPPORTED, layer->qfmt != QF_NONE ? "low-bit experts run on the tensor-core paths only"
+                                                                : "cooperative launch unavailable on this device");
+    if (path == MOE_PATH_STREAM && layer->qfmt != QF_NONE)
+        return fail(MOE_ERR_UNSUPPORTED, "low-bit experts run on the tensor-core paths only");
     if (path == MOE_PATH_TC && !layer->tc_capable) {
         std::string why;
         tc_supported(*layer, why);

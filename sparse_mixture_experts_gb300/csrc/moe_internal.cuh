@@ -44,6 +44,13 @@ struct RouteMeta {
 
 struct TensorMaps;  // defined in expert_tc.cu
 
+// the routed experts' storage
+enum QuantFormat : int {
+    QF_NONE = 0,   // w_dtype (bf16 or fp32) tensors
+    QF_MXFP4 = 1,  // MXFP4 blocks, packed (lowbit.cuh)
+    QF_Q4 = 2,     // Q4 records, packed (lowbit.cuh)
+};
+
 struct Layer {
     moe_config cfg{};
     int device = 0;
@@ -85,7 +92,8 @@ struct Layer {
     void *h = nullptr;         // [Tmax*K + Tmax][Fmax] activations (routed rows sorted by expert, then shared)
     void *xp = nullptr;        // [Tmax*K + Tmax][H] x rows gathered in expert order, then x (tensor-core path)
     float *ys = nullptr;       // [Tmax][K+1][H] weighted expert outputs per (token, slot), fp32
-    bool mxfp4 = false;        // routed experts in MXFP4 (fp4_gu / fp4_dn; gate_w, up_w, down_w unused)
+    int qfmt = 0;              // QF_NONE, or the routed experts' low-bit format (fp4_gu / fp4_dn; gate_w,
+                               // up_w, down_w unused)
     int *gfirst = nullptr;     // [5][E + 2] per group: first gate/up tile (and the total), first down tile
                                // (and the total), expert (E = shared), rows, first row in the sorted buffers
     int *status = nullptr;     // DeviceError
@@ -106,8 +114,8 @@ struct Layer {
     // MXFP4 experts: codes and scales packed per (row block, 64-wide K block)
     // so that a pipeline stage is one contiguous copy; both tensor-core paths
     // widen them to bf16 on chip
-    uint8_t *fp4_gu = nullptr;       // [E][F/64][H/64] packed blocks (128 rows: 64 gate, 64 up; codes, scales)
-    uint8_t *fp4_dn = nullptr;       // [E][ceil(H/128)][F/64] packed blocks
+    uint8_t *fp4_gu = nullptr;       // [E][F/64][H/64] packed low-bit blocks (128 rows: 64 gate, 64 up)
+    uint8_t *fp4_dn = nullptr;       // [E][ceil(H/128)][F/64] packed low-bit blocks
 
     // per-kernel timing (moe_timing_enable / moe_timing_read)
     int timing_max = 0;         // forwards recorded per window; 0 = off
@@ -425,6 +433,8 @@ int dectc_prepare(Layer &L);
 size_t dectc_fp4_bytes(const Layer &L, bool gate_up);  // packed MXFP4 bytes of gate/up or down
 int dectc_pack_fp4(Layer &L, const uint8_t *gu_blocks, const uint8_t *gu_scales, const uint8_t *dn_blocks,
                    const uint8_t *dn_scales);
+// Q4 layers: pack the records (gate/up interleaved, or gate and up apart) on the device; 0 on success
+int dectc_pack_q4(Layer &L, const uint8_t *gate_up, const uint8_t *gate, const uint8_t *up, const uint8_t *down);
 void dectc_release(Layer &L);
 // which: 0 = router logits, 1 = selection + gate/up + down (writes out)
 int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s);

@@ -34,7 +34,8 @@ def moe_config(spec: synth.LayerSpec, max_tokens: int, out_dtype: str = "f32"):
         act=moe.ACT_SWIGLU if spec.act == "swiglu" else moe.ACT_CLAMP_GLU,
         act_alpha=spec.act_alpha, act_limit=spec.act_limit, has_bias=spec.has_bias,
         gate_up_interleaved=spec.gate_up_interleaved,
-        w_dtype=moe.DT_MXFP4 if getattr(spec, "expert_format", "dense") == "mxfp4" else dt[spec.dtype],
+        w_dtype={"mxfp4": moe.DT_MXFP4, "q4": moe.DT_Q4}.get(getattr(spec, "expert_format", "dense"),
+                                                              dt[spec.dtype]),
         act_dtype=dt[spec.dtype],
         out_dtype=dt[out_dtype], max_tokens=max_tokens)
 
@@ -58,6 +59,10 @@ def make_layer(spec, weights: dict, max_tokens: int, out_dtype: str = "f32", pat
         # the ABI takes the MXFP4 blocks in the gate_up_w / down_w slots
         w["gate_up_w"] = w.pop("gate_up_blocks")
         w["down_w"] = w.pop("down_blocks")
+    elif getattr(spec, "expert_format", "dense") == "q4":
+        # and the Q4 records in the slots of the tensors they stand for
+        for n in [n for n in w if n.endswith("_q4")]:
+            w[n[:-3]] = w.pop(n)
     layer = moe.MoELayer(moe_config(spec, max_tokens, out_dtype), w)
     if path:
         layer.set_path(path)

@@ -32,6 +32,9 @@ CASES = [
     ("mixtral", 1, 1), ("mixtral", 16, 16), ("mixtral", 256, 40), ("mixtral", 4096, 24), ("mixtral", 16384, 24),
     # MXFP4 experts: the decode path reads the codes and scales; the others the layer's bf16 values
     ("gptoss_mxfp4", 1, 1), ("gptoss_mxfp4", 4, 4), ("gptoss_mxfp4", 16, 16), ("gptoss_mxfp4", 64, 32),
+    # Q4 expert records: both tensor-core paths widen them on chip
+    ("qwen_q4", 1, 1), ("qwen_q4", 8, 8), ("qwen_q4", 300, 40),
+    ("gptoss_q4", 1, 1), ("gptoss_q4", 16, 16), ("gptoss_q4", 2048, 48),
 ]
 
 # CUDA-core flops budget for the streaming path in a test (it is the decode path)
@@ -237,6 +240,12 @@ EDGE_SPECS = [
                                                        expert_ff=128), 45),
     ("mxfp4_ragged", synth.GPTOSS_MXFP4.replace(name="mxfp4 small", hidden=192, n_expert=8, top_k=4,
                                                 expert_ff=128), 133),
+    # Q4 records: every expert selected, a single expert, ragged tails in both forms
+    ("q4_k_equals_E", synth.QWEN_Q4.replace(name="q4 k=E", hidden=128, n_expert=4, top_k=4, expert_ff=64), 37),
+    ("q4_single_expert", synth.QWEN_Q4.replace(name="q4 E=1", hidden=192, n_expert=1, top_k=1, expert_ff=128), 45),
+    ("q4_ragged", synth.QWEN_Q4.replace(name="q4 small", hidden=256, n_expert=16, top_k=4, expert_ff=192), 300),
+    ("q4_gptoss_ragged", synth.GPTOSS_Q4.replace(name="q4 gpt-oss-like small", hidden=192, n_expert=8, top_k=4,
+                                                 expert_ff=128), 133),
 ]
 
 
@@ -387,6 +396,92 @@ def test_mxfp4_small_layer_paths_agree(T):
     layer.close()
 
 
+Q4_SMALL = synth.QWEN_Q4.replace(name="qwen-like, Q4 expert records, small", hidden=256, n_expert=8, top_k=2,
+                                 expert_ff=192)
+
+
+def _q4_records(w):
+    return [n for n in w if n.endswith("_q4")]
+
+
+@pytest.mark.parametrize("scales", ["synthetic", "edges"])
+@pytest.mark.parametrize("T", [5, 200])
+def test_q4_scales_take_the_packed_path(scales, T):
+    """Q4 records stay packed: a decode batch runs the kernel that streams them
+    (timed as its own kind) and a prefill batch the grouped GEMMs that widen
+    them; both agree with the oracle on the same records -- with the synthetic
+    scales, and with edge scales: 0, negative, the smallest binary16
+    subnormal, the largest finite binary16 (65504) on blocks of codes 8 (value
+    0), and blocks whose codes are all 0 or all 15 (values -8 d and 7 d)."""
+    spec = Q4_SMALL
+    w = synth.make_weights(spec, seed=6)
+    if scales == "edges":
+        for name in _q4_records(w):
+            r = w[name].copy().reshape(-1, 18)
+            d = r[:, 0].astype(np.uint16) | (r[:, 1].astype(np.uint16) << 8)
+            d[3::97] = 0x0000                       # 0
+            d[11::89] = d[11::89] | 0x8000          # negative
+            d[5::53] = 0x0001                       # 2^-24
+            r[19::71, 2:] = 0x00                    # codes 0: -8 d
+            r[23::67, 2:] = 0xFF                    # codes 15: 7 d
+            big = np.arange(d.size)[7::61]
+            d[big] = 0x7BFF                         # 65504
+            r[big, 2:] = 0x88                       # codes 8: value 0
+            r[:, 0] = (d & 0xFF).astype(np.uint8)
+            r[:, 1] = (d >> 8).astype(np.uint8)
+            w[name] = r.reshape(w[name].shape)
+    x = synth.make_x(spec, T, seed=6)
+    layer = helpers.make_layer(spec, w, T)
+    layer.timing_enable(4)
+    out = layer.forward(helpers.to_torch(x)).float().cpu().numpy()
+    kinds = layer.timing_read()
+    idx, _ = layer.routing(T)
+    idx = idx.cpu().numpy()
+    layer.status()
+    layer.close()
+    if T <= DECODE_TC_MAX_TOKENS:
+        assert kinds["experts_q4"][1] == 1 and kinds["experts"][1] == 0 and kinds["experts_mxfp4"][1] == 0, kinds
+    else:
+        assert kinds["up"][1] == 1 and kinds["down"][1] == 1, kinds
+    orc = oracle.Oracle(spec, w)
+    mism, ties, invalid, _ = helpers.index_parity_all(orc, x, idx)
+    assert not mism and not invalid
+    rep = helpers.compare(orc, x, np.arange(T), out, idx)
+    print(f"[q4 {scales} T={T}] {rep}")
+    assert rep.ok(spec.dtype), str(rep)
+
+
+def test_q4_layer_keeps_only_the_packed_experts():
+    """A Q4 gpt-oss-shaped layer holds its experts as 4.5-bit records: its
+    device bytes are the packed experts plus the rest of the layer and the
+    workspace."""
+    spec = synth.GPTOSS_Q4
+    w = synth.make_weights(spec, seed=0)
+    layer = helpers.make_layer(spec, w, 16)
+    nbytes = layer.device_bytes
+    layer.close()
+    E, H, F = spec.n_expert, spec.hidden, spec.expert_ff
+    packed = E * 3 * H * F * (0.5 + 2 / 32)          # 448 MB
+    bf16_experts = E * 3 * H * F * 2                 # 1.59 GB
+    assert packed <= nbytes <= packed + 0.1e9, (nbytes, packed)
+    assert nbytes < 0.3 * bf16_experts
+
+
+@pytest.mark.parametrize("T", [1, 7, 16])
+def test_q4_small_layer_paths_agree(T):
+    """Ragged batches on a small Q4 layer: both tensor-core paths give the
+    oracle's result; the CUDA-core paths are refused."""
+    for path in (moe.PATH_DECODE_TC, moe.PATH_TC):
+        rep = _small_case(Q4_SMALL, T, path, seed=10)
+        assert rep.ok(Q4_SMALL.dtype), (path, str(rep))
+    layer = helpers.make_layer(Q4_SMALL, synth.make_weights(Q4_SMALL, seed=10), T)
+    for path in (moe.PATH_STREAM, moe.PATH_FUSED):
+        with pytest.raises(moe.MoEError) as ei:
+            layer.set_path(path)
+        assert ei.value.status == moe.ERR_UNSUPPORTED
+    layer.close()
+
+
 def _bf16_bits_to_f32(a):
     return (a.astype(np.uint32) << 16).view(np.float32)
 
@@ -399,6 +494,7 @@ INTER_CASES = [
     ("gptoss", 64, moe.PATH_TC, 24, 0),
     ("mixtral", 256, moe.PATH_TC, 12, 0),
     ("gptoss_mxfp4", 64, moe.PATH_TC, 16, 0),
+    ("qwen_q4", 300, moe.PATH_TC, 24, 0),
 ]
 
 
