@@ -35,9 +35,10 @@
 //             All gate/up units are claimed before any down unit, so a waiting
 //             down unit only depends on work that CTAs already hold.
 // The producer hands each claimed unit to the MMA and epilogue roles through a
-// queue of 8 slots.  Two MMA threads take alternate stages of the stream, each
-// into its own TMEM accumulator of the unit's slot, and the epilogue adds the
-// two.  All waits are bounded (about a second); results are deterministic.
+// queue (8 slots for bf16 weights, 4 for low-bit ones).  Two MMA threads (four
+// for low-bit weights) take the stages of the stream in turn, each into its
+// own TMEM accumulator of the unit's slot, and the epilogue adds them.  All
+// waits are bounded (about a second); results are deterministic.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -57,28 +58,31 @@ constexpr int DT_ACC = 8;                       // unit queue slots (each owns a
 constexpr int DT_EP_LD = DT_TOK + 1;            // row pitch (floats) of the epilogue's accumulator copy
 constexpr int DT_XCH_BYTES = 128 * DT_EP_LD * 4; // the accumulator tile in shared memory
 constexpr int DT_MAX_PAIRS = DT_TOK * 32;       // tokens * top_k
-// MXFP4 weights: a stage is DT_FP4_KPS 64-wide K blocks, each a token tile and
-// one packed block of codes and scales (128 rows x 64 K; see lowbit.cuh);
-// with two blocks per stage a unit's odd last block makes a one-block stage and
-// the blocks of a stage may come from different groups (down units).  Two
-// blocks per stage measured no faster than one, so one is used.  The
-// producer's ring holds DT_FP4_RS stages.  Eight more warps widen each block to
-// bf16 (exactly, for every scale byte: a table lookup per code, see lowbit.cuh)
-// and store it straight into tensor memory, where the MMA reads its A operand
-// (DT_FP4_AS tiles of 32 columns per K block); the token operand is x and h'
-// in bf16 as for bf16 weights.  The widened tile never touches shared memory,
-// whose bandwidth would otherwise bound the stage rate.
-// What bounds this pipeline instead is the length of each role's per-stage
-// instruction path (one warp or thread per stage), hence several producer
-// threads, two dequantising groups and two MMA threads taking stages in turn.
-constexpr int DT_FP4_KPS = 1;                   // K blocks per stage (1 or 2)
-constexpr int DT_FP4_RS = 24;                   // raw stages
-constexpr int DT_FP4_AS = 8;                    // A tiles (stages) in tensor memory, 32 columns per K block
-constexpr int DT_FP4_DQW = 8;                   // dequantising warps
+// Low-bit weights (MXFP4, Q4): a stage is one 64-wide K block: a token tile
+// and one packed block of codes and scales (128 rows x 64 K; see lowbit.cuh).
+// The producers' ring holds DT_FP4_RS stages.  DT_FP4_DQG groups of four
+// warps take the stages in turn and widen each block to bf16 (MXFP4 exactly,
+// by a table lookup per code; Q4 with three bf16 pair FMAs per two codes),
+// storing it straight into tensor memory, where the MMA reads its A operand
+// (DT_FP4_AS tiles of 32 columns); the token operand is x and h' in bf16 as
+// for bf16 weights.  The widened tile never touches shared memory, whose
+// bandwidth would otherwise bound the stage rate.
+// Measured on the gpt-oss-shaped layer at 16 tokens (per SM, per stage):
+// the conversion alone is ALU-bound near 300 cycles, whatever the number of
+// groups beyond two; one issuing thread hands the tensor cores an MMA or a
+// commit about every 128 cycles (five per stage), so DT_FP4_NM threads issue
+// in turn; more A tiles (up to 12) and fewer queue slots changed nothing.
+// Three groups beat two and four (four run out of registers).
+constexpr int DT_FP4_KPS = 1;                   // K blocks per stage
+constexpr int DT_FP4_RS = 24 / DT_FP4_KPS;       // raw stages
+constexpr int DT_FP4_DQG = 3;                   // dequantising groups of 4 warps, taking the stages in turn
+constexpr int DT_FP4_DQW = 4 * DT_FP4_DQG;      // dequantising warps
 constexpr int DT_FP4_NP = 4;                    // producer threads
-constexpr int DT_FP4_DQG = 2;                   // dequantising groups of 4 warps, taking alternate stages
-constexpr int DT_FP4_A_COL = 256;               // first A-tile column (accumulators use 0..255)
+constexpr int DT_FP4_NM = 4;                    // MMA issuing threads
+constexpr int DT_FP4_ACC = 4;                   // unit queue slots
 constexpr int DT_FP4_TMEM_COLS = 512;
+constexpr int DT_FP4_A_COL = DT_FP4_ACC * DT_FP4_NM * DT_TOK;  // first A-tile column, after the accumulators
+constexpr int DT_FP4_AS = (DT_FP4_TMEM_COLS - DT_FP4_A_COL) / (32 * DT_FP4_KPS);  // A tiles in tensor memory
 
 // QF: the routed experts' format -- 0 bf16 (TMA tiles), 1 MXFP4, 2 Q4 (packed
 // low-bit blocks, widened to bf16 in tensor memory)
@@ -86,13 +90,22 @@ template <int QF>
 struct DtShape {
     static constexpr bool FP4 = QF != 0;  // packed low-bit weights (either format)
     static constexpr int BLK = QF == 2 ? LOWBIT_BLK_Q4 : LOWBIT_BLK_MXFP4;  // bytes of a packed block
-    // bf16: producer, MMA, 4 epilogue warps; MXFP4: + 8 dequantising warps, a second MMA warp and a
-    // warp of three more producer threads
-    static constexpr int THREADS = FP4 ? DT_THREADS + 32 * (DT_FP4_DQW + 2) : DT_THREADS + 32;
-    static constexpr int NM = 2;                                    // MMA warps
-    static constexpr int MMA2_WARP = FP4 ? 6 + DT_FP4_DQW : 6;      // the second one
+    // bf16: producer, MMA, 4 epilogue warps, a second MMA warp; low-bit: producer, MMA, 4 epilogue
+    // warps, DQW dequantising warps, a second MMA warp, a warp of three more producer threads and
+    // NM - 2 more MMA warps
+    static constexpr int NM = FP4 ? DT_FP4_NM : 2;                  // MMA warps (one issuing thread each)
+    static constexpr int THREADS = FP4 ? DT_THREADS + 32 * (DT_FP4_DQW + 2 + NM - 2) : DT_THREADS + 32;
+    static constexpr int ACC = FP4 ? DT_FP4_ACC : DT_ACC;           // unit queue slots
+    // the MMA warps in issuing order: warp 1, then 6 (bf16) or 6 + DQW, 8 + DQW, 9 + DQW (low-bit)
+    static __device__ __forceinline__ int mma_index(int warp)
+    {
+        if (warp == 1) return 0;
+        if (warp == (FP4 ? 6 + DT_FP4_DQW : 6)) return 1;
+        if (FP4 && warp >= 8 + DT_FP4_DQW && warp < 6 + DT_FP4_DQW + NM) return warp - 6 - DT_FP4_DQW;
+        return -1;
+    }
     static constexpr int RS = FP4 ? DT_FP4_RS : DT_STAGES;   // producer ring
-    static constexpr int TMEM_COLS = FP4 ? DT_FP4_TMEM_COLS : DT_ACC * 2 * DT_TOK;
+    static constexpr int TMEM_COLS = FP4 ? DT_FP4_TMEM_COLS : ACC * NM * DT_TOK;
     static constexpr int KPS = FP4 ? DT_FP4_KPS : 1;        // K blocks per stage
     // smem: bf16 [RS][A | B]; MXFP4 [RS][KPS][B] [RS][KPS][block]
     static constexpr int B_OFF = FP4 ? 0 : DT_A_BYTES;      // first B tile
@@ -104,9 +117,13 @@ struct DtShape {
     static constexpr int TAB_BYTES = QF == 1 ? 256 * (int)sizeof(Fp4Table) : 0;  // MXFP4 -> bf16 tables, one per scale byte
     static constexpr size_t SMEM = (size_t)RING + 1024 + DT_XCH_BYTES + 1024 + TAB_BYTES;
 };
-static_assert(DT_FP4_KPS == 1 || DT_FP4_KPS == 2, "one or two K blocks per MXFP4 stage");
-static_assert(DT_ACC * 2 * DT_TOK <= DT_FP4_A_COL && DT_FP4_A_COL + DT_FP4_AS * DT_FP4_KPS * 32 <= DT_FP4_TMEM_COLS,
-              "MXFP4 accumulators and A tiles fit the tensor memory allocation");
+static_assert(DT_FP4_KPS == 1, "one K block per low-bit stage (two per stage faulted in a timing variant)");
+static_assert(DtShape<1>::ACC * DtShape<1>::NM * DT_TOK <= DT_FP4_A_COL &&
+                  DT_FP4_A_COL + DT_FP4_AS * DT_FP4_KPS * 32 <= DT_FP4_TMEM_COLS,
+              "low-bit accumulators and A tiles fit the tensor memory allocation");
+static_assert(DtShape<0>::TMEM_COLS <= 512 && DtShape<0>::ACC * DtShape<0>::NM <= 16 && DtShape<1>::NM <= 4 &&
+                  DT_FP4_AS >= 4 && DT_FP4_AS <= 16 && DT_FP4_ACC <= DT_ACC,
+              "accumulators fit; the drain, queue and tile barriers fit their shared-memory slots");
 static_assert(DT_FP4_RS <= 32 && DT_STAGES <= 32, "the producer's per-stage masks are 32 bits");
 static_assert(DtShape<1>::SMEM + 11 * 1024 <= 227 * 1024, "MXFP4 ring, tables and static shared memory fit a CTA");
 static_assert(DtShape<2>::SMEM + 11 * 1024 <= 227 * 1024, "Q4 ring and static shared memory fit a CTA");
@@ -404,13 +421,14 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
     Fp4Table *fp4tab = reinterpret_cast<Fp4Table *>(smem + Sh::RING + DT_XCH_BYTES + 1024);  // MXFP4 only
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Sh::RING + DT_XCH_BYTES);  // [RS] raw stage landed
     uint64_t *empty = full + RS;              // [RS] raw stage consumed
-    uint64_t *acc_full = empty + RS;          // [DT_ACC]
-    uint64_t *uq_full = acc_full + DT_ACC;    // [DT_ACC] unit handed out
-    uint64_t *uq_empty = uq_full + DT_ACC;    // [DT_ACC] unit finished, slot and accumulator free
-    uint64_t *deq = uq_empty + DT_ACC;        // [DT_FP4_AS] MXFP4: the A tile is in tensor memory
-    uint64_t *drain = deq + DT_FP4_AS;        // [2] an MMA thread's own completion, after an abort
-    int *uq = reinterpret_cast<int *>(drain + 2);  // [DT_ACC]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(uq + DT_ACC);
+    constexpr int ACC = Sh::ACC;
+    uint64_t *acc_full = empty + RS;          // [ACC]
+    uint64_t *uq_full = acc_full + ACC;       // [ACC] unit handed out
+    uint64_t *uq_empty = uq_full + ACC;       // [ACC] unit finished, slot and accumulator free
+    uint64_t *deq = uq_empty + ACC;           // [DT_FP4_AS] low-bit: the A tile is in tensor memory
+    uint64_t *drain = deq + DT_FP4_AS;        // [NM] an MMA thread's own completion, after an abort
+    int *uq = reinterpret_cast<int *>(drain + Sh::NM);  // [ACC]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(uq + ACC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *bcast = reinterpret_cast<int *>(tmem_slot + 2);  // [4]
 
@@ -435,14 +453,14 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
             mbar_init(&empty[s], 1);
         }
         mbar_init(&s_bnd_bar, 1);
-        for (int b = 0; b < DT_ACC; ++b) {
+        for (int b = 0; b < ACC; ++b) {
             mbar_init(&acc_full[b], Sh::NM);
             mbar_init(&uq_full[b], 1);
             mbar_init(&uq_empty[b], FP4 ? DT_FP4_NP : 1);  // MXFP4: the epilogue and the following producers
         }
         if (FP4)
             for (int s = 0; s < DT_FP4_AS; ++s) mbar_init(&deq[s], DT_FP4_DQW / DT_FP4_DQG);
-        for (int m = 0; m < 2; ++m) mbar_init(&drain[m], 1);
+        for (int m = 0; m < Sh::NM; ++m) mbar_init(&drain[m], 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -593,7 +611,7 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
                     // the slot may be handed out again only once this thread has read it
                     mbar_arrive(&uq_empty[qi]);
                 }
-                if (++qi == DT_ACC) qi = 0, qph ^= 1;
+                if (++qi == ACC) qi = 0, qph ^= 1;
                 if (u < 0) break;
                 const bool is_up = u < sc.up_units;
                 UpUnit ux;
@@ -721,30 +739,31 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
             }
             if (pw == 0 && *abort_flag) {
                 // let the other roles leave: hand out the end-of-work marker
-                for (int i = 0; i < DT_ACC; ++i) {
+                for (int i = 0; i < ACC; ++i) {
                     uq[qi] = -1;
                     mbar_arrive(&uq_full[qi]);
-                    if (++qi == DT_ACC) qi = 0, qph ^= 1;
+                    if (++qi == ACC) qi = 0, qph ^= 1;
                 }
             }
             volatile int never = 0;
             for (int s = 0; s < RS; ++s)
                 if ((used >> s) & 1u) mbar_wait(&full[s], (last_phase >> s) & 1u, &never);
         }
-    } else if (warp == 1 || warp == Sh::MMA2_WARP) {
+    } else if (Sh::mma_index(warp) >= 0) {
         // ------------------------------ MMA issuers ------------------------------
-        // Two threads take alternate stages (by their index in the stream) into
-        // accumulators of their own, which the epilogue adds: at N = 16 an MMA
-        // costs its issuing thread about as much as at N = 256, so one thread's
-        // issue rate would bound the stream.  MXFP4: A is the tile the
+        // NM threads, each in a warp of its own, take the stages in turn (by
+        // their index in the stream) into accumulators of their own, which the
+        // epilogue adds.  An issuing thread can hand the tensor cores about one
+        // MMA (or commit) per 128 cycles, whatever N is, while the tensor cores
+        // take them from several threads at once; so at N = 16 one thread's
+        // issue rate would bound the stream (two for bf16 weights, four for the
+        // smaller low-bit stages).  Low-bit weights: A is the tile the
         // dequantising warps left in tensor memory.
         constexpr int NM = Sh::NM;
-        const int mw = warp == 1 ? 0 : 1;
+        const int mw = Sh::mma_index(warp);
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(128, DT_TOK);
-            int stage = 0, ast = 0;  // raw stage; MXFP4: A tile
-            uint32_t phase = 0, aph = 0;
-            uint32_t gs = 0;         // index of the next stage in the stream
+            uint32_t gs = 0;         // stream index of the unit's first stage
             int qi = 0;
             uint32_t qph = 0;
             bool issued = false;  // any MMA of this thread
@@ -767,44 +786,45 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
                     nk = d.kb1 - d.kb0;
                 }
                 bool ok = true, first = true;
-                for (int j = 0; j * Sh::KPS < nk; ++j, ++gs) {
-                    if ((int)(gs % NM) == mw) {
-                        // MXFP4: the A tile is in tensor memory once the block it came
-                        // from has landed, so the token tile has too
-                        if (FP4 ? !mbar_wait(&deq[ast], aph, abort_flag) : !mbar_wait(&full[stage], phase, abort_flag)) {
-                            record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
-                            *abort_flag = 1;
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t sb = smem_u32(smem + Sh::B_OFF + stage * Sh::B_STRIDE);
-                        if (FP4) {
-                            const int nkb = min(Sh::KPS, nk - j * Sh::KPS);
-                            const uint32_t at = tmem_base + (uint32_t)(DT_FP4_A_COL + ast * 32 * Sh::KPS);
-                            for (int sub = 0; sub < nkb; ++sub)
-#pragma unroll
-                                for (int k = 0; k < 4; ++k)
-                                    mma_ta(d_tmem, at + sub * 32 + k * 8,
-                                               smem_desc_sw128(sb + sub * DT_B_BYTES + k * 32), idesc,
-                                               !first || sub != 0 || k != 0);
-                        } else {
-                            const uint32_t sa = smem_u32(smem + stage * Sh::A_STRIDE);
+                // this thread's stages of the unit: stream indices g in [gs, gs + nst)
+                // with g = mw mod NM; raw stage g mod RS (low-bit: A tile g mod AS)
+                const uint32_t nst = (uint32_t)((nk + Sh::KPS - 1) / Sh::KPS);
+                for (uint32_t g = gs + (uint32_t)((mw + NM - (int)(gs % NM)) % NM); g < gs + nst; g += NM) {
+                    const int stage = (int)(g % RS), ast = (int)(g % DT_FP4_AS);
+                    // low-bit: the A tile is in tensor memory once the block it came
+                    // from has landed, so the token tile has too
+                    if (FP4 ? !mbar_wait(&deq[ast], (g / DT_FP4_AS) & 1u, abort_flag)
+                            : !mbar_wait(&full[stage], (g / RS) & 1u, abort_flag)) {
+                        record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sb = smem_u32(smem + Sh::B_OFF + stage * Sh::B_STRIDE);
+                    if (FP4) {
+                        const int nkb = min(Sh::KPS, nk - (int)(g - gs) * Sh::KPS);
+                        const uint32_t at = tmem_base + (uint32_t)(DT_FP4_A_COL + ast * 32 * Sh::KPS);
+                        for (int sub = 0; sub < nkb; ++sub)
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
-                                mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
-                                         !first || k != 0);
-                        }
-                        mma_commit(&empty[stage]);  // the raw stage (and MXFP4: the A tile) is free
-                        first = false;
-                        issued = true;
+                                mma_ta(d_tmem, at + sub * 32 + k * 8, smem_desc_sw128(sb + sub * DT_B_BYTES + k * 32),
+                                       idesc, !first || sub != 0 || k != 0);
+                    } else {
+                        const uint32_t sa = smem_u32(smem + stage * Sh::A_STRIDE);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
+                                     !first || k != 0);
                     }
-                    if (++stage == RS) stage = 0, phase ^= 1;
-                    if (FP4 && ++ast == DT_FP4_AS) ast = 0, aph ^= 1;
+                    mma_commit(&empty[stage]);  // the raw stage (and low-bit: the A tile) is free
+                    first = false;
+                    issued = true;
                 }
+                gs += nst;
                 if (!ok) break;
                 mma_commit(&acc_full[qi]);  // MXFP4: also when this thread had no stage of the unit
-                if (++qi == DT_ACC) qi = 0, qph ^= 1;
+                if (++qi == ACC) qi = 0, qph ^= 1;
             }
             if (issued) {
                 // no MMA of this thread may still write tensor memory at teardown
@@ -869,7 +889,9 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
                 const int nst = (nk + Sh::KPS - 1) / Sh::KPS;  // stages of the unit
 #pragma unroll
                 for (int m = 0; m < Sh::NM; ++m) {
-                    if (nst < Sh::NM && (int)(e_gs % Sh::NM) != m) continue;
+                    // MMA thread m had a stage of the unit iff one of its nst stages,
+                    // stream indices e_gs .. e_gs + nst - 1, is m mod NM
+                    if ((m - (int)(e_gs % Sh::NM) + Sh::NM) % Sh::NM >= nst) continue;
                     tmem_ld16(tmem_base + lane_addr + (uint32_t)((qi * Sh::NM + m) * DT_TOK), raw);
                     tmem_ld_wait();
 #pragma unroll
@@ -963,12 +985,12 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
             tc_fence_before();
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (et == 0) mbar_arrive(&uq_empty[qi]);
-            if (++qi == DT_ACC) qi = 0, qph ^= 1;
+            if (++qi == ACC) qi = 0, qph ^= 1;
         }
     } else if (FP4 && warp < 6 + DT_FP4_DQW) {
-        // ------------------------------ MXFP4 dequantisation (warps 6..13) ------------------------------
-        // Follows the units in queue order like the MMA threads.  Two groups of
-        // four warps take alternate stages (by their index in the stream); in a
+        // ------------------------------ low-bit dequantisation (warps 6 .. 5 + DQW) ------------------------------
+        // Follows the units in queue order like the MMA threads.  DQG groups of
+        // four warps take the stages in turn (by their index in the stream); in a
         // group, warp w widens the rows of its 32-lane quadrant w % 4, lane =
         // row, straight into the A tile in tensor memory (a warp reaches only
         // its own quadrant's lanes).  A tile is rewritten once the MMA
@@ -982,9 +1004,9 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
         const int q = warp & 3, grp = (warp - 6) >> 2;
         const int row = q * 32 + lane;
         const uint32_t t_a = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)DT_FP4_A_COL;
-        int qi = 0, stage = 0, ast = 0, ps = 0;   // ps: raw stage of the stage DT_FP4_AS back
-        uint32_t qph = 0, phase = 0, pph = 0;
-        uint32_t gs = 0;
+        int qi = 0;
+        uint32_t qph = 0;
+        uint32_t gs = 0;  // stream index of the unit's first stage
         for (;;) {
             if (dr == 0) {
                 int go = 1;
@@ -1009,37 +1031,40 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
                 const DnUnit d = dn_unit(sc, u - sc.up_units, s_dnb);
                 nk = d.kb1 - d.kb0;
             }
-            for (int j = 0; j * DT_FP4_KPS < nk; ++j, ++gs) {
-                if ((int)(gs % DT_FP4_DQG) == grp) {
-                    bool ok = mbar_wait(&full[stage], phase, abort_flag);
-                    if (ok && gs >= (uint32_t)DT_FP4_AS) ok = mbar_wait(&empty[ps], pph, abort_flag);
-                    if (ok) {
-                        tc_fence_after();
-                        const int nkb = min(DT_FP4_KPS, nk - j * DT_FP4_KPS);
-                        for (int sub = 0; sub < nkb; ++sub) {
-                            const uint8_t *blk = smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * Sh::BLK;
-                            const uint32_t col = (uint32_t)((ast * DT_FP4_KPS + sub) * 32);
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {  // one half at a time: 16 words live
-                                uint32_t v[16];
-                                lowbit_dequant_half<QF>(blk, h, row, fp4tab, v);
-                                tmem_st16(t_a + col + 16 * h, v);
-                            }
-                        }
-                        tmem_st_wait();
-                    } else if (!*abort_flag) {
-                        record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
-                        *abort_flag = 1;
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&deq[ast]);
+            // this group's stages of the unit: stream indices g in [gs, gs + nst) with
+            // g = grp mod DQG; raw stage g mod RS, A tile g mod AS
+            const uint32_t nst = (uint32_t)((nk + DT_FP4_KPS - 1) / DT_FP4_KPS);
+            for (uint32_t g = gs + (uint32_t)((grp + DT_FP4_DQG - (int)(gs % DT_FP4_DQG)) % DT_FP4_DQG); g < gs + nst;
+                 g += DT_FP4_DQG) {
+                const int stage = (int)(g % RS), ast = (int)(g % DT_FP4_AS);
+                bool ok = mbar_wait(&full[stage], (g / RS) & 1u, abort_flag);
+                if (ok && g >= (uint32_t)DT_FP4_AS) {
+                    // the tile's last reader, the MMA of stream stage g - AS, has completed
+                    // (it released its raw stage)
+                    const uint32_t gp = g - DT_FP4_AS;
+                    ok = mbar_wait(&empty[gp % RS], (gp / RS) & 1u, abort_flag);
                 }
-                if (++stage == RS) stage = 0, phase ^= 1;
-                if (++ast == DT_FP4_AS) ast = 0;
-                if (gs >= (uint32_t)DT_FP4_AS && ++ps == RS) ps = 0, pph ^= 1;
+                if (ok) {
+                    tc_fence_after();
+                    const int nkb = min(DT_FP4_KPS, nk - (int)(g - gs) * DT_FP4_KPS);
+                    for (int sub = 0; sub < nkb; ++sub) {
+                        const uint8_t *blk = smem + Sh::BLK_OFF + stage * Sh::BLK_STRIDE + sub * Sh::BLK;
+                        const uint32_t col = (uint32_t)((ast * DT_FP4_KPS + sub) * 32);
+                        uint32_t v[32];
+                        lowbit_dequant_row<QF>(blk, row, fp4tab, v);
+                        tmem_st32(t_a + col, v);
+                    }
+                    tmem_st_wait();
+                } else if (!*abort_flag) {
+                    record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
+                    *abort_flag = 1;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&deq[ast]);
             }
-            if (++qi == DT_ACC) qi = 0, qph ^= 1;
+            gs += nst;
+            if (++qi == ACC) qi = 0, qph ^= 1;
         }
     }
 
@@ -1244,33 +1269,31 @@ __global__ void pack_fp4_down_kernel(const uint8_t *blocks, const uint8_t *scale
     }
 }
 
-// Q4: the same block layout with a binary16 scale per row and half, and each
-// record's codes rearranged so that byte b holds elements 2b (low nibble) and
-// 2b + 1 (a record's byte j holds elements j and j + 16).  Rows past H get
-// scale 0 (value 0).
+// Q4: the same block layout with a binary16 scale per row and half.  The
+// codes of each record are rearranged so that the eight elements 8q .. 8q+7
+// of a half form 32-bit word q, element 8q + i in nibble q4_nibble_of(i)
+// (evens in nibbles 0..3, odds in 4..7; see q4_to_bf16x8).  A record's byte
+// j holds elements j (low nibble) and j + 16.  Rows past H get scale 0
+// (value 0).
 __device__ __forceinline__ void q4_pack_row(uint8_t *blk, int trow, const uint8_t *rec0, const uint8_t *rec1)
 {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const uint8_t *rec = h ? rec1 : rec0;
-        uint8_t codes[16];
+        uint32_t words[4] = {0u, 0u, 0u, 0u};
         uint16_t d = 0;
         if (rec) {
             d = (uint16_t)(rec[0] | (rec[1] << 8));
 #pragma unroll
-            for (int b = 0; b < 16; ++b) {
-                const int e0 = 2 * b, e1 = 2 * b + 1;
-                const uint32_t c0 = e0 < 16 ? (rec[2 + e0] & 15u) : (rec[2 + e0 - 16] >> 4);
-                const uint32_t c1 = e1 < 16 ? (rec[2 + e1] & 15u) : (rec[2 + e1 - 16] >> 4);
-                codes[b] = (uint8_t)(c0 | (c1 << 4));
+            for (int e = 0; e < 32; ++e) {
+                const uint32_t c = e < 16 ? (rec[2 + e] & 15u) : (rec[2 + e - 16] >> 4);
+                words[e >> 3] |= c << (4 * q4_nibble_of(e & 7));
             }
         } else {
 #pragma unroll
-            for (int b = 0; b < 16; ++b) codes[b] = 0x88;
+            for (int q = 0; q < 4; ++q) words[q] = 0x88888888u;
         }
-        uint8_t *dst = blk + (h * 128 + trow) * 16;
-#pragma unroll
-        for (int b = 0; b < 16; ++b) dst[b] = codes[b];
+        reinterpret_cast<uint4 *>(blk + (h * 128 + trow) * 16)[0] = make_uint4(words[0], words[1], words[2], words[3]);
         reinterpret_cast<uint16_t *>(blk + LOWBIT_CODE_BYTES)[h * 128 + trow] = d;
     }
 }

@@ -410,14 +410,11 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
 #pragma unroll
                     for (int j = 0; j < 8; ++j) dst[j ^ (rr & 7)] = make_uint4(0, 0, 0, 0);
                 } else {
+                    uint32_t v[32];
+                    lowbit_dequant_row<QF>(pb, brow, fp4tab, v);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t v[16];
-                        lowbit_dequant_half<QF>(pb, h, brow, fp4tab, v);
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-                            dst[(h * 4 + w) ^ (rr & 7)] = make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        dst[j ^ (rr & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
                 fence_proxy_async_shared();
                 mbar_arrive(&bready[stage]);

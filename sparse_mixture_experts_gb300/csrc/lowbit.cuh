@@ -139,41 +139,81 @@ MXFP4_HD float q4_half_to_float(uint32_t h)
     return mxfp4_bits_float(sign | ((e + 112u) << 23) | (m << 13));
 }
 
-// two floats -> bf16 pair (a in the low half), round to nearest even
-MXFP4_HD uint32_t q4_pack_bf16x2(float a, float b)
+// float -> bf16 bits, round to nearest even (NaN stays NaN)
+MXFP4_HD uint32_t q4_bf16_rne(float f)
 {
 #if defined(__CUDA_ARCH__)
-    uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
-    return d;
+    uint16_t h;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+    return h;
 #else
-    auto rne = [](float f) -> uint32_t {
-        const uint32_t u = mxfp4_float_bits(f);
-        if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x7fffffu)) return (u >> 16) | 0x40u;  // NaN stays NaN
-        return (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
-    };
-    return rne(a) | (rne(b) << 16);
+    const uint32_t u = mxfp4_float_bits(f);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x7fffffu)) return (u >> 16) | 0x40u;
+    return (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
 #endif
 }
 
-// (code - 8) as a float, exactly: code in the low mantissa bits of 2^23
-MXFP4_HD float q4_code_value(uint32_t code)
+MXFP4_HD float q4_bf16_float(uint32_t b) { return mxfp4_bits_float(b << 16); }
+
+// A Q4 scale d (binary16 bits) split into two bf16 values, d = hi + lo
+// exactly: hi = d truncated to bf16 (toward zero), lo = d - hi, which has at
+// most three significant bits and d's sign, so it is a bf16 value too (lo = 0
+// for an infinite or NaN d).  A zero lo carries d's sign as well, so that
+// code 8 times d gives the zero of d's sign.  Returned as bf16 pairs (the
+// value in both halves).
+MXFP4_HD void q4_split_scale(uint32_t h16, uint32_t &hi2, uint32_t &lo2)
 {
-    return mxfp4_bits_float(0x4b000000u | code) - 8388616.0f;
+    const float d = q4_half_to_float(h16);
+    const uint32_t hi = mxfp4_float_bits(d) >> 16;
+    const bool finite = ((h16 >> 10) & 31u) != 31u;
+    uint32_t lo = finite ? q4_bf16_rne(d - q4_bf16_float(hi)) : 0u;  // d - hi is exact, and so is lo
+    if ((lo & 0x7fffu) == 0u) lo = h16 & 0x8000u;
+    hi2 = hi | (hi << 16);
+    lo2 = lo | (lo << 16);
 }
 
-// eight codes (nibble i = element i) with the block's scale d -> four bf16
-// pairs: o[j] holds elements 2j (low half) and 2j + 1
-MXFP4_HD void q4_to_bf16x8(uint32_t w, float d, uint32_t (&o)[4])
+// d = a * b + c on bf16 pairs with one rounding (to nearest even) per half
+MXFP4_HD uint32_t q4_fma_bf16x2(uint32_t a, uint32_t b, uint32_t c)
+{
+#if defined(__CUDA_ARCH__)
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+#else
+    // the operands of the conversion below keep a * b + c exact in fp32:
+    // products of at most 12 significant bits, sums spanning at most 22
+    uint32_t d = 0;
+    for (int k = 0; k < 2; ++k) {
+        const float x = q4_bf16_float((a >> (16 * k)) & 0xffffu), y = q4_bf16_float((b >> (16 * k)) & 0xffffu),
+                    z = q4_bf16_float((c >> (16 * k)) & 0xffffu);
+        d |= q4_bf16_rne(x * y + z) << (16 * k);
+    }
+    return d;
+#endif
+}
+
+// Eight codes of a packed Q4 word with the split scale of their record ->
+// four bf16 pairs: o[j] holds elements 2j (low half) and 2j + 1.  The packed
+// word keeps element 2j in nibble j and element 2j + 1 in nibble j + 4, so
+// one mask takes both codes of a pair into the low bits of a bf16 pair:
+//   p = 128 + code (bf16: exponent 7, the code in the low mantissa bits),
+//   v = p - 136 = code - 8 (exact), t = v * lo (exact: at most 7 bits),
+//   o = v * hi + t, rounded once: the bf16 rounding of (code - 8) * d.
+MXFP4_HD void q4_to_bf16x8(uint32_t w, uint32_t hi2, uint32_t lo2, uint32_t (&o)[4])
 {
 #if defined(__CUDACC__)
 #pragma unroll
 #endif
     for (int j = 0; j < 4; ++j) {
-        const uint32_t byte = (w >> (8 * j)) & 0xffu;
-        o[j] = q4_pack_bf16x2(q4_code_value(byte & 15u) * d, q4_code_value(byte >> 4) * d);
+        const uint32_t p = ((w >> (4 * j)) & 0x000f000fu) | 0x43004300u;
+        const uint32_t v = q4_fma_bf16x2(p, 0x3f803f80u, 0xc308c308u);  // p * 1 - 136
+        const uint32_t t = q4_fma_bf16x2(v, lo2, 0x80008000u);           // v * lo - 0
+        o[j] = q4_fma_bf16x2(v, hi2, t);
     }
 }
+
+// nibble position, in its packed word, of element i (0..7) of the word
+MXFP4_HD int q4_nibble_of(int i) { return (i & 1) ? 4 + (i >> 1) : (i >> 1); }
 
 // bytes of one packed block: codes, then the scales
 constexpr int LOWBIT_CODE_BYTES = 128 * 32;
@@ -181,31 +221,36 @@ constexpr int LOWBIT_BLK_MXFP4 = LOWBIT_CODE_BYTES + 128 * 2;      // an E8M0 by
 constexpr int LOWBIT_BLK_Q4 = LOWBIT_CODE_BYTES + 128 * 2 * 2;     // a binary16 per row and half
 
 #if defined(__CUDACC__)
-// Half h (elements 32h .. 32h+31, one scale) of row r of a packed low-bit
-// block (QF 1: MXFP4, 2: Q4), widened to 16 bf16 pairs: v[c] holds elements
-// 32h + 2c (low half) and 32h + 2c + 1.  MXFP4: exact, by the scale byte's
-// table (tabs, in shared memory); Q4: (code - 8) * d rounded once to bf16.
+// Row r of a packed low-bit block (QF 1: MXFP4, 2: Q4) widened to bf16:
+// v[c] holds elements 2c (low half) and 2c + 1, c = 0..31, i.e. the 64 K
+// elements of the block in order.  The loads of both halves come first, so
+// that their latencies overlap.  MXFP4: exact, by the scale byte's table
+// (tabs, in shared memory); Q4: (code - 8) * d rounded once to bf16.
 template <int QF>
-__device__ __forceinline__ void lowbit_dequant_half(const uint8_t *blk, int h, int r, const Fp4Table *tabs,
-                                                    uint32_t (&v)[16])
+__device__ __forceinline__ void lowbit_dequant_row(const uint8_t *blk, int r, const Fp4Table *tabs, uint32_t (&v)[32])
 {
-    const uint4 c = *reinterpret_cast<const uint4 *>(blk + (h * 128 + r) * 16);
-    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    const uint4 c0 = *reinterpret_cast<const uint4 *>(blk + r * 16);
+    const uint4 c1 = *reinterpret_cast<const uint4 *>(blk + (128 + r) * 16);
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     if constexpr (QF == 1) {
-        const Fp4Table t = tabs[blk[LOWBIT_CODE_BYTES + h * 128 + r]];
+        const Fp4Table t0 = tabs[blk[LOWBIT_CODE_BYTES + r]];
+        const Fp4Table t1 = tabs[blk[LOWBIT_CODE_BYTES + 128 + r]];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
             uint32_t o[4];
-            mxfp4_to_bf16x8(words[q], t, o);
+            mxfp4_to_bf16x8(words[q], q < 4 ? t0 : t1, o);
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
         }
     } else {
-        const float d = q4_half_to_float(reinterpret_cast<const uint16_t *>(blk + LOWBIT_CODE_BYTES)[h * 128 + r]);
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(blk + LOWBIT_CODE_BYTES);
+        uint32_t hi0, lo0, hi1, lo1;
+        q4_split_scale(sc[r], hi0, lo0);
+        q4_split_scale(sc[128 + r], hi1, lo1);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
             uint32_t o[4];
-            q4_to_bf16x8(words[q], d, o);
+            q4_to_bf16x8(words[q], q < 4 ? hi0 : hi1, q < 4 ? lo0 : lo1, o);
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
         }

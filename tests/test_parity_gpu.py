@@ -461,10 +461,10 @@ def test_q4_layer_keeps_only_the_packed_experts():
     nbytes = layer.device_bytes
     layer.close()
     E, H, F = spec.n_expert, spec.hidden, spec.expert_ff
-    packed = E * 3 * H * F * (0.5 + 2 / 32)          # 448 MB
+    packed = E * 3 * H * F * (0.5 + 2 / 32)          # 448 MB: 0.28 of the bf16 experts
     bf16_experts = E * 3 * H * F * 2                 # 1.59 GB
     assert packed <= nbytes <= packed + 0.1e9, (nbytes, packed)
-    assert nbytes < 0.3 * bf16_experts
+    assert nbytes < 0.35 * bf16_experts
 
 
 @pytest.mark.parametrize("T", [1, 7, 16])
