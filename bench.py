@@ -315,24 +315,25 @@ def run_reference(args, spec, T):
 # ---------------------------------------------------------------------------
 # roofline model: algorithmic bytes and flops per step and per kernel launch
 # ---------------------------------------------------------------------------
-def _traffic_from_profiles(kernel: str, workload: str):
-    """dram bytes per launch recorded under profiles/ for (kernel, workload),
-    if the kernel source has not changed since (its sha256 is recorded)."""
+def _traffic_from_profiles(kernel: str, workload: str, tokens: int):
+    """dram bytes per launch recorded under profiles/ for (kernel, workload,
+    tokens per step), if the kernel source has not changed since (its
+    sha256[:16] is recorded)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
     for line in open(path):
         cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 5 and cells[0] == kernel and cells[1] == workload:
-            src, sha = cells[3], cells[4]
+        if len(cells) >= 6 and cells[0] == kernel and cells[1] == workload and cells[2] == str(tokens):
+            src, sha = cells[4], cells[5]
             p = os.path.join(ROOT, src)
             if not os.path.exists(p):
                 return None
             if hashlib.sha256(open(p, "rb").read()).hexdigest()[:16] != sha:
                 return None
             try:
-                return float(cells[2])
+                return float(cells[3])
             except ValueError:
                 return None
     return None
@@ -404,7 +405,7 @@ def roofline_of(model, kind, T, d, avg_us, hbm, tc, tc_kind, workload):
     else:
         ach, peak, unit, bound, alg = b / t / 1e9, hbm, "GB/s", "hbm", b
     return {"kernel": kind, "bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
-            "traffic": _traffic_from_profiles(kind, workload), "algorithmic_per_launch": alg,
+            "traffic": _traffic_from_profiles(kind, workload, T), "algorithmic_per_launch": alg,
             "avg_us": avg_us, "peak_kind": "hbm" if bound == "hbm" else tc_kind}
 
 

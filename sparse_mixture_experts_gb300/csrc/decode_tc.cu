@@ -78,6 +78,7 @@ constexpr int DT_FP4_RS = 24 / DT_FP4_KPS;       // raw stages
 constexpr int DT_FP4_DQG = 3;                   // dequantising groups of 4 warps, taking the stages in turn
 constexpr int DT_FP4_DQW = 4 * DT_FP4_DQG;      // dequantising warps
 constexpr int DT_FP4_NP = 4;                    // producer threads
+constexpr int DT_BF16_NP = 1;                   // producer threads, bf16 weights
 constexpr int DT_FP4_NM = 4;                    // MMA issuing threads
 constexpr int DT_FP4_ACC = 4;                   // unit queue slots
 constexpr int DT_FP4_TMEM_COLS = 512;
@@ -94,7 +95,11 @@ struct DtShape {
     // warps, DQW dequantising warps, a second MMA warp, a warp of three more producer threads and
     // NM - 2 more MMA warps
     static constexpr int NM = FP4 ? DT_FP4_NM : 2;                  // MMA warps (one issuing thread each)
-    static constexpr int THREADS = FP4 ? DT_THREADS + 32 * (DT_FP4_DQW + 2 + NM - 2) : DT_THREADS + 32;
+    static constexpr int NP = FP4 ? DT_FP4_NP : DT_BF16_NP;         // producer threads
+    // the warp of producer threads 1 .. NP - 1
+    static constexpr int PROD2_WARP = FP4 ? 7 + DT_FP4_DQW : 7;
+    static constexpr int THREADS = FP4 ? DT_THREADS + 32 * (DT_FP4_DQW + 2 + NM - 2)
+                                       : DT_THREADS + 32 + (NP > 1 ? 32 : 0);
     static constexpr int ACC = FP4 ? DT_FP4_ACC : DT_ACC;           // unit queue slots
     // the MMA warps in issuing order: warp 1, then 6 (bf16) or 6 + DQW, 8 + DQW, 9 + DQW (low-bit)
     static __device__ __forceinline__ int mma_index(int warp)
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
         for (int b = 0; b < ACC; ++b) {
             mbar_init(&acc_full[b], Sh::NM);
             mbar_init(&uq_full[b], 1);
-            mbar_init(&uq_empty[b], FP4 ? DT_FP4_NP : 1);  // MXFP4: the epilogue and the following producers
+            mbar_init(&uq_empty[b], Sh::NP);  // the epilogue and the following producers
         }
         if (FP4)
             for (int s = 0; s < DT_FP4_AS; ++s) mbar_init(&deq[s], DT_FP4_DQW / DT_FP4_DQG);
@@ -562,13 +567,13 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
     int *group_done = a.counters + DT_GROUP_DONE;
     int *next_unit = a.counters + DT_NEXT_UNIT;
 
-    if (warp == 0 || (FP4 && warp == 7 + DT_FP4_DQW)) {
+    if (warp == 0 || (Sh::NP > 1 && warp == Sh::PROD2_WARP)) {
         // ------------------------------ producer(s) ------------------------------
-        // Producer 0 claims the units and hands them out.  MXFP4: three more
+        // Producer 0 claims the units and hands them out.  NP - 1 more
         // producer threads follow the queue, and producer p issues the stages
-        // whose index in the stream is p mod 4, since one thread's issue rate
-        // bounds the small stages.
-        constexpr int NP = FP4 ? DT_FP4_NP : 1;
+        // whose index in the stream is p mod NP, since one thread hands the
+        // copy engine a copy only every few hundred cycles.
+        constexpr int NP = Sh::NP;
         const int pw = warp == 0 ? (lane == 0 ? 0 : NP) : (lane < NP - 1 ? 1 + lane : NP);
         if (pw < NP) {
             int stage = 0;
