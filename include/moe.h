@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 5
+#define MOE_ABI_VERSION 6
 
 typedef enum {
     MOE_OK = 0,
@@ -142,6 +142,21 @@ typedef struct {
     int32_t act_dtype;           /* moe_dtype of x; must equal w_dtype (bf16 with MOE_DT_MXFP4, MOE_DT_Q4) */
     int32_t out_dtype;           /* moe_dtype of out */
     int32_t max_tokens;          /* workspace is sized once for this many tokens */
+    /* Expert residency ("Engine" (cherenkov), sections "Decode and expert
+     * IO" and "Memory ownership": a bounded pool of resident experts, the
+     * rest streamed in on demand, resident experts addressed through a
+     * table).  0: every routed expert stays in device memory.  S in
+     * [min(E, 16 * top_k), E): the routed experts' weights (after repacking)
+     * live in pinned host memory, read by the GPU over the host link, and S
+     * device slots hold the resident ones; every forward runs as chunks of
+     * up to 16 tokens, each chunk selecting its experts, keeping resident
+     * ones (hits) and copying the others from host memory into the least
+     * recently used slots that no expert of the chunk needs (ties: lowest
+     * slot), then running the weight-streaming tensor-core kernel through the
+     * slot table.  Results are bitwise those of the fully resident layer.
+     * Needs the weight-streaming tensor-core path (bf16, MXFP4 or Q4 experts;
+     * H, F, Fs multiples of 64); slots start with experts 0 .. S - 1. */
+    int32_t resident_experts;
 } moe_config;
 
 /* Weights: pointers to memory that cudaMemcpy can read (device memory, or
@@ -272,7 +287,8 @@ typedef enum {
                                 (weight-streaming tensor-core decode path) */
     MOE_KERNEL_EXPERTS_MXFP4 = 9, /* the same kernel streaming MXFP4 codes and scales */
     MOE_KERNEL_EXPERTS_Q4 = 10,   /* the same kernel streaming Q4 records */
-    MOE_KERNEL_COUNT = 11
+    MOE_KERNEL_RESIDENCY = 11,    /* expert residency: slot assignment and the copies from host memory */
+    MOE_KERNEL_COUNT = 12
 } moe_kernel_kind;
 
 /* Synchronises the device, then writes, per kernel kind, the summed device
@@ -287,6 +303,13 @@ moe_status moe_timing_read(moe_layer *layer, float *total_ms, int32_t *launches)
  * layer's inter-block counters so that the next forward starts clean (the
  * output of the forward that failed is not valid).  MOE_OK if none. */
 moe_status moe_get_status(moe_layer *layer);
+
+/* Expert residency (config.resident_experts > 0).  Synchronises the device
+ * and writes, when non-NULL: expert_of[S] = the expert each slot holds (-1:
+ * none yet), and stats[3] = hits, misses (experts copied from host memory)
+ * and bytes copied, counted over every chunk since create.  Errors:
+ * INVALID_ARG (NULL layer), UNSUPPORTED (no residency on this layer), CUDA. */
+moe_status moe_get_residency(moe_layer *layer, int32_t *expert_of, int64_t *stats);
 
 /* Bound, in nanoseconds, of every wait of the layer's kernels on work of
  * another thread block (a grid barrier, another block's activations, the

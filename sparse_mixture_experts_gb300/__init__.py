@@ -28,7 +28,7 @@ ACT_SWIGLU, ACT_CLAMP_GLU = 0, 1
 PATH_AUTO, PATH_STREAM, PATH_TC, PATH_FUSED, PATH_DECODE_TC = 0, 1, 2, 3, 4
 INTER_OFFSETS, INTER_PERM, INTER_H, INTER_YS = 0, 1, 2, 3
 KERNEL_KINDS = ("router", "select", "group", "up", "down", "combine", "gather", "fused", "experts",
-                "experts_mxfp4", "experts_q4")
+                "experts_mxfp4", "experts_q4", "residency")
 
 _DT = {"f32": DT_F32, "bf16": DT_BF16}
 _TORCH_DT = {DT_F32: torch.float32, DT_BF16: torch.bfloat16}
@@ -46,7 +46,7 @@ class _Config(ctypes.Structure):
                 ("norm_topk_prob", ctypes.c_int32), ("weights_scale", ctypes.c_float), ("act", ctypes.c_int32),
                 ("act_alpha", ctypes.c_float), ("act_limit", ctypes.c_float), ("has_bias", ctypes.c_int32),
                 ("gate_up_interleaved", ctypes.c_int32), ("w_dtype", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32), ("max_tokens", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("max_tokens", ctypes.c_int32), ("resident_experts", ctypes.c_int32)]
 
 
 WEIGHT_NAMES = ("router_w", "router_b", "gate_w", "up_w", "gate_up_w", "gate_up_b", "down_w", "down_b",
@@ -90,6 +90,7 @@ def load_library(path: str = LIB_PATH):
         "moe_get_intermediate": ([VP, I32, VP, ctypes.c_size_t, P(ctypes.c_size_t), VP], ctypes.c_int),
         "moe_set_wait_limit": ([VP, ctypes.c_int64], ctypes.c_int),
         "moe_set_fault_injection": ([VP, I32], ctypes.c_int),
+        "moe_get_residency": ([VP, VP, VP], ctypes.c_int),
         "moe_ep_send_plan": ([I32, I32, VP, VP, VP, VP], ctypes.c_int),
         "moe_ep_recv_plan": ([I32, I32, VP, VP, VP, VP, VP], ctypes.c_int),
     }
@@ -125,6 +126,7 @@ class MoEConfig:
     act_dtype: int = DT_BF16
     out_dtype: int = DT_F32
     max_tokens: int = 1
+    resident_experts: int = 0  # 0: every routed expert in device memory; else slots (see include/moe.h)
 
     def _c(self) -> _Config:
         c = _Config()
@@ -228,6 +230,15 @@ class MoELayer:
 
     def set_path(self, path: int) -> None:
         _check(_lib.moe_set_path(self._h, int(path)))
+
+    def residency(self):
+        """Expert residency: (expert held by each slot, {"hits", "misses",
+        "bytes"} counted over every chunk since creation)."""
+        S = self.config.resident_experts
+        slots = (ctypes.c_int32 * max(S, 1))()
+        stats = (ctypes.c_int64 * 3)()
+        _check(_lib.moe_get_residency(self._h, slots, stats))
+        return list(slots[:S]), {"hits": int(stats[0]), "misses": int(stats[1]), "bytes": int(stats[2])}
 
     def status(self) -> None:
         _check(_lib.moe_get_status(self._h))

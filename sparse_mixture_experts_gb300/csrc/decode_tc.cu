@@ -130,8 +130,8 @@ static_assert(DtShape<0>::TMEM_COLS <= 512 && DtShape<0>::ACC * DtShape<0>::NM <
                   DT_FP4_AS >= 4 && DT_FP4_AS <= 16 && DT_FP4_ACC <= DT_ACC,
               "accumulators fit; the drain, queue and tile barriers fit their shared-memory slots");
 static_assert(DT_FP4_RS <= 32 && DT_STAGES <= 32, "the producer's per-stage masks are 32 bits");
-static_assert(DtShape<1>::SMEM + 11 * 1024 <= 227 * 1024, "MXFP4 ring, tables and static shared memory fit a CTA");
-static_assert(DtShape<2>::SMEM + 11 * 1024 <= 227 * 1024, "Q4 ring and static shared memory fit a CTA");
+static_assert(DtShape<1>::SMEM + 13 * 1024 <= 227 * 1024, "MXFP4 ring, tables and static shared memory fit a CTA");
+static_assert(DtShape<2>::SMEM + 13 * 1024 <= 227 * 1024, "Q4 ring and static shared memory fit a CTA");
 constexpr int DT_UNITS_PER_CTA = 16;            // partial-sum slots per CTA
 constexpr int DT_SATURATING_CTAS = 128;         // CTAs streaming at once that saturate HBM
 constexpr int DT_UP_MIN_KB = 8;                 // smallest gate/up split, in 64-wide K blocks
@@ -176,6 +176,8 @@ struct DecArgs {
     int max_units;
     unsigned long long wait_ns;  // bound of a wait on another CTA's activations
     int inject;                  // test-only: dependency waits that never complete
+    const int *slot_of;          // expert residency: [E] the slot holding each expert's weights (else NULL)
+    int accumulate;              // a later chunk of a forward: the expert counts add up
 };
 
 // ---------------------------------------------------------------------------
@@ -443,6 +445,7 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
     __shared__ int s_cnt[1024];
     __shared__ uint32_t s_mask[32];  // bit e: expert e has at least one pair
     __shared__ int s_act[DT_MAX_PAIRS];
+    __shared__ int s_wslot[DT_MAX_PAIRS];  // where each active expert's weights are: s_act, or its slot
     __shared__ int s_dnb[DT_MAX_DOWN_SPLITS + 1];  // down split boundaries
     __shared__ int s_sdn;                          // down split count
     __shared__ __align__(8) uint64_t s_bnd_bar;    // s_dnb and s_sdn are written
@@ -545,6 +548,15 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
             int r = __popc(m & ((1u << (e & 31)) - 1u));
             for (int wd = 0; wd < (e >> 5); ++wd) r += __popc(s_mask[wd]);
             s_act[r] = e;
+            int w = e;
+            if (a.slot_of) {
+                w = a.slot_of[e];
+                if (w < 0) {  // not resident: an inconsistent table; slot 0 keeps the reads in bounds
+                    record_error(a.status, DEV_NOT_RESIDENT);
+                    w = 0;
+                }
+            }
+            s_wslot[r] = w;
         }
     }
     __syncthreads();
@@ -553,7 +565,7 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
             a.topk_idx[p] = s_idx[p];
             a.topk_w[p] = s_w[p];
         }
-        for (int e = threadIdx.x; e < E; e += THREADS) a.counts[e] = s_cnt[e];
+        for (int e = threadIdx.x; e < E; e += THREADS) a.counts[e] = (a.accumulate ? a.counts[e] : 0) + s_cnt[e];
         for (int g = threadIdx.x; g < n_act; g += THREADS) a.active[g] = s_act[g];
         if (a.Fs > 0)
             for (int t = threadIdx.x; t < T; t += THREADS) a.sh_gate[t] = s_gsh[t];
@@ -647,9 +659,9 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
                     if (is_up) {
                         kb0 = seg_k; kb1 = seg_end;
                         seg_k = seg_end;
-                        wexp = ux.shared ? 0 : s_act[ux.g];
+                        wexp = ux.shared ? 0 : s_wslot[ux.g];
                         if (ux.shared) { ma = &maps.sh_gate; mb = &maps.sh_up; arow = ux.ft * 64; }
-                        else { ma = &maps.gate; mb = &maps.up; arow = s_act[ux.g] * a.F + ux.ft * 64; }
+                        else { ma = &maps.gate; mb = &maps.up; arow = s_wslot[ux.g] * a.F + ux.ft * 64; }
                         brow = 0;
                     } else {
                         int local;
@@ -659,9 +671,9 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
                         const int n = min(fd / 64 - local, seg_end - seg_k);
                         kb0 = local; kb1 = local + n;
                         seg_k += n;
-                        wexp = shared ? 0 : s_act[gi];
+                        wexp = shared ? 0 : s_wslot[gi];
                         if (shared) { ma = &maps.sh_down; arow = dn.tile * 128; }
-                        else { ma = &maps.down; arow = s_act[gi] * a.H + dn.tile * 128; }
+                        else { ma = &maps.down; arow = s_wslot[gi] * a.H + dn.tile * 128; }
                         brow = gi * DT_TOK;
                         // h'[gi] is complete once every gate/up tile of the group is
                         // (only waited for by a producer with a stage in the segment:
@@ -1137,9 +1149,10 @@ int dectc_prepare(Layer &L)
         // the experts stream as packed low-bit blocks (bulk copies), not through tensor maps
         m->gate = m->up = m->down = m->hp;
     } else {
-        ok = ok && dec_encode(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, 64) &&
-             dec_encode(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, 64) &&
-             dec_encode(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, 128);
+        // (the weight arrays hold wslots experts: every one, or the resident slots)
+        ok = ok && dec_encode(&m->gate, L.gate_w, L.H, (uint64_t)L.wslots * L.F, 64) &&
+             dec_encode(&m->up, L.up_w, L.H, (uint64_t)L.wslots * L.F, 64) &&
+             dec_encode(&m->down, L.down_w, L.F, (uint64_t)L.wslots * L.H, 128);
     }
     if (ok && L.Fs) {
         ok = dec_encode(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, 64) && dec_encode(&m->sh_up, L.sh_up_w, L.H, L.Fs, 64) &&
@@ -1168,14 +1181,14 @@ void dectc_release(Layer &L)
 }
 
 // which: 0 = router logits, 1 = selection + experts (writes out)
-int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s)
+int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s, int t0)
 {
     if (which == 0) {
         DecRouteArgs r;
         r.x = (const __nv_bfloat16 *)x;
         r.router_w = (const __nv_bfloat16 *)L.router_w;
         r.router_b = L.router_b;
-        r.logits = L.logits;
+        r.logits = L.logits + (size_t)t0 * L.R;
         r.counters = L.dec_tickets;
         r.T = T; r.E = L.E; r.H = L.H; r.R = L.R;
         r.n_reset = dectc_groups_max(L);
@@ -1185,8 +1198,13 @@ int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cud
     DecMaps m = *L.dectc;
     if (!dec_encode(&m.x, x, L.H, (uint64_t)T, DT_TOK)) return -1;
     DecArgs a;
-    a.logits = L.logits;
-    a.topk_idx = L.topk_idx; a.topk_w = L.topk_w; a.sh_gate = L.sh_gate; a.counts = L.counts; a.active = L.active;
+    a.logits = L.logits + (size_t)t0 * L.R;
+    a.topk_idx = L.topk_idx + (size_t)t0 * L.K;
+    a.topk_w = L.topk_w + (size_t)t0 * L.K;
+    a.sh_gate = L.sh_gate + t0;
+    a.counts = L.counts; a.active = L.active;
+    a.slot_of = L.S > 0 ? L.slot_of : nullptr;
+    a.accumulate = t0 > 0;
     a.meta = L.meta;
     a.gate_b = L.gate_b; a.up_b = L.up_b; a.down_b = L.down_b;
     a.hp = L.dec_hp;

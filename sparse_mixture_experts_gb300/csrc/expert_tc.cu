@@ -629,9 +629,11 @@ int tc_prepare(Layer &L)
         // the experts' B operand is dequantised from the packed blocks in the kernel
         m->gate = m->up = m->down = m->router;
     } else {
-        ok = ok && encode_2d(&m->gate, L.gate_w, L.H, (uint64_t)L.E * L.F, TC_BN_UP / 2) &&
-             encode_2d(&m->up, L.up_w, L.H, (uint64_t)L.E * L.F, TC_BN_UP / 2) &&
-             encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.E * L.H, TC_BN_DOWN);
+        // (the weight arrays hold wslots experts: every one, or the resident slots, a
+        // layer that never runs these GEMMs)
+        ok = ok && encode_2d(&m->gate, L.gate_w, L.H, (uint64_t)L.wslots * L.F, TC_BN_UP / 2) &&
+             encode_2d(&m->up, L.up_w, L.H, (uint64_t)L.wslots * L.F, TC_BN_UP / 2) &&
+             encode_2d(&m->down, L.down_w, L.F, (uint64_t)L.wslots * L.H, TC_BN_DOWN);
     }
     if (ok && L.Fs) {
         ok = encode_2d(&m->sh_gate, L.sh_gate_w, L.H, L.Fs, TC_BN_UP / 2) &&

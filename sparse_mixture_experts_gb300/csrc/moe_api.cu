@@ -70,6 +70,7 @@ void timing_free(Layer &L)
 void free_all(Layer &L)
 {
     timing_free(L);
+    residency_release(L);
     if (L.tmaps) tc_release(L);
     if (L.dectc) dectc_release(L);
     for (void *p : L.allocations) cudaFree(p);
@@ -194,6 +195,15 @@ moe_status validate(const moe_config &c)
     if (c.hidden % 8 || c.expert_ff % 8 || c.shared_ff % 8)
         return fail(MOE_ERR_UNSUPPORTED, "hidden, expert_ff and shared_ff must be multiples of 8");
     if ((long long)c.max_tokens * c.top_k > (1LL << 30)) return fail(MOE_ERR_UNSUPPORTED, "max_tokens too large");
+    if (c.resident_experts < 0 || (c.resident_experts > 0 && c.resident_experts >= c.n_expert))
+        return fail(MOE_ERR_INVALID_ARG, "resident_experts must be 0 or below n_expert");
+    if (c.resident_experts > 0) {
+        // a chunk of 16 tokens must find a slot for every expert it selects
+        const int most = c.n_expert < 16 * c.top_k ? c.n_expert : 16 * c.top_k;
+        if (c.resident_experts < most)
+            return fail(MOE_ERR_INVALID_ARG, "resident_experts below min(n_expert, 16 * top_k)");
+        if (c.w_dtype == MOE_DT_F32) return fail(MOE_ERR_UNSUPPORTED, "expert residency needs bf16 or low-bit experts");
+    }
     return MOE_OK;
 }
 
@@ -214,6 +224,8 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
     L.R = L.E + (L.Fs > 0 ? 1 : 0);
     L.Fmax = L.F > L.Fs ? L.F : L.Fs;
     L.Tmax = c.max_tokens > 0 ? c.max_tokens : 1;
+    L.S = c.resident_experts;
+    L.wslots = L.E;
     L.wbytes = c.w_dtype == MOE_DT_BF16 ? 2 : 4;
     const size_t E = L.E, H = L.H, F = L.F, Fs = L.Fs, K = L.K, T = L.Tmax, eb = L.wbytes;
 
@@ -335,6 +347,8 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
         if ((st = dev_alloc(L, &L.xp, (T * K + T) * H * eb))) return st;
         if ((st = dev_alloc_t(L, &L.gfirst, 5 * (E + 2)))) return st;
         if ((st = dev_alloc_t(L, &L.router_parts, (size_t)TC_ROUTER_MAX_SPLITS * T * L.R))) return st;
+        // bf16 experts move to host memory before any tensor map names them
+        if (L.S > 0 && L.qfmt == QF_NONE && (st = residency_setup(L))) return st;
         if (tc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "tensor map creation failed");
         if (L.qfmt != QF_NONE) {
             // one contiguous block per (row block, 64-wide K block) for both
@@ -347,6 +361,7 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
                 dectc_pack_q4(L, c.gate_up_interleaved ? q4a.blocks : nullptr,
                               c.gate_up_interleaved ? nullptr : q4a.blocks, q4a.scales, q4b.blocks) != 0)
                 return fail(MOE_ERR_CUDA, "Q4 packing failed");
+            if (L.S > 0 && (st = residency_setup(L))) return st;
         }
         size_t hp_b, part_b, tab_b, tick_b;
         dectc_workspace(L, hp_b, part_b, tab_b, tick_b);
@@ -358,6 +373,8 @@ moe_status create_impl(const moe_config *cfg, const moe_weights *w, Layer &L)
         CUDA_TRY(cudaMemset(L.dec_hp, 0, hp_b));
         if (dectc_prepare(L) != 0) return fail(MOE_ERR_CUDA, "decode tensor map creation failed");
     }
+    if (L.S > 0 && !L.dectc)
+        return fail(MOE_ERR_UNSUPPORTED, "expert residency needs the weight-streaming tensor-core kernels: " + why);
     CUDA_TRY(cudaDeviceSynchronize());
     return MOE_OK;
 }
@@ -379,6 +396,46 @@ Route choose_path(const Layer &L, int T)
     return Route::Stream;
 }
 
+// Expert residency: chunks of up to 16 tokens, each through the router, the
+// slot assignment and copies of its missing experts, and the weight-streaming
+// tensor-core kernel reading the experts through the slot table.
+moe_status forward_resident(Layer &L, const void *x, int T, void *out, cudaStream_t s)
+{
+    const bool rec = L.timing_max > 0 && L.timing_recorded < L.timing_max;
+    const size_t xrow = (size_t)L.H * L.wbytes, orow = (size_t)L.H * (L.cfg.out_dtype == MOE_DT_BF16 ? 2 : 4);
+    const int kinds[3] = {MOE_KERNEL_ROUTER, MOE_KERNEL_RESIDENCY,
+                          L.qfmt == QF_MXFP4 ? MOE_KERNEL_EXPERTS_MXFP4
+                                             : L.qfmt == QF_Q4 ? MOE_KERNEL_EXPERTS_Q4 : MOE_KERNEL_EXPERTS};
+    int n = 0;
+    bool bad = false;
+    for (int t0 = 0; t0 < T && !bad; t0 += RESIDENT_CHUNK) {
+        const int Tc = T - t0 < RESIDENT_CHUNK ? T - t0 : RESIDENT_CHUNK;
+        const void *xc = (const char *)x + (size_t)t0 * xrow;
+        void *oc = (char *)out + (size_t)t0 * orow;
+        for (int step = 0; step < 3 && !bad; ++step) {
+            // per-kernel events while the window has room (a long forward records its first chunks)
+            const bool ev = rec && L.timing_pairs < (int)L.timing_kind.size();
+            if (ev) {
+                cudaEventRecord(L.timing_events[2 * L.timing_pairs], s);
+                L.timing_kind[L.timing_pairs] = kinds[step];
+            }
+            const int r = step == 0   ? launch_dectc(L, xc, Tc, oc, 0, s, t0)
+                          : step == 1 ? launch_residency(L, L.logits + (size_t)t0 * L.R, Tc, s)
+                                      : launch_dectc(L, xc, Tc, oc, 1, s, t0);
+            if (ev) cudaEventRecord(L.timing_events[2 * L.timing_pairs + 1], s), ++L.timing_pairs;
+            if (r < 0) bad = true;
+            else n += r;
+        }
+    }
+    if (rec) ++L.timing_recorded;
+    cudaError_t e = cudaGetLastError();
+    if (bad || e != cudaSuccess) return cuda_fail(e != cudaSuccess ? e : cudaErrorLaunchFailure, "resident decode launch");
+    L.last_T = T;
+    L.last_launches = n;
+    L.last_grouped = 0;
+    return MOE_OK;
+}
+
 moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t s)
 {
     if (T < 0) return fail(MOE_ERR_INVALID_ARG, "n_tokens < 0");
@@ -394,6 +451,7 @@ moe_status forward_impl(Layer &L, const void *x, int T, void *out, cudaStream_t 
     const size_t ob = (size_t)T * L.H * (L.cfg.out_dtype == MOE_DT_BF16 ? 2 : 4);
     const char *xs = (const char *)x, *os = (const char *)out;
     if (xs < os + ob && os < xs + xb) return fail(MOE_ERR_INVALID_ARG, "x and out overlap");
+    if (L.S > 0) return forward_resident(L, x, T, out, s);
     const Route route = choose_path(L, T);
     if (route == Route::Fused && !decode_supported(L, T))
         return fail(MOE_ERR_UNSUPPORTED, "fused decode path forced for a batch it does not cover");
@@ -595,6 +653,8 @@ moe_status moe_set_path(moe_layer *layer, int32_t path)
                                                                 : "cooperative launch unavailable on this device");
     if (path == MOE_PATH_STREAM && layer->qfmt != QF_NONE)
         return fail(MOE_ERR_UNSUPPORTED, "low-bit experts run on the tensor-core paths only");
+    if (layer->S > 0 && path != MOE_PATH_AUTO && path != MOE_PATH_DECODE_TC)
+        return fail(MOE_ERR_UNSUPPORTED, "a layer with streamed experts runs the weight-streaming tensor-core path only");
     if (path == MOE_PATH_TC && !layer->tc_capable) {
         std::string why;
         tc_supported(*layer, why);
@@ -696,6 +756,13 @@ void moe_destroy(moe_layer *layer)
     cudaDeviceSynchronize();
     free_all(*layer);
     delete layer;
+}
+
+moe_status moe_get_residency(moe_layer *layer, int32_t *expert_of, int64_t *stats)
+{
+    if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    set_last_error("");
+    return residency_read(*layer, expert_of, stats);
 }
 
 const char *moe_last_error(void) { return g_error.c_str(); }

@@ -26,6 +26,7 @@ enum DeviceError : int {
     DEV_TIMEOUT_GRID_BARRIER = 6,   // a block of the cooperative decode kernel never arrived
     DEV_TIMEOUT_DEPENDENCY = 7,     // a group's activations never completed (weight-streaming decode kernel)
     DEV_TIMEOUT_INJECTED = 8,       // the test-only injected wait ran out (tensor-core GEMMs)
+    DEV_NOT_RESIDENT = 9,           // a selected expert had no slot (expert residency)
 };
 
 // Groups of rows a grouped kernel walks over: the routed experts that
@@ -116,6 +117,20 @@ struct Layer {
     // widen them to bf16 on chip
     uint8_t *fp4_gu = nullptr;       // [E][F/64][H/64] packed low-bit blocks (128 rows: 64 gate, 64 up)
     uint8_t *fp4_dn = nullptr;       // [E][ceil(H/128)][F/64] packed low-bit blocks
+    // expert residency (cfg.resident_experts = S > 0): the routed experts'
+    // weights in pinned host memory, and gate_w / up_w / down_w (or fp4_gu /
+    // fp4_dn) holding S experts, one per slot
+    int S = 0;                       // slots (0: every routed expert resident)
+    int wslots = 0;                  // experts the device weight arrays hold (S, or E)
+    int n_regions = 0;               // per-expert weight regions: 3 (gate, up, down) or 2 (low-bit)
+    void *host_w[3] = {};            // pinned host copies, [E] experts each
+    size_t region_bytes[3] = {};     // bytes per expert of each region
+    void *dev_region[3] = {};        // the device slot arrays of the regions, [S] experts each
+    int *slot_of = nullptr;          // [E] slot holding each expert, -1 if none
+    int *expert_of = nullptr;        // [S] expert held by each slot, -1 if none
+    unsigned *last_used = nullptr;   // [S] chunk stamp of each slot's last use
+    int *res_jobs = nullptr;         // [1 + 2S] copies of the current chunk: count, (expert, slot) pairs
+    unsigned long long *res_stats = nullptr;  // [4] hits, misses, bytes copied, chunks
 
     // per-kernel timing (moe_timing_enable / moe_timing_read)
     int timing_max = 0;         // forwards recorded per window; 0 = off
@@ -433,11 +448,21 @@ int dectc_prepare(Layer &L);
 size_t dectc_fp4_bytes(const Layer &L, bool gate_up);  // packed MXFP4 bytes of gate/up or down
 int dectc_pack_fp4(Layer &L, const uint8_t *gu_blocks, const uint8_t *gu_scales, const uint8_t *dn_blocks,
                    const uint8_t *dn_scales);
+// expert residency (residency.cu): move the routed experts' weights to pinned
+// host memory and keep S slots on the device (at create, after the weights are
+// final); per chunk of a forward, assign slots and copy the misses
+moe_status residency_setup(Layer &L);
+void residency_release(Layer &L);
+int launch_residency(const Layer &L, const float *logits, int T, cudaStream_t s);
+moe_status residency_read(Layer &L, int32_t *expert_of, int64_t *stats);
 // Q4 layers: pack the records (gate/up interleaved, or gate and up apart) on the device; 0 on success
 int dectc_pack_q4(Layer &L, const uint8_t *gate_up, const uint8_t *gate, const uint8_t *up, const uint8_t *down);
 void dectc_release(Layer &L);
 // which: 0 = router logits, 1 = selection + gate/up + down (writes out)
-int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s);
+// t0: the chunk's first token within the forward (the logits and routing
+// outputs of the chunk go to that offset; the expert counts accumulate)
+int launch_dectc(const Layer &L, const void *x, int T, void *out, int which, cudaStream_t s, int t0 = 0);
+constexpr int RESIDENT_CHUNK = 16;  // tokens per chunk of a layer with streamed experts
 
 // tensor-core path (expert_tc.cu)
 bool tc_supported(const Layer &L, std::string &why);

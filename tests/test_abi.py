@@ -43,13 +43,13 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.moe_abi_version() == 5
+    assert lib.moe_abi_version() == 6
 
 
 def test_config_struct_layout_matches_header():
     import sparse_mixture_experts_gb300 as moe
-    # 17 four-byte fields, no padding
-    assert ctypes.sizeof(moe._Config) == 17 * 4
+    # 18 four-byte fields, no padding
+    assert ctypes.sizeof(moe._Config) == 18 * 4
     assert ctypes.sizeof(moe._Weights) == 14 * ctypes.sizeof(ctypes.c_void_p)
 
 
@@ -60,7 +60,11 @@ def test_config_struct_layout_matches_header():
     dict(hidden=60),               # not a multiple of 8
     dict(router_mode=7),
     dict(act=5),
-    dict(w_dtype=3),
+    dict(w_dtype=7),               # no such dtype
+    dict(w_dtype=3, act_dtype=0),  # Q4 needs bf16 activations
+    dict(resident_experts=-1),
+    dict(resident_experts=8),      # not below n_expert
+    dict(resident_experts=4),      # below min(n_expert, 16 * top_k): a chunk could select 8
     dict(w_dtype=2, act_dtype=1, gate_up_interleaved=0),  # MXFP4 needs the interleaved gate_up
     dict(w_dtype=2, act_dtype=0, gate_up_interleaved=1),  # MXFP4 needs bf16 activations
     dict(act_dtype=1, w_dtype=0),  # mixed activation / weight dtype
@@ -102,3 +106,4 @@ def test_settings_reject_a_null_layer(lib):
     assert lib.moe_set_wait_limit(None, 1000) == moe.ERR_INVALID_ARG
     assert lib.moe_set_fault_injection(None, 1) == moe.ERR_INVALID_ARG
     assert lib.moe_get_intermediate(None, 0, None, 0, None, None) == moe.ERR_INVALID_ARG
+    assert lib.moe_get_residency(None, None, None) == moe.ERR_INVALID_ARG
