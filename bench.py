@@ -66,6 +66,7 @@ WORKLOADS = {
     "gptoss_mxfp4_decode": (synth.GPTOSS_MXFP4, 1, (4, 16), 6),
     "gptoss_mxfp4_prefill": (synth.GPTOSS_MXFP4, 2048, (64,), 3),
     "qwen_q4_decode": (synth.QWEN_Q4, 8, (1,), 8),
+    "qwen_streamed_decode": (synth.QWEN_STREAMED, 8, (1,), 4),
     "gptoss_q4_prefill": (synth.GPTOSS_Q4, 2048, (16,), 3),
     "tiny": (synth.TINY, 16, (), 1),
 }
@@ -78,6 +79,7 @@ SWEEP = {
     "gptoss20b": (synth.GPTOSS, (1, 64, 2048), 4),
     "gptoss20b_mxfp4": (synth.GPTOSS_MXFP4, (1, 4, 16, 64, 2048), 4),
     "qwen35moe_q4": (synth.QWEN_Q4, (1, 8, 300), 8),
+    "qwen35moe_streamed": (synth.QWEN_STREAMED, (1, 8), 4),
     "gptoss20b_q4": (synth.GPTOSS_Q4, (1, 16, 2048), 4),
     "mixtral": (synth.MIXTRAL, (1, 16, 256, 4096, 16384), 2),
 }
@@ -412,6 +414,29 @@ def roofline_of(model, kind, T, d, avg_us, hbm, tc, tc_kind, workload):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+_LINK_PEAK = {}
+
+
+def host_link_peak(torch, dev):
+    """GB/s of a pinned host -> device copy (the host link), measured once."""
+    if dev in _LINK_PEAK:
+        return _LINK_PEAK[dev]
+    n = 512 << 20
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev)
+    d.copy_(h, non_blocking=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(4):
+        d.copy_(h, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize(dev)
+    _LINK_PEAK[dev] = 4 * n / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del h, d
+    return _LINK_PEAK[dev]
+
+
 class Runner:
     """One layer configuration on the GPU: n_layers layers with distinct weight
     memory, N_BATCHES token batches, and the measurements of a token count."""
@@ -447,7 +472,8 @@ class Runner:
             act_limit=spec.act_limit, has_bias=spec.has_bias, gate_up_interleaved=spec.gate_up_interleaved,
             w_dtype=moe.DT_MXFP4 if self.mxfp4 else moe.DT_Q4 if self.q4 else (
                 moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32),
-            act_dtype=moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32, out_dtype=moe.DT_F32, max_tokens=Tmax)
+            act_dtype=moe.DT_BF16 if spec.dtype == "bf16" else moe.DT_F32, out_dtype=moe.DT_F32, max_tokens=Tmax,
+            resident_experts=spec.resident_experts)
         self.layers = [moe.MoELayer(cfg, wt, device=dev) for _ in range(n_layers)]
         del wt
         torch.cuda.empty_cache()
@@ -545,7 +571,9 @@ class Runner:
             l.status()
         t0 = time.time()
         self.keep_loaded(n_tok, load_s)           # bring the clocks to their loaded state
+        res0 = self.residency_totals()
         ms = self.timed(n_tok, K)
+        res1 = self.residency_totals()
         t_timed = time.time()
         med = self.per_step_median(n_tok, max(K, MEDIAN_MIN_STEPS))
         self.keep_loaded(n_tok, 0.1)
@@ -574,8 +602,18 @@ class Runner:
         else:
             path = "stream"
         top = max(kernels, key=lambda k: kernels[k]["avg_us"] * kernels[k]["launches"])
-        roof = roofline_of(m, top, n_tok, d_avg, kernels[top]["avg_us"], self.hbm, tc, tc_kind, workload)
-        roof["peak_source"] = self.peak_src
+        residency = self.residency_summary(res0, res1, K, kernels)
+        if top == "residency" and residency and residency["host_link_gbs"]:
+            # the copies of the missing experts over the host link, against that link's
+            # copy rate measured in this run
+            peak = host_link_peak(self.torch, self.dev)
+            roof = {"kernel": "residency", "bound": "host-link", "achieved": residency["host_link_gbs"],
+                    "peak": peak, "unit": "GB/s", "frac": residency["host_link_gbs"] / peak, "traffic": None,
+                    "algorithmic_per_launch": residency["host_bytes_per_step"], "avg_us": kernels[top]["avg_us"],
+                    "peak_kind": "host-link", "peak_source": "pinned host -> device cudaMemcpyAsync, measured in this run"}
+        else:
+            roof = roofline_of(m, top, n_tok, d_avg, kernels[top]["avg_us"], self.hbm, tc, tc_kind, workload)
+            roof["peak_source"] = self.peak_src
         return {
             "tokens": n_tok, "steps": K, "ms_per_step": mps, "ms_per_step_median": med,
             "median_steps": max(K, MEDIAN_MIN_STEPS), "tokens_per_s": ws * n_tok / (mps * 1e-3),
@@ -586,7 +624,30 @@ class Runner:
                               "frac_of_max_floor": floor / (mps * 1e-3), "tc_peak": tc, "tc_peak_kind": tc_kind},
             "roofline": roof, "kernels": kernels, "clocks": clocks, "gpu_launches_per_step": launches,
             "timed_region_s": t_timed - t0,
+            "residency": residency,
         }
+
+    def residency_totals(self):
+        """Summed hit / miss / byte counters of the layers (expert residency)."""
+        if not self.spec.resident_experts:
+            return None
+        tot = {"hits": 0, "misses": 0, "bytes": 0}
+        for l in self.layers:
+            _, st = l.residency()
+            for k in tot:
+                tot[k] += st[k]
+        return tot
+
+    def residency_summary(self, a, b, K, kernels):
+        if a is None:
+            return None
+        d = {k: (b[k] - a[k]) / K for k in a}
+        r = kernels.get("residency")
+        us_step = r["avg_us"] * r["launches"] / K if r else None  # residency time per step
+        return {"slots": self.spec.resident_experts, "hits_per_step": d["hits"], "misses_per_step": d["misses"],
+                "host_bytes_per_step": d["bytes"],
+                "host_link_gbs": (d["bytes"] / (us_step * 1e-6) / 1e9) if us_step and d["bytes"] else None,
+                "note": "misses are copied from pinned host memory over the host link by the residency step"}
 
     def e2e(self, n_tok, K, warmup):
         """The metric through moe_forward_host: pinned host buffers, the copies
@@ -700,9 +761,12 @@ def run_ours(args, spec, T, extra_T, n_layers, workload):
             "other_token_counts": {k: {"tokens_per_s": v["tokens_per_s"], "ms_per_step": v["ms_per_step"], "kernels": v["kernels"],
                                        "distinct_experts": v["distinct_experts"],
                                        "hbm_frac": v["step_roofline"]["hbm_frac"],
-                                       "roofline": v["roofline"]} for k, v in extra.items()},
+                                       "roofline": v["roofline"], "residency": v["residency"]}
+                                   for k, v in extra.items()},
             "workloads": workloads,
         }
+        if head["residency"]:
+            line["residency"] = head["residency"]
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -153,6 +153,7 @@ class LayerSpec:
     router_init: str = "normal"            # "normal" / "uniform" / "zipf"
     zipf_s: float = 1.1
     expert_format: str = "dense"           # "dense" (dtype), "mxfp4" or "q4" (routed experts; rest bf16)
+    resident_experts: int = 0              # layer option (not an input): device slots for routed experts
 
     def replace(self, **kw) -> "LayerSpec":
         return dataclasses.replace(self, **kw)
@@ -172,6 +173,9 @@ QWEN_Q4 = QWEN.replace(name="qwen35moe-shaped routed experts, Q4 records (H=2048
                        shared_ff=0, expert_format="q4")
 GPTOSS_Q4 = GPTOSS.replace(name="gpt-oss-20b-shaped, Q4 expert records (H=2880, E=32, top-4, F=2880, biases)",
                            expert_format="q4")
+
+QWEN_STREAMED = QWEN.replace(name="qwen35moe-shaped, 128 of 256 experts resident, the rest streamed from host memory",
+                             resident_experts=128)
 
 # workload -> token counts exercised
 WORKLOADS = {

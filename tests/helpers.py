@@ -37,7 +37,8 @@ def moe_config(spec: synth.LayerSpec, max_tokens: int, out_dtype: str = "f32"):
         w_dtype={"mxfp4": moe.DT_MXFP4, "q4": moe.DT_Q4}.get(getattr(spec, "expert_format", "dense"),
                                                               dt[spec.dtype]),
         act_dtype=dt[spec.dtype],
-        out_dtype=dt[out_dtype], max_tokens=max_tokens)
+        out_dtype=dt[out_dtype], max_tokens=max_tokens,
+        resident_experts=getattr(spec, "resident_experts", 0))
 
 
 def to_torch(a: np.ndarray, device="cuda"):
