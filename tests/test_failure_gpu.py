@@ -41,9 +41,9 @@ def test_injected_wait_runs_out_and_the_layer_recovers(name, path, T):
     layer = helpers.make_layer(SPEC, w, T)
     try:
         layer.set_path(path)
-    except moe.MoEError as e:
+    except moe.MoEError:
         layer.close()
-        pytest.skip(str(e))
+        raise
     xd = helpers.to_torch(x)
     ref = layer.forward(xd).clone()
     torch.cuda.synchronize()
