@@ -46,21 +46,31 @@ struct TcShape {
     static constexpr bool LOWBIT = QF != QF_NONE;
     static constexpr int BLK = QF == QF_Q4 ? LOWBIT_BLK_Q4 : LOWBIT_BLK_MXFP4;
     static constexpr int B_BYTES = BN * TC_BK * 2;
-    // low-bit weights: two packed blocks (codes and scales of 2 x 128 rows x 64 K)
-    // land next to the tiles; dequantising warps write the bf16 B tile from them
-    static constexpr int RAW_BYTES = LOWBIT ? 2 * BLK : 0;
-    static constexpr int STAGE = (A_TILE_BYTES + B_BYTES + RAW_BYTES + 1023) / 1024 * 1024;
+    static constexpr int STAGE = (A_TILE_BYTES + B_BYTES + 1023) / 1024 * 1024;
     static constexpr int STAGES = LOWBIT ? 3 : (BN == 256 ? 4 : 6);
+    // low-bit weights: the packed blocks (codes and scales of 2 x 128 rows x
+    // 64 K) of each stage's B tile land in a ring of their own, filled further
+    // ahead than the A/B ring (a raw stage is a fifth of an A/B stage), from
+    // which dequantising warps write the bf16 B tile
+    static constexpr int RAW_STAGE = LOWBIT ? 2 * BLK : 0;
+    static constexpr int RAW_STAGES = LOWBIT ? 6 : 0;
+    static constexpr int RAW_OFF = STAGES * STAGE;
+    static constexpr int BAR_OFF = RAW_OFF + (RAW_STAGES * RAW_STAGE + 1023) / 1024 * 1024;
     static constexpr int TMEM_COLS = 2 * BN;
-    // after the ring: barriers, then the epilogue's staging (4 warps x 32 rows x
-    // 16 fp32), then (MXFP4) the conversion tables of the 256 scale bytes
-    static constexpr int STAGING_OFF = STAGES * STAGE + 256;
+    // after the rings: barriers, then the epilogue's staging (4 warps x 32 rows
+    // x 16 fp32), then (MXFP4) the conversion tables of the 256 scale bytes
+    static constexpr int STAGING_OFF = BAR_OFF + 512;
     static constexpr int STAGING_BYTES = 4 * 32 * 16 * 4;
     static constexpr int TAB_OFF = STAGING_OFF + STAGING_BYTES;
     static constexpr int TAB_BYTES = QF == QF_MXFP4 ? 256 * (int)sizeof(Fp4Table) : 0;
     static constexpr size_t SMEM = (size_t)TAB_OFF + TAB_BYTES + 1024 /*align*/;
-    static constexpr int DQ_THREADS = LOWBIT ? 256 : 0;                    // dequantising warps: one B row each
-    static constexpr int THREADS = TC_THREADS + DQ_THREADS;
+    static constexpr int DQ_THREADS = LOWBIT ? 256 : 0;  // dequantising warps: one B row each
+    static constexpr int RAW_WARP = (TC_THREADS + DQ_THREADS) / 32;  // the raw ring's producer (low-bit)
+    static constexpr int THREADS = TC_THREADS + DQ_THREADS + (LOWBIT ? 32 : 0);
+    // barriers: full, empty, bready per A/B stage; two accumulators' full and
+    // empty; drain; raw full and empty per raw stage; the TMEM address and the
+    // abort word
+    static_assert((3 * STAGES + 5 + 2 * RAW_STAGES) * 8 + 8 <= 512, "barrier area");
 };
 
 struct TensorMaps {
@@ -177,6 +187,37 @@ __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, 
     return ti.m0 >= 0 && ti.m0 < ti.rows && ti.n0 >= 0;
 }
 
+// 16 consecutive fp32 biases (zeros for a layer without them); p is 16-byte aligned
+__device__ __forceinline__ void bias16(const float *p, float (&b)[16])
+{
+    if (p) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(p) + q);
+            b[4 * q] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) b[i] = 0.0f;
+    }
+}
+
+// 16 (gate, up) accumulator pairs plus their biases through the activation,
+// packed as 8 bf16 pairs (feature 2i in the low half)
+template <int ACT>
+__device__ __forceinline__ void glu_pack16(const uint32_t (&g)[16], const uint32_t (&u)[16], const float (&gb)[16],
+                                           const float (&ub)[16], float alpha, float limit, uint32_t (&packed)[8])
+{
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float v0 = activation<ACT>(__uint_as_float(g[i]) + gb[i], __uint_as_float(u[i]) + ub[i], alpha, limit);
+        const float v1 =
+            activation<ACT>(__uint_as_float(g[i + 1]) + gb[i + 1], __uint_as_float(u[i + 1]) + ub[i + 1], alpha, limit);
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(v0, v1);
+        packed[i / 2] = *reinterpret_cast<uint32_t *>(&p2);
+    }
+}
+
 template <int EPI, int BN, typename Maps, int QF = QF_NONE>
 __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ Maps maps,
                                                                                const TcArgs a)
@@ -190,13 +231,15 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
     constexpr int TMEM_COLS = Sh::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + TC_STAGES * STAGE_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Sh::BAR_OFF);
     uint64_t *empty = full + TC_STAGES;
     uint64_t *acc_full = empty + TC_STAGES;   // [2]
     uint64_t *acc_empty = acc_full + 2;       // [2]
     uint64_t *drain = acc_empty + 2;          // the MMA thread's own completion, after an abort
     uint64_t *bready = drain + 1;             // [TC_STAGES] low-bit weights: the B tile is dequantised
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bready + TC_STAGES);
+    uint64_t *raw_full = bready + TC_STAGES;  // [RAW_STAGES] low-bit weights: the packed blocks landed
+    uint64_t *raw_empty = raw_full + Sh::RAW_STAGES;  // [RAW_STAGES] ... and were read
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(raw_empty + Sh::RAW_STAGES);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -213,8 +256,13 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             mbar_init(&acc_empty[b], 128);
         }
         mbar_init(drain, 1);
-        if (FP4)
+        if (FP4) {
             for (int st = 0; st < TC_STAGES; ++st) mbar_init(&bready[st], Sh::DQ_THREADS);
+            for (int st = 0; st < Sh::RAW_STAGES; ++st) {
+                mbar_init(&raw_full[st], 1);
+                mbar_init(&raw_empty[st], Sh::DQ_THREADS);
+            }
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -274,21 +322,10 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     uint8_t *sb = sa + A_TILE_BYTES;
                     const int kc = (ti.kb0 + kb) * TC_BK;
                     if constexpr (FP4) {
-                        // the A tile, and the packed blocks of the tile's 2 x 128 weight rows
-                        // (gate/up: features n0 .. n0+127 as two blocks of 64 gate + 64 up
-                        // rows; down: output rows n0 .. n0+255); a block past the matrix is
-                        // not copied (its rows are written as zeros)
-                        const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
-                        const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
-                        const int nvalid = min(2, nb - b0);
-                        const int nkbt = EPI == EPI_UP ? a.H / TC_BK : a.F / TC_BK;
-                        mbar_arrive_expect_tx(&full[stage], A_TILE_BYTES + nvalid * LB_BLK);
+                        // the A tile only: the raw ring's producer copies the packed
+                        // weight blocks, and the dequantising warps write the B tile
+                        mbar_arrive_expect_tx(&full[stage], A_TILE_BYTES);
                         tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
-                        for (int q = 0; q < nvalid; ++q) {
-                            const size_t blk = ((size_t)ti.g * nb + b0 + q) * nkbt + ti.kb0 + kb;
-                            bulk_load(sb + B_TILE_BYTES + q * LB_BLK, a.fp4 + blk * LB_BLK, LB_BLK,
-                                      &full[stage]);
-                        }
                         used |= 1u << stage;
                         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                         if (++stage == TC_STAGES) stage = 0, phase ^= 1;
@@ -370,48 +407,100 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                 mbar_wait(drain, 0, &never);
             }
         }
+    } else if (FP4 && warp == Sh::RAW_WARP) {
+        // ------------------------------ raw ring producer (low-bit, last warp) ------------------------------
+        // The packed blocks of each stage's 2 x 128 weight rows (gate/up:
+        // features n0 .. n0+127 as two blocks of 64 gate + 64 up rows; down:
+        // output rows n0 .. n0+255), in the A/B ring's order; a block past the
+        // matrix is not copied (its rows are written as zeros).
+        if (lane == 0) {
+            int rs = 0;
+            uint32_t rph = 0;
+            uint32_t used = 0, last_phase = 0;  // per raw stage: copies issued, parity of the last
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                TileInfo ti;
+                if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;  // the A producer records it
+                const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
+                const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
+                const int nvalid = min(2, nb - b0);
+                const int nkbt = EPI == EPI_UP ? a.H / TC_BK : a.F / TC_BK;
+                for (int kb = 0; kb < ti.nk; ++kb) {
+                    if (!mbar_wait(&raw_empty[rs], rph ^ 1, abort_flag)) {
+                        record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *dst = smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE;
+                    mbar_arrive_expect_tx(&raw_full[rs], nvalid * LB_BLK);
+                    for (int q = 0; q < nvalid; ++q) {
+                        const size_t blk = ((size_t)ti.g * nb + b0 + q) * nkbt + ti.kb0 + kb;
+                        bulk_load(dst + q * LB_BLK, a.fp4 + blk * LB_BLK, LB_BLK, &raw_full[rs]);
+                    }
+                    used |= 1u << rs;
+                    last_phase = (last_phase & ~(1u << rs)) | (rph << rs);
+                    if (++rs == Sh::RAW_STAGES) rs = 0, rph ^= 1;
+                }
+            }
+            // drain: no copy of ours may still be landing when the CTA exits
+            volatile int never = 0;
+            for (int st = 0; st < Sh::RAW_STAGES; ++st)
+                if ((used >> st) & 1u) mbar_wait(&raw_full[st], (last_phase >> st) & 1u, &never);
+        }
     } else if (FP4 && warp >= 6) {
         // ------------------------------ low-bit dequantisation (warps 6..13) ------------------------------
-        // Per stage: the 256 rows of the B tile, one per thread, each 64 codes
-        // widened to bf16 (MXFP4 exactly, Q4 rounded once) and written as eight 16-byte chunks at their
-        // 128-byte-swizzle positions (chunk j of row r at r * 128 + ((j ^ (r & 7)) << 4),
-        // the layout the TMA would have written).  Then the writes are made
-        // visible to the tensor cores' reads and the stage is released to the MMA.
+        // Per stage: the 256 rows of the B tile, one per thread.  A thread loads
+        // its row's codes and scales from the raw ring and releases the raw
+        // stage, waits until the MMA has finished with the A/B stage, widens
+        // the 64 codes to bf16 (MXFP4 exactly, Q4 rounded once) and writes them
+        // as eight 16-byte chunks at their 128-byte-swizzle positions (chunk j
+        // of row r at r * 128 + ((j ^ (r & 7)) << 4), the layout the TMA would
+        // have written).  Then the writes are made visible to the tensor cores'
+        // reads and the stage is released to the MMA.
         const int rr = threadIdx.x - TC_THREADS;  // the B-tile row of this thread: 0 .. 255
-        int stage = 0;
-        uint32_t phase = 0;
+        int stage = 0, rs = 0;
+        uint32_t phase = 0, rph = 0;
         bool ok = true;
+        int q, brow;  // the packed block of the tile holding row rr, and the row in it
+        if (EPI == EPI_UP) {
+            const int f = rr & 127;
+            q = f >> 6;
+            brow = (rr < 128 ? 0 : 64) + (f & 63);
+        } else {
+            q = rr >> 7;
+            brow = rr & 127;
+        }
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
             TileInfo ti;
             if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
             const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
             const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
+            const bool zero = b0 + q >= nb;
             for (int kb = 0; kb < ti.nk; ++kb) {
-                if (!mbar_wait(&full[stage], phase, abort_flag)) {
+                if (!mbar_wait(&raw_full[rs], rph, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
                     *abort_flag = 1;
                     ok = false;
                     break;
                 }
-                uint8_t *bt = smem + stage * STAGE_BYTES + A_TILE_BYTES;
-                const uint8_t *raw = bt + B_TILE_BYTES;
-                int q, brow;  // the packed block of the tile holding row rr, and the row in it
-                if (EPI == EPI_UP) {
-                    const int f = rr & 127;
-                    q = f >> 6;
-                    brow = (rr < 128 ? 0 : 64) + (f & 63);
-                } else {
-                    q = rr >> 7;
-                    brow = rr & 127;
+                LowbitRow row;
+                if (!zero) lowbit_load_row<QF>(smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE + q * LB_BLK, brow, row);
+                mbar_arrive(&raw_empty[rs]);
+                if (++rs == Sh::RAW_STAGES) rs = 0, rph ^= 1;
+                if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+                    record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(bt + rr * 128);
-                const uint8_t *pb = raw + q * LB_BLK;
-                if (b0 + q >= nb) {
+                uint4 *dst = reinterpret_cast<uint4 *>(smem + stage * STAGE_BYTES + A_TILE_BYTES + rr * 128);
+                if (zero) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) dst[j ^ (rr & 7)] = make_uint4(0, 0, 0, 0);
                 } else {
                     uint32_t v[32];
-                    lowbit_dequant_row<QF>(pb, brow, fp4tab, v);
+                    lowbit_widen_row<QF>(row, fp4tab, v);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         dst[j ^ (rr & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
@@ -448,6 +537,14 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
             const int b = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
+            // gate/up: the tile's gate and up biases (lane l: features 4l .. 4l+3),
+            // loaded before the accumulator wait so that their latency is hidden
+            float4 bgl = make_float4(0.0f, 0.0f, 0.0f, 0.0f), bul = bgl;
+            if (EPI == EPI_UP && !ti.shared && 4 * lane < min(BN / 2, a.F - ti.n0)) {
+                const size_t o = (size_t)ti.g * a.F + ti.n0 + 4 * lane;
+                if (a.gate_b) bgl = __ldg(reinterpret_cast<const float4 *>(a.gate_b + o));
+                if (a.up_b) bul = __ldg(reinterpret_cast<const float4 *>(a.up_b + o));
+            }
             if (!mbar_wait(&acc_full[b], acc_phase, abort_flag)) {
                 record_error(a.status, DEV_TIMEOUT_ACCUM_BARRIER);
                 *abort_flag = 1;
@@ -483,32 +580,31 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             } else if (EPI == EPI_UP) {
                 const int fd = ti.shared ? a.Fs : a.F;
                 const int hcols = min(BN / 2, fd - ti.n0);  // a multiple of 64 (fd is)
-                const float *bg = (!ti.shared && a.gate_b) ? a.gate_b + (size_t)ti.g * a.F + ti.n0 : nullptr;
-                const float *bu = (!ti.shared && a.up_b) ? a.up_b + (size_t)ti.g * a.F + ti.n0 : nullptr;
                 __nv_bfloat16 *hrow = a.h + (size_t)(ti.a_row0 + j) * a.Fmax + ti.n0;
+                const bool swiglu = ti.shared || a.act == MOE_ACT_SWIGLU;
+                // the biases through this warp's staging area: [gate 128][up 128]
+                float4 *bs = reinterpret_cast<float4 *>(smem + Sh::STAGING_OFF) + q * 128;
+                __syncwarp();  // the previous tile's reads are done
+                bs[lane] = bgl;
+                bs[32 + lane] = bul;
+                __syncwarp();
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 16) {
                     if (c >= hcols) break;
                     uint32_t g[16], u[16];
                     tmem_ld16(tbase + c, g);
                     tmem_ld16(tbase + BN / 2 + c, u);
+                    float gb[16], ub[16];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 x = bs[c / 4 + k], y = bs[32 + c / 4 + k];
+                        gb[4 * k] = x.x; gb[4 * k + 1] = x.y; gb[4 * k + 2] = x.z; gb[4 * k + 3] = x.w;
+                        ub[4 * k] = y.x; ub[4 * k + 1] = y.y; ub[4 * k + 2] = y.z; ub[4 * k + 3] = y.w;
+                    }
                     tmem_ld_wait();
                     uint32_t packed[8];
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        float v[2];
-#pragma unroll
-                        for (int z = 0; z < 2; ++z) {
-                            float gv = __uint_as_float(g[i + z]), uv = __uint_as_float(u[i + z]);
-                            if (bg) gv += bg[c + i + z];
-                            if (bu) uv += bu[c + i + z];
-                            v[z] = (ti.shared || a.act == MOE_ACT_SWIGLU)
-                                       ? activation<MOE_ACT_SWIGLU>(gv, uv, a.alpha, a.limit)
-                                       : activation<MOE_ACT_CLAMP_GLU>(gv, uv, a.alpha, a.limit);
-                        }
-                        __nv_bfloat162 p2 = __floats2bfloat162_rn(v[0], v[1]);
-                        packed[i / 2] = *reinterpret_cast<uint32_t *>(&p2);
-                    }
+                    if (swiglu) glu_pack16<MOE_ACT_SWIGLU>(g, u, gb, ub, a.alpha, a.limit, packed);
+                    else glu_pack16<MOE_ACT_CLAMP_GLU>(g, u, gb, ub, a.alpha, a.limit, packed);
                     if (valid) {
                         uint4 *dst = reinterpret_cast<uint4 *>(hrow + c);
                         dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -541,10 +637,12 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                 for (int c = 0; c < ncols; c += 16) {
                     uint32_t v[16];
                     tmem_ld16(tbase + c, v);
+                    float bb[16];
+                    bias16(bd ? bd + c : nullptr, bb);
                     tmem_ld_wait();
                     float o[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = wgt * (__uint_as_float(v[i]) + (bd ? bd[c + i] : 0.0f));
+                    for (int i = 0; i < 16; ++i) o[i] = wgt * (__uint_as_float(v[i]) + bb[i]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =

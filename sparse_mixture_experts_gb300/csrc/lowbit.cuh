@@ -155,19 +155,34 @@ MXFP4_HD uint32_t q4_bf16_rne(float f)
 
 MXFP4_HD float q4_bf16_float(uint32_t b) { return mxfp4_bits_float(b << 16); }
 
+// binary16 bit pattern -> float (exact): the hardware conversion on the device
+MXFP4_HD float q4_scale_float(uint32_t h)
+{
+#if defined(__CUDA_ARCH__)
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"((unsigned short)h));
+    return f;
+#else
+    return q4_half_to_float(h);
+#endif
+}
+
 // A Q4 scale d (binary16 bits) split into two bf16 values, d = hi + lo
-// exactly: hi = d truncated to bf16 (toward zero), lo = d - hi, which has at
-// most three significant bits and d's sign, so it is a bf16 value too (lo = 0
-// for an infinite or NaN d).  A zero lo carries d's sign as well, so that
-// code 8 times d gives the zero of d's sign.  Returned as bf16 pairs (the
-// value in both halves).
+// exactly: hi = d truncated to bf16 (toward zero: the high half of d's fp32
+// pattern), lo = d - hi, computed exactly in fp32; d has at most 11
+// significant bits and hi keeps the first 8, so lo has at most three and d's
+// sign and is a bf16 value too (the high half of its fp32 pattern).  A zero
+// lo carries d's sign as well, so that code 8 times d gives the zero of d's
+// sign; lo = 0 (with d's sign) for an infinite or NaN d.  Returned as bf16
+// pairs (the value in both halves).
 MXFP4_HD void q4_split_scale(uint32_t h16, uint32_t &hi2, uint32_t &lo2)
 {
-    const float d = q4_half_to_float(h16);
-    const uint32_t hi = mxfp4_float_bits(d) >> 16;
-    const bool finite = ((h16 >> 10) & 31u) != 31u;
-    uint32_t lo = finite ? q4_bf16_rne(d - q4_bf16_float(hi)) : 0u;  // d - hi is exact, and so is lo
-    if ((lo & 0x7fffu) == 0u) lo = h16 & 0x8000u;
+    const float d = q4_scale_float(h16);
+    const uint32_t db = mxfp4_float_bits(d);
+    const uint32_t hi = db >> 16;
+    const float r = d - mxfp4_bits_float(db & 0xffff0000u);  // exact
+    uint32_t lo = ((mxfp4_float_bits(r) >> 16) & 0x7fffu) | (h16 & 0x8000u);
+    if (((h16 >> 10) & 31u) == 31u) lo = h16 & 0x8000u;
     hi2 = hi | (hi << 16);
     lo2 = lo | (lo << 16);
 }
@@ -221,40 +236,72 @@ constexpr int LOWBIT_BLK_MXFP4 = LOWBIT_CODE_BYTES + 128 * 2;      // an E8M0 by
 constexpr int LOWBIT_BLK_Q4 = LOWBIT_CODE_BYTES + 128 * 2 * 2;     // a binary16 per row and half
 
 #if defined(__CUDACC__)
-// Row r of a packed low-bit block (QF 1: MXFP4, 2: Q4) widened to bf16:
-// v[c] holds elements 2c (low half) and 2c + 1, c = 0..31, i.e. the 64 K
-// elements of the block in order.  The loads of both halves come first, so
-// that their latencies overlap.  MXFP4: exact, by the scale byte's table
-// (tabs, in shared memory); Q4: (code - 8) * d rounded once to bf16.
+// Row r of a packed low-bit block as loaded from shared memory: its eight
+// code words (K elements 0..31, then 32..63) and its two scales (an E8M0
+// byte, or a binary16, per half).
+struct LowbitRow {
+    uint32_t w[8];
+    uint32_t s0, s1;
+};
+
+// The loads of row r of a block (both halves first, so that their latencies
+// overlap).  The caller may release the block once this returns.
 template <int QF>
-__device__ __forceinline__ void lowbit_dequant_row(const uint8_t *blk, int r, const Fp4Table *tabs, uint32_t (&v)[32])
+__device__ __forceinline__ void lowbit_load_row(const uint8_t *blk, int r, LowbitRow &row)
 {
     const uint4 c0 = *reinterpret_cast<const uint4 *>(blk + r * 16);
     const uint4 c1 = *reinterpret_cast<const uint4 *>(blk + (128 + r) * 16);
-    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    row.w[0] = c0.x; row.w[1] = c0.y; row.w[2] = c0.z; row.w[3] = c0.w;
+    row.w[4] = c1.x; row.w[5] = c1.y; row.w[6] = c1.z; row.w[7] = c1.w;
     if constexpr (QF == 1) {
-        const Fp4Table t0 = tabs[blk[LOWBIT_CODE_BYTES + r]];
-        const Fp4Table t1 = tabs[blk[LOWBIT_CODE_BYTES + 128 + r]];
+        row.s0 = blk[LOWBIT_CODE_BYTES + r];
+        row.s1 = blk[LOWBIT_CODE_BYTES + 128 + r];
+    } else {
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(blk + LOWBIT_CODE_BYTES);
+        row.s0 = sc[r];
+        row.s1 = sc[128 + r];
+    }
+}
+
+// A loaded row widened to bf16: v[c] holds elements 2c (low half) and 2c + 1,
+// c = 0..31, i.e. the 64 K elements of the block in order.  MXFP4: exact, by
+// the scale byte's table (tabs, in shared memory); Q4: (code - 8) * d rounded
+// once to bf16.
+template <int QF>
+__device__ __forceinline__ void lowbit_widen_row(const LowbitRow &row, const Fp4Table *tabs, uint32_t (&v)[32])
+{
+    if constexpr (QF == 1) {
+        const Fp4Table t0 = tabs[row.s0];
+        const Fp4Table t1 = tabs[row.s1];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             uint32_t o[4];
-            mxfp4_to_bf16x8(words[q], q < 4 ? t0 : t1, o);
+            mxfp4_to_bf16x8(row.w[q], q < 4 ? t0 : t1, o);
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
         }
     } else {
-        const uint16_t *sc = reinterpret_cast<const uint16_t *>(blk + LOWBIT_CODE_BYTES);
         uint32_t hi0, lo0, hi1, lo1;
-        q4_split_scale(sc[r], hi0, lo0);
-        q4_split_scale(sc[128 + r], hi1, lo1);
+        q4_split_scale(row.s0, hi0, lo0);
+        q4_split_scale(row.s1, hi1, lo1);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             uint32_t o[4];
-            q4_to_bf16x8(words[q], q < 4 ? hi0 : hi1, q < 4 ? lo0 : lo1, o);
+            q4_to_bf16x8(row.w[q], q < 4 ? hi0 : hi1, q < 4 ? lo0 : lo1, o);
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
         }
     }
+}
+
+// Row r of a packed low-bit block (QF 1: MXFP4, 2: Q4) widened to bf16 (the
+// two steps above).
+template <int QF>
+__device__ __forceinline__ void lowbit_dequant_row(const uint8_t *blk, int r, const Fp4Table *tabs, uint32_t (&v)[32])
+{
+    LowbitRow row;
+    lowbit_load_row<QF>(blk, r, row);
+    lowbit_widen_row<QF>(row, tabs, v);
 }
 #endif
 

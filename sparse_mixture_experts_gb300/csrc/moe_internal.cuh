@@ -152,7 +152,11 @@ struct Layer {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// logistic function with the fast exponential and the fast (approximate)
+// reciprocal: a few fp32 ulps, far below the bf16 rounding of the activations
+// that follows on every bf16 path (an IEEE division here cost the gate/up
+// epilogue about half of its time); 1 / inf gives 0 for very negative z
+__device__ __forceinline__ float sigmoidf_(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // routed-expert activation; ACT = moe_act
 template <int ACT>
