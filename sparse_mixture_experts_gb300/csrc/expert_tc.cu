@@ -38,25 +38,30 @@ constexpr int TC_THREADS = 192;
 constexpr int A_TILE_BYTES = TC_BM * TC_BK * 2;        // 16 KB
 
 // Per tile width BN (the MMA's N): the B tile, the stage, the ring depth and
-// the TMEM columns (two accumulators of BN fp32 columns).  N = 256 halves the
-// A bytes staged per weight byte, which matters because a CTA's TMA stream,
-// not HBM, limits these GEMMs once the A rows are re-read from L2.
+// the TMEM columns (two accumulators of BN fp32 columns per M half).  N = 256
+// halves the A bytes staged per weight byte, which matters because a CTA's TMA
+// stream, not HBM, limits these GEMMs once the A rows are re-read from L2.
+// Low-bit weights take tiles of TC_LB_TM = 256 token rows: two M = 128 halves,
+// each with its own MMA-issuing thread and accumulators, multiply the same
+// widened B tile, so that the widening -- the work that paces these kernels --
+// is done once per 256 rows.
 template <int BN, int QF = QF_NONE>
 struct TcShape {
     static constexpr bool LOWBIT = QF != QF_NONE;
+    static constexpr int MH = LOWBIT ? TC_LB_TM / TC_BM : 1;  // M halves per tile
     static constexpr int BLK = QF == QF_Q4 ? LOWBIT_BLK_Q4 : LOWBIT_BLK_MXFP4;
+    static constexpr int A_BYTES = MH * A_TILE_BYTES;
     static constexpr int B_BYTES = BN * TC_BK * 2;
-    static constexpr int STAGE = (A_TILE_BYTES + B_BYTES + 1023) / 1024 * 1024;
+    static constexpr int STAGE = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
     static constexpr int STAGES = LOWBIT ? 3 : (BN == 256 ? 4 : 6);
-    // low-bit weights: the packed blocks (codes and scales of 2 x 128 rows x
-    // 64 K) of each stage's B tile land in a ring of their own, filled further
-    // ahead than the A/B ring (a raw stage is a fifth of an A/B stage), from
-    // which dequantising warps write the bf16 B tile
-    static constexpr int RAW_STAGE = LOWBIT ? 2 * BLK : 0;
-    static constexpr int RAW_STAGES = LOWBIT ? 6 : 0;
+    // low-bit weights: the packed block (codes and scales of 128 rows x 64 K)
+    // of each stage's B tile lands in a ring of its own, filled further ahead
+    // than the A/B ring, from which dequantising warps write the bf16 B tile
+    static constexpr int RAW_STAGE = LOWBIT ? BLK : 0;
+    static constexpr int RAW_STAGES = LOWBIT ? 8 : 0;
     static constexpr int RAW_OFF = STAGES * STAGE;
     static constexpr int BAR_OFF = RAW_OFF + (RAW_STAGES * RAW_STAGE + 1023) / 1024 * 1024;
-    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int TMEM_COLS = 2 * MH * BN;
     // after the rings: barriers, then the epilogue's staging (4 warps x 32 rows
     // x 16 fp32), then (MXFP4) the conversion tables of the 256 scale bytes
     static constexpr int STAGING_OFF = BAR_OFF + 512;
@@ -64,13 +69,18 @@ struct TcShape {
     static constexpr int TAB_OFF = STAGING_OFF + STAGING_BYTES;
     static constexpr int TAB_BYTES = QF == QF_MXFP4 ? 256 * (int)sizeof(Fp4Table) : 0;
     static constexpr size_t SMEM = (size_t)TAB_OFF + TAB_BYTES + 1024 /*align*/;
-    static constexpr int DQ_THREADS = LOWBIT ? 256 : 0;  // dequantising warps: one B row each
+    static constexpr int DQ_THREADS = LOWBIT ? 256 : 0;  // dequantising warps: one (B row, K half) each
     static constexpr int RAW_WARP = (TC_THREADS + DQ_THREADS) / 32;  // the raw ring's producer (low-bit)
-    static constexpr int THREADS = TC_THREADS + DQ_THREADS + (LOWBIT ? 32 : 0);
+    static constexpr int MMA2_WARP = RAW_WARP + 1;                   // the second M half's MMA issuer (low-bit)
+    static constexpr int THREADS = TC_THREADS + DQ_THREADS + (LOWBIT ? 64 : 0);
+    // tile geometry (tc_geometry gives the same to the grouping kernel)
+    static constexpr int TM = LOWBIT ? TC_LB_TM : TC_BM;
     // barriers: full, empty, bready per A/B stage; two accumulators' full and
-    // empty; drain; raw full and empty per raw stage; the TMEM address and the
-    // abort word
-    static_assert((3 * STAGES + 5 + 2 * RAW_STAGES) * 8 + 8 <= 512, "barrier area");
+    // empty; a drain per M half; raw full and empty per raw stage; the TMEM
+    // address and the abort word
+    static_assert((3 * STAGES + 6 + 2 * RAW_STAGES) * 8 + 8 <= 512, "barrier area");
+    static_assert(TMEM_COLS <= 512, "tensor memory");
+    static_assert(!LOWBIT || BN == TC_LB_BN, "low-bit tiles are one packed block wide");
 };
 
 struct TensorMaps {
@@ -142,7 +152,7 @@ struct GroupTab {
 
 // gcur: the caller's group cursor (each role visits its tiles in increasing
 // order, so the group only moves forward); start at 0
-template <int EPI>
+template <int EPI, int TM, int TNU, int TND>
 __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, const GroupTab &gt, int &gcur)
 {
     if (EPI == EPI_ROUTER) {
@@ -176,12 +186,12 @@ __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, 
     if (ti.g < 0 || ti.g > a.E || (ti.shared && a.Fs == 0)) return false;
     ti.rows = gt.rows[lo];
     ti.a_row0 = gt.row0[lo];
-    const int mt = (ti.rows + TC_BM - 1) / TC_BM;
+    const int mt = (ti.rows + TM - 1) / TM;
     if (mt <= 0) return false;
     const int local = t - gt.first[lo];
     const int n = local / mt;
-    ti.m0 = (local - n * mt) * TC_BM;
-    ti.n0 = n * (EPI == EPI_UP ? TC_BN_UP / 2 : TC_BN_DOWN);
+    ti.m0 = (local - n * mt) * TM;
+    ti.n0 = n * (EPI == EPI_UP ? TNU : TND);
     if (EPI == EPI_UP) ti.nk = a.H / TC_BK;
     else ti.nk = (ti.shared ? a.Fs : a.F) / TC_BK;
     return ti.m0 >= 0 && ti.m0 < ti.rows && ti.n0 >= 0;
@@ -229,14 +239,17 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
     constexpr int STAGE_BYTES = Sh::STAGE;
     constexpr int B_TILE_BYTES = Sh::B_BYTES;
     constexpr int TMEM_COLS = Sh::TMEM_COLS;
+    constexpr int MH = Sh::MH;
+    constexpr int TNU = FP4 ? TC_LB_BN / 2 : TC_BN_UP / 2;  // gate/up features per tile
+    constexpr int TND = FP4 ? TC_LB_BN : TC_BN_DOWN;        // down output columns per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Sh::BAR_OFF);
     uint64_t *empty = full + TC_STAGES;
     uint64_t *acc_full = empty + TC_STAGES;   // [2]
     uint64_t *acc_empty = acc_full + 2;       // [2]
-    uint64_t *drain = acc_empty + 2;          // the MMA thread's own completion, after an abort
-    uint64_t *bready = drain + 1;             // [TC_STAGES] low-bit weights: the B tile is dequantised
+    uint64_t *drain = acc_empty + 2;          // [2] each MMA thread's own completion, after an abort
+    uint64_t *bready = drain + 2;             // [TC_STAGES] low-bit weights: the B tile is dequantised
     uint64_t *raw_full = bready + TC_STAGES;  // [RAW_STAGES] low-bit weights: the packed blocks landed
     uint64_t *raw_empty = raw_full + Sh::RAW_STAGES;  // [RAW_STAGES] ... and were read
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(raw_empty + Sh::RAW_STAGES);
@@ -247,15 +260,16 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                                           : (EPI == EPI_UP ? a.meta->n_up_tiles : a.meta->n_down_tiles);
 
     if (threadIdx.x == 0) {
+        // empty and acc_full: one arrival per M half's MMA thread
         for (int s = 0; s < TC_STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], MH);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_full[b], MH);
             mbar_init(&acc_empty[b], 128);
+            mbar_init(&drain[b], 1);
         }
-        mbar_init(drain, 1);
         if (FP4) {
             for (int st = 0; st < TC_STAGES; ++st) mbar_init(&bready[st], Sh::DQ_THREADS);
             for (int st = 0; st < Sh::RAW_STAGES; ++st) {
@@ -306,7 +320,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 TileInfo ti;
-                if (!tile_info<EPI>(a, t, ti, gt, gcur)) {
+                if (!tile_info<EPI, Sh::TM, TNU, TND>(a, t, ti, gt, gcur)) {
                     record_error(a.status, DEV_BAD_TILE);
                     *abort_flag = 1;
                     break;
@@ -322,10 +336,13 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     uint8_t *sb = sa + A_TILE_BYTES;
                     const int kc = (ti.kb0 + kb) * TC_BK;
                     if constexpr (FP4) {
-                        // the A tile only: the raw ring's producer copies the packed
-                        // weight blocks, and the dequantising warps write the B tile
-                        mbar_arrive_expect_tx(&full[stage], A_TILE_BYTES);
+                        // the A tiles only (rows m0 .. m0+127, and m0+128 .. m0+255 where
+                        // the group has such rows): the raw ring's producer copies the
+                        // packed weight block, and the dequantising warps write the B tile
+                        const bool two = ti.m0 + TC_BM < ti.rows;
+                        mbar_arrive_expect_tx(&full[stage], two ? 2 * A_TILE_BYTES : A_TILE_BYTES);
                         tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
+                        if (two) tma_load_2d(sa + A_TILE_BYTES, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0 + TC_BM);
                         used |= 1u << stage;
                         last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
                         if (++stage == TC_STAGES) stage = 0, phase ^= 1;
@@ -352,9 +369,14 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             for (int s = 0; s < TC_STAGES; ++s)
                 if ((used >> s) & 1u) mbar_wait(&full[s], (last_phase >> s) & 1u, &never);
         }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer ------------------------------
+    } else if (warp == 1 || (FP4 && warp == Sh::MMA2_WARP)) {
+        // ------------------------------ MMA issuers ------------------------------
+        // One thread per M half (low-bit tiles have two): half h multiplies the
+        // A rows m0 + 128h .. m0 + 128h + 127 with the stage's B tile into its
+        // own accumulator columns.  A half without rows in the tile issues
+        // nothing and arrives on the barriers its MMAs would have signalled.
         if (lane == 0) {
+            const int half = warp == 1 ? 0 : 1;
             constexpr uint32_t idesc = idesc_bf16_f32(TC_BM, BN);
             int stage = 0;
             uint32_t phase = 0;
@@ -363,7 +385,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             bool issued = false;  // any MMA of this thread
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
                 TileInfo ti;
-                if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
+                if (!tile_info<EPI, Sh::TM, TNU, TND>(a, t, ti, gt, gcur)) break;
                 const int b = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!mbar_wait(&acc_empty[b], acc_phase ^ 1, abort_flag)) {
@@ -372,7 +394,8 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(b * BN);
+                const bool active = ti.m0 + half * TC_BM < ti.rows;
+                const uint32_t d_tmem = tmem_base + (uint32_t)((b * MH + half) * BN);
                 for (int kb = 0; kb < ti.nk; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort_flag) ||
                         (FP4 && !mbar_wait(&bready[stage], phase, abort_flag))) {
@@ -382,20 +405,25 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-                    const uint32_t sb = sa + A_TILE_BYTES;
+                    if (active) {
+                        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES) + half * A_TILE_BYTES;
+                        const uint32_t sb = smem_u32(smem + stage * STAGE_BYTES) + Sh::A_BYTES;
 #pragma unroll
-                    for (int k = 0; k < TC_BK / 16; ++k) {
-                        // advance 16 bf16 = 32 bytes along K inside the swizzled row
-                        mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
-                                 (kb | k) != 0);
+                        for (int k = 0; k < TC_BK / 16; ++k) {
+                            // advance 16 bf16 = 32 bytes along K inside the swizzled row
+                            mma_bf16(d_tmem, smem_desc_sw128(sa + k * 32), smem_desc_sw128(sb + k * 32), idesc,
+                                     (kb | k) != 0);
+                        }
+                        mma_commit(&empty[stage]);
+                        issued = true;
+                    } else {
+                        mbar_arrive(&empty[stage]);
                     }
-                    mma_commit(&empty[stage]);
-                    issued = true;
                     if (++stage == TC_STAGES) stage = 0, phase ^= 1;
                 }
                 if (!ok) break;
-                mma_commit(&acc_full[b]);
+                if (active) mma_commit(&acc_full[b]);
+                else mbar_arrive(&acc_full[b]);
             }
             // every MMA this thread issued completes before the shared memory it
             // reads and the tensor memory it writes are released: after an abort
@@ -403,16 +431,15 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             // MMAs may not be committed to one)
             if (issued) {
                 volatile int never = 0;
-                mma_commit(drain);
-                mbar_wait(drain, 0, &never);
+                mma_commit(&drain[half]);
+                mbar_wait(&drain[half], 0, &never);
             }
         }
     } else if (FP4 && warp == Sh::RAW_WARP) {
         // ------------------------------ raw ring producer (low-bit, last warp) ------------------------------
-        // The packed blocks of each stage's 2 x 128 weight rows (gate/up:
-        // features n0 .. n0+127 as two blocks of 64 gate + 64 up rows; down:
-        // output rows n0 .. n0+255), in the A/B ring's order; a block past the
-        // matrix is not copied (its rows are written as zeros).
+        // The packed block of each stage's 128 weight rows (gate/up: features
+        // n0 .. n0+63 as 64 gate + 64 up rows; down: output rows n0 .. n0+127),
+        // in the A/B ring's order.
         if (lane == 0) {
             int rs = 0;
             uint32_t rph = 0;
@@ -420,10 +447,9 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 TileInfo ti;
-                if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;  // the A producer records it
+                if (!tile_info<EPI, Sh::TM, TNU, TND>(a, t, ti, gt, gcur)) break;  // the A producer records it
                 const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
-                const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
-                const int nvalid = min(2, nb - b0);
+                const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;  // < nb
                 const int nkbt = EPI == EPI_UP ? a.H / TC_BK : a.F / TC_BK;
                 for (int kb = 0; kb < ti.nk; ++kb) {
                     if (!mbar_wait(&raw_empty[rs], rph ^ 1, abort_flag)) {
@@ -433,11 +459,9 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                         break;
                     }
                     uint8_t *dst = smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE;
-                    mbar_arrive_expect_tx(&raw_full[rs], nvalid * LB_BLK);
-                    for (int q = 0; q < nvalid; ++q) {
-                        const size_t blk = ((size_t)ti.g * nb + b0 + q) * nkbt + ti.kb0 + kb;
-                        bulk_load(dst + q * LB_BLK, a.fp4 + blk * LB_BLK, LB_BLK, &raw_full[rs]);
-                    }
+                    mbar_arrive_expect_tx(&raw_full[rs], LB_BLK);
+                    const size_t blk = ((size_t)ti.g * nb + b0) * nkbt + ti.kb0 + kb;
+                    bulk_load(dst, a.fp4 + blk * LB_BLK, LB_BLK, &raw_full[rs]);
                     used |= 1u << rs;
                     last_phase = (last_phase & ~(1u << rs)) | (rph << rs);
                     if (++rs == Sh::RAW_STAGES) rs = 0, rph ^= 1;
@@ -450,33 +474,23 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
         }
     } else if (FP4 && warp >= 6) {
         // ------------------------------ low-bit dequantisation (warps 6..13) ------------------------------
-        // Per stage: the 256 rows of the B tile, one per thread.  A thread loads
-        // its row's codes and scales from the raw ring and releases the raw
-        // stage, waits until the MMA has finished with the A/B stage, widens
-        // the 64 codes to bf16 (MXFP4 exactly, Q4 rounded once) and writes them
-        // as eight 16-byte chunks at their 128-byte-swizzle positions (chunk j
-        // of row r at r * 128 + ((j ^ (r & 7)) << 4), the layout the TMA would
+        // Per stage: the 128 rows of the B tile (the rows of the stage's packed
+        // block, in order), each K half of a row by one thread.  A thread loads
+        // its 32 codes and their scale from the raw ring and releases the raw
+        // stage, waits until the MMAs have finished with the A/B stage, widens
+        // the codes to bf16 (MXFP4 exactly, Q4 rounded once) and writes them as
+        // four 16-byte chunks at their 128-byte-swizzle positions (chunk c of
+        // row r at r * 128 + ((c ^ (r & 7)) << 4), the layout the TMA would
         // have written).  Then the writes are made visible to the tensor cores'
-        // reads and the stage is released to the MMA.
-        const int rr = threadIdx.x - TC_THREADS;  // the B-tile row of this thread: 0 .. 255
+        // reads and the stage is released to the MMAs.
+        const int rr = (threadIdx.x - TC_THREADS) & 127;  // the B-tile row of this thread
+        const int hk = (threadIdx.x - TC_THREADS) >> 7;   // its K half
         int stage = 0, rs = 0;
         uint32_t phase = 0, rph = 0;
         bool ok = true;
-        int q, brow;  // the packed block of the tile holding row rr, and the row in it
-        if (EPI == EPI_UP) {
-            const int f = rr & 127;
-            q = f >> 6;
-            brow = (rr < 128 ? 0 : 64) + (f & 63);
-        } else {
-            q = rr >> 7;
-            brow = rr & 127;
-        }
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
             TileInfo ti;
-            if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
-            const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
-            const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
-            const bool zero = b0 + q >= nb;
+            if (!tile_info<EPI, Sh::TM, TNU, TND>(a, t, ti, gt, gcur)) break;
             for (int kb = 0; kb < ti.nk; ++kb) {
                 if (!mbar_wait(&raw_full[rs], rph, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
@@ -484,8 +498,8 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     ok = false;
                     break;
                 }
-                LowbitRow row;
-                if (!zero) lowbit_load_row<QF>(smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE + q * LB_BLK, brow, row);
+                LowbitHalf x;
+                lowbit_load_half<QF>(smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE, rr, hk, x);
                 mbar_arrive(&raw_empty[rs]);
                 if (++rs == Sh::RAW_STAGES) rs = 0, rph ^= 1;
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
@@ -494,17 +508,12 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     ok = false;
                     break;
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(smem + stage * STAGE_BYTES + A_TILE_BYTES + rr * 128);
-                if (zero) {
+                uint4 *dst = reinterpret_cast<uint4 *>(smem + stage * STAGE_BYTES + Sh::A_BYTES + rr * 128);
+                uint32_t v[16];
+                lowbit_widen_half<QF>(x, fp4tab, v);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) dst[j ^ (rr & 7)] = make_uint4(0, 0, 0, 0);
-                } else {
-                    uint32_t v[32];
-                    lowbit_widen_row<QF>(row, fp4tab, v);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[j ^ (rr & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                }
+                for (int j = 0; j < 4; ++j)
+                    dst[(4 * hk + j) ^ (rr & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 fence_proxy_async_shared();
                 mbar_arrive(&bready[stage]);
                 if (++stage == TC_STAGES) stage = 0, phase ^= 1;
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
         }
         for (int t = blockIdx.x; run && t < n_tiles; t += gridDim.x, ++it) {
             TileInfo ti;
-            if (!tile_info<EPI>(a, t, ti, gt, gcur)) break;
+            if (!tile_info<EPI, Sh::TM, TNU, TND>(a, t, ti, gt, gcur)) break;
             const int b = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             // gate/up: the tile's gate and up biases (lane l: features 4l .. 4l+3),
@@ -551,111 +560,118 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                 break;
             }
             tc_fence_after();
-            const uint32_t tbase = tmem_base + lane_addr + (uint32_t)(b * BN);
-            const int j = ti.m0 + r;              // row within the group
-            const bool valid = j < ti.rows;
-            if (EPI == EPI_ROUTER) {
-                // logits[t][n] (+ router bias), fp32, or with K split the partial
-                // sum of this K range (the bias in the first); R need not be a
-                // multiple of 4
-                float *dst = a.router_S > 1 ? a.rparts + (size_t)ti.split * a.T * a.R : a.logits;
-                const bool with_bias = a.router_b && ti.split == 0;
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
-                    if (ti.n0 + c >= a.R) break;  // the same for the whole warp
-                    uint32_t v[16];
-                    tmem_ld16(tbase + c, v);
-                    tmem_ld_wait();
-                    if (valid) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int n = ti.n0 + c + i;
-                            if (n < a.R) {
-                                const float b = (with_bias && n < a.E) ? a.router_b[n] : 0.0f;
-                                dst[(size_t)j * a.R + n] = __uint_as_float(v[i]) + b;
-                            }
-                        }
-                    }
-                }
-            } else if (EPI == EPI_UP) {
-                const int fd = ti.shared ? a.Fs : a.F;
-                const int hcols = min(BN / 2, fd - ti.n0);  // a multiple of 64 (fd is)
-                __nv_bfloat16 *hrow = a.h + (size_t)(ti.a_row0 + j) * a.Fmax + ti.n0;
-                const bool swiglu = ti.shared || a.act == MOE_ACT_SWIGLU;
+            if (EPI == EPI_UP) {
                 // the biases through this warp's staging area: [gate 128][up 128]
                 float4 *bs = reinterpret_cast<float4 *>(smem + Sh::STAGING_OFF) + q * 128;
                 __syncwarp();  // the previous tile's reads are done
                 bs[lane] = bgl;
                 bs[32 + lane] = bul;
                 __syncwarp();
-#pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 16) {
-                    if (c >= hcols) break;
-                    uint32_t g[16], u[16];
-                    tmem_ld16(tbase + c, g);
-                    tmem_ld16(tbase + BN / 2 + c, u);
-                    float gb[16], ub[16];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float4 x = bs[c / 4 + k], y = bs[32 + c / 4 + k];
-                        gb[4 * k] = x.x; gb[4 * k + 1] = x.y; gb[4 * k + 2] = x.z; gb[4 * k + 3] = x.w;
-                        ub[4 * k] = y.x; ub[4 * k + 1] = y.y; ub[4 * k + 2] = y.z; ub[4 * k + 3] = y.w;
+            }
+            // each M half of the tile that has rows (low-bit tiles have two)
+            for (int hm = 0; hm < MH; ++hm) {
+                if (ti.m0 + hm * TC_BM >= ti.rows) break;  // the same for the whole CTA
+                const uint32_t tbase = tmem_base + lane_addr + (uint32_t)((b * MH + hm) * BN);
+                const int j = ti.m0 + hm * TC_BM + r;  // row within the group
+                const bool valid = j < ti.rows;
+                if (EPI == EPI_ROUTER) {
+                    // logits[t][n] (+ router bias), fp32, or with K split the partial
+                    // sum of this K range (the bias in the first); R need not be a
+                    // multiple of 4
+                    float *dst = a.router_S > 1 ? a.rparts + (size_t)ti.split * a.T * a.R : a.logits;
+                    const bool with_bias = a.router_b && ti.split == 0;
+    #pragma unroll 1
+                    for (int c = 0; c < BN; c += 16) {
+                        if (ti.n0 + c >= a.R) break;  // the same for the whole warp
+                        uint32_t v[16];
+                        tmem_ld16(tbase + c, v);
+                        tmem_ld_wait();
+                        if (valid) {
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int n = ti.n0 + c + i;
+                                if (n < a.R) {
+                                    const float b = (with_bias && n < a.E) ? a.router_b[n] : 0.0f;
+                                    dst[(size_t)j * a.R + n] = __uint_as_float(v[i]) + b;
+                                }
+                            }
+                        }
                     }
-                    tmem_ld_wait();
-                    uint32_t packed[8];
-                    if (swiglu) glu_pack16<MOE_ACT_SWIGLU>(g, u, gb, ub, a.alpha, a.limit, packed);
-                    else glu_pack16<MOE_ACT_CLAMP_GLU>(g, u, gb, ub, a.alpha, a.limit, packed);
+                } else if (EPI == EPI_UP) {
+                    const int fd = ti.shared ? a.Fs : a.F;
+                    const int hcols = min(BN / 2, fd - ti.n0);  // a multiple of 64 (fd is)
+                    __nv_bfloat16 *hrow = a.h + (size_t)(ti.a_row0 + j) * a.Fmax + ti.n0;
+                    const bool swiglu = ti.shared || a.act == MOE_ACT_SWIGLU;
+                    const float4 *bs = reinterpret_cast<const float4 *>(smem + Sh::STAGING_OFF) + q * 128;
+    #pragma unroll 1
+                    for (int c = 0; c < BN / 2; c += 16) {
+                        if (c >= hcols) break;
+                        uint32_t g[16], u[16];
+                        tmem_ld16(tbase + c, g);
+                        tmem_ld16(tbase + BN / 2 + c, u);
+                        float gb[16], ub[16];
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float4 x = bs[c / 4 + k], y = bs[32 + c / 4 + k];
+                            gb[4 * k] = x.x; gb[4 * k + 1] = x.y; gb[4 * k + 2] = x.z; gb[4 * k + 3] = x.w;
+                            ub[4 * k] = y.x; ub[4 * k + 1] = y.y; ub[4 * k + 2] = y.z; ub[4 * k + 3] = y.w;
+                        }
+                        tmem_ld_wait();
+                        uint32_t packed[8];
+                        if (swiglu) glu_pack16<MOE_ACT_SWIGLU>(g, u, gb, ub, a.alpha, a.limit, packed);
+                        else glu_pack16<MOE_ACT_CLAMP_GLU>(g, u, gb, ub, a.alpha, a.limit, packed);
+                        if (valid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(hrow + c);
+                            dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                            dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                        }
+                    }
+                } else {
+                    int tok = 0, slot = 0;
+                    float wgt = 0.0f;
                     if (valid) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(hrow + c);
-                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                        if (ti.shared) { tok = j; slot = a.K; wgt = a.sh_gate[tok]; }
+                        else {
+                            const int p = a.expert_rows[ti.a_row0 + j];
+                            tok = p / a.K; slot = p - tok * a.K; wgt = a.topk_w[p];
+                        }
                     }
-                }
-            } else {
-                int tok = 0, slot = 0;
-                float wgt = 0.0f;
-                if (valid) {
-                    if (ti.shared) { tok = j; slot = a.K; wgt = a.sh_gate[tok]; }
-                    else {
-                        const int p = a.expert_rows[ti.a_row0 + j];
-                        tok = p / a.K; slot = p - tok * a.K; wgt = a.topk_w[p];
+                    const float *bd = (!ti.shared && a.down_b) ? a.down_b + (size_t)ti.g * a.H + ti.n0 : nullptr;
+                    // this thread's fp32 row of the per-slot buffer (0: a row past the group's end)
+                    const unsigned long long yrow =
+                        valid ? reinterpret_cast<unsigned long long>(a.ys + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n0)
+                              : 0ull;
+                    const int ncols = min(BN, a.H - ti.n0);  // the same for the whole tile; a multiple of 64 (H is)
+                    // Each thread holds one row; the warp's 32 rows x 16 columns go
+                    // through shared memory so that each store instruction writes 8
+                    // rows x 64 contiguous bytes (whole sectors) instead of 32 rows x
+                    // 16 bytes.  Row r's float4 q sits at r * 4 + (q ^ ((r >> 1) & 3)):
+                    // no bank conflicts for the row-wise writes or the column-wise reads.
+                    float4 *stg = reinterpret_cast<float4 *>(smem + Sh::STAGING_OFF) + q * 128;
+    #pragma unroll 1
+                    for (int c = 0; c < ncols; c += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tbase + c, v);
+                        float bb[16];
+                        bias16(bd ? bd + c : nullptr, bb);
+                        tmem_ld_wait();
+                        float o[16];
+    #pragma unroll
+                        for (int i = 0; i < 16; ++i) o[i] = wgt * (__uint_as_float(v[i]) + bb[i]);
+    #pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =
+                                make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                        __syncwarp();
+    #pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int f = i * 32 + lane, rr = f >> 2, qq = f & 3;
+                            const float4 val = stg[rr * 4 + (qq ^ ((rr >> 1) & 3))];
+                            const unsigned long long dst = __shfl_sync(0xffffffffu, yrow, rr);
+                            if (dst) reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + c)[qq] = val;
+                        }
+                        __syncwarp();
                     }
-                }
-                const float *bd = (!ti.shared && a.down_b) ? a.down_b + (size_t)ti.g * a.H + ti.n0 : nullptr;
-                // this thread's fp32 row of the per-slot buffer (0: a row past the group's end)
-                const unsigned long long yrow =
-                    valid ? reinterpret_cast<unsigned long long>(a.ys + ((size_t)tok * (a.K + 1) + slot) * a.H + ti.n0)
-                          : 0ull;
-                const int ncols = min(BN, a.H - ti.n0);  // the same for the whole tile; a multiple of 64 (H is)
-                // Each thread holds one row; the warp's 32 rows x 16 columns go
-                // through shared memory so that each store instruction writes 8
-                // rows x 64 contiguous bytes (whole sectors) instead of 32 rows x
-                // 16 bytes.  Row r's float4 q sits at r * 4 + (q ^ ((r >> 1) & 3)):
-                // no bank conflicts for the row-wise writes or the column-wise reads.
-                float4 *stg = reinterpret_cast<float4 *>(smem + Sh::STAGING_OFF) + q * 128;
-#pragma unroll 1
-                for (int c = 0; c < ncols; c += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tbase + c, v);
-                    float bb[16];
-                    bias16(bd ? bd + c : nullptr, bb);
-                    tmem_ld_wait();
-                    float o[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = wgt * (__uint_as_float(v[i]) + bb[i]);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =
-                            make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int f = i * 32 + lane, rr = f >> 2, qq = f & 3;
-                        const float4 val = stg[rr * 4 + (qq ^ ((rr >> 1) & 3))];
-                        const unsigned long long dst = __shfl_sync(0xffffffffu, yrow, rr);
-                        if (dst) reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + c)[qq] = val;
-                    }
-                    __syncwarp();
                 }
             }
             tc_fence_before();
@@ -749,18 +765,18 @@ int tc_prepare(Layer &L)
                              (int)TcShape<TC_BN_DOWN>::SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<EPI_ROUTER, 128, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)TcShape<128>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, QF_MXFP4>,
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_LB_BN, TcMaps, QF_MXFP4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_BN_UP, QF_MXFP4>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, QF_MXFP4>,
+                             (int)TcShape<TC_LB_BN, QF_MXFP4>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_LB_BN, TcMaps, QF_MXFP4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_BN_DOWN, QF_MXFP4>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, QF_Q4>,
+                             (int)TcShape<TC_LB_BN, QF_MXFP4>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_LB_BN, TcMaps, QF_Q4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_BN_UP, QF_Q4>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, QF_Q4>,
+                             (int)TcShape<TC_LB_BN, QF_Q4>::SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_LB_BN, TcMaps, QF_Q4>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_BN_DOWN, QF_Q4>::SMEM) != cudaSuccess) {
+                             (int)TcShape<TC_LB_BN, QF_Q4>::SMEM) != cudaSuccess) {
         delete m;
         return -1;
     }
@@ -805,12 +821,12 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
         if (L.Fs > 0 && !encode_2d(&mu.sa, x, L.H, (uint64_t)T, TC_BM)) return -1;
         if (L.qfmt == QF_MXFP4) {
             a.fp4 = L.fp4_gu;
-            using Sh = TcShape<TC_BN_UP, QF_MXFP4>;
-            tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, QF_MXFP4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
+            using Sh = TcShape<TC_LB_BN, QF_MXFP4>;
+            tc_gemm_kernel<EPI_UP, TC_LB_BN, TcMaps, QF_MXFP4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
         } else if (L.qfmt == QF_Q4) {
             a.fp4 = L.fp4_gu;
-            using Sh = TcShape<TC_BN_UP, QF_Q4>;
-            tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps, QF_Q4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
+            using Sh = TcShape<TC_LB_BN, QF_Q4>;
+            tc_gemm_kernel<EPI_UP, TC_LB_BN, TcMaps, QF_Q4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
         } else {
             tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_UP>::SMEM, s>>>(mu, a);
         }
@@ -818,12 +834,12 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
         TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down, m.h};
         if (L.qfmt == QF_MXFP4) {
             a.fp4 = L.fp4_dn;
-            using Sh = TcShape<TC_BN_DOWN, QF_MXFP4>;
-            tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, QF_MXFP4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
+            using Sh = TcShape<TC_LB_BN, QF_MXFP4>;
+            tc_gemm_kernel<EPI_DOWN, TC_LB_BN, TcMaps, QF_MXFP4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
         } else if (L.qfmt == QF_Q4) {
             a.fp4 = L.fp4_dn;
-            using Sh = TcShape<TC_BN_DOWN, QF_Q4>;
-            tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps, QF_Q4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
+            using Sh = TcShape<TC_LB_BN, QF_Q4>;
+            tc_gemm_kernel<EPI_DOWN, TC_LB_BN, TcMaps, QF_Q4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
         } else {
             tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_DOWN>::SMEM, s>>>(md, a);
         }

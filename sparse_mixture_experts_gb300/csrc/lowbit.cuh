@@ -294,8 +294,50 @@ __device__ __forceinline__ void lowbit_widen_row(const LowbitRow &row, const Fp4
     }
 }
 
+// Half h (K elements 32h .. 32h+31) of row r of a packed block: its four code
+// words and its scale.
+struct LowbitHalf {
+    uint32_t w[4];
+    uint32_t s;
+};
+
+template <int QF>
+__device__ __forceinline__ void lowbit_load_half(const uint8_t *blk, int r, int h, LowbitHalf &x)
+{
+    const uint4 c = *reinterpret_cast<const uint4 *>(blk + (h * 128 + r) * 16);
+    x.w[0] = c.x; x.w[1] = c.y; x.w[2] = c.z; x.w[3] = c.w;
+    if constexpr (QF == 1) x.s = blk[LOWBIT_CODE_BYTES + h * 128 + r];
+    else x.s = reinterpret_cast<const uint16_t *>(blk + LOWBIT_CODE_BYTES)[h * 128 + r];
+}
+
+// A loaded half widened to bf16: v[c] holds its elements 2c (low half) and 2c + 1
+template <int QF>
+__device__ __forceinline__ void lowbit_widen_half(const LowbitHalf &x, const Fp4Table *tabs, uint32_t (&v)[16])
+{
+    if constexpr (QF == 1) {
+        const Fp4Table t = tabs[x.s];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t o[4];
+            mxfp4_to_bf16x8(x.w[q], t, o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
+        }
+    } else {
+        uint32_t hi, lo;
+        q4_split_scale(x.s, hi, lo);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t o[4];
+            q4_to_bf16x8(x.w[q], hi, lo, o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[q * 4 + i] = o[i];
+        }
+    }
+}
+
 // Row r of a packed low-bit block (QF 1: MXFP4, 2: Q4) widened to bf16 (the
-// two steps above).
+// two row steps above).
 template <int QF>
 __device__ __forceinline__ void lowbit_dequant_row(const uint8_t *blk, int r, const Fp4Table *tabs, uint32_t (&v)[32])
 {

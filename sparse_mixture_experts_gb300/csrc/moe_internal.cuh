@@ -485,5 +485,21 @@ constexpr int TC_BN_UP = 256;    // gate/up tile: 128 gate + 128 up columns -> 1
 constexpr int TC_BN_DOWN = 256;  // down tile: output columns
 constexpr int TC_BK = 64;        // K elements per pipeline stage (128 bytes of bf16)
 constexpr int TC_ROUTER_MAX_SPLITS = 4;  // K ranges of the tensor-core router GEMM
+// low-bit experts: a tile is 256 token rows (two M = 128 halves sharing one
+// widened weight tile, so that each weight block is widened once per 256
+// rows) by one packed block of 128 weight rows (64 gate + 64 up features, or
+// 128 down output columns)
+constexpr int TC_LB_TM = 256;
+constexpr int TC_LB_BN = 128;
+
+// token rows, gate/up features and down output columns per tile of the
+// expert GEMMs, for a layer of routed-expert format qfmt
+struct TcGeometry {
+    int tm, tnu, tnd;
+};
+inline TcGeometry tc_geometry(int qfmt)
+{
+    return qfmt != QF_NONE ? TcGeometry{TC_LB_TM, TC_LB_BN / 2, TC_LB_BN} : TcGeometry{TC_BM, TC_BN_UP / 2, TC_BN_DOWN};
+}
 
 }  // namespace moe

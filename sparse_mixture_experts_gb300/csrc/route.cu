@@ -198,6 +198,7 @@ struct GroupArgs {
     int *gfirst;      // [5][E + 2]: per group first gate/up tile (+ total), first down tile (+ total), expert, rows, first row
     RouteMeta *meta;
     int build_tiles;
+    int tm, tnu, tnd; // tile geometry of the expert GEMMs (tc_geometry)
 };
 
 __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
@@ -262,14 +263,14 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
     int n_up = 0, n_down = 0;
     if (a.build_tiles) {
         const int n_groups = n_act + (a.has_shared ? 1 : 0);  // <= E + 1
-        const int n_dn = (a.H + TC_BN_DOWN - 1) / TC_BN_DOWN;
+        const int n_dn = (a.H + a.tnd - 1) / a.tnd;
         const int gper = (n_groups + GT - 1) / GT;
         const int gb = min(n_groups, tid * gper), ge = min(n_groups, gb + gper);
         int cu = 0, cd = 0;
         for (int g = gb; g < ge; ++g) {
             const bool shared = g >= n_act;
-            const int mt = ((shared ? a.T : s_cnt[s_act[g]]) + TC_BM - 1) / TC_BM;
-            cu += mt * (((shared ? a.Fs : a.F) + TC_BN_UP / 2 - 1) / (TC_BN_UP / 2));
+            const int mt = ((shared ? a.T : s_cnt[s_act[g]]) + a.tm - 1) / a.tm;
+            cu += mt * (((shared ? a.Fs : a.F) + a.tnu - 1) / a.tnu);
             cd += mt * n_dn;
         }
         int fu = block_exclusive_scan(cu, &n_up);
@@ -279,13 +280,13 @@ __global__ void __launch_bounds__(GT) group_kernel(GroupArgs a)
         for (int g = gb; g < ge; ++g) {
             const bool shared = g >= n_act;
             const int rows = shared ? a.T : s_cnt[s_act[g]];
-            const int mt = (rows + TC_BM - 1) / TC_BM;
+            const int mt = (rows + a.tm - 1) / a.tm;
             gu[g] = fu;
             gd[g] = fd;
             gx[g] = shared ? E : s_act[g];
             gr[g] = rows;
             g0[g] = shared ? a.T * a.K : __ldcg(&a.offsets[s_act[g]]);
-            fu += mt * (((shared ? a.Fs : a.F) + TC_BN_UP / 2 - 1) / (TC_BN_UP / 2));
+            fu += mt * (((shared ? a.Fs : a.F) + a.tnu - 1) / a.tnu);
             fd += mt * n_dn;
         }
         if (tid == 0) { gu[n_groups] = n_up; gd[n_groups] = n_down; }
@@ -309,6 +310,8 @@ int launch_group(const Layer &L, int T, bool build_tiles, cudaStream_t s)
     a.gfirst = L.gfirst;
     a.meta = L.meta;
     a.build_tiles = build_tiles ? 1 : 0;
+    const TcGeometry geo = tc_geometry(L.qfmt);
+    a.tm = geo.tm; a.tnu = geo.tnu; a.tnd = geo.tnd;
     group_kernel<<<L.E, GT, 0, s>>>(a);
     return 1;
 }
