@@ -899,16 +899,18 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
             uint32_t raw[16];
             float v[DT_TOK];
             {
-                // the two MMA threads' accumulators; one that got no stage of the
-                // unit (a single-stage unit) holds nothing
+                // the MMA threads' accumulators: the one holding the unit's stages
+                // j, j + NM, j + 2 NM, ... is that of thread (e_gs + j) mod NM (its
+                // stream indices are e_gs .. e_gs + nst - 1); they are added in the
+                // order of j, which does not depend on where the unit fell in this
+                // CTA's stream, so that the sum is the same bits on every run
 #pragma unroll
                 for (int t = 0; t < DT_TOK; ++t) v[t] = 0.0f;
                 const int nst = (nk + Sh::KPS - 1) / Sh::KPS;  // stages of the unit
 #pragma unroll
-                for (int m = 0; m < Sh::NM; ++m) {
-                    // MMA thread m had a stage of the unit iff one of its nst stages,
-                    // stream indices e_gs .. e_gs + nst - 1, is m mod NM
-                    if ((m - (int)(e_gs % Sh::NM) + Sh::NM) % Sh::NM >= nst) continue;
+                for (int j = 0; j < Sh::NM; ++j) {
+                    if (j >= nst) break;  // a unit of fewer stages than MMA threads
+                    const int m = (int)((e_gs + (uint32_t)j) % Sh::NM);
                     tmem_ld16(tmem_base + lane_addr + (uint32_t)((qi * Sh::NM + m) * DT_TOK), raw);
                     tmem_ld_wait();
 #pragma unroll
@@ -1071,6 +1073,9 @@ __global__ void __launch_bounds__(DtShape<QF>::THREADS, 1) dec_experts_kernel(co
                         lowbit_dequant_row<QF>(blk, row, fp4tab, v);
                         tmem_st32(t_a + col, v);
                     }
+                    // the raw stage is refilled by a bulk copy (async proxy) once the
+                    // MMA releases it: order these generic reads before that copy
+                    fence_proxy_async_shared();
                     tmem_st_wait();
                 } else if (!*abort_flag) {
                     record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);

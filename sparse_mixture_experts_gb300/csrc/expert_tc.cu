@@ -53,12 +53,12 @@ struct TcShape {
     static constexpr int A_BYTES = MH * A_TILE_BYTES;
     static constexpr int B_BYTES = BN * TC_BK * 2;
     static constexpr int STAGE = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
-    static constexpr int STAGES = LOWBIT ? 3 : (BN == 256 ? 4 : 6);
+    static constexpr int STAGES = BN == 256 || LOWBIT ? 4 : 6;
     // low-bit weights: the packed block (codes and scales of 128 rows x 64 K)
-    // of each stage's B tile lands in a ring of its own, filled further ahead
-    // than the A/B ring, from which dequantising warps write the bf16 B tile
+    // of each stage's B tile lands in a ring of its own, filled ahead of the
+    // A/B ring, from which dequantising warps write the bf16 B tile
     static constexpr int RAW_STAGE = LOWBIT ? BLK : 0;
-    static constexpr int RAW_STAGES = LOWBIT ? 8 : 0;
+    static constexpr int RAW_STAGES = LOWBIT ? 4 : 0;
     static constexpr int RAW_OFF = STAGES * STAGE;
     static constexpr int BAR_OFF = RAW_OFF + (RAW_STAGES * RAW_STAGE + 1023) / 1024 * 1024;
     static constexpr int TMEM_COLS = 2 * MH * BN;
@@ -80,6 +80,7 @@ struct TcShape {
     // address and the abort word
     static_assert((3 * STAGES + 6 + 2 * RAW_STAGES) * 8 + 8 <= 512, "barrier area");
     static_assert(TMEM_COLS <= 512, "tensor memory");
+    static_assert(SMEM <= 232448, "shared memory per block");
     static_assert(!LOWBIT || BN == TC_LB_BN, "low-bit tiles are one packed block wide");
 };
 
@@ -140,9 +141,10 @@ struct TileInfo {
     bool shared;
 };
 
-// group tables of this launch in shared memory: first tile of each group (and
-// the total), each group's expert (E for the shared expert), its rows and its
-// first row in the expert-sorted buffers
+// group tables of this launch (global memory, written by the grouping kernel
+// before the launch; read through the read-only path): first tile of each
+// group (and the total), each group's expert (E for the shared expert), its
+// rows and its first row in the expert-sorted buffers
 struct GroupTab {
     const int *first;
     const int *expert;
@@ -176,19 +178,28 @@ __device__ __forceinline__ bool tile_info(const TcArgs &a, int t, TileInfo &ti, 
     ti.split = 0;
     // the group of tile t: the last one whose first tile is <= t; within a
     // group the tiles run (n, m) with m fastest
-    if (gt.n <= 0 || t < 0 || t >= gt.first[gt.n]) return false;
+    if (gt.n <= 0 || t < 0 || t >= __ldg(gt.first + gt.n)) return false;
     int lo = gcur;
-    if (lo < 0 || lo >= gt.n || gt.first[lo] > t) lo = 0;
-    while (lo + 1 < gt.n && gt.first[lo + 1] <= t) ++lo;
+    if (lo < 0 || lo >= gt.n || __ldg(gt.first + lo) > t || __ldg(gt.first + lo + 1) <= t) {
+        // binary search (every group has a tile, so first[] increases strictly
+        // from first[0] = 0)
+        int l = 0, h = gt.n - 1;
+        while (l < h) {
+            const int m = (l + h + 1) >> 1;
+            if (__ldg(gt.first + m) <= t) l = m;
+            else h = m - 1;
+        }
+        lo = l;
+    }
     gcur = lo;
-    ti.g = gt.expert[lo];
+    ti.g = __ldg(gt.expert + lo);
     ti.shared = ti.g == a.E;
     if (ti.g < 0 || ti.g > a.E || (ti.shared && a.Fs == 0)) return false;
-    ti.rows = gt.rows[lo];
-    ti.a_row0 = gt.row0[lo];
+    ti.rows = __ldg(gt.rows + lo);
+    ti.a_row0 = __ldg(gt.row0 + lo);
     const int mt = (ti.rows + TM - 1) / TM;
     if (mt <= 0) return false;
-    const int local = t - gt.first[lo];
+    const int local = t - __ldg(gt.first + lo);
     const int n = local / mt;
     ti.m0 = (local - n * mt) * TM;
     ti.n0 = n * (EPI == EPI_UP ? TNU : TND);
@@ -285,21 +296,15 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    __shared__ int s_gfirst[1026];
-    __shared__ int s_gexp[1025], s_grows[1025], s_grow0[1025];
-    GroupTab gt{s_gfirst, s_gexp, s_grows, s_grow0, 0};
+    GroupTab gt{nullptr, nullptr, nullptr, nullptr, 0};
     int gcur = 0;  // this thread's group cursor
     if constexpr (EPI != EPI_ROUTER) {
-        const int n_act = a.meta->n_active;
-        gt.n = n_act + (a.Fs > 0 ? 1 : 0);
         const int P = a.E + 2;
-        const int *gf = a.gfirst + (EPI == EPI_UP ? 0 : P);
-        for (int i = threadIdx.x; i <= gt.n; i += Sh::THREADS) s_gfirst[i] = gf[i];
-        for (int i = threadIdx.x; i < gt.n; i += Sh::THREADS) {
-            s_gexp[i] = a.gfirst[2 * P + i];
-            s_grows[i] = a.gfirst[3 * P + i];
-            s_grow0[i] = a.gfirst[4 * P + i];
-        }
+        gt.first = a.gfirst + (EPI == EPI_UP ? 0 : P);
+        gt.expert = a.gfirst + 2 * P;
+        gt.rows = a.gfirst + 3 * P;
+        gt.row0 = a.gfirst + 4 * P;
+        gt.n = a.meta->n_active + (a.Fs > 0 ? 1 : 0);
     }
     Fp4Table *fp4tab = reinterpret_cast<Fp4Table *>(smem + Sh::TAB_OFF);
     if constexpr (QF == QF_MXFP4)
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
         // Per stage: the 128 rows of the B tile (the rows of the stage's packed
         // block, in order), each K half of a row by one thread.  A thread loads
         // its 32 codes and their scale from the raw ring and releases the raw
-        // stage, waits until the MMAs have finished with the A/B stage, widens
+        // stage (after a proxy fence), waits until the MMAs have finished with the A/B stage, widens
         // the codes to bf16 (MXFP4 exactly, Q4 rounded once) and writes them as
         // four 16-byte chunks at their 128-byte-swizzle positions (chunk c of
         // row r at r * 128 + ((c ^ (r & 7)) << 4), the layout the TMA would
@@ -500,6 +505,11 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                 }
                 LowbitHalf x;
                 lowbit_load_half<QF>(smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE, rr, hk, x);
+                // the raw stage is refilled by the async proxy (a bulk copy): these
+                // generic reads are ordered before it by a proxy fence, not by the
+                // barrier alone (without it the copy could land in rows still being
+                // read, which showed as nondeterministic weight rows)
+                fence_proxy_async_shared();
                 mbar_arrive(&raw_empty[rs]);
                 if (++rs == Sh::RAW_STAGES) rs = 0, rph ^= 1;
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {

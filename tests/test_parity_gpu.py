@@ -149,15 +149,29 @@ def test_layer_parity(name, T, n_rows, path):
     assert rep.ok(spec.dtype), str(rep)
 
 
-@pytest.mark.parametrize("path", PATHS, ids=PATH_IDS)
-def test_deterministic_bitwise(path):
-    wl = workload("qwen_prefill_zipf")
+DETERMINISM = [
+    ("qwen_prefill_zipf", 1024, moe.PATH_STREAM), ("qwen_prefill_zipf", 1024, moe.PATH_TC),
+    ("qwen_prefill_zipf", 8, moe.PATH_FUSED), ("qwen_prefill_zipf", 8, moe.PATH_DECODE_TC),
+    # low-bit experts: the widening warps' rings and the split-K sums of both
+    # tensor-core paths, at sizes with many stages per CTA
+    ("gptoss_q4", 2048, moe.PATH_TC), ("gptoss_q4", 16, moe.PATH_DECODE_TC),
+    ("gptoss_mxfp4", 64, moe.PATH_TC), ("gptoss_mxfp4", 16, moe.PATH_DECODE_TC),
+    ("qwen_q4", 8, moe.PATH_DECODE_TC), ("qwen_q4", 300, moe.PATH_TC),
+]
+
+
+@pytest.mark.parametrize("name,T,path", DETERMINISM,
+                         ids=[f"{n}-T{T}-{PATH_IDS[PATHS.index(p)]}" for n, T, p in DETERMINISM])
+def test_deterministic_bitwise(name, T, path):
+    """The same input gives the same bits on every forward (no race, and no
+    reduction whose order depends on scheduling)."""
+    wl = workload(name)
     wl.layer.set_path(path)
-    T = 8 if path in (moe.PATH_FUSED, moe.PATH_DECODE_TC) else 1024
     a = wl.layer.forward(wl.x_dev[:T]).clone()
-    b = wl.layer.forward(wl.x_dev[:T]).clone()
-    torch.cuda.synchronize()
-    assert torch.equal(a, b)
+    for _ in range(4):
+        b = wl.layer.forward(wl.x_dev[:T])
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
 
 
 def test_forward_host_matches_forward():
