@@ -481,13 +481,13 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
         // ------------------------------ low-bit dequantisation (warps 6..13) ------------------------------
         // Per stage: the 128 rows of the B tile (the rows of the stage's packed
         // block, in order), each K half of a row by one thread.  A thread loads
-        // its 32 codes and their scale from the raw ring and releases the raw
-        // stage (after a proxy fence), waits until the MMAs have finished with the A/B stage, widens
-        // the codes to bf16 (MXFP4 exactly, Q4 rounded once) and writes them as
-        // four 16-byte chunks at their 128-byte-swizzle positions (chunk c of
-        // row r at r * 128 + ((c ^ (r & 7)) << 4), the layout the TMA would
-        // have written).  Then the writes are made visible to the tensor cores'
-        // reads and the stage is released to the MMAs.
+        // its 32 codes and their scale from the raw ring, waits until the MMAs
+        // have finished with the A/B stage, widens the codes to bf16 (MXFP4
+        // exactly, Q4 rounded once) and writes them as four 16-byte chunks at
+        // their 128-byte-swizzle positions (chunk c of row r at r * 128 +
+        // ((c ^ (r & 7)) << 4), the layout the TMA would have written).  Then
+        // the writes are made visible to the tensor cores' reads, the stage is
+        // released to the MMAs and the raw stage to its producer.
         const int rr = (threadIdx.x - TC_THREADS) & 127;  // the B-tile row of this thread
         const int hk = (threadIdx.x - TC_THREADS) >> 7;   // its K half
         int stage = 0, rs = 0;
@@ -505,12 +505,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                 }
                 LowbitHalf x;
                 lowbit_load_half<QF>(smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE, rr, hk, x);
-                // the raw stage is refilled by the async proxy (a bulk copy): these
-                // generic reads are ordered before it by a proxy fence, not by the
-                // barrier alone (without it the copy could land in rows still being
-                // read, which showed as nondeterministic weight rows)
-                fence_proxy_async_shared();
-                mbar_arrive(&raw_empty[rs]);
+                const int rs_read = rs;  // released after the proxy fence below
                 if (++rs == Sh::RAW_STAGES) rs = 0, rph ^= 1;
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_EMPTY_BARRIER);
@@ -524,8 +519,15 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     dst[(4 * hk + j) ^ (rr & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                // one proxy fence orders this thread's B-tile writes before the MMAs'
+                // reads and its raw-stage reads before the bulk copy that refills
+                // the stage (both async proxy): the barriers alone do not order
+                // generic accesses with async-proxy ones (without the fence on the
+                // raw reads the copy could land in rows still being read, which
+                // showed as nondeterministic weight rows)
                 fence_proxy_async_shared();
                 mbar_arrive(&bready[stage]);
+                mbar_arrive(&raw_empty[rs_read]);
                 if (++stage == TC_STAGES) stage = 0, phase ^= 1;
             }
         }
