@@ -41,23 +41,27 @@ constexpr int A_TILE_BYTES = TC_BM * TC_BK * 2;        // 16 KB
 // the TMEM columns (two accumulators of BN fp32 columns per M half).  N = 256
 // halves the A bytes staged per weight byte, which matters because a CTA's TMA
 // stream, not HBM, limits these GEMMs once the A rows are re-read from L2.
-// Low-bit weights take tiles of TC_LB_TM = 256 token rows: two M = 128 halves,
-// each with its own MMA-issuing thread and accumulators, multiply the same
-// widened B tile, so that the widening -- the work that paces these kernels --
-// is done once per 256 rows.
+// Low-bit weights come in two shapes.  BN = 128: tiles of TC_LB_TM = 256 token
+// rows, two M = 128 halves, each with its own MMA-issuing thread and
+// accumulators, multiply the same widened B tile (one packed block), so that
+// the widening -- the work that paces these kernels -- is done once per 256
+// rows; for experts with more than 128 rows.  BN = 256: 128-row tiles against
+// two packed blocks, half the stages (and their fixed costs) where the experts
+// have fewer rows and the second half would stay empty.
 template <int BN, int QF = QF_NONE>
 struct TcShape {
     static constexpr bool LOWBIT = QF != QF_NONE;
-    static constexpr int MH = LOWBIT ? TC_LB_TM / TC_BM : 1;  // M halves per tile
+    static constexpr int MH = LOWBIT && BN == TC_LB_BN ? TC_LB_TM / TC_BM : 1;  // M halves per tile
+    static constexpr int NBLK = BN / 128;  // low-bit: packed blocks per stage
     static constexpr int BLK = QF == QF_Q4 ? LOWBIT_BLK_Q4 : LOWBIT_BLK_MXFP4;
     static constexpr int A_BYTES = MH * A_TILE_BYTES;
     static constexpr int B_BYTES = BN * TC_BK * 2;
     static constexpr int STAGE = (A_BYTES + B_BYTES + 1023) / 1024 * 1024;
-    static constexpr int STAGES = BN == 256 || LOWBIT ? 4 : 6;
-    // low-bit weights: the packed block (codes and scales of 128 rows x 64 K)
-    // of each stage's B tile lands in a ring of its own, filled ahead of the
-    // A/B ring, from which dequantising warps write the bf16 B tile
-    static constexpr int RAW_STAGE = LOWBIT ? BLK : 0;
+    static constexpr int STAGES = LOWBIT ? (MH == 2 ? 4 : 3) : (BN == 256 ? 4 : 6);
+    // low-bit weights: the packed blocks (codes and scales of 128 rows x 64 K
+    // each) of each stage's B tile land in a ring of their own, filled ahead
+    // of the A/B ring, from which dequantising warps write the bf16 B tile
+    static constexpr int RAW_STAGE = LOWBIT ? NBLK * BLK : 0;
     static constexpr int RAW_STAGES = LOWBIT ? 4 : 0;
     static constexpr int RAW_OFF = STAGES * STAGE;
     static constexpr int BAR_OFF = RAW_OFF + (RAW_STAGES * RAW_STAGE + 1023) / 1024 * 1024;
@@ -69,19 +73,20 @@ struct TcShape {
     static constexpr int TAB_OFF = STAGING_OFF + STAGING_BYTES;
     static constexpr int TAB_BYTES = QF == QF_MXFP4 ? 256 * (int)sizeof(Fp4Table) : 0;
     static constexpr size_t SMEM = (size_t)TAB_OFF + TAB_BYTES + 1024 /*align*/;
-    static constexpr int DQ_THREADS = LOWBIT ? 256 : 0;  // dequantising warps: one (B row, K half) each
+    // dequantising warps: one (B row, K half) per thread (BN = 128), or one B row (BN = 256)
+    static constexpr int DQ_THREADS = LOWBIT ? 256 : 0;
     static constexpr int RAW_WARP = (TC_THREADS + DQ_THREADS) / 32;  // the raw ring's producer (low-bit)
-    static constexpr int MMA2_WARP = RAW_WARP + 1;                   // the second M half's MMA issuer (low-bit)
-    static constexpr int THREADS = TC_THREADS + DQ_THREADS + (LOWBIT ? 64 : 0);
+    static constexpr int MMA2_WARP = RAW_WARP + 1;                   // the second M half's MMA issuer (MH = 2)
+    static constexpr int THREADS = TC_THREADS + DQ_THREADS + (LOWBIT ? 32 * MH : 0);
     // tile geometry (tc_geometry gives the same to the grouping kernel)
-    static constexpr int TM = LOWBIT ? TC_LB_TM : TC_BM;
+    static constexpr int TM = MH * TC_BM;
     // barriers: full, empty, bready per A/B stage; two accumulators' full and
     // empty; a drain per M half; raw full and empty per raw stage; the TMEM
     // address and the abort word
     static_assert((3 * STAGES + 6 + 2 * RAW_STAGES) * 8 + 8 <= 512, "barrier area");
     static_assert(TMEM_COLS <= 512, "tensor memory");
     static_assert(SMEM <= 232448, "shared memory per block");
-    static_assert(!LOWBIT || BN == TC_LB_BN, "low-bit tiles are one packed block wide");
+    static_assert(!LOWBIT || BN == 128 || BN == 256, "low-bit tiles are one or two packed blocks wide");
 };
 
 struct TensorMaps {
@@ -251,8 +256,8 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
     constexpr int B_TILE_BYTES = Sh::B_BYTES;
     constexpr int TMEM_COLS = Sh::TMEM_COLS;
     constexpr int MH = Sh::MH;
-    constexpr int TNU = FP4 ? TC_LB_BN / 2 : TC_BN_UP / 2;  // gate/up features per tile
-    constexpr int TND = FP4 ? TC_LB_BN : TC_BN_DOWN;        // down output columns per tile
+    constexpr int TNU = BN / 2;  // gate/up features per tile
+    constexpr int TND = BN;      // down output columns per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Sh::BAR_OFF);
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                         // the A tiles only (rows m0 .. m0+127, and m0+128 .. m0+255 where
                         // the group has such rows): the raw ring's producer copies the
                         // packed weight block, and the dequantising warps write the B tile
-                        const bool two = ti.m0 + TC_BM < ti.rows;
+                        const bool two = MH == 2 && ti.m0 + TC_BM < ti.rows;
                         mbar_arrive_expect_tx(&full[stage], two ? 2 * A_TILE_BYTES : A_TILE_BYTES);
                         tma_load_2d(sa, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0);
                         if (two) tma_load_2d(sa + A_TILE_BYTES, &maps.a, &full[stage], kc, ti.a_row0 + ti.m0 + TC_BM);
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
             for (int s = 0; s < TC_STAGES; ++s)
                 if ((used >> s) & 1u) mbar_wait(&full[s], (last_phase >> s) & 1u, &never);
         }
-    } else if (warp == 1 || (FP4 && warp == Sh::MMA2_WARP)) {
+    } else if (warp == 1 || (MH == 2 && warp == Sh::MMA2_WARP)) {
         // ------------------------------ MMA issuers ------------------------------
         // One thread per M half (low-bit tiles have two): half h multiplies the
         // A rows m0 + 128h .. m0 + 128h + 127 with the stage's B tile into its
@@ -442,9 +447,10 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
         }
     } else if (FP4 && warp == Sh::RAW_WARP) {
         // ------------------------------ raw ring producer (low-bit, last warp) ------------------------------
-        // The packed block of each stage's 128 weight rows (gate/up: features
-        // n0 .. n0+63 as 64 gate + 64 up rows; down: output rows n0 .. n0+127),
-        // in the A/B ring's order.
+        // The packed blocks of each stage's BN weight rows (gate/up: per block 64
+        // features as 64 gate + 64 up rows; down: 128 output rows), in the A/B
+        // ring's order; a block past the matrix is not copied (its rows are
+        // written as zeros).
         if (lane == 0) {
             int rs = 0;
             uint32_t rph = 0;
@@ -455,6 +461,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                 if (!tile_info<EPI, Sh::TM, TNU, TND>(a, t, ti, gt, gcur)) break;  // the A producer records it
                 const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
                 const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;  // < nb
+                const int nvalid = min(Sh::NBLK, nb - b0);
                 const int nkbt = EPI == EPI_UP ? a.H / TC_BK : a.F / TC_BK;
                 for (int kb = 0; kb < ti.nk; ++kb) {
                     if (!mbar_wait(&raw_empty[rs], rph ^ 1, abort_flag)) {
@@ -464,9 +471,11 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                         break;
                     }
                     uint8_t *dst = smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE;
-                    mbar_arrive_expect_tx(&raw_full[rs], LB_BLK);
-                    const size_t blk = ((size_t)ti.g * nb + b0) * nkbt + ti.kb0 + kb;
-                    bulk_load(dst, a.fp4 + blk * LB_BLK, LB_BLK, &raw_full[rs]);
+                    mbar_arrive_expect_tx(&raw_full[rs], nvalid * LB_BLK);
+                    for (int q = 0; q < nvalid; ++q) {
+                        const size_t blk = ((size_t)ti.g * nb + b0 + q) * nkbt + ti.kb0 + kb;
+                        bulk_load(dst + q * LB_BLK, a.fp4 + blk * LB_BLK, LB_BLK, &raw_full[rs]);
+                    }
                     used |= 1u << rs;
                     last_phase = (last_phase & ~(1u << rs)) | (rph << rs);
                     if (++rs == Sh::RAW_STAGES) rs = 0, rph ^= 1;
@@ -479,23 +488,43 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
         }
     } else if (FP4 && warp >= 6) {
         // ------------------------------ low-bit dequantisation (warps 6..13) ------------------------------
-        // Per stage: the 128 rows of the B tile (the rows of the stage's packed
-        // block, in order), each K half of a row by one thread.  A thread loads
-        // its 32 codes and their scale from the raw ring, waits until the MMAs
-        // have finished with the A/B stage, widens the codes to bf16 (MXFP4
-        // exactly, Q4 rounded once) and writes them as four 16-byte chunks at
-        // their 128-byte-swizzle positions (chunk c of row r at r * 128 +
-        // ((c ^ (r & 7)) << 4), the layout the TMA would have written).  Then
-        // the writes are made visible to the tensor cores' reads, the stage is
-        // released to the MMAs and the raw stage to its producer.
-        const int rr = (threadIdx.x - TC_THREADS) & 127;  // the B-tile row of this thread
-        const int hk = (threadIdx.x - TC_THREADS) >> 7;   // its K half
+        // Per stage: the rows of the B tile, in their 128-byte-swizzled layout
+        // (chunk c of row r at r * 128 + ((c ^ (r & 7)) << 4), the layout the TMA
+        // would have written).  BN = 128: the 128 rows of the stage's packed
+        // block, in order, each K half of a row by one thread (32 codes, four
+        // chunks).  BN = 256: one row per thread (64 codes, eight chunks) from
+        // two blocks (gate/up: B rows 0..127 are the gate rows of features
+        // n0 .. n0+127, 128..255 the up rows, block q holding features 64q ..
+        // 64q+63 as 64 gate then 64 up rows; down: block q holds B rows 128q ..
+        // 128q+127); a block past the matrix gives zero rows.  A thread loads
+        // its codes and scales from the raw ring, waits until the MMAs have
+        // finished with the A/B stage, widens the codes to bf16 (MXFP4 exactly,
+        // Q4 rounded once) and writes them; then the writes are made visible to
+        // the tensor cores' reads, the stage is released to the MMAs and the raw
+        // stage to its producer.
+        const int dq = threadIdx.x - TC_THREADS;  // 0 .. 255
+        const int rr = MH == 2 ? dq & 127 : dq;   // the B-tile row of this thread
+        const int hk = MH == 2 ? dq >> 7 : 0;     // its K half (BN = 128)
+        int q = 0, brow = rr;                     // its packed block and the row in it
+        if (MH == 1) {
+            if (EPI == EPI_UP) {
+                const int f = rr & 127;
+                q = f >> 6;
+                brow = (rr < 128 ? 0 : 64) + (f & 63);
+            } else {
+                q = rr >> 7;
+                brow = rr & 127;
+            }
+        }
         int stage = 0, rs = 0;
         uint32_t phase = 0, rph = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
             TileInfo ti;
             if (!tile_info<EPI, Sh::TM, TNU, TND>(a, t, ti, gt, gcur)) break;
+            const int nb = EPI == EPI_UP ? a.F / 64 : (a.H + 127) / 128;
+            const int b0 = EPI == EPI_UP ? ti.n0 / 64 : ti.n0 / 128;
+            const bool zero = b0 + q >= nb;
             for (int kb = 0; kb < ti.nk; ++kb) {
                 if (!mbar_wait(&raw_full[rs], rph, abort_flag)) {
                     record_error(a.status, DEV_TIMEOUT_FULL_BARRIER);
@@ -503,8 +532,11 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     ok = false;
                     break;
                 }
-                LowbitHalf x;
-                lowbit_load_half<QF>(smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE, rr, hk, x);
+                const uint8_t *blk = smem + Sh::RAW_OFF + rs * Sh::RAW_STAGE + q * LB_BLK;
+                LowbitHalf xh;
+                LowbitRow xr;
+                if (MH == 2) lowbit_load_half<QF>(blk, rr, hk, xh);
+                else if (!zero) lowbit_load_row<QF>(blk, brow, xr);
                 const int rs_read = rs;  // released after the proxy fence below
                 if (++rs == Sh::RAW_STAGES) rs = 0, rph ^= 1;
                 if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
@@ -514,11 +546,22 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     break;
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(smem + stage * STAGE_BYTES + Sh::A_BYTES + rr * 128);
-                uint32_t v[16];
-                lowbit_widen_half<QF>(x, fp4tab, v);
+                if (MH == 2) {
+                    uint32_t v[16];
+                    lowbit_widen_half<QF>(xh, fp4tab, v);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    dst[(4 * hk + j) ^ (rr & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    for (int j = 0; j < 4; ++j)
+                        dst[(4 * hk + j) ^ (rr & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                } else if (zero) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) dst[j ^ (rr & 7)] = make_uint4(0, 0, 0, 0);
+                } else {
+                    uint32_t v[32];
+                    lowbit_widen_row<QF>(xr, fp4tab, v);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[j ^ (rr & 7)] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
                 // one proxy fence orders this thread's B-tile writes before the MMAs'
                 // reads and its raw-stage reads before the bulk copy that refills
                 // the stage (both async proxy): the barriers alone do not order
@@ -744,6 +787,33 @@ bool tc_supported(const Layer &L, std::string &why)
 }
 
 
+template <int EPI, int BN, int QF>
+static bool set_smem()
+{
+    return cudaFuncSetAttribute(tc_gemm_kernel<EPI, BN, TcMaps, QF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)TcShape<BN, QF>::SMEM) == cudaSuccess;
+}
+
+// both tile shapes of both low-bit GEMMs
+template <int QF>
+static bool lowbit_smem()
+{
+    return set_smem<EPI_UP, TC_LB_BN, QF>() && set_smem<EPI_DOWN, TC_LB_BN, QF>() && set_smem<EPI_UP, 256, QF>() &&
+           set_smem<EPI_DOWN, 256, QF>();
+}
+
+template <int EPI, int QF>
+static void launch_lowbit(const TcMaps &maps, const TcArgs &a, bool two_halves, int grid, cudaStream_t s)
+{
+    if (two_halves) {
+        using Sh = TcShape<TC_LB_BN, QF>;
+        tc_gemm_kernel<EPI, TC_LB_BN, TcMaps, QF><<<grid, Sh::THREADS, Sh::SMEM, s>>>(maps, a);
+    } else {
+        using Sh = TcShape<256, QF>;
+        tc_gemm_kernel<EPI, 256, TcMaps, QF><<<grid, Sh::THREADS, Sh::SMEM, s>>>(maps, a);
+    }
+}
+
 int tc_prepare(Layer &L)
 {
     TensorMaps *m = new (std::nothrow) TensorMaps();
@@ -777,18 +847,7 @@ int tc_prepare(Layer &L)
                              (int)TcShape<TC_BN_DOWN>::SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_gemm_kernel<EPI_ROUTER, 128, TcMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)TcShape<128>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_LB_BN, TcMaps, QF_MXFP4>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_LB_BN, QF_MXFP4>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_LB_BN, TcMaps, QF_MXFP4>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_LB_BN, QF_MXFP4>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_UP, TC_LB_BN, TcMaps, QF_Q4>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_LB_BN, QF_Q4>::SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<EPI_DOWN, TC_LB_BN, TcMaps, QF_Q4>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcShape<TC_LB_BN, QF_Q4>::SMEM) != cudaSuccess) {
+        !lowbit_smem<QF_MXFP4>() || !lowbit_smem<QF_Q4>()) {
         delete m;
         return -1;
     }
@@ -828,17 +887,16 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
     const TensorMaps &m = *L.tmaps;
     TcArgs a = make_tc_args(L, T);
     const int grid = L.num_sms;
+    const bool two = tc_lowbit_two_halves(L, T);  // the grouping kernel used the same tiles
     if (which == 1) {
         TcMaps mu{m.xp, m.gate, m.up, m.sh_gate, m.sh_up, m.xp};
         if (L.Fs > 0 && !encode_2d(&mu.sa, x, L.H, (uint64_t)T, TC_BM)) return -1;
         if (L.qfmt == QF_MXFP4) {
             a.fp4 = L.fp4_gu;
-            using Sh = TcShape<TC_LB_BN, QF_MXFP4>;
-            tc_gemm_kernel<EPI_UP, TC_LB_BN, TcMaps, QF_MXFP4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
+            launch_lowbit<EPI_UP, QF_MXFP4>(mu, a, two, grid, s);
         } else if (L.qfmt == QF_Q4) {
             a.fp4 = L.fp4_gu;
-            using Sh = TcShape<TC_LB_BN, QF_Q4>;
-            tc_gemm_kernel<EPI_UP, TC_LB_BN, TcMaps, QF_Q4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(mu, a);
+            launch_lowbit<EPI_UP, QF_Q4>(mu, a, two, grid, s);
         } else {
             tc_gemm_kernel<EPI_UP, TC_BN_UP, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_UP>::SMEM, s>>>(mu, a);
         }
@@ -846,12 +904,10 @@ int launch_experts_tc(const Layer &L, const void *x, int T, int which, cudaStrea
         TcMaps md{m.h, m.down, m.down, m.sh_down, m.sh_down, m.h};
         if (L.qfmt == QF_MXFP4) {
             a.fp4 = L.fp4_dn;
-            using Sh = TcShape<TC_LB_BN, QF_MXFP4>;
-            tc_gemm_kernel<EPI_DOWN, TC_LB_BN, TcMaps, QF_MXFP4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
+            launch_lowbit<EPI_DOWN, QF_MXFP4>(md, a, two, grid, s);
         } else if (L.qfmt == QF_Q4) {
             a.fp4 = L.fp4_dn;
-            using Sh = TcShape<TC_LB_BN, QF_Q4>;
-            tc_gemm_kernel<EPI_DOWN, TC_LB_BN, TcMaps, QF_Q4><<<grid, Sh::THREADS, Sh::SMEM, s>>>(md, a);
+            launch_lowbit<EPI_DOWN, QF_Q4>(md, a, two, grid, s);
         } else {
             tc_gemm_kernel<EPI_DOWN, TC_BN_DOWN, TcMaps><<<grid, TC_THREADS, TcShape<TC_BN_DOWN>::SMEM, s>>>(md, a);
         }

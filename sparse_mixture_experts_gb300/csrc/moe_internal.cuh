@@ -492,14 +492,26 @@ constexpr int TC_ROUTER_MAX_SPLITS = 4;  // K ranges of the tensor-core router G
 constexpr int TC_LB_TM = 256;
 constexpr int TC_LB_BN = 128;
 
+// Low-bit layers take 256-row tiles (two M halves sharing each widened weight
+// block) when a forward's routed experts have more than 128 rows on average
+// (T k pairs over min(E, T k) experts), else 128-row tiles against two packed
+// blocks, which halve the stages where the second half would stay empty.
+inline bool tc_lowbit_two_halves(const Layer &L, int T)
+{
+    const long long pairs = (long long)T * L.K;
+    const long long groups = pairs < L.E ? pairs : L.E;
+    return L.qfmt != QF_NONE && pairs > 128LL * groups;
+}
+
 // token rows, gate/up features and down output columns per tile of the
-// expert GEMMs, for a layer of routed-expert format qfmt
+// expert GEMMs of a forward of T tokens
 struct TcGeometry {
     int tm, tnu, tnd;
 };
-inline TcGeometry tc_geometry(int qfmt)
+inline TcGeometry tc_geometry(const Layer &L, int T)
 {
-    return qfmt != QF_NONE ? TcGeometry{TC_LB_TM, TC_LB_BN / 2, TC_LB_BN} : TcGeometry{TC_BM, TC_BN_UP / 2, TC_BN_DOWN};
+    return tc_lowbit_two_halves(L, T) ? TcGeometry{TC_LB_TM, TC_LB_BN / 2, TC_LB_BN}
+                                      : TcGeometry{TC_BM, TC_BN_UP / 2, TC_BN_DOWN};
 }
 
 }  // namespace moe

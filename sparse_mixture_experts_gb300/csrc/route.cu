@@ -310,7 +310,7 @@ int launch_group(const Layer &L, int T, bool build_tiles, cudaStream_t s)
     a.gfirst = L.gfirst;
     a.meta = L.meta;
     a.build_tiles = build_tiles ? 1 : 0;
-    const TcGeometry geo = tc_geometry(L.qfmt);
+    const TcGeometry geo = tc_geometry(L, T);
     a.tm = geo.tm; a.tnu = geo.tnu; a.tnd = geo.tnd;
     group_kernel<<<L.E, GT, 0, s>>>(a);
     return 1;

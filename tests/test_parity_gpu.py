@@ -265,6 +265,11 @@ EDGE_SPECS = [
     ("q4_ragged", synth.QWEN_Q4.replace(name="q4 small", hidden=256, n_expert=16, top_k=4, expert_ff=192), 300),
     ("q4_gptoss_ragged", synth.GPTOSS_Q4.replace(name="q4 gpt-oss-like small", hidden=192, n_expert=8, top_k=4,
                                                  expert_ff=128), 133),
+    # more than 128 rows per expert: the low-bit GEMMs' 256-row tiles (two M
+    # halves), with ragged second tiles and halves
+    ("q4_many_rows", synth.QWEN_Q4.replace(name="q4 many rows", hidden=256, n_expert=4, top_k=2, expert_ff=192), 700),
+    ("mxfp4_many_rows", synth.GPTOSS_MXFP4.replace(name="mxfp4 many rows", hidden=192, n_expert=4, top_k=2,
+                                                   expert_ff=128), 600),
 ]
 
 
