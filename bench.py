@@ -427,12 +427,16 @@ def host_link_peak(torch, dev):
     s = torch.cuda.current_stream(dev)
     d.copy_(h, non_blocking=True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for _ in range(4):
-        d.copy_(h, non_blocking=True)
-    e1.record(s)
-    torch.cuda.synchronize(dev)
-    _LINK_PEAK[dev] = 4 * n / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    best = 0.0
+    # the best of three timings: a single one has read far low on one box
+    for _ in range(3):
+        e0.record(s)
+        for _ in range(4):
+            d.copy_(h, non_blocking=True)
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+        best = max(best, 4 * n / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    _LINK_PEAK[dev] = best
     del h, d
     return _LINK_PEAK[dev]
 
