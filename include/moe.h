@@ -204,8 +204,14 @@ moe_status moe_forward(moe_layer *layer, const void *x, int32_t n_tokens, void *
 
 /* Same as moe_forward with x and out in HOST memory (pinned memory makes the
  * copies asynchronous).  The copies in and out go through device staging
- * buffers allocated at create and are issued on `stream`; the caller must
- * synchronise `stream` before reading out. */
+ * buffers allocated at create: x is copied in on a stream of the layer's own
+ * (created at the first call), after the previous forward of this layer has
+ * read the staging buffer, so that the copy overlaps the work still queued
+ * on `stream`, which waits for it.  out is copied on `stream`, except for a
+ * batch the weight-streaming decode kernels take (and with expert residency)
+ * when out is pinned memory mapped into the device's address space: that
+ * kernel then writes out directly.  The caller must synchronise `stream`
+ * before reading out, and keep x valid until then. */
 moe_status moe_forward_host(moe_layer *layer, const void *x_host, int32_t n_tokens, void *out_host,
                             void *stream);
 

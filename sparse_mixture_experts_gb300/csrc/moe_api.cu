@@ -70,6 +70,13 @@ void timing_free(Layer &L)
 void free_all(Layer &L)
 {
     timing_free(L);
+    if (L.h2d_stream) {
+        cudaStreamSynchronize(L.h2d_stream);
+        cudaStreamDestroy(L.h2d_stream);
+        L.h2d_stream = nullptr;
+    }
+    if (L.x_ready) cudaEventDestroy(L.x_ready), L.x_ready = nullptr;
+    if (L.x_free) cudaEventDestroy(L.x_free), L.x_free = nullptr;
     residency_release(L);
     if (L.tmaps) tc_release(L);
     if (L.dectc) dectc_release(L);
@@ -575,10 +582,37 @@ moe_status moe_forward_host(moe_layer *layer, const void *x_host, int32_t n_toke
     cudaStream_t s = (cudaStream_t)stream;
     const size_t xb = (size_t)n_tokens * L.H * L.wbytes;
     const size_t ob = (size_t)n_tokens * L.H * (L.cfg.out_dtype == MOE_DT_BF16 ? 2 : 4);
-    CUDA_TRY(cudaMemcpyAsync(L.x_stage, x_host, xb, cudaMemcpyHostToDevice, s));
-    moe_status st = forward_impl(L, L.x_stage, n_tokens, L.out_stage, s);
+    if (!L.h2d_stream) {
+        CUDA_TRY(cudaStreamCreateWithFlags(&L.h2d_stream, cudaStreamNonBlocking));
+        CUDA_TRY(cudaEventCreateWithFlags(&L.x_ready, cudaEventDisableTiming));
+        CUDA_TRY(cudaEventCreateWithFlags(&L.x_free, cudaEventDisableTiming));
+        CUDA_TRY(cudaEventRecord(L.x_free, s));  // nothing has read x_stage yet
+    }
+    // x in on the layer's copy stream, after the last forward that read
+    // x_stage, so that the copy overlaps whatever `stream` is still running;
+    // `stream` waits for it, so synchronising `stream` covers both copies
+    CUDA_TRY(cudaStreamWaitEvent(L.h2d_stream, L.x_free, 0));
+    CUDA_TRY(cudaMemcpyAsync(L.x_stage, x_host, xb, cudaMemcpyHostToDevice, L.h2d_stream));
+    CUDA_TRY(cudaEventRecord(L.x_ready, L.h2d_stream));
+    CUDA_TRY(cudaStreamWaitEvent(s, L.x_ready, 0));
+    // A decode batch on the weight-streaming kernel (whose epilogue writes the
+    // few KB of out itself) writes straight into out when the host buffer is
+    // mapped into the device's address space: no copy out, so nothing sits
+    // between this forward and the next one's router on `stream`.  Otherwise
+    // out goes through the staging buffer and a copy.
+    void *out_dev = nullptr;
+    if (L.S > 0 || choose_path(L, n_tokens) == Route::DecodeTC) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, out_host) == cudaSuccess && pa.type == cudaMemoryTypeHost && pa.devicePointer &&
+            ((uintptr_t)pa.devicePointer & 15) == 0)
+            out_dev = pa.devicePointer;
+        else
+            cudaGetLastError();  // an unregistered pointer: clear the query's error
+    }
+    moe_status st = forward_impl(L, L.x_stage, n_tokens, out_dev ? out_dev : L.out_stage, s);
+    CUDA_TRY(cudaEventRecord(L.x_free, s));
     if (st) return st;
-    CUDA_TRY(cudaMemcpyAsync(out_host, L.out_stage, ob, cudaMemcpyDeviceToHost, s));
+    if (!out_dev) CUDA_TRY(cudaMemcpyAsync(out_host, L.out_stage, ob, cudaMemcpyDeviceToHost, s));
     return MOE_OK;
 }
 

@@ -105,6 +105,11 @@ struct Layer {
     int decode_grid = 0;       // blocks of the cooperative decode kernel (0 = unavailable)
     void *x_stage = nullptr;   // [Tmax][H] for moe_forward_host
     void *out_stage = nullptr; // [Tmax][H]
+    // moe_forward_host: the copy of x in runs on a stream of the layer's own,
+    // ordered after the previous forward's reads of x_stage (x_free) and
+    // before this forward (x_ready), so that it overlaps the work before it
+    cudaStream_t h2d_stream = nullptr;
+    cudaEvent_t x_ready = nullptr, x_free = nullptr;
     TensorMaps *tmaps = nullptr;  // host copy of the tensor maps (tensor-core path)
     // weight-streaming tensor-core decode path
     struct DecMaps *dectc = nullptr;

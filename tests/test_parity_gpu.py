@@ -187,6 +187,24 @@ def test_forward_host_matches_forward():
     assert torch.equal(dev, out_host)
 
 
+def test_forward_host_back_to_back():
+    """Several host-buffer forwards queued without a synchronisation between
+    them (the input copies overlap the work queued before them) give each
+    batch's own result."""
+    wl = workload("qwen_decode")
+    wl.layer.set_path(moe.PATH_AUTO)
+    T, n = 8, 4
+    x_host = helpers.to_torch(synth.make_x(wl.spec, T * n, seed=7), device="cpu").pin_memory()
+    outs = [torch.empty((T, wl.spec.hidden), dtype=torch.float32).pin_memory() for _ in range(n)]
+    s = torch.cuda.current_stream()
+    for i in range(n):
+        wl.layer.forward_host(x_host[i * T:(i + 1) * T], outs[i], s)
+    s.synchronize()
+    for i in range(n):
+        ref = wl.layer.forward(x_host[i * T:(i + 1) * T].cuda()).cpu()
+        assert torch.equal(ref, outs[i]), i
+
+
 def test_zero_tokens_and_too_many():
     wl = workload("qwen_decode")
     empty = torch.empty((0, wl.spec.hidden), dtype=torch.bfloat16, device="cuda")
