@@ -632,25 +632,37 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                 if (EPI == EPI_ROUTER) {
                     // logits[t][n] (+ router bias), fp32, or with K split the partial
                     // sum of this K range (the bias in the first); R need not be a
-                    // multiple of 4
+                    // multiple of 4.  Each 32-row x 16-column chunk of the warp goes
+                    // through its staging area (the layout of the down epilogue), so
+                    // that a store instruction writes 2 rows x 16 consecutive logits
+                    // instead of one logit in each of 32 rows.
                     float *dst = a.router_S > 1 ? a.rparts + (size_t)ti.split * a.T * a.R : a.logits;
                     const bool with_bias = a.router_b && ti.split == 0;
-    #pragma unroll 1
+                    float4 *stg = reinterpret_cast<float4 *>(smem + Sh::STAGING_OFF) + q * 128;
+                    const float *stf = reinterpret_cast<const float *>(stg);
+                    const int cc = lane & 15;  // the column this lane stores
+#pragma unroll 1
                     for (int c = 0; c < BN; c += 16) {
                         if (ti.n0 + c >= a.R) break;  // the same for the whole warp
                         uint32_t v[16];
                         tmem_ld16(tbase + c, v);
+                        const int n = ti.n0 + c + cc;
+                        const float b = (with_bias && n < a.E) ? a.router_b[n] : 0.0f;
                         tmem_ld_wait();
-                        if (valid) {
-    #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int n = ti.n0 + c + i;
-                                if (n < a.R) {
-                                    const float b = (with_bias && n < a.E) ? a.router_b[n] : 0.0f;
-                                    dst[(size_t)j * a.R + n] = __uint_as_float(v[i]) + b;
-                                }
-                            }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =
+                                make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                            __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                        __syncwarp();
+#pragma unroll 4
+                        for (int it = 0; it < 16; ++it) {
+                            const int rr = 2 * it + (lane >> 4);  // row of the warp's 32
+                            const float val = stf[(rr * 4 + ((cc >> 2) ^ ((rr >> 1) & 3))) * 4 + (cc & 3)];
+                            const int jr = ti.m0 + hm * TC_BM + q * 32 + rr;
+                            if (jr < ti.rows && n < a.R) dst[(size_t)jr * a.R + n] = val + b;
                         }
+                        __syncwarp();
                     }
                 } else if (EPI == EPI_UP) {
                     const int fd = ti.shared ? a.Fs : a.F;
@@ -658,14 +670,14 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     __nv_bfloat16 *hrow = a.h + (size_t)(ti.a_row0 + j) * a.Fmax + ti.n0;
                     const bool swiglu = ti.shared || a.act == MOE_ACT_SWIGLU;
                     const float4 *bs = reinterpret_cast<const float4 *>(smem + Sh::STAGING_OFF) + q * 128;
-    #pragma unroll 1
+#pragma unroll 1
                     for (int c = 0; c < BN / 2; c += 16) {
                         if (c >= hcols) break;
                         uint32_t g[16], u[16];
                         tmem_ld16(tbase + c, g);
                         tmem_ld16(tbase + BN / 2 + c, u);
                         float gb[16], ub[16];
-    #pragma unroll
+#pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const float4 x = bs[c / 4 + k], y = bs[32 + c / 4 + k];
                             gb[4 * k] = x.x; gb[4 * k + 1] = x.y; gb[4 * k + 2] = x.z; gb[4 * k + 3] = x.w;
@@ -703,7 +715,7 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                     // 16 bytes.  Row r's float4 q sits at r * 4 + (q ^ ((r >> 1) & 3)):
                     // no bank conflicts for the row-wise writes or the column-wise reads.
                     float4 *stg = reinterpret_cast<float4 *>(smem + Sh::STAGING_OFF) + q * 128;
-    #pragma unroll 1
+#pragma unroll 1
                     for (int c = 0; c < ncols; c += 16) {
                         uint32_t v[16];
                         tmem_ld16(tbase + c, v);
@@ -711,14 +723,14 @@ __global__ void __launch_bounds__(TcShape<BN, QF>::THREADS, 1) tc_gemm_kernel(co
                         bias16(bd ? bd + c : nullptr, bb);
                         tmem_ld_wait();
                         float o[16];
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 16; ++i) o[i] = wgt * (__uint_as_float(v[i]) + bb[i]);
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 4; ++i)
                             stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =
                                 make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
                         __syncwarp();
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int f = i * 32 + lane, rr = f >> 2, qq = f & 3;
                             const float4 val = stg[rr * 4 + (qq ^ ((rr >> 1) & 3))];
