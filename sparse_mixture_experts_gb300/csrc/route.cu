@@ -349,7 +349,17 @@ __global__ void __launch_bounds__(256) scatter_kernel(const __nv_bfloat16 *__res
     if (lane == 0) expert_rows[dst] = r;
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)tok * H);
     uint4 *d = reinterpret_cast<uint4 *>(xp + (size_t)dst * H);
-    for (int c = lane; c < H / 8; c += 32) d[c] = __ldg(src + c);
+    // four 16-byte loads in flight per lane before their stores
+    const int n16 = H / 8;
+    int c = lane;
+    for (; c + 96 < n16; c += 128) {
+        const uint4 v0 = __ldg(src + c), v1 = __ldg(src + c + 32), v2 = __ldg(src + c + 64), v3 = __ldg(src + c + 96);
+        d[c] = v0;
+        d[c + 32] = v1;
+        d[c + 64] = v2;
+        d[c + 96] = v3;
+    }
+    for (; c < n16; c += 32) d[c] = __ldg(src + c);
 }
 
 int launch_scatter(const Layer &L, const void *x, int T, bool rows, cudaStream_t s)
