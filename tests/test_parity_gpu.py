@@ -230,7 +230,7 @@ def test_misaligned_and_overlapping_pointers_rejected():
     assert rc == moe.ERR_INVALID_ARG
 
 
-def _small_case(spec, T, path, seed=21, out_dtype="f32", mutate=None):
+def _small_case(spec, T, path, seed=21, out_dtype="f32", mutate=None, repeats=0):
     if path == moe.PATH_FUSED and T > FUSED_MAX_TOKENS:
         T = 7  # a ragged decode batch
     if path == moe.PATH_DECODE_TC and T > DECODE_TC_MAX_TOKENS:
@@ -242,7 +242,11 @@ def _small_case(spec, T, path, seed=21, out_dtype="f32", mutate=None):
     layer = helpers.make_layer(spec, w, T, out_dtype=out_dtype)
     try:
         layer.set_path(path)
-        out = layer.forward(helpers.to_torch(x)).float().cpu().numpy()
+        xt = helpers.to_torch(x)
+        out = layer.forward(xt).float().cpu().numpy()
+        for _ in range(repeats):  # the same bits on every forward
+            again = layer.forward(xt).float().cpu().numpy()
+            assert np.array_equal(out, again, equal_nan=True)
     except moe.MoEError:
         layer.close()
         raise
@@ -290,6 +294,19 @@ EDGE_SPECS = [
                                                    expert_ff=128), 600),
 ]
 
+# Deep K (16 K blocks for gate/up, 8 for down) over few tiles, fewer than
+# half the SMs, in bf16 and both low-bit forms, with 128- and 256-row tiles
+DEEP_K_SPECS = [
+    ("deep_k_bf16", synth.QWEN.replace(name="deep K bf16", hidden=1024, n_expert=8, top_k=2, expert_ff=512,
+                                      shared_ff=512), 150),
+    ("deep_k_q4", synth.QWEN_Q4.replace(name="deep K q4", hidden=1024, n_expert=8, top_k=2, expert_ff=512), 150),
+    ("deep_k_q4_two_halves", synth.QWEN_Q4.replace(name="deep K q4 256 rows", hidden=1024, n_expert=4, top_k=2,
+                                                  expert_ff=512), 700),
+    ("deep_k_mxfp4", synth.GPTOSS_MXFP4.replace(name="deep K mxfp4", hidden=1024, n_expert=8, top_k=4,
+                                               expert_ff=512), 64),
+]
+EDGE_SPECS += DEEP_K_SPECS
+
 
 EDGE = [pytest.param(name, spec, T, path, id=f"{pid}-{name}")
         for name, spec, T in EDGE_SPECS for path, pid in zip(PATHS, PATH_IDS) if _applies(spec, path)]
@@ -299,6 +316,12 @@ EDGE = [pytest.param(name, spec, T, path, id=f"{pid}-{name}")
 def test_edge_cases(name, spec, T, path):
     rep = _small_case(spec, T, path)
     print(f"[{name} path={path}] {rep}")
+    assert rep.ok(spec.dtype), str(rep)
+
+
+@pytest.mark.parametrize("name,spec,T", DEEP_K_SPECS, ids=[n for n, _, _ in DEEP_K_SPECS])
+def test_deep_k_deterministic(name, spec, T):
+    rep = _small_case(spec, T, moe.PATH_TC, repeats=3)
     assert rep.ok(spec.dtype), str(rep)
 
 
