@@ -173,10 +173,35 @@ class MoELayer:
         self.x_dtype = _TORCH_DT[config.act_dtype]
 
     # ------------------------------------------------------------------
+    def _rows(self, t: torch.Tensor, name: str, dtype: torch.dtype, T: Optional[int], host: bool) -> int:
+        """The C ABI takes bare pointers, so the shape, dtype, layout and
+        device of a token-row tensor are checked here: a tensor that is
+        smaller than the layer assumes would be read or written past its
+        end.  Returns the number of rows."""
+        H = self.config.hidden
+        if t.dim() != 2 or t.shape[1] != H or (T is not None and t.shape[0] != T):
+            want = f"({T if T is not None else 'n_tokens'}, {H})"
+            raise ValueError(f"{name}: expected shape {want}, got {tuple(t.shape)}")
+        if t.dtype != dtype:
+            raise ValueError(f"{name}: expected dtype {dtype}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous tensor")
+        if host and t.device.type != "cpu":
+            raise ValueError(f"{name}: expected a host (CPU) tensor, got {t.device}")
+        if not host and t.device != self.device:
+            raise ValueError(f"{name}: expected a tensor on {self.device}, got {t.device}")
+        return int(t.shape[0])
+
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        T = x.shape[0]
+        """out = the layer applied to the token rows x [n_tokens, hidden] (the
+        activation dtype, on the layer's device); out [n_tokens, hidden] in
+        the output dtype is allocated when not given.  Asynchronous on
+        `stream` (default: the current stream)."""
+        T = self._rows(x, "x", self.x_dtype, None, host=False)
         if out is None:
             out = torch.empty((T, self.config.hidden), dtype=self.out_dtype, device=x.device)
+        else:
+            self._rows(out, "out", self.out_dtype, T, host=False)
         _check(_lib.moe_forward(self._h, x.data_ptr() if T else None, T, out.data_ptr() if T else None,
                                 _stream_handle(stream)))
         return out
@@ -186,7 +211,8 @@ class MoELayer:
     def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, stream=None) -> None:
         """x_host / out_host: CPU tensors (pinned for asynchronous copies).
         The caller synchronises the stream before reading out_host."""
-        T = x_host.shape[0]
+        T = self._rows(x_host, "x_host", self.x_dtype, None, host=True)
+        self._rows(out_host, "out_host", self.out_dtype, T, host=True)
         _check(_lib.moe_forward_host(self._h, x_host.data_ptr() if T else None, T,
                                      out_host.data_ptr() if T else None, _stream_handle(stream)))
 

@@ -107,3 +107,59 @@ def test_settings_reject_a_null_layer(lib):
     assert lib.moe_set_fault_injection(None, 1) == moe.ERR_INVALID_ARG
     assert lib.moe_get_intermediate(None, 0, None, 0, None, None) == moe.ERR_INVALID_ARG
     assert lib.moe_get_residency(None, None, None) == moe.ERR_INVALID_ARG
+
+
+def _unbound_layer(monkeypatch, calls):
+    """A MoELayer with its checks intact but no device layer behind it: the
+    library is a stand-in that records the calls it gets."""
+    import torch
+    import sparse_mixture_experts_gb300 as moe
+
+    class _Lib:
+        def moe_forward(self, *args):
+            calls.append(("moe_forward",) + args)
+            return moe.OK
+
+        def moe_forward_host(self, *args):
+            calls.append(("moe_forward_host",) + args)
+            return moe.OK
+
+    monkeypatch.setattr(moe, "_lib", _Lib())
+    layer = object.__new__(moe.MoELayer)
+    layer.config = moe.MoEConfig(hidden=64, n_expert=8, top_k=2, expert_ff=32, max_tokens=16)
+    layer.device = torch.device("cuda", 0)
+    layer.x_dtype, layer.out_dtype = torch.bfloat16, torch.float32
+    layer._h = ctypes.c_void_p()
+    return layer
+
+
+def test_binding_checks_token_rows_before_the_call(monkeypatch):
+    """The ABI takes bare pointers, so a tensor of the wrong shape, dtype,
+    layout or device is refused by the binding before any call."""
+    import torch
+    calls = []
+    layer = _unbound_layer(monkeypatch, calls)
+    x = torch.zeros((4, 64), dtype=torch.bfloat16)
+    out = torch.zeros((4, 64), dtype=torch.float32)
+    bad_x = [torch.zeros((4, 63), dtype=torch.bfloat16),        # hidden
+             torch.zeros((4, 64), dtype=torch.float32),         # dtype
+             torch.zeros((64, 4), dtype=torch.bfloat16).t(),    # layout
+             torch.zeros((4, 1, 64), dtype=torch.bfloat16),     # rank
+             x]                                                 # a host tensor for the device entry point
+    for t in bad_x:
+        with pytest.raises(ValueError):
+            layer.forward(t, stream=0)
+    bad_out = [torch.zeros((3, 64), dtype=torch.float32),       # rows
+               torch.zeros((4, 64), dtype=torch.bfloat16),      # dtype
+               torch.zeros((64, 4), dtype=torch.float32).t()]   # layout
+    for o in bad_out:
+        with pytest.raises(ValueError):
+            layer.forward_host(x, o, stream=0)
+    with pytest.raises(ValueError):
+        layer.forward_host(torch.zeros((4, 64), dtype=torch.float32), out, stream=0)
+    assert not calls
+    # well-formed host buffers reach the library with their pointers and count
+    layer.forward_host(x, out, stream=0)
+    layer.forward_host(x[:0], out[:0], stream=0)
+    assert calls == [("moe_forward_host", layer._h, x.data_ptr(), 4, out.data_ptr(), 0),
+                     ("moe_forward_host", layer._h, None, 0, None, 0)]
