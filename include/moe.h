@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 6
+#define MOE_ABI_VERSION 7
 
 typedef enum {
     MOE_OK = 0,
@@ -339,6 +339,11 @@ moe_status moe_set_fault_injection(moe_layer *layer, int32_t on);
 
 /* Number of kernel launches the last forward issued. */
 int32_t moe_last_launch_count(const moe_layer *layer);
+
+/* n_tokens of the last forward that returned MOE_OK (0 before the first, or
+ * for a NULL layer): the row count n that moe_get_routing, moe_get_logits and
+ * moe_get_intermediate write, so that a caller can size its buffers. */
+int32_t moe_last_token_count(const moe_layer *layer);
 
 /* Device bytes owned by the layer (weights + workspace). */
 size_t moe_device_bytes(const moe_layer *layer);

@@ -81,6 +81,7 @@ def load_library(path: str = LIB_PATH):
         "moe_timing_enable": ([VP, I32], ctypes.c_int),
         "moe_timing_read": ([VP, VP, VP], ctypes.c_int),
         "moe_last_launch_count": ([VP], I32),
+        "moe_last_token_count": ([VP], I32),
         "moe_device_bytes": ([VP], ctypes.c_size_t),
         "moe_destroy": ([VP], None),
         "moe_last_error": ([], ctypes.c_char_p),
@@ -216,14 +217,27 @@ class MoELayer:
         _check(_lib.moe_forward_host(self._h, x_host.data_ptr() if T else None, T,
                                      out_host.data_ptr() if T else None, _stream_handle(stream)))
 
-    def routing(self, n_tokens: int, stream=None):
+    def _last_tokens(self, n_tokens: Optional[int]) -> int:
+        """Rows of the last successful forward, which the getters write; a
+        caller's n_tokens must agree (a smaller buffer would overflow)."""
+        n = int(_lib.moe_last_token_count(self._h))
+        if n_tokens is not None and int(n_tokens) != n:
+            raise ValueError(f"the last forward had {n} tokens, not {n_tokens}")
+        return n
+
+    def routing(self, n_tokens: Optional[int] = None, stream=None):
+        """(idx [n, k] int32, w [n, k] fp32) of the last forward."""
+        n_tokens = self._last_tokens(n_tokens)
         k = self.config.top_k
         idx = torch.empty((n_tokens, k), dtype=torch.int32, device=self.device)
         w = torch.empty((n_tokens, k), dtype=torch.float32, device=self.device)
         _check(_lib.moe_get_routing(self._h, idx.data_ptr(), w.data_ptr(), _stream_handle(stream)))
         return idx, w
 
-    def logits(self, n_tokens: int, stream=None):
+    def logits(self, n_tokens: Optional[int] = None, stream=None):
+        """(router logits [n, E] fp32, shared-expert gate logits [n]) of the
+        last forward."""
+        n_tokens = self._last_tokens(n_tokens)
         l = torch.empty((n_tokens, self.config.n_expert), dtype=torch.float32, device=self.device)
         s = torch.zeros((n_tokens,), dtype=torch.float32, device=self.device)
         _check(_lib.moe_get_logits(self._h, l.data_ptr(), s.data_ptr(), _stream_handle(stream)))

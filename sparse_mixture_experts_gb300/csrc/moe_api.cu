@@ -781,6 +781,7 @@ moe_status moe_set_fault_injection(moe_layer *layer, int32_t on)
 }
 
 int32_t moe_last_launch_count(const moe_layer *layer) { return layer ? layer->last_launches : 0; }
+int32_t moe_last_token_count(const moe_layer *layer) { return layer ? layer->last_T : 0; }
 
 size_t moe_device_bytes(const moe_layer *layer) { return layer ? layer->device_bytes : 0; }
 

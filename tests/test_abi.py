@@ -43,7 +43,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.moe_abi_version() == 6
+    header = open(os.path.join(ROOT, "include", "moe.h")).read()
+    version = int(re.search(r"#define MOE_ABI_VERSION (\d+)", header).group(1))
+    assert lib.moe_abi_version() == version == 7
 
 
 def test_config_struct_layout_matches_header():
@@ -107,6 +109,7 @@ def test_settings_reject_a_null_layer(lib):
     assert lib.moe_set_fault_injection(None, 1) == moe.ERR_INVALID_ARG
     assert lib.moe_get_intermediate(None, 0, None, 0, None, None) == moe.ERR_INVALID_ARG
     assert lib.moe_get_residency(None, None, None) == moe.ERR_INVALID_ARG
+    assert lib.moe_last_token_count(None) == 0 and lib.moe_last_launch_count(None) == 0
 
 
 def _unbound_layer(monkeypatch, calls):
@@ -123,6 +126,9 @@ def _unbound_layer(monkeypatch, calls):
         def moe_forward_host(self, *args):
             calls.append(("moe_forward_host",) + args)
             return moe.OK
+
+        def moe_last_token_count(self, h):
+            return 4
 
     monkeypatch.setattr(moe, "_lib", _Lib())
     layer = object.__new__(moe.MoELayer)
@@ -163,3 +169,16 @@ def test_binding_checks_token_rows_before_the_call(monkeypatch):
     layer.forward_host(x[:0], out[:0], stream=0)
     assert calls == [("moe_forward_host", layer._h, x.data_ptr(), 4, out.data_ptr(), 0),
                      ("moe_forward_host", layer._h, None, 0, None, 0)]
+
+
+def test_binding_getters_take_the_last_forwards_rows(monkeypatch):
+    """routing() and logits() size their buffers from the layer's last
+    forward; a caller's different count is refused before any allocation."""
+    calls = []
+    layer = _unbound_layer(monkeypatch, calls)
+    assert layer._last_tokens(None) == 4 and layer._last_tokens(4) == 4
+    for n in (3, 5):
+        with pytest.raises(ValueError):
+            layer.routing(n)
+        with pytest.raises(ValueError):
+            layer.logits(n)
