@@ -39,9 +39,11 @@ moe_status moe_ep_send_plan(int32_t n_expert, int32_t n_ranks, const int32_t *fi
     if (n_expert <= 0 || n_ranks <= 0 || !first_expert || !counts || !send_counts || !send_displs)
         return ep_fail("sizes must be positive and pointers non-NULL");
     if (first_expert[0] != 0 || first_expert[n_ranks] != n_expert) return ep_fail("ranges must cover 0 .. n_expert");
+    // every bound checked before any count is read: ascending from 0 to n_expert
+    for (int g = 0; g < n_ranks; ++g)
+        if (first_expert[g + 1] < first_expert[g]) return ep_fail("expert ranges must be ascending");
     int64_t displ = 0;
     for (int g = 0; g < n_ranks; ++g) {
-        if (first_expert[g + 1] < first_expert[g]) return ep_fail("expert ranges must be ascending");
         int64_t c = 0;
         for (int e = first_expert[g]; e < first_expert[g + 1]; ++e) {
             if (counts[e] < 0) return ep_fail("negative count");

@@ -44,6 +44,8 @@ def send_plan(counts, first):
     G = len(first) - 1
     c = torch.as_tensor(counts, dtype=torch.int32).contiguous().cpu()
     f = torch.tensor(first, dtype=torch.int32)
+    if G < 1 or c.dim() != 1 or c.numel() != int(f[-1]):
+        raise ValueError("counts must hold one entry per expert of the partition")
     sc = torch.empty(G, dtype=torch.int32)
     sd = torch.empty(G, dtype=torch.int32)
     _check(lib.moe_ep_send_plan(int(f[-1]), G, _i32(f), _i32(c), _i32(sc), _i32(sd)))
@@ -55,6 +57,8 @@ def recv_plan(counts_from):
     counts the ranks send this one."""
     lib = load_library()
     cf = torch.as_tensor(counts_from, dtype=torch.int32).contiguous().cpu()
+    if cf.dim() != 2:
+        raise ValueError("counts_from must be [n_ranks][n_local]")
     G, n_local = cf.shape
     rc = torch.empty(G, dtype=torch.int32)
     rd = torch.empty(G, dtype=torch.int32)

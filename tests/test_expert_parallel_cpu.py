@@ -137,3 +137,25 @@ def test_two_gloo_ranks_reproduce_the_oracle():
     assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
     assert set(results.keys()) == {0, 1}
     assert max(results.values()) <= 1e-12, dict(results)
+
+
+def test_plans_reject_bad_partitions_and_counts():
+    """Bounds that run past n_expert, descend, or leave experts out are
+    refused before any count is read; a count list of the wrong length is
+    refused by the binding."""
+    import ctypes
+    import sparse_mixture_experts_gb300 as moe
+    from sparse_mixture_experts_gb300 import expert_parallel as ep
+    lib = moe.load_library()
+    counts = (ctypes.c_int32 * 8)(*range(8))
+    sc, sd = (ctypes.c_int32 * 2)(), (ctypes.c_int32 * 2)()
+    for first in ([0, 10, 8], [0, 5, 3, 8][:3], [1, 4, 8], [0, 4, 7]):
+        f = (ctypes.c_int32 * len(first))(*first)
+        assert lib.moe_ep_send_plan(8, 2, f, counts, sc, sd) == moe.ERR_INVALID_ARG, first
+    f = (ctypes.c_int32 * 3)(0, 4, 8)
+    assert lib.moe_ep_send_plan(8, 2, f, counts, sc, sd) == moe.OK
+    assert list(sc) == [0 + 1 + 2 + 3, 4 + 5 + 6 + 7] and list(sd) == [0, 6]
+    with pytest.raises(ValueError):
+        ep.send_plan(list(range(7)), [0, 4, 8])
+    with pytest.raises(ValueError):
+        ep.recv_plan([1, 2, 3])
